@@ -1,0 +1,91 @@
+"""Oracle-side graph spec of a Llama-style decode step.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/forward.py``).
+
+Writes the decoder-layer listing of "mega kernel initial" (1y33.com, the
+"building the graph" part) as plain op records for ``oracle.lowering.lower``:
+embed -> per layer [qkv matmul with RMSNorm input, attention, o_proj with
+residual, gate_up with RMSNorm input and SiLU*mul, down with residual] ->
+lm_head matmul with the final RMSNorm fused and the per-tile argmax
+epilogue -> SAMPLE.
+
+Buffers are registered append-only, in this order (the library's Python
+builder follows the same convention, so indices agree):
+  0 state [B, 2] int32 (token, pos)     1, 2 RoPE cos / sin tables
+  weights in ``synth.weight_names`` order
+  per layer: K cache, V cache ([B*Hkv, cap*D] bf16)
+  history [B, cap] int32
+  then activations and scratch as each op allocates its output.
+"""
+from __future__ import annotations
+
+from .lowering import (F_SILU_MUL, F_ADD_RESIDUAL, F_RMS_NORM_INPUT, F_ARGMAX_EPI,
+                       NO_BUF, tiles, partials_per_sequence)
+
+BF16, F32, I32, PAIR = 1, 2, 3, 4
+
+
+def llama_decode_spec(model, B: int, len0, cap: int, chunk: int, num_ctas: int,
+                      tiles_target: int = 0, col_align: int = 16) -> dict:
+    m = model
+    tt = tiles_target or num_ctas
+    bufs = [(I32, B, 2), (F32, cap, m.D // 2), (F32, cap, m.D // 2)]
+    idx = {}
+
+    def reg(name, dtype, rows, cols):
+        bufs.append((dtype, rows, cols))
+        idx[name] = len(bufs) - 1
+        return idx[name]
+
+    reg("embed", BF16, m.V, m.H)
+    for l in range(m.L):
+        reg(f"layer{l}.attn_norm", BF16, 1, m.H)
+        reg(f"layer{l}.wqkv", BF16, m.n_qkv, m.H)
+        reg(f"layer{l}.wo", BF16, m.H, m.Hq * m.D)
+        reg(f"layer{l}.mlp_norm", BF16, 1, m.H)
+        reg(f"layer{l}.wgu", BF16, 2 * m.F, m.H)
+        reg(f"layer{l}.wd", BF16, m.H, m.F)
+    reg("final_norm", BF16, 1, m.H)
+    lm = idx["embed"] if m.tied else reg("lm_head", BF16, m.V, m.H)
+    for l in range(m.L):
+        reg(f"layer{l}.k_cache", BF16, B * m.Hkv, cap * m.D)
+        reg(f"layer{l}.v_cache", BF16, B * m.Hkv, cap * m.D)
+    hist = reg("history", I32, B, cap)
+
+    ops = []
+    act = [0]
+
+    def fresh(dtype, rows, cols):
+        act[0] += 1
+        return reg(f"act{act[0]}", dtype, rows, cols)
+
+    def matmul(x, w, n, k, aux=NO_BUF, flags=0, eps=0.0, pairs=NO_BUF, out=None):
+        out = fresh(F32, B, n) if out is None else out
+        ops.append(dict(kind="matmul", x=x, w=w, out=out, aux=aux, pairs=pairs,
+                        flags=flags, m=B, n=n, k=k, eps=eps))
+        return out
+
+    h = fresh(F32, B, m.H)
+    ops.append(dict(kind="embed", table=idx["embed"], out=h, B=B, H=m.H))
+    G = m.Hq // m.Hkv
+    P = partials_per_sequence(len0, m.Hkv, chunk, num_ctas)
+    for l in range(m.L):
+        qkv = matmul(h, idx[f"layer{l}.wqkv"], m.n_qkv, m.H, aux=idx[f"layer{l}.attn_norm"],
+                     flags=F_RMS_NORM_INPUT, eps=m.eps)
+        scr = fresh(F32, B * m.Hkv * 0 + sum(P) * m.Hkv, G * (m.D + 2))
+        att = fresh(F32, B, m.Hq * m.D)
+        ops.append(dict(kind="attention", qkv=qkv, k=idx[f"layer{l}.k_cache"],
+                        v=idx[f"layer{l}.v_cache"], out=att, scratch=scr, B=B, Hq=m.Hq,
+                        Hkv=m.Hkv, D=m.D, capacity=cap, len0=list(len0), chunk=chunk))
+        h1 = matmul(att, idx[f"layer{l}.wo"], m.H, m.Hq * m.D, aux=h, flags=F_ADD_RESIDUAL)
+        gu = matmul(h1, idx[f"layer{l}.wgu"], m.F, m.H, aux=idx[f"layer{l}.mlp_norm"],
+                    flags=F_RMS_NORM_INPUT | F_SILU_MUL, eps=m.eps)
+        h = matmul(gu, idx[f"layer{l}.wd"], m.H, m.F, aux=h1, flags=F_ADD_RESIDUAL)
+    T = len(tiles(m.V, tt, col_align))
+    logits = fresh(F32, B, m.V)
+    pairs = fresh(PAIR, B, T)
+    matmul(h, lm, m.V, m.H, aux=idx["final_norm"], flags=F_RMS_NORM_INPUT | F_ARGMAX_EPI,
+           eps=m.eps, pairs=pairs, out=logits)
+    ops.append(dict(kind="sample", pairs=pairs, history=hist, B=B, V=m.V, capacity=cap))
+    return dict(num_ctas=num_ctas, tiles_target=tiles_target, col_align=col_align,
+                buffers=bufs, ops=ops, names=idx)

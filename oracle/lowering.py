@@ -1,0 +1,239 @@
+"""Oracle lowering: graph ops -> 64-byte task descriptors + dependents edges.
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/forward.py``).  Written independently
+of the C++ lowering in the library; the two must emit identical bytes.
+
+Source: "mega kernel initial" (1y33.com).
+* Each op becomes one or more 64-byte task descriptors (the lowering part
+  and its TaskDescriptor listing: op_id@0, config_id@2, step@4, flags@6,
+  remaining_deps@8, num_dependents@12, dependents_offset@16, in_buf[3]@20,
+  out_buf@26, m@28, n@32, k@36, kv_len@40, reserved[5]@44).
+* A matmul fans out into one GEMV task per output-column tile, roughly one
+  per SM; 3072 columns over 8 tiles gives 8 tasks of 384 columns.
+* Attention becomes ATTENTION_PARTIAL tasks per (sequence, KV-head group,
+  KV chunk) followed by a combine (plain flash decoding); the current k/v
+  are RoPE-appended by ATTENTION_APPEND (the OpId table).
+* RMSNorm-on-input, residual add and SiLU*mul are flags on the GEMV
+  (bit0 SILU_MUL, bit1 ADD_RESIDUAL, bit2 RMS_NORM_INPUT).
+* Every op output remembers which task wrote which column range; a reader
+  depends on the writers of what it reads.  Parents are then flipped into
+  per-task dependents lists flattened into one edge array, and tasks are
+  emitted in topological order.
+
+Readings taken where the page is silent (the same frozen spec the library
+implements): the tile rule col_tile = round_up(ceil(n / tiles_target),
+col_align); one COMBINE per (sequence, KV head); the split-KV chunk rule in
+``partials_per_sequence``; bit3 ARGMAX_EPI on the lm_head GEMV; the embedding
+row gather as a MEMCPY task; field maps per op as in ``_desc_*`` below.
+Access ranges are tracked as row x column rectangles of each buffer's 2-D
+view, so per-sequence writes (embedding, combine) do not alias.
+"""
+from __future__ import annotations
+
+import struct
+
+import numpy as np
+
+ABI_VERSION = 1
+
+OP_NOP, OP_MEMCPY, OP_GEMV, OP_RMSNORM, OP_ATTENTION, OP_MLP, OP_SAMPLE = 0, 1, 2, 3, 4, 5, 6
+OP_ATT_APPEND, OP_ATT_PARTIAL, OP_ATT_COMBINE = 7, 8, 9
+
+F_SILU_MUL, F_ADD_RESIDUAL, F_RMS_NORM_INPUT, F_ARGMAX_EPI = 1, 2, 4, 8
+
+NO_BUF = 0xFFFF
+BUF_STATE, BUF_ROPE_COS, BUF_ROPE_SIN = 0, 1, 2
+
+TASK_DTYPE = np.dtype([
+    ("op_id", "<u2"), ("config_id", "<u2"), ("step", "<u2"), ("flags", "<u2"),
+    ("remaining_deps", "<i4"), ("num_dependents", "<i4"), ("dependents_offset", "<u4"),
+    ("in_buf", "<u2", (3,)), ("out_buf", "<u2"),
+    ("m", "<i4"), ("n", "<i4"), ("k", "<i4"), ("kv_len", "<i4"),
+    ("reserved", "<u4", (5,)),
+])
+assert TASK_DTYPE.itemsize == 64
+
+
+def ceil_div(a: int, b: int) -> int:
+    return -(-a // b)
+
+
+def tile_width(n: int, tiles_target: int, col_align: int) -> int:
+    return ceil_div(ceil_div(n, tiles_target), col_align) * col_align
+
+
+def tiles(n: int, tiles_target: int, col_align: int):
+    """[(col_begin, col_count)] of the GEMV column tiles of an n-column op."""
+    w = tile_width(n, tiles_target, col_align)
+    return [(c, min(w, n - c)) for c in range(0, n, w)]
+
+
+def partials_per_sequence(len0, Hkv: int, chunk: int, num_ctas: int):
+    """Split-KV chunk count P_s per sequence (fixed at lowering time).
+    chunk > 0: ceil(len0_s / chunk).  chunk == 0: chunks of about
+    E = max(256, ceil(Hkv * sum(len0) / num_ctas)) keys, so the partial tasks
+    of a ragged batch carry about the same bytes and number about one per SM."""
+    if chunk > 0:
+        return [max(1, ceil_div(int(l), chunk)) for l in len0]
+    E = max(256, ceil_div(Hkv * sum(int(l) for l in len0), num_ctas))
+    return [max(1, ceil_div(int(l), E)) for l in len0]
+
+
+def f32_bits(x: float) -> int:
+    return struct.unpack("<I", struct.pack("<f", float(x)))[0]
+
+
+class _Writes:
+    """Per-buffer record of which task wrote which row x column rectangle."""
+
+    def __init__(self):
+        self.by_buf = {}
+
+    def add(self, buf, task, r0, r1, c0, c1):
+        self.by_buf.setdefault(buf, []).append((task, r0, r1, c0, c1))
+
+    def writers(self, buf, r0, r1, c0, c1):
+        out = set()
+        for (t, a0, a1, b0, b1) in self.by_buf.get(buf, ()):
+            if a0 < r1 and r0 < a1 and b0 < c1 and c0 < b1:
+                out.add(t)
+        return out
+
+
+def lower(spec: dict):
+    """Lower a graph spec to (tasks [N] TASK_DTYPE, edges [E] uint32).
+
+    spec = {"num_ctas", "tiles_target" (0 = num_ctas), "col_align",
+            "buffers": [(dtype, rows, cols)] indexed by buffer id,
+            "ops": [dict(kind=..., ...)] in call order}."""
+    num_ctas = spec["num_ctas"]
+    tt = spec.get("tiles_target", 0) or num_ctas
+    align = spec.get("col_align", 16)
+    bufs = spec["buffers"]
+    descs = []       # list of dict fields
+    parents = []     # list of sets
+    W = _Writes()
+
+    def emit(fields, reads, writes):
+        t = len(descs)
+        ps = set()
+        for (b, r0, r1, c0, c1) in reads:
+            ps |= W.writers(b, r0, r1, c0, c1)
+        for (b, r0, r1, c0, c1) in writes:
+            W.add(b, t, r0, r1, c0, c1)
+        descs.append(fields)
+        parents.append(ps)
+
+    for op in spec["ops"]:
+        kind = op["kind"]
+        if kind == "embed":
+            B, H = op["B"], op["H"]
+            for s in range(B):
+                emit(dict(op_id=OP_MEMCPY, in_buf=(op["table"], NO_BUF, NO_BUF),
+                          out_buf=op["out"], m=B, n=H, reserved=(s, 0, 0, 0, 0)),
+                     reads=[(BUF_STATE, s, s + 1, 0, 2)],
+                     writes=[(op["out"], s, s + 1, 0, H)])
+        elif kind == "matmul":
+            B, n, K, fl = op["m"], op["n"], op["k"], op["flags"]
+            aux = op.get("aux", NO_BUF)
+            pairs = op.get("pairs", NO_BUF)
+            eps_bits = f32_bits(op["eps"]) if fl & F_RMS_NORM_INPUT else 0
+            for t, (c0, cn) in enumerate(tiles(n, tt, align)):
+                reads = [(op["x"], 0, B, 0, K)]
+                if fl & F_ADD_RESIDUAL:
+                    reads.append((aux, 0, B, c0, c0 + cn))
+                writes = [(op["out"], 0, B, c0, c0 + cn)]
+                if fl & F_ARGMAX_EPI:
+                    writes.append((pairs, 0, B, t, t + 1))
+                emit(dict(op_id=OP_GEMV, config_id=0 if B < 8 else 1, flags=fl,
+                          in_buf=(op["x"], op["w"], aux), out_buf=op["out"],
+                          m=B, n=n, k=K,
+                          reserved=(c0, cn, eps_bits,
+                                    pairs if fl & F_ARGMAX_EPI else 0, 0)),
+                     reads, writes)
+        elif kind == "attention":
+            B, Hq, Hkv, D, cap = op["B"], op["Hq"], op["Hkv"], op["D"], op["capacity"]
+            G = Hq // Hkv
+            cfg = 0 if D == 64 else 1
+            qkv, kc, vc, out, scr = op["qkv"], op["k"], op["v"], op["out"], op["scratch"]
+            P = partials_per_sequence(op["len0"], Hkv, op["chunk"], num_ctas)
+            base = []
+            acc = 0
+            for s in range(B):
+                base.append([acc + g * P[s] for g in range(Hkv)])
+                acc += Hkv * P[s]
+            common = dict(m=B, n=D, k=Hq, kv_len=cap)
+            for s in range(B):
+                for g in range(Hkv):
+                    kcol = Hq * D + g * D
+                    vcol = (Hq + Hkv) * D + g * D
+                    row = s * Hkv + g
+                    emit(dict(op_id=OP_ATT_APPEND, config_id=cfg, in_buf=(qkv, kc, vc),
+                              out_buf=kc, reserved=(s, g, Hkv, 0, 0), **common),
+                         reads=[(qkv, s, s + 1, kcol, kcol + D),
+                                (qkv, s, s + 1, vcol, vcol + D),
+                                (BUF_STATE, s, s + 1, 0, 2)],
+                         writes=[(kc, row, row + 1, 0, cap * D),
+                                 (vc, row, row + 1, 0, cap * D)])
+            for s in range(B):
+                for g in range(Hkv):
+                    row = s * Hkv + g
+                    for c in range(P[s]):
+                        slot = base[s][g] + c
+                        emit(dict(op_id=OP_ATT_PARTIAL, config_id=cfg, in_buf=(qkv, kc, vc),
+                                  out_buf=scr,
+                                  reserved=(s, g, Hkv, c | (P[s] << 16), base[s][g]),
+                                  **common),
+                             reads=[(qkv, s, s + 1, g * G * D, (g + 1) * G * D),
+                                    (kc, row, row + 1, 0, cap * D),
+                                    (vc, row, row + 1, 0, cap * D),
+                                    (BUF_STATE, s, s + 1, 0, 2)],
+                             writes=[(scr, slot, slot + 1, 0, G * (D + 2))])
+            for s in range(B):
+                for g in range(Hkv):
+                    emit(dict(op_id=OP_ATT_COMBINE, config_id=cfg,
+                              in_buf=(scr, NO_BUF, NO_BUF), out_buf=out,
+                              reserved=(s, g, Hkv, P[s], base[s][g]), **common),
+                         reads=[(scr, base[s][g], base[s][g] + P[s], 0, G * (D + 2))],
+                         writes=[(out, s, s + 1, g * G * D, (g + 1) * G * D)])
+        elif kind == "sample":
+            B, V, cap = op["B"], op["V"], op["capacity"]
+            T = len(tiles(V, tt, align))
+            for s in range(B):
+                emit(dict(op_id=OP_SAMPLE, in_buf=(op["pairs"], NO_BUF, NO_BUF),
+                          out_buf=op["history"], m=B, n=V, k=T, kv_len=cap,
+                          reserved=(s, 0, 0, 0, 0)),
+                     reads=[(op["pairs"], s, s + 1, 0, T), (BUF_STATE, s, s + 1, 0, 2)],
+                     writes=[(op["history"], s, s + 1, 0, cap),
+                             (BUF_STATE, s, s + 1, 0, 2)])
+        else:
+            raise ValueError(kind)
+
+    N = len(descs)
+    children = [[] for _ in range(N)]
+    for t in range(N):
+        for p in sorted(parents[t]):
+            assert p < t
+            children[p].append(t)
+    tasks = np.zeros(N, dtype=TASK_DTYPE)
+    off = 0
+    edges = []
+    for t, f in enumerate(descs):
+        d = tasks[t]
+        d["op_id"] = f["op_id"]
+        d["config_id"] = f.get("config_id", 0)
+        d["step"] = 0
+        d["flags"] = f.get("flags", 0)
+        d["remaining_deps"] = len(parents[t])
+        d["num_dependents"] = len(children[t])
+        d["dependents_offset"] = off
+        d["in_buf"] = f["in_buf"]
+        d["out_buf"] = f["out_buf"]
+        d["m"] = f.get("m", 0)
+        d["n"] = f.get("n", 0)
+        d["k"] = f.get("k", 0)
+        d["kv_len"] = f.get("kv_len", 0)
+        d["reserved"] = f["reserved"]
+        edges.extend(children[t])
+        off += len(children[t])
+    return tasks, np.array(edges, dtype=np.uint32)

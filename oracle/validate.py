@@ -1,0 +1,211 @@
+"""DAG validator for a lowered task graph (descriptors + dependents edges).
+
+TEST INFRASTRUCTURE ONLY (see ``oracle/forward.py``).
+
+Checks the properties that "mega kernel initial" (1y33.com) states for its
+lowered graph and that the interpreter's correctness rests on:
+
+* tasks are in topological order: every edge points to a later task
+  (the edge-array part: "a task can never depend on one emitted after it");
+* each task's dependency count equals its number of parents, and the edge
+  array is the flattened, offset-indexed dependents lists;
+* a task's level is 1 + the max level of its parents, and two tasks of the
+  same level are independent (the levels part);
+* every pair of tasks touching overlapping data, at least one writing, is
+  ordered by a path in the DAG (no read/write or write/write race);
+* every read of a buffer that the graph writes is covered by earlier writes,
+  except reads of the decode state (carried in from the previous step) and
+  reads of buffers whose writers all come later.
+
+Access rectangles are decoded from the descriptor fields alone, by code
+separate from the lowering that produced them.
+"""
+from __future__ import annotations
+
+from collections import defaultdict
+
+import numpy as np
+
+from .lowering import (OP_MEMCPY, OP_GEMV, OP_SAMPLE, OP_ATT_APPEND, OP_ATT_PARTIAL,
+                       OP_ATT_COMBINE, F_ADD_RESIDUAL, F_ARGMAX_EPI, NO_BUF, BUF_STATE)
+
+
+class ValidationError(AssertionError):
+    pass
+
+
+def task_accesses(d) -> tuple:
+    """(reads, writes) as lists of (buf, r0, r1, c0, c1) for one descriptor."""
+    op = int(d["op_id"])
+    ib = [int(x) for x in d["in_buf"]]
+    ob = int(d["out_buf"])
+    rs = [int(x) for x in d["reserved"]]
+    m, n, k, kv = int(d["m"]), int(d["n"]), int(d["k"]), int(d["kv_len"])
+    R, Wr = [], []
+    if op == OP_MEMCPY:
+        s = rs[0]
+        R.append((BUF_STATE, s, s + 1, 0, 2))
+        Wr.append((ob, s, s + 1, 0, n))
+    elif op == OP_GEMV:
+        c0, cn = rs[0], rs[1]
+        R.append((ib[0], 0, m, 0, k))
+        if int(d["flags"]) & F_ADD_RESIDUAL:
+            R.append((ib[2], 0, m, c0, c0 + cn))
+        Wr.append((ob, 0, m, c0, c0 + cn))
+        if int(d["flags"]) & F_ARGMAX_EPI:
+            # the tile index is the tile's position among equal-width tiles
+            Wr.append((rs[3], 0, m, -1, -1))     # resolved below
+    elif op in (OP_ATT_APPEND, OP_ATT_PARTIAL, OP_ATT_COMBINE):
+        s, g, Hkv = rs[0], rs[1], rs[2]
+        D, Hq, cap = n, k, kv
+        G = Hq // Hkv
+        row = s * Hkv + g
+        if op == OP_ATT_APPEND:
+            R += [(ib[0], s, s + 1, Hq * D + g * D, Hq * D + (g + 1) * D),
+                  (ib[0], s, s + 1, (Hq + Hkv) * D + g * D, (Hq + Hkv) * D + (g + 1) * D),
+                  (BUF_STATE, s, s + 1, 0, 2)]
+            Wr += [(ib[1], row, row + 1, 0, cap * D), (ib[2], row, row + 1, 0, cap * D)]
+        elif op == OP_ATT_PARTIAL:
+            c, P = rs[3] & 0xFFFF, rs[3] >> 16
+            assert c < P
+            slot = rs[4] + c
+            R += [(ib[0], s, s + 1, g * G * D, (g + 1) * G * D),
+                  (ib[1], row, row + 1, 0, cap * D), (ib[2], row, row + 1, 0, cap * D),
+                  (BUF_STATE, s, s + 1, 0, 2)]
+            Wr.append((ob, slot, slot + 1, 0, G * (D + 2)))
+        else:
+            P, base = rs[3], rs[4]
+            R.append((ib[0], base, base + P, 0, G * (D + 2)))
+            Wr.append((ob, s, s + 1, g * G * D, (g + 1) * G * D))
+    elif op == OP_SAMPLE:
+        s = rs[0]
+        R += [(ib[0], s, s + 1, 0, k), (BUF_STATE, s, s + 1, 0, 2)]
+        Wr += [(ob, s, s + 1, 0, kv), (BUF_STATE, s, s + 1, 0, 2)]
+    else:
+        raise ValidationError(f"unknown op_id {op}")
+    return R, Wr
+
+
+def _resolve_pairs_columns(tasks, acc):
+    """ARGMAX_EPI tiles write column t of the pairs buffer, t being the tile's
+    rank among the tiles of its op (consecutive GEMV tasks with one out_buf)."""
+    rank = {}
+    prev = None
+    for t in range(len(tasks)):
+        d = tasks[t]
+        if int(d["op_id"]) == OP_GEMV and int(d["flags"]) & F_ARGMAX_EPI:
+            key = (int(d["out_buf"]), int(d["reserved"][3]))
+            rank[t] = rank[prev] + 1 if prev is not None and prev_key == key else 0
+            prev, prev_key = t, key
+        else:
+            prev = None
+    for t, r in rank.items():
+        R, W = acc[t]
+        acc[t] = (R, [(b, r0, r1, r if c0 == -1 else c0, r + 1 if c1 == -1 else c1)
+                      for (b, r0, r1, c0, c1) in W])
+
+
+def _covered(intervals, c0, c1) -> bool:
+    cur = c0
+    for a, b in sorted(intervals):
+        if a > cur:
+            return False
+        cur = max(cur, b)
+        if cur >= c1:
+            return True
+    return cur >= c1
+
+
+def validate(tasks: np.ndarray, edges: np.ndarray, check_hazards: bool = True) -> dict:
+    """Raise ValidationError on the first violated property; return stats."""
+    N = len(tasks)
+    deps = tasks["remaining_deps"].astype(np.int64)
+    cnt = tasks["num_dependents"].astype(np.int64)
+    off = tasks["dependents_offset"].astype(np.int64)
+    if int(cnt.sum()) != len(edges):
+        raise ValidationError("edge array length != sum of num_dependents")
+    expect_off = np.concatenate([[0], np.cumsum(cnt)[:-1]]) if N else cnt
+    if not np.array_equal(off, expect_off):
+        raise ValidationError("dependents_offset is not the exclusive prefix sum")
+    parents = [[] for _ in range(N)]
+    for t in range(N):
+        ch = edges[off[t]: off[t] + cnt[t]].astype(np.int64)
+        if len(ch) and (ch.min() <= t):
+            raise ValidationError(f"task {t} has an edge to an earlier task")
+        if len(ch) > 1 and not np.all(np.diff(ch) > 0):
+            raise ValidationError(f"task {t} children not strictly ascending")
+        for c in ch:
+            parents[int(c)].append(t)
+    for t in range(N):
+        if len(parents[t]) != deps[t]:
+            raise ValidationError(f"task {t}: remaining_deps {deps[t]} != {len(parents[t])} parents")
+        if int(tasks["step"][t]) != 0:
+            raise ValidationError("step field must be 0")
+    level = np.zeros(N, dtype=np.int64)
+    for t in range(N):
+        if parents[t]:
+            level[t] = 1 + max(level[p] for p in parents[t])
+    acc = [task_accesses(tasks[t]) for t in range(N)]
+    _resolve_pairs_columns(tasks, acc)
+
+    # read coverage
+    writes_by_buf = defaultdict(list)
+    for t in range(N):
+        for (b, r0, r1, c0, c1) in acc[t][1]:
+            writes_by_buf[b].append((t, r0, r1, c0, c1))
+    for t in range(N):
+        for (b, r0, r1, c0, c1) in acc[t][0]:
+            ws = writes_by_buf.get(b)
+            if b == BUF_STATE or not ws or min(w[0] for w in ws) >= t:
+                continue      # carried in from the previous step (state) or external
+            for r in range(r0, r1):
+                iv = [(a0, a1) for (wt, q0, q1, a0, a1) in ws if wt < t and q0 <= r < q1]
+                if not _covered(iv, c0, c1):
+                    raise ValidationError(f"task {t} reads buf {b} row {r} [{c0},{c1}) "
+                                          f"not covered by earlier writes")
+    stats = dict(tasks=N, edges=len(edges), levels=int(level.max()) + 1 if N else 0)
+    if not check_hazards:
+        return stats
+
+    # ancestry bitsets (python ints) in topological order
+    anc = [0] * N
+    for t in range(N):
+        a = 0
+        for p in parents[t]:
+            a |= anc[p] | (1 << p)
+        anc[t] = a
+
+    def ordered(a, b):
+        lo, hi = (a, b) if a < b else (b, a)
+        return (anc[hi] >> lo) & 1 == 1
+
+    by_buf = defaultdict(list)
+    for t in range(N):
+        for (b, r0, r1, c0, c1) in acc[t][0]:
+            by_buf[b].append((t, r0, r1, c0, c1, False))
+        for (b, r0, r1, c0, c1) in acc[t][1]:
+            by_buf[b].append((t, r0, r1, c0, c1, True))
+    for b, lst in by_buf.items():
+        ws = [x for x in lst if x[5]]
+        for (wt, a0, a1, b0, b1, _) in ws:
+            for (t, r0, r1, c0, c1, isw) in lst:
+                if t == wt or not (a0 < r1 and r0 < a1 and b0 < c1 and c0 < b1):
+                    continue
+                if not ordered(wt, t):
+                    kind = "write/write" if isw else "read/write"
+                    raise ValidationError(f"{kind} race on buf {b}: tasks {wt} and {t}")
+                if level[wt] == level[t]:
+                    raise ValidationError(f"same-level tasks {wt},{t} touch buf {b}")
+    return stats
+
+
+def levels(tasks: np.ndarray, edges: np.ndarray) -> np.ndarray:
+    """Level of every task: 0 without parents, else 1 + max parent level."""
+    N = len(tasks)
+    level = np.zeros(N, dtype=np.int64)
+    cnt = tasks["num_dependents"].astype(np.int64)
+    off = tasks["dependents_offset"].astype(np.int64)
+    for t in range(N):
+        for c in edges[off[t]: off[t] + cnt[t]]:
+            level[c] = max(level[c], level[t] + 1)
+    return level
