@@ -1,0 +1,283 @@
+/*
+ * mk.h -- C ABI of libmk, a decode "megakernel" that interprets a static task
+ * DAG on one GB300 (sm_103a).
+ *
+ * Model.  A decode step of a Llama-style decoder is composed by calling ops
+ * on a graph object ("mega kernel initial", 1y33.com: the graph-building
+ * part, where a decoder layer is written as matmul / attention calls with
+ * gamma=, residual= and silu_mul= keywords).  mk_lower() turns the ops into
+ * 64-byte task descriptors in topological order plus a flat dependents edge
+ * array (same page: the lowering part with its TaskDescriptor listing, and
+ * the part on flipping parents into a dependents edge array).  mk_upload()
+ * copies descriptors, edges and the buffer pointer table to the device
+ * (same page: the buffer-table and upload part).  mk_decode_step() runs one
+ * persistent kernel, one CTA per SM, that walks a static per-CTA queue of
+ * tasks; each task waits only for its own producers through per-task
+ * counters in global memory, with no grid-wide barrier ("Megakernels",
+ * runhoid.com: the "Hoid's approach to megakernels" section and its Fig. 5,
+ * the on-GPU interpreter in which a block waits only for its producers).
+ *
+ * Conventions.
+ *  - Every function returns an int: MK_OK (0) or a negative MK_ERR_* code;
+ *    mk_last_error() gives a message for the calling thread's last error.
+ *  - A graph is not thread-safe; use one graph from one thread at a time.
+ *  - `stream` is a cudaStream_t passed as void*.  Device work is enqueued
+ *    asynchronously on it.  Only mk_upload (pageable copies) and mk_status
+ *    synchronise the stream.
+ *  - The CALLER owns every tensor registered with mk_add_buffer/mk_set_state
+ *    (weights, KV caches, activations, scratch, state, history): it
+ *    allocates them, keeps them alive while the graph exists and frees them
+ *    after mk_destroy.  The LIBRARY owns what it allocates in mk_upload:
+ *    the device blob (descriptors, edges, buffer table, per-CTA queues,
+ *    dependency counters, status word, RoPE tables, trace ring).
+ *  - Functions up to mk_get_queues need no GPU unless num_ctas is 0.
+ *  - Sizes are elements unless stated; all device pointers must be 256-byte
+ *    aligned (PyTorch allocations are).
+ */
+#ifndef MK_H
+#define MK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MK_ABI_VERSION 1u
+
+/* ---- return codes ------------------------------------------------------ */
+#define MK_OK 0
+#define MK_ERR_ARG (-1)    /* bad index, dtype, shape or argument */
+#define MK_ERR_STATE (-2)  /* call out of order (add after lower, step before upload) */
+#define MK_ERR_LIMIT (-3)  /* more than 65535 buffers, or a size over a stated limit */
+#define MK_ERR_ABI (-4)    /* mk_config.abi_version != MK_ABI_VERSION */
+#define MK_ERR_CUDA (-5)   /* a CUDA runtime call failed (message has details) */
+#define MK_ERR_NOMEM (-6)  /* host or device allocation failed */
+
+/* ---- device status codes reported by mk_status ------------------------- */
+#define MK_DEV_OK 0
+#define MK_DEV_DEP_TIMEOUT (-10)   /* a dependency wait exceeded wait_timeout_us */
+#define MK_DEV_BAD_OP (-11)        /* a descriptor had an unknown op_id */
+#define MK_DEV_RING_TIMEOUT (-12)  /* a shared-memory pipeline wait timed out */
+#define MK_DEV_CAPACITY (-13)      /* pos + 1 reached the KV / history capacity */
+#define MK_DEV_ABORTED (-14)       /* stopped because another CTA failed */
+#define MK_DEV_BAD_INDEX (-15)     /* a token id outside the embedding table */
+
+/* ---- op ids: "mega kernel initial", the OpId table --------------------- */
+#define MK_OP_NOP 0
+#define MK_OP_MEMCPY 1            /* used as the embedding row gather */
+#define MK_OP_GEMV 2
+#define MK_OP_RMSNORM 3
+#define MK_OP_ATTENTION 4
+#define MK_OP_MLP 5
+#define MK_OP_SAMPLE 6
+#define MK_OP_ATTENTION_APPEND 7
+#define MK_OP_ATTENTION_PARTIAL 8
+#define MK_OP_ATTENTION_COMBINE 9
+
+/* ---- epilogue flags: "mega kernel initial", the flags paragraph after
+ *      the descriptor listing (bit0..bit2); bit3 is this library's ------- */
+#define MK_F_SILU_MUL 1u
+#define MK_F_ADD_RESIDUAL 2u
+#define MK_F_RMS_NORM_INPUT 4u
+#define MK_F_ARGMAX_EPI 8u        /* per-tile (max, index) pairs for SAMPLE */
+
+/* ---- buffer dtypes ------------------------------------------------------ */
+#define MK_BF16 1
+#define MK_F32 2
+#define MK_I32 3
+#define MK_PAIR 4                  /* mk_argmax_pair, 8 bytes */
+
+/* ---- execution modes for mk_decode_step_ex ------------------------------ */
+#define MK_MODE_MEGA 0            /* persistent kernel, per-task counters */
+#define MK_MODE_PER_OP 1          /* one kernel launch per op, one CTA per task */
+#define MK_MODE_PER_OP_GRAPH 2    /* MK_MODE_PER_OP captured once into a CUDA graph */
+#define MK_MODE_LEVELS 3          /* persistent kernel, barrier per topological level */
+
+#define MK_NO_BUF 0xFFFFu
+#define MK_BUF_STATE 0u           /* int32 [B, 2]: (next token, its position) */
+#define MK_BUF_ROPE_COS 1u        /* library-owned float [capacity, D/2] */
+#define MK_BUF_ROPE_SIN 2u
+
+/* The 64-byte task descriptor, field for field as "mega kernel initial"
+ * gives it (the TaskDescriptor listing): standard layout, trivially
+ * copyable, remaining_deps 4-byte aligned for atomics. */
+typedef struct mk_task_descriptor {
+  uint16_t op_id;              /*  0 */
+  uint16_t config_id;          /*  2  GEMV: 0 if m < 8 else 1; attention: 0 if D=64, 1 if D=128 */
+  uint16_t step;               /*  4  speculative draft step tag; always 0 */
+  uint16_t flags;              /*  6  MK_F_* */
+  int32_t remaining_deps;      /*  8  number of distinct parents */
+  int32_t num_dependents;      /* 12  edges leaving the task */
+  uint32_t dependents_offset;  /* 16  index into the edge array */
+  uint16_t in_buf[3];          /* 20  buffer-table indices */
+  uint16_t out_buf;            /* 26 */
+  int32_t m;                   /* 28  batch */
+  int32_t n;                   /* 32  GEMV: output columns; attention: D */
+  int32_t k;                   /* 36  GEMV: inner dim; attention: Hq; SAMPLE: tile count */
+  int32_t kv_len;              /* 40  attention / SAMPLE: cache capacity */
+  uint32_t reserved[5];        /* 44  per-op scalars (see mk_lower) */
+} mk_task_descriptor;
+
+typedef struct mk_argmax_pair {
+  float value;
+  int32_t index;
+} mk_argmax_pair;
+
+typedef struct mk_graph mk_graph;
+
+typedef struct mk_config {
+  uint32_t abi_version;      /* must be MK_ABI_VERSION */
+  int32_t num_ctas;          /* persistent CTAs; 0 = SM count of the current device */
+  int32_t tiles_target;      /* GEMV tiles per op; 0 = num_ctas */
+  int32_t col_align;         /* GEMV tile width alignment; 0 = 16 */
+  uint32_t wait_timeout_us;  /* bound on every device wait; 0 = 2,000,000 */
+} mk_config;
+
+/* Create an empty graph.  Errors: MK_ERR_ABI on a version mismatch,
+ * MK_ERR_ARG on negative sizes, MK_ERR_CUDA if num_ctas == 0 and no device
+ * can be queried.  Buffer indices 1 and 2 are reserved for the RoPE tables. */
+int mk_graph_create(const mk_config* cfg, mk_graph** out);
+
+/* Register the decode state as buffer 0: int32 [B, 2], row s = (token the
+ * next step consumes, its position).  SAMPLE tasks overwrite it each step.
+ * Must precede every other registration.  Errors: MK_ERR_ARG, MK_ERR_STATE. */
+int mk_set_state(mk_graph* g, void* state_dptr, int B);
+
+/* Append a caller-owned device tensor to the buffer table ("mega kernel
+ * initial", buffer-table part: an append-only table of device pointers
+ * indexed by uint16).  rows x cols in elements of dtype, row-major,
+ * contiguous.  *out_idx receives the index.  Errors: MK_ERR_ARG (null
+ * pointer, misalignment, bad dtype), MK_ERR_LIMIT (table full),
+ * MK_ERR_STATE (after mk_lower). */
+int mk_add_buffer(mk_graph* g, void* dptr, int dtype, int64_t rows, int64_t cols,
+                  uint16_t* out_idx);
+
+/* Embedding row gather (a MEMCPY task per sequence, our reading: the OpId
+ * table lists MEMCPY as a utility and no embedding op):
+ * out[s, :] = float(table[state[s].token, :]).  table bf16 [V, H],
+ * out f32 [B, H]. */
+int mk_add_embed(mk_graph* g, uint16_t table, uint16_t out, int B, int H);
+
+/* y = epilogue(W x) fanned out into one GEMV task per output-column tile
+ * ("mega kernel initial", lowering part: one task per column tile, roughly
+ * one per SM; RMSNorm, residual and SiLU*mul as epilogue flags).
+ *  x   f32 [m, k]                W bf16 [n, k], or [2n, k] = [gate; up] with SILU_MUL
+ *  out f32 [m, n]                aux: gamma bf16 [1, k] (RMS_NORM_INPUT) or
+ *                                     residual f32 [m, n] (ADD_RESIDUAL) or MK_NO_BUF
+ *  pairs MK_PAIR [T, m] (tile-major; T = mk_gemv_tiles(n)) with ARGMAX_EPI, else MK_NO_BUF.
+ *  RMS_NORM_INPUT: x_hat = x / sqrt(mean(x^2) + eps) * gamma.
+ *  SILU_MUL: out = silu(W_gate x) * (W_up x).  ADD_RESIDUAL: out += residual.
+ * Limits: 1 <= m <= 8; k a multiple of 256 and at most 65536.
+ * Errors: MK_ERR_ARG (shape/dtype mismatch, both RMS_NORM_INPUT and
+ * ADD_RESIDUAL, missing pairs), MK_ERR_STATE. */
+int mk_add_matmul(mk_graph* g, uint16_t x, uint16_t w, uint16_t out, uint16_t aux,
+                  uint16_t pairs, uint32_t flags, int m, int n, int k, float eps);
+
+/* Attention for one decode token per sequence, lowered to ATTENTION_APPEND
+ * per (sequence, KV head), ATTENTION_PARTIAL per (sequence, KV head, KV
+ * chunk) and ATTENTION_COMBINE per (sequence, KV head): plain flash
+ * decoding with a log-sum-exp merge ("mega kernel initial", lowering part
+ * and the OpId table; the combine is per KV head, our reading).
+ *  qkv  f32 [B, (Hq + 2 Hkv) D]: q heads, then k heads, then v heads.
+ *  kcache / vcache bf16 [B * Hkv, capacity * D] (= [B, Hkv, capacity, D]).
+ *  out  f32 [B, Hq D].     scratch f32 [mk_attention_scratch_rows, G (D + 2)].
+ *  len0[B]: cached keys per sequence when the graph is built (fixes the chunk
+ *  count).  chunk: keys per chunk, 0 = automatic.  D in {64, 128}; Hq/Hkv <= 4.
+ * APPEND applies rotate-half RoPE (base rope_theta) to k at position pos and
+ * stores bf16 k, v at row pos; PARTIAL applies RoPE to q and runs an online
+ * softmax (scale 1/sqrt(D)) over its chunk of the pos + 1 keys. */
+int mk_add_attention(mk_graph* g, uint16_t qkv, uint16_t kcache, uint16_t vcache,
+                     uint16_t out, uint16_t scratch, int B, int Hq, int Hkv, int D,
+                     int capacity, const int32_t* len0, int chunk, double rope_theta);
+
+/* SAMPLE per sequence: token = argmax over the lm_head tiles' pairs (first
+ * index on ties); history[s, pos + 1] = token; state[s] = (token, pos + 1).
+ * pairs MK_PAIR [T, B] (tile-major), history int32 [B, capacity]. */
+int mk_add_sample(mk_graph* g, uint16_t pairs, uint16_t history, int B, int V, int capacity);
+
+/* Rows the scratch buffer of mk_add_attention needs (its columns are
+ * G * (D + 2) floats). */
+int mk_attention_scratch_rows(const mk_graph* g, int B, int Hkv, const int32_t* len0,
+                              int chunk, int64_t* rows);
+
+/* Number of column tiles an n-column GEMV fans out into. */
+int mk_gemv_tiles(const mk_graph* g, int n, int32_t* tiles);
+
+/* Lower every op to descriptors and edges and build the per-CTA queues;
+ * freezes the graph.  Descriptor fields by op (unused in_buf = MK_NO_BUF,
+ * unused fields 0):
+ *  GEMV     in={x,W,aux} out=y m=B n k; reserved={col_begin, col_count,
+ *           float bits of eps (RMS_NORM_INPUT) or 0, pairs idx or 0,
+ *           tile index (ARGMAX_EPI) or 0}
+ *  APPEND   in={qkv,K,V} out=K m=B n=D k=Hq kv_len=capacity reserved={s,g,Hkv,0,0}
+ *  PARTIAL  in={qkv,K,V} out=scratch, same m/n/k/kv_len,
+ *           reserved={s,g,Hkv, c | (P_s << 16), first slot of (s,g)}
+ *  COMBINE  in={scratch} out=att, same m/n/k/kv_len, reserved={s,g,Hkv,P_s,first slot}
+ *  MEMCPY   in={table} out=h m=B n=H reserved={s, rows of the table}
+ *  SAMPLE   in={pairs} out=history m=B n=V k=T kv_len=capacity reserved={s}
+ * Errors: MK_ERR_STATE (already lowered or no ops). */
+int mk_lower(mk_graph* g);
+
+/* Lowered descriptors (mk_task_descriptor[count]) and edges (uint32[count]);
+ * the memory belongs to the graph and lives until mk_destroy. */
+int mk_get_tasks(const mk_graph* g, const void** bytes, size_t* nbytes);
+int mk_get_edges(const mk_graph* g, const uint32_t** edges, size_t* count);
+
+/* Test hook for fault-detection tests: overwrite descriptor `task` of a
+ * lowered, not yet uploaded graph (e.g. a dependency count one too high, or
+ * an unknown op_id).  The device then reports MK_DEV_DEP_TIMEOUT or
+ * MK_DEV_BAD_OP through mk_status instead of hanging or faulting.
+ * Errors: MK_ERR_STATE (not lowered, or already uploaded), MK_ERR_ARG. */
+int mk_debug_patch_task(mk_graph* g, int task, const mk_task_descriptor* d);
+
+/* Per-CTA task queues: offsets int32[num_ctas + 1] into tasks int32[]. */
+int mk_get_queues(const mk_graph* g, const int32_t** offsets, const int32_t** tasks,
+                  int* num_ctas);
+
+/* Copy descriptors, edges, queues and the buffer pointer table to the
+ * current device, build the RoPE tables (float64 on the host, stored as
+ * float), and zero the dependency counters.  Synchronises `stream`.
+ * Errors: MK_ERR_STATE (not lowered), MK_ERR_CUDA, MK_ERR_NOMEM. */
+int mk_upload(mk_graph* g, void* stream);
+
+/* One decode step with the persistent kernel (MK_MODE_MEGA). */
+int mk_decode_step(mk_graph* g, void* stream);
+
+/* One decode step in `mode` (MK_MODE_*).  trace != 0 records, per task, the
+ * CTA, SM and %globaltimer stamps (wait begin, start, end) readable with
+ * mk_get_trace after the stream synchronises.  MK_MODE_PER_OP_GRAPH
+ * captures the per-op launches into a CUDA graph on first use. */
+int mk_decode_step_ex(mk_graph* g, void* stream, int mode, uint32_t trace);
+
+/* One MK_MODE_MEGA step driven from host memory: copies state_in (int32
+ * [B, 2], pinned host memory recommended; NULL = keep the device state)
+ * to the state buffer, runs the step, and copies the sampled tokens
+ * (int32 [B]) to tokens_out, all enqueued on `stream`; the caller
+ * synchronises before reading tokens_out. */
+int mk_decode_step_host(mk_graph* g, void* stream, const int32_t* state_in,
+                        int32_t* tokens_out);
+
+/* Synchronise `stream`, then read and clear the device status word:
+ * *dev_code = MK_DEV_* and *task_id = the failing task (or -1). */
+int mk_status(mk_graph* g, void* stream, int* dev_code, int32_t* task_id);
+
+/* Trace records of the last traced step: uint64[count * 4] as
+ * (cta << 32 | smid, t_wait_begin_ns, t_start_ns, t_end_ns) per task. */
+int mk_get_trace(mk_graph* g, const uint64_t** records, size_t* count);
+
+/* Bytes of shared memory the kernel uses per CTA and its thread count. */
+int mk_kernel_info(const mk_graph* g, int* smem_bytes, int* threads, int* stages);
+
+/* Release everything the library allocated.  Safe on NULL. */
+void mk_destroy(mk_graph* g);
+
+/* Message for the calling thread's last error ("" if none). */
+const char* mk_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MK_H */

@@ -83,7 +83,7 @@ def llama_decode_spec(model, B: int, len0, cap: int, chunk: int, num_ctas: int,
         h = matmul(gu, idx[f"layer{l}.wd"], m.H, m.F, aux=h1, flags=F_ADD_RESIDUAL)
     T = len(tiles(m.V, tt, col_align))
     logits = fresh(F32, B, m.V)
-    pairs = fresh(PAIR, B, T)
+    pairs = fresh(PAIR, T, B)
     matmul(h, lm, m.V, m.H, aux=idx["final_norm"], flags=F_RMS_NORM_INPUT | F_ARGMAX_EPI,
            eps=m.eps, pairs=pairs, out=logits)
     ops.append(dict(kind="sample", pairs=pairs, history=hist, B=B, V=m.V, capacity=cap))

@@ -23,8 +23,11 @@ Source: "mega kernel initial" (1y33.com).
 Readings taken where the page is silent (the same frozen spec the library
 implements): the tile rule col_tile = round_up(ceil(n / tiles_target),
 col_align); one COMBINE per (sequence, KV head); the split-KV chunk rule in
-``partials_per_sequence``; bit3 ARGMAX_EPI on the lm_head GEMV; the embedding
-row gather as a MEMCPY task; field maps per op as in ``_desc_*`` below.
+``partials_per_sequence``; bit3 ARGMAX_EPI on the lm_head GEMV, whose tiles
+carry their tile index in reserved[4] (the pair column they write); the embedding
+row gather as a MEMCPY task carrying the table's row count in reserved[1];
+the per-tile (max, index) pairs stored tile-major ([T, B]); field maps per
+op as in ``lower`` below.
 Access ranges are tracked as row x column rectangles of each buffer's 2-D
 view, so per-sequence writes (embedding, combine) do not alias.
 """
@@ -130,7 +133,8 @@ def lower(spec: dict):
             B, H = op["B"], op["H"]
             for s in range(B):
                 emit(dict(op_id=OP_MEMCPY, in_buf=(op["table"], NO_BUF, NO_BUF),
-                          out_buf=op["out"], m=B, n=H, reserved=(s, 0, 0, 0, 0)),
+                          out_buf=op["out"], m=B, n=H,
+                          reserved=(s, bufs[op["table"]][1], 0, 0, 0)),
                      reads=[(BUF_STATE, s, s + 1, 0, 2)],
                      writes=[(op["out"], s, s + 1, 0, H)])
         elif kind == "matmul":
@@ -144,12 +148,13 @@ def lower(spec: dict):
                     reads.append((aux, 0, B, c0, c0 + cn))
                 writes = [(op["out"], 0, B, c0, c0 + cn)]
                 if fl & F_ARGMAX_EPI:
-                    writes.append((pairs, 0, B, t, t + 1))
+                    writes.append((pairs, t, t + 1, 0, B))
                 emit(dict(op_id=OP_GEMV, config_id=0 if B < 8 else 1, flags=fl,
                           in_buf=(op["x"], op["w"], aux), out_buf=op["out"],
                           m=B, n=n, k=K,
                           reserved=(c0, cn, eps_bits,
-                                    pairs if fl & F_ARGMAX_EPI else 0, 0)),
+                                    pairs if fl & F_ARGMAX_EPI else 0,
+                                    t if fl & F_ARGMAX_EPI else 0)),
                      reads, writes)
         elif kind == "attention":
             B, Hq, Hkv, D, cap = op["B"], op["Hq"], op["Hkv"], op["D"], op["capacity"]
@@ -203,7 +208,7 @@ def lower(spec: dict):
                 emit(dict(op_id=OP_SAMPLE, in_buf=(op["pairs"], NO_BUF, NO_BUF),
                           out_buf=op["history"], m=B, n=V, k=T, kv_len=cap,
                           reserved=(s, 0, 0, 0, 0)),
-                     reads=[(op["pairs"], s, s + 1, 0, T), (BUF_STATE, s, s + 1, 0, 2)],
+                     reads=[(op["pairs"], 0, T, s, s + 1), (BUF_STATE, s, s + 1, 0, 2)],
                      writes=[(op["history"], s, s + 1, 0, cap),
                              (BUF_STATE, s, s + 1, 0, 2)])
         else:

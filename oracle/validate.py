@@ -53,8 +53,8 @@ def task_accesses(d) -> tuple:
             R.append((ib[2], 0, m, c0, c0 + cn))
         Wr.append((ob, 0, m, c0, c0 + cn))
         if int(d["flags"]) & F_ARGMAX_EPI:
-            # the tile index is the tile's position among equal-width tiles
-            Wr.append((rs[3], 0, m, -1, -1))     # resolved below
+            # the tile writes its (max, index) pairs into column reserved[4]
+            Wr.append((rs[3], rs[4], rs[4] + 1, 0, m))
     elif op in (OP_ATT_APPEND, OP_ATT_PARTIAL, OP_ATT_COMBINE):
         s, g, Hkv = rs[0], rs[1], rs[2]
         D, Hq, cap = n, k, kv
@@ -79,30 +79,11 @@ def task_accesses(d) -> tuple:
             Wr.append((ob, s, s + 1, g * G * D, (g + 1) * G * D))
     elif op == OP_SAMPLE:
         s = rs[0]
-        R += [(ib[0], s, s + 1, 0, k), (BUF_STATE, s, s + 1, 0, 2)]
+        R += [(ib[0], 0, k, s, s + 1), (BUF_STATE, s, s + 1, 0, 2)]
         Wr += [(ob, s, s + 1, 0, kv), (BUF_STATE, s, s + 1, 0, 2)]
     else:
         raise ValidationError(f"unknown op_id {op}")
     return R, Wr
-
-
-def _resolve_pairs_columns(tasks, acc):
-    """ARGMAX_EPI tiles write column t of the pairs buffer, t being the tile's
-    rank among the tiles of its op (consecutive GEMV tasks with one out_buf)."""
-    rank = {}
-    prev = None
-    for t in range(len(tasks)):
-        d = tasks[t]
-        if int(d["op_id"]) == OP_GEMV and int(d["flags"]) & F_ARGMAX_EPI:
-            key = (int(d["out_buf"]), int(d["reserved"][3]))
-            rank[t] = rank[prev] + 1 if prev is not None and prev_key == key else 0
-            prev, prev_key = t, key
-        else:
-            prev = None
-    for t, r in rank.items():
-        R, W = acc[t]
-        acc[t] = (R, [(b, r0, r1, r if c0 == -1 else c0, r + 1 if c1 == -1 else c1)
-                      for (b, r0, r1, c0, c1) in W])
 
 
 def _covered(intervals, c0, c1) -> bool:
@@ -146,7 +127,6 @@ def validate(tasks: np.ndarray, edges: np.ndarray, check_hazards: bool = True) -
         if parents[t]:
             level[t] = 1 + max(level[p] for p in parents[t])
     acc = [task_accesses(tasks[t]) for t in range(N)]
-    _resolve_pairs_columns(tasks, acc)
 
     # read coverage
     writes_by_buf = defaultdict(list)

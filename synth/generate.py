@@ -203,8 +203,9 @@ def normal_bf16_torch(name: str, shape, mu: float, sigma: float, seed: int = 0,
     if out is None:
         out = torch.empty(n, dtype=torch.bfloat16, device=device)
     flat = out.view(-1)
-    for s in range(0, n, _CHUNK * 4):
-        e = min(n, s + _CHUNK * 4)
+    step = _CHUNK * (64 if str(device).startswith("cuda") else 4)
+    for s in range(0, n, step):
+        e = min(n, s + step)
         idx = torch.arange(s, e, dtype=torch.int64, device=device)
         flat[s:e] = _normal_chunk_t(idx, k1, k2, mu, sigma, table)
     return out.view(*shape)

@@ -1,0 +1,580 @@
+// Host side of libmk: graph building, lowering to task descriptors and the
+// dependents edge array, per-CTA static queues and topological levels.
+//
+// Lowering follows "mega kernel initial" (1y33.com):
+//  * lowering part: each op becomes one or more 64-byte descriptors; a matmul
+//    fans out into one GEMV task per output-column tile (about one per SM;
+//    3072 columns over 8 tiles -> 8 tasks of 384); attention becomes
+//    ATTENTION_PARTIAL tasks per (sequence, KV-head group, KV chunk) plus a
+//    combine; norm, residual and SiLU*mul are GEMV flags;
+//  * every output remembers which task wrote which column range, and a
+//    reader's parents are the writers of what it reads; parents are flipped
+//    into dependents lists flattened into one edge array; tasks come out in
+//    topological order (the edge-array part);
+//  * levels: level = 1 + max parent level (the levels part), kept for the
+//    level-synchronous ablation mode.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+#include <limits>
+#include <numeric>
+#include <string>
+#include <vector>
+
+#include "graph.h"
+
+namespace mk {
+
+static thread_local std::string g_last_error;
+
+void set_error(const std::string& msg) { g_last_error = msg; }
+int fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+
+static inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int tile_width(int n, int tiles_target, int col_align) {
+  return (int)(cdiv(cdiv(n, tiles_target), col_align) * col_align);
+}
+
+int tile_count(int n, int tiles_target, int col_align) {
+  return (int)cdiv(n, tile_width(n, tiles_target, col_align));
+}
+
+// Split-KV chunk count per sequence, fixed at lowering time.  chunk > 0:
+// ceil(len0 / chunk).  chunk == 0: chunks of about
+// E = max(256, ceil(Hkv * sum(len0) / num_ctas)) keys, so that the partials
+// of a ragged batch carry similar bytes and number about one per SM.
+std::vector<int> partials_per_sequence(const std::vector<int32_t>& len0, int Hkv, int chunk,
+                                       int num_ctas) {
+  std::vector<int> P(len0.size());
+  if (chunk > 0) {
+    for (size_t s = 0; s < len0.size(); ++s) P[s] = (int)std::max<int64_t>(1, cdiv(len0[s], chunk));
+    return P;
+  }
+  int64_t tot = 0;
+  for (int32_t l : len0) tot += l;
+  int64_t E = std::max<int64_t>(256, cdiv((int64_t)Hkv * tot, num_ctas));
+  for (size_t s = 0; s < len0.size(); ++s) P[s] = (int)std::max<int64_t>(1, cdiv(len0[s], E));
+  return P;
+}
+
+}  // namespace mk
+
+using namespace mk;
+
+extern "C" const char* mk_last_error(void) { return g_last_error.c_str(); }
+
+extern "C" int mk_graph_create(const mk_config* cfg, mk_graph** out) {
+  if (!cfg || !out) return fail(MK_ERR_ARG, "mk_graph_create: null argument");
+  *out = nullptr;
+  if (cfg->abi_version != MK_ABI_VERSION)
+    return fail(MK_ERR_ABI, "mk_graph_create: abi_version " + std::to_string(cfg->abi_version) +
+                                " != " + std::to_string(MK_ABI_VERSION));
+  if (cfg->num_ctas < 0 || cfg->tiles_target < 0 || cfg->col_align < 0)
+    return fail(MK_ERR_ARG, "mk_graph_create: negative size");
+  int ctas = cfg->num_ctas;
+  if (ctas == 0) {
+    int rc = query_sm_count(&ctas);
+    if (rc != MK_OK) return rc;
+  }
+  auto* g = new (std::nothrow) mk_graph();
+  if (!g) return fail(MK_ERR_NOMEM, "mk_graph_create: out of memory");
+  g->cfg = *cfg;
+  g->num_ctas = ctas;
+  g->tiles_target = cfg->tiles_target ? cfg->tiles_target : ctas;
+  g->col_align = cfg->col_align ? cfg->col_align : 16;
+  g->timeout_us = cfg->wait_timeout_us ? cfg->wait_timeout_us : 2000000u;
+  g->bufs.resize(3);  // 0 state (set later), 1/2 RoPE tables (built at upload)
+  *out = g;
+  return MK_OK;
+}
+
+extern "C" int mk_set_state(mk_graph* g, void* state_dptr, int B) {
+  if (!g) return fail(MK_ERR_ARG, "mk_set_state: null graph");
+  if (g->lowered) return fail(MK_ERR_STATE, "mk_set_state: graph already lowered");
+  if (g->state_set) return fail(MK_ERR_STATE, "mk_set_state: state already set");
+  if (!state_dptr || B < 1 || B > 8) return fail(MK_ERR_ARG, "mk_set_state: need a pointer and 1 <= B <= 8");
+  if (((uintptr_t)state_dptr) % 16) return fail(MK_ERR_ARG, "mk_set_state: pointer not 16-byte aligned");
+  g->bufs[0] = BufferRec{state_dptr, MK_I32, B, 2};
+  g->B = B;
+  g->state_set = true;
+  return MK_OK;
+}
+
+extern "C" int mk_add_buffer(mk_graph* g, void* dptr, int dtype, int64_t rows, int64_t cols,
+                             uint16_t* out_idx) {
+  if (!g || !out_idx) return fail(MK_ERR_ARG, "mk_add_buffer: null argument");
+  if (g->lowered) return fail(MK_ERR_STATE, "mk_add_buffer: graph already lowered");
+  if (!g->state_set) return fail(MK_ERR_STATE, "mk_add_buffer: call mk_set_state first");
+  if (!dptr) return fail(MK_ERR_ARG, "mk_add_buffer: null device pointer");
+  if (((uintptr_t)dptr) % 16) return fail(MK_ERR_ARG, "mk_add_buffer: pointer not 16-byte aligned");
+  if (dtype < MK_BF16 || dtype > MK_PAIR) return fail(MK_ERR_ARG, "mk_add_buffer: bad dtype");
+  if (rows <= 0 || cols <= 0) return fail(MK_ERR_ARG, "mk_add_buffer: rows and cols must be positive");
+  if (g->bufs.size() >= 0xFFFF) return fail(MK_ERR_LIMIT, "mk_add_buffer: buffer table full (65535)");
+  g->bufs.push_back(BufferRec{dptr, dtype, rows, cols});
+  *out_idx = (uint16_t)(g->bufs.size() - 1);
+  return MK_OK;
+}
+
+static int check_buf(const mk_graph* g, uint16_t idx, int dtype, int64_t rows, int64_t cols,
+                     const char* what) {
+  if (idx >= g->bufs.size() || idx < 3)
+    return fail(MK_ERR_ARG, std::string(what) + ": bad buffer index " + std::to_string(idx));
+  const BufferRec& b = g->bufs[idx];
+  if (b.dtype != dtype)
+    return fail(MK_ERR_ARG, std::string(what) + ": buffer " + std::to_string(idx) + " has wrong dtype");
+  if ((rows >= 0 && b.rows != rows) || (cols >= 0 && b.cols != cols))
+    return fail(MK_ERR_ARG, std::string(what) + ": buffer " + std::to_string(idx) + " is [" +
+                                std::to_string(b.rows) + ", " + std::to_string(b.cols) + "], expected [" +
+                                std::to_string(rows) + ", " + std::to_string(cols) + "]");
+  return MK_OK;
+}
+
+#define CHECK(x)            \
+  do {                      \
+    int rc__ = (x);         \
+    if (rc__) return rc__;  \
+  } while (0)
+
+static int add_common(mk_graph* g, const char* what) {
+  if (!g) return fail(MK_ERR_ARG, std::string(what) + ": null graph");
+  if (g->lowered) return fail(MK_ERR_STATE, std::string(what) + ": graph already lowered");
+  if (!g->state_set) return fail(MK_ERR_STATE, std::string(what) + ": call mk_set_state first");
+  return MK_OK;
+}
+
+extern "C" int mk_add_embed(mk_graph* g, uint16_t table, uint16_t out, int B, int H) {
+  CHECK(add_common(g, "mk_add_embed"));
+  if (B != g->B || H <= 0 || H % 8) return fail(MK_ERR_ARG, "mk_add_embed: B must equal the state's B, H a multiple of 8");
+  CHECK(check_buf(g, table, MK_BF16, -1, H, "mk_add_embed table"));
+  CHECK(check_buf(g, out, MK_F32, B, H, "mk_add_embed out"));
+  OpRec op{K_EMBED};
+  op.a[0] = table;
+  op.a[1] = out;
+  op.B = B;
+  op.H = H;
+  g->ops.push_back(op);
+  return MK_OK;
+}
+
+extern "C" int mk_add_matmul(mk_graph* g, uint16_t x, uint16_t w, uint16_t out, uint16_t aux,
+                             uint16_t pairs, uint32_t flags, int m, int n, int k, float eps) {
+  CHECK(add_common(g, "mk_add_matmul"));
+  if (flags & ~(MK_F_SILU_MUL | MK_F_ADD_RESIDUAL | MK_F_RMS_NORM_INPUT | MK_F_ARGMAX_EPI))
+    return fail(MK_ERR_ARG, "mk_add_matmul: unknown flag bits");
+  if ((flags & MK_F_RMS_NORM_INPUT) && (flags & MK_F_ADD_RESIDUAL))
+    return fail(MK_ERR_ARG, "mk_add_matmul: RMS_NORM_INPUT and ADD_RESIDUAL share the aux slot");
+  if (m < 1 || m > 8 || m != g->B) return fail(MK_ERR_ARG, "mk_add_matmul: need 1 <= m <= 8 and m == B");
+  if (n < 1) return fail(MK_ERR_ARG, "mk_add_matmul: n must be positive");
+  if (k < 256 || k % 256 || k > 65536) return fail(MK_ERR_ARG, "mk_add_matmul: k must be a multiple of 256 in [256, 65536]");
+  if (!std::isfinite(eps) || eps < 0.f) return fail(MK_ERR_ARG, "mk_add_matmul: eps must be finite and >= 0");
+  CHECK(check_buf(g, x, MK_F32, m, k, "mk_add_matmul x"));
+  CHECK(check_buf(g, w, MK_BF16, (flags & MK_F_SILU_MUL) ? 2 * (int64_t)n : n, k, "mk_add_matmul W"));
+  CHECK(check_buf(g, out, MK_F32, m, n, "mk_add_matmul out"));
+  if (flags & MK_F_RMS_NORM_INPUT) {
+    CHECK(check_buf(g, aux, MK_BF16, 1, k, "mk_add_matmul gamma"));
+  } else if (flags & MK_F_ADD_RESIDUAL) {
+    CHECK(check_buf(g, aux, MK_F32, m, n, "mk_add_matmul residual"));
+    if (aux == out) return fail(MK_ERR_ARG, "mk_add_matmul: residual must not alias the output");
+  } else if (aux != MK_NO_BUF) {
+    return fail(MK_ERR_ARG, "mk_add_matmul: aux given without RMS_NORM_INPUT or ADD_RESIDUAL");
+  }
+  if (flags & MK_F_ARGMAX_EPI) {
+    CHECK(check_buf(g, pairs, MK_PAIR, tile_count(n, g->tiles_target, g->col_align), m,
+                    "mk_add_matmul pairs"));
+    if (flags & MK_F_SILU_MUL) return fail(MK_ERR_ARG, "mk_add_matmul: ARGMAX_EPI with SILU_MUL is not supported");
+  } else if (pairs != MK_NO_BUF) {
+    return fail(MK_ERR_ARG, "mk_add_matmul: pairs given without ARGMAX_EPI");
+  }
+  if (x == out) return fail(MK_ERR_ARG, "mk_add_matmul: x must not alias the output");
+  OpRec op{K_MATMUL};
+  op.a[0] = x; op.a[1] = w; op.a[2] = out; op.a[3] = aux; op.a[4] = pairs;
+  op.B = m; op.n = n; op.k = k; op.flags = flags; op.eps = eps;
+  g->ops.push_back(op);
+  if (m > g->max_m) g->max_m = m;
+  return MK_OK;
+}
+
+extern "C" int mk_attention_scratch_rows(const mk_graph* g, int B, int Hkv, const int32_t* len0,
+                                         int chunk, int64_t* rows) {
+  if (!g || !len0 || !rows || B < 1 || Hkv < 1 || chunk < 0)
+    return fail(MK_ERR_ARG, "mk_attention_scratch_rows: bad argument");
+  std::vector<int32_t> l(len0, len0 + B);
+  auto P = partials_per_sequence(l, Hkv, chunk, g->num_ctas);
+  int64_t r = 0;
+  for (int p : P) r += (int64_t)p * Hkv;
+  *rows = r;
+  return MK_OK;
+}
+
+extern "C" int mk_gemv_tiles(const mk_graph* g, int n, int32_t* tiles) {
+  if (!g || !tiles || n < 1) return fail(MK_ERR_ARG, "mk_gemv_tiles: bad argument");
+  *tiles = tile_count(n, g->tiles_target, g->col_align);
+  return MK_OK;
+}
+
+extern "C" int mk_add_attention(mk_graph* g, uint16_t qkv, uint16_t kcache, uint16_t vcache,
+                                uint16_t out, uint16_t scratch, int B, int Hq, int Hkv, int D,
+                                int capacity, const int32_t* len0, int chunk, double rope_theta) {
+  CHECK(add_common(g, "mk_add_attention"));
+  if (B != g->B) return fail(MK_ERR_ARG, "mk_add_attention: B must equal the state's B");
+  if (D != 64 && D != 128) return fail(MK_ERR_ARG, "mk_add_attention: D must be 64 or 128");
+  if (Hkv < 1 || Hq < Hkv || Hq % Hkv || Hq / Hkv > 4)
+    return fail(MK_ERR_ARG, "mk_add_attention: need Hq a multiple of Hkv with Hq/Hkv <= 4");
+  if (capacity < 2 || capacity > (1 << 24)) return fail(MK_ERR_ARG, "mk_add_attention: bad capacity");
+  if (!len0) return fail(MK_ERR_ARG, "mk_add_attention: null len0");
+  if (chunk < 0) return fail(MK_ERR_ARG, "mk_add_attention: negative chunk");
+  if (!(rope_theta > 0.0) || !std::isfinite(rope_theta)) return fail(MK_ERR_ARG, "mk_add_attention: bad rope_theta");
+  for (int s = 0; s < B; ++s)
+    if (len0[s] < 0 || len0[s] >= capacity) return fail(MK_ERR_ARG, "mk_add_attention: len0 out of [0, capacity)");
+  if (g->rope_D && (g->rope_D != D || g->rope_theta != rope_theta || g->rope_cap != capacity))
+    return fail(MK_ERR_ARG, "mk_add_attention: every attention op must share D, rope_theta and capacity");
+  const int G = Hq / Hkv;
+  CHECK(check_buf(g, qkv, MK_F32, B, (int64_t)(Hq + 2 * Hkv) * D, "mk_add_attention qkv"));
+  CHECK(check_buf(g, kcache, MK_BF16, (int64_t)B * Hkv, (int64_t)capacity * D, "mk_add_attention kcache"));
+  CHECK(check_buf(g, vcache, MK_BF16, (int64_t)B * Hkv, (int64_t)capacity * D, "mk_add_attention vcache"));
+  CHECK(check_buf(g, out, MK_F32, B, (int64_t)Hq * D, "mk_add_attention out"));
+  int64_t need = 0;
+  CHECK(mk_attention_scratch_rows(g, B, Hkv, len0, chunk, &need));
+  CHECK(check_buf(g, scratch, MK_F32, -1, (int64_t)G * (D + 2), "mk_add_attention scratch"));
+  if (g->bufs[scratch].rows < need)
+    return fail(MK_ERR_ARG, "mk_add_attention: scratch needs " + std::to_string(need) + " rows");
+  if (kcache == vcache) return fail(MK_ERR_ARG, "mk_add_attention: kcache and vcache must differ");
+  OpRec op{K_ATTENTION};
+  op.a[0] = qkv; op.a[1] = kcache; op.a[2] = vcache; op.a[3] = out; op.a[4] = scratch;
+  op.B = B; op.Hq = Hq; op.Hkv = Hkv; op.D = D; op.cap = capacity; op.chunk = chunk;
+  op.len0.assign(len0, len0 + B);
+  g->ops.push_back(op);
+  g->rope_D = D;
+  g->rope_theta = rope_theta;
+  g->rope_cap = capacity;
+  return MK_OK;
+}
+
+extern "C" int mk_add_sample(mk_graph* g, uint16_t pairs, uint16_t history, int B, int V, int capacity) {
+  CHECK(add_common(g, "mk_add_sample"));
+  if (B != g->B || V < 1 || capacity < 2) return fail(MK_ERR_ARG, "mk_add_sample: bad B, V or capacity");
+  CHECK(check_buf(g, pairs, MK_PAIR, tile_count(V, g->tiles_target, g->col_align), B, "mk_add_sample pairs"));
+  CHECK(check_buf(g, history, MK_I32, B, capacity, "mk_add_sample history"));
+  OpRec op{K_SAMPLE};
+  op.a[0] = pairs; op.a[1] = history;
+  op.B = B; op.V = V; op.cap = capacity;
+  g->ops.push_back(op);
+  return MK_OK;
+}
+
+// ------------------------------------------------------------------ lowering
+namespace {
+
+struct Rect {
+  int buf;
+  int64_t r0, r1, c0, c1;
+};
+
+struct Writer {
+  int task;
+  int64_t r0, r1, c0, c1;
+};
+
+struct Lowerer {
+  mk_graph* g;
+  std::vector<std::vector<Writer>> writes;  // per buffer
+  std::vector<std::vector<int>> parents;
+  std::vector<double> cost;                  // bytes-equivalent estimate per task
+
+  explicit Lowerer(mk_graph* gr) : g(gr), writes(gr->bufs.size()) {}
+
+  int emit(const mk_task_descriptor& d, const std::vector<Rect>& reads, const std::vector<Rect>& wr,
+           double c) {
+    int t = (int)g->tasks.size();
+    std::vector<int> ps;
+    for (const Rect& r : reads)
+      for (const Writer& w : writes[r.buf])
+        if (w.r0 < r.r1 && r.r0 < w.r1 && w.c0 < r.c1 && r.c0 < w.c1) ps.push_back(w.task);
+    std::sort(ps.begin(), ps.end());
+    ps.erase(std::unique(ps.begin(), ps.end()), ps.end());
+    for (const Rect& r : wr) writes[r.buf].push_back(Writer{t, r.r0, r.r1, r.c0, r.c1});
+    g->tasks.push_back(d);
+    parents.push_back(std::move(ps));
+    cost.push_back(c);
+    return t;
+  }
+};
+
+mk_task_descriptor blank(uint16_t op) {
+  mk_task_descriptor d;
+  std::memset(&d, 0, sizeof(d));
+  d.op_id = op;
+  d.in_buf[0] = d.in_buf[1] = d.in_buf[2] = MK_NO_BUF;
+  d.out_buf = MK_NO_BUF;
+  return d;
+}
+
+uint32_t f32_bits(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  return u;
+}
+
+constexpr double kTaskOverhead = 32768.0;  // fixed cost per task, in bytes of streaming
+constexpr double kSyncLatency = 32768.0;   // cross-CTA dependency latency, same units
+
+}  // namespace
+
+extern "C" int mk_lower(mk_graph* g) {
+  if (!g) return fail(MK_ERR_ARG, "mk_lower: null graph");
+  if (g->lowered) return fail(MK_ERR_STATE, "mk_lower: already lowered");
+  if (g->ops.empty()) return fail(MK_ERR_STATE, "mk_lower: no ops");
+  Lowerer L(g);
+  const int tt = g->tiles_target, al = g->col_align;
+  g->group_off.clear();
+  for (const OpRec& op : g->ops) {
+    switch (op.kind) {
+      case K_EMBED: {
+        g->group_off.push_back((int)g->tasks.size());
+        for (int s = 0; s < op.B; ++s) {
+          mk_task_descriptor d = blank(MK_OP_MEMCPY);
+          d.in_buf[0] = op.a[0];
+          d.out_buf = op.a[1];
+          d.m = op.B;
+          d.n = op.H;
+          d.reserved[0] = s;
+          d.reserved[1] = (uint32_t)g->bufs[op.a[0]].rows;
+          L.emit(d, {{(int)MK_BUF_STATE, s, s + 1, 0, 2}}, {{op.a[1], s, s + 1, 0, op.H}},
+                 kTaskOverhead);
+        }
+        break;
+      }
+      case K_MATMUL: {
+        g->group_off.push_back((int)g->tasks.size());
+        const int w = tile_width(op.n, tt, al);
+        int t = 0;
+        for (int c0 = 0; c0 < op.n; c0 += w, ++t) {
+          const int cn = std::min(w, op.n - c0);
+          mk_task_descriptor d = blank(MK_OP_GEMV);
+          d.config_id = op.B < 8 ? 0 : 1;
+          d.flags = (uint16_t)op.flags;
+          d.in_buf[0] = op.a[0];
+          d.in_buf[1] = op.a[1];
+          d.in_buf[2] = op.a[3];
+          d.out_buf = op.a[2];
+          d.m = op.B;
+          d.n = op.n;
+          d.k = op.k;
+          d.reserved[0] = c0;
+          d.reserved[1] = cn;
+          d.reserved[2] = (op.flags & MK_F_RMS_NORM_INPUT) ? f32_bits(op.eps) : 0u;
+          d.reserved[3] = (op.flags & MK_F_ARGMAX_EPI) ? op.a[4] : 0u;
+          d.reserved[4] = (op.flags & MK_F_ARGMAX_EPI) ? (uint32_t)t : 0u;
+          std::vector<Rect> rd{{op.a[0], 0, op.B, 0, op.k}};
+          if (op.flags & MK_F_ADD_RESIDUAL) rd.push_back({op.a[3], 0, op.B, c0, c0 + cn});
+          std::vector<Rect> wr{{op.a[2], 0, op.B, c0, c0 + cn}};
+          if (op.flags & MK_F_ARGMAX_EPI) wr.push_back({op.a[4], t, t + 1, 0, op.B});
+          double rows = (op.flags & MK_F_SILU_MUL) ? 2.0 * cn : cn;
+          L.emit(d, rd, wr, rows * op.k * 2.0 + kTaskOverhead);
+        }
+        break;
+      }
+      case K_ATTENTION: {
+        const int B = op.B, Hq = op.Hq, Hkv = op.Hkv, D = op.D, cap = op.cap, G = Hq / Hkv;
+        const uint16_t cfg = D == 64 ? 0 : 1;
+        const uint16_t qkv = op.a[0], kc = op.a[1], vc = op.a[2], out = op.a[3], scr = op.a[4];
+        auto P = partials_per_sequence(op.len0, Hkv, op.chunk, g->num_ctas);
+        std::vector<int> base(B * Hkv);
+        int acc = 0;
+        for (int s = 0; s < B; ++s) {
+          for (int gg = 0; gg < Hkv; ++gg) base[s * Hkv + gg] = acc + gg * P[s];
+          acc += Hkv * P[s];
+        }
+        auto common = [&](mk_task_descriptor& d) {
+          d.config_id = cfg;
+          d.m = B;
+          d.n = D;
+          d.k = Hq;
+          d.kv_len = cap;
+        };
+        const int64_t cacheCols = (int64_t)cap * D;
+        g->group_off.push_back((int)g->tasks.size());
+        for (int s = 0; s < B; ++s)
+          for (int gg = 0; gg < Hkv; ++gg) {
+            mk_task_descriptor d = blank(MK_OP_ATTENTION_APPEND);
+            common(d);
+            d.in_buf[0] = qkv; d.in_buf[1] = kc; d.in_buf[2] = vc;
+            d.out_buf = kc;
+            d.reserved[0] = s; d.reserved[1] = gg; d.reserved[2] = Hkv;
+            const int64_t kcol = (int64_t)Hq * D + gg * D, vcol = (int64_t)(Hq + Hkv) * D + gg * D;
+            const int64_t row = (int64_t)s * Hkv + gg;
+            L.emit(d,
+                   {{qkv, s, s + 1, kcol, kcol + D}, {qkv, s, s + 1, vcol, vcol + D},
+                    {(int)MK_BUF_STATE, s, s + 1, 0, 2}},
+                   {{kc, row, row + 1, 0, cacheCols}, {vc, row, row + 1, 0, cacheCols}}, kTaskOverhead);
+          }
+        g->group_off.push_back((int)g->tasks.size());
+        for (int s = 0; s < B; ++s)
+          for (int gg = 0; gg < Hkv; ++gg) {
+            const int64_t row = (int64_t)s * Hkv + gg;
+            const double keys = std::ceil((op.len0[s] + 1.0) / P[s]);
+            for (int c = 0; c < P[s]; ++c) {
+              mk_task_descriptor d = blank(MK_OP_ATTENTION_PARTIAL);
+              common(d);
+              d.in_buf[0] = qkv; d.in_buf[1] = kc; d.in_buf[2] = vc;
+              d.out_buf = scr;
+              d.reserved[0] = s; d.reserved[1] = gg; d.reserved[2] = Hkv;
+              d.reserved[3] = (uint32_t)c | ((uint32_t)P[s] << 16);
+              d.reserved[4] = base[s * Hkv + gg];
+              const int64_t slot = base[s * Hkv + gg] + c;
+              L.emit(d,
+                     {{qkv, s, s + 1, (int64_t)gg * G * D, (int64_t)(gg + 1) * G * D},
+                      {kc, row, row + 1, 0, cacheCols}, {vc, row, row + 1, 0, cacheCols},
+                      {(int)MK_BUF_STATE, s, s + 1, 0, 2}},
+                     {{scr, slot, slot + 1, 0, (int64_t)G * (D + 2)}},
+                     keys * D * 4.0 + kTaskOverhead);
+            }
+          }
+        g->group_off.push_back((int)g->tasks.size());
+        for (int s = 0; s < B; ++s)
+          for (int gg = 0; gg < Hkv; ++gg) {
+            mk_task_descriptor d = blank(MK_OP_ATTENTION_COMBINE);
+            common(d);
+            d.in_buf[0] = scr;
+            d.out_buf = out;
+            d.reserved[0] = s; d.reserved[1] = gg; d.reserved[2] = Hkv;
+            d.reserved[3] = P[s];
+            d.reserved[4] = base[s * Hkv + gg];
+            const int64_t b0 = base[s * Hkv + gg];
+            L.emit(d, {{scr, b0, b0 + P[s], 0, (int64_t)G * (D + 2)}},
+                   {{out, s, s + 1, (int64_t)gg * G * D, (int64_t)(gg + 1) * G * D}}, kTaskOverhead);
+          }
+        break;
+      }
+      case K_SAMPLE: {
+        g->group_off.push_back((int)g->tasks.size());
+        const int T = tile_count(op.V, tt, al);
+        for (int s = 0; s < op.B; ++s) {
+          mk_task_descriptor d = blank(MK_OP_SAMPLE);
+          d.in_buf[0] = op.a[0];
+          d.out_buf = op.a[1];
+          d.m = op.B;
+          d.n = op.V;
+          d.k = T;
+          d.kv_len = op.cap;
+          d.reserved[0] = s;
+          L.emit(d, {{op.a[0], 0, T, s, s + 1}, {(int)MK_BUF_STATE, s, s + 1, 0, 2}},
+                 {{op.a[1], s, s + 1, 0, op.cap}, {(int)MK_BUF_STATE, s, s + 1, 0, 2}}, kTaskOverhead);
+        }
+        break;
+      }
+    }
+  }
+  const int N = (int)g->tasks.size();
+  g->group_off.push_back(N);
+  // drop empty groups (an op with no tasks cannot happen, but keep ranges tidy)
+  g->group_off.erase(std::unique(g->group_off.begin(), g->group_off.end()), g->group_off.end());
+
+  // parents -> dependents, flattened in task order (children ascending)
+  std::vector<std::vector<int>> children(N);
+  for (int t = 0; t < N; ++t)
+    for (int p : L.parents[t]) children[p].push_back(t);
+  g->edges.clear();
+  uint32_t off = 0;
+  for (int t = 0; t < N; ++t) {
+    g->tasks[t].remaining_deps = (int32_t)L.parents[t].size();
+    g->tasks[t].num_dependents = (int32_t)children[t].size();
+    g->tasks[t].dependents_offset = off;
+    for (int c : children[t]) g->edges.push_back((uint32_t)c);
+    off += (uint32_t)children[t].size();
+  }
+
+  // topological levels
+  std::vector<int> level(N, 0);
+  int nlev = 0;
+  for (int t = 0; t < N; ++t) {
+    for (int p : L.parents[t]) level[t] = std::max(level[t], level[p] + 1);
+    nlev = std::max(nlev, level[t] + 1);
+  }
+  g->level_off.assign(nlev + 1, 0);
+  for (int t = 0; t < N; ++t) g->level_off[level[t] + 1]++;
+  for (int i = 0; i < nlev; ++i) g->level_off[i + 1] += g->level_off[i];
+  g->level_tasks.assign(N, 0);
+  {
+    std::vector<int> fill(g->level_off.begin(), g->level_off.end() - 1);
+    for (int t = 0; t < N; ++t) g->level_tasks[fill[level[t]]++] = t;
+  }
+
+  // Static per-CTA queues by list scheduling on an estimated timeline: each
+  // task (in topological order) goes to the CTA that can finish it first;
+  // ties go to the CTA that has been idle longest, then the lowest index.
+  // Every queue is increasing in task index, so the lowest unfinished task is
+  // always at the head of its queue and runnable: no deadlock while all CTAs
+  // are co-resident.
+  const int C = g->num_ctas;
+  std::vector<double> freeAt(C, 0.0), finish(N, 0.0);
+  std::vector<std::vector<int32_t>> q(C);
+  for (int t = 0; t < N; ++t) {
+    double ready = 0.0;
+    for (int p : L.parents[t]) ready = std::max(ready, finish[p] + kSyncLatency);
+    int best = 0;
+    double bestFin = std::numeric_limits<double>::infinity(), bestFree = 0.0;
+    for (int c = 0; c < C; ++c) {
+      double fin = std::max(freeAt[c], ready) + L.cost[t];
+      if (fin < bestFin || (fin == bestFin && freeAt[c] < bestFree)) {
+        best = c;
+        bestFin = fin;
+        bestFree = freeAt[c];
+      }
+    }
+    finish[t] = bestFin;
+    freeAt[best] = bestFin;
+    q[best].push_back(t);
+  }
+  g->queue_off.assign(C + 1, 0);
+  g->queue.clear();
+  for (int c = 0; c < C; ++c) {
+    g->queue_off[c + 1] = g->queue_off[c] + (int32_t)q[c].size();
+    g->queue.insert(g->queue.end(), q[c].begin(), q[c].end());
+  }
+  g->lowered = true;
+  return MK_OK;
+}
+
+extern "C" int mk_get_tasks(const mk_graph* g, const void** bytes, size_t* nbytes) {
+  if (!g || !bytes || !nbytes) return fail(MK_ERR_ARG, "mk_get_tasks: null argument");
+  if (!g->lowered) return fail(MK_ERR_STATE, "mk_get_tasks: not lowered");
+  *bytes = g->tasks.data();
+  *nbytes = g->tasks.size() * sizeof(mk_task_descriptor);
+  return MK_OK;
+}
+
+extern "C" int mk_get_edges(const mk_graph* g, const uint32_t** edges, size_t* count) {
+  if (!g || !edges || !count) return fail(MK_ERR_ARG, "mk_get_edges: null argument");
+  if (!g->lowered) return fail(MK_ERR_STATE, "mk_get_edges: not lowered");
+  *edges = g->edges.data();
+  *count = g->edges.size();
+  return MK_OK;
+}
+
+extern "C" int mk_debug_patch_task(mk_graph* g, int task, const mk_task_descriptor* d) {
+  if (!g || !d) return fail(MK_ERR_ARG, "mk_debug_patch_task: null argument");
+  if (!g->lowered || g->uploaded) return fail(MK_ERR_STATE, "mk_debug_patch_task: needs a lowered, not uploaded graph");
+  if (task < 0 || task >= (int)g->tasks.size()) return fail(MK_ERR_ARG, "mk_debug_patch_task: bad task index");
+  g->tasks[task] = *d;
+  return MK_OK;
+}
+
+extern "C" int mk_get_queues(const mk_graph* g, const int32_t** offsets, const int32_t** tasks,
+                             int* num_ctas) {
+  if (!g || !offsets || !tasks || !num_ctas) return fail(MK_ERR_ARG, "mk_get_queues: null argument");
+  if (!g->lowered) return fail(MK_ERR_STATE, "mk_get_queues: not lowered");
+  *offsets = g->queue_off.data();
+  *tasks = g->queue.data();
+  *num_ctas = g->num_ctas;
+  return MK_OK;
+}
+
+static_assert(sizeof(mk_task_descriptor) == 64, "ABI: descriptor must be 64 bytes");
+static_assert(offsetof(mk_task_descriptor, remaining_deps) % 4 == 0, "remaining_deps must be 4-byte aligned");
+static_assert(offsetof(mk_task_descriptor, in_buf) == 20, "ABI: in_buf at 20");
+static_assert(offsetof(mk_task_descriptor, reserved) == 44, "ABI: reserved at 44");

@@ -1,0 +1,71 @@
+// Internal host-side state of an mk_graph (not part of the public ABI).
+#pragma once
+
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "mk.h"
+
+namespace mk {
+
+void set_error(const std::string& msg);
+int fail(int code, const std::string& msg);
+
+struct BufferRec {
+  void* ptr = nullptr;
+  int dtype = 0;
+  int64_t rows = 0, cols = 0;
+};
+
+enum OpKind { K_EMBED, K_MATMUL, K_ATTENTION, K_SAMPLE };
+
+struct OpRec {
+  OpKind kind;
+  // embed: a0=table a1=out
+  // matmul: a0=x a1=w a2=out a3=aux a4=pairs
+  // attention: a0=qkv a1=k a2=v a3=out a4=scratch
+  // sample: a0=pairs a1=history
+  uint16_t a[5] = {MK_NO_BUF, MK_NO_BUF, MK_NO_BUF, MK_NO_BUF, MK_NO_BUF};
+  int B = 0, n = 0, k = 0, H = 0;
+  int Hq = 0, Hkv = 0, D = 0, cap = 0, chunk = 0, V = 0;
+  uint32_t flags = 0;
+  float eps = 0.f;
+  std::vector<int32_t> len0;
+};
+
+// Device-side resources owned by the library (runtime.cu).
+struct DeviceState;
+
+}  // namespace mk
+
+struct mk_graph {
+  mk_config cfg{};
+  int num_ctas = 0, tiles_target = 0, col_align = 16;
+  uint32_t timeout_us = 2000000;
+  int B = 0;                       // from mk_set_state
+  bool state_set = false, lowered = false, uploaded = false;
+  std::vector<mk::BufferRec> bufs;  // index 0 state, 1/2 rope tables
+  std::vector<mk::OpRec> ops;
+  // rope parameters (shared by every attention op)
+  double rope_theta = 0.0;
+  int rope_D = 0, rope_cap = 0;
+  // lowering output
+  std::vector<mk_task_descriptor> tasks;
+  std::vector<uint32_t> edges;
+  std::vector<int32_t> queue_off, queue;       // per-CTA static queues
+  std::vector<int32_t> level_off, level_tasks;  // topological levels
+  std::vector<int32_t> group_off;               // per-op launch groups (task ranges)
+  // kernel geometry
+  int max_m = 1;
+  mk::DeviceState* dev = nullptr;
+  std::vector<uint64_t> trace_host;
+};
+
+namespace mk {
+int query_sm_count(int* out);  // runtime.cu
+int tile_width(int n, int tiles_target, int col_align);
+int tile_count(int n, int tiles_target, int col_align);
+std::vector<int> partials_per_sequence(const std::vector<int32_t>& len0, int Hkv, int chunk,
+                                       int num_ctas);
+}  // namespace mk

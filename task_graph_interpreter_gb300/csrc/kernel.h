@@ -1,0 +1,54 @@
+// Parameters and geometry shared by the persistent kernel and its host
+// launcher (internal, not part of the public ABI).
+#pragma once
+
+#include <cstdint>
+
+#include "mk.h"
+
+namespace mk {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 128;  // + one producer warpgroup
+constexpr int kLaunchRegs = 168;    // registers per thread at launch (384 threads, 1 CTA/SM)
+constexpr int kProducerRegs = 40;   // after setmaxnreg.dec in the producer warpgroup
+constexpr int kConsumerRegs = 232;  // after setmaxnreg.inc in the consumer warpgroups
+static_assert(128 * kProducerRegs + 2 * 128 * kConsumerRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
+constexpr int kStageBytes = 32768;               // one ring slot
+constexpr int kStageElems = kStageBytes / 2;     // bf16 elements per slot
+constexpr int kMaxStages = 6;
+constexpr int kScratchBytes = 24576;             // per-task shared scratch
+constexpr int kSlotFloats = 4096;                // GEMV per-warp partial slots
+constexpr int kAccFloats = 1024;                 // GEMV per-row accumulators
+
+// Status word layout (int32[4]): code, task, abort flag, spare.
+constexpr int kStatusCode = 0, kStatusTask = 1, kStatusAbort = 2;
+
+struct KParams {
+  const mk_task_descriptor* tasks;
+  const uint32_t* edges;
+  void* const* bufs;          // buffer table (device pointers by index)
+  uint32_t* counters;         // per-task dependency counters (monotone)
+  const int32_t* queue_off;   // MEGA: per-CTA queue offsets
+  const int32_t* queue;       // MEGA: task ids
+  const int32_t* level_off;   // LEVELS: task range of each level
+  const int32_t* level_tasks; // LEVELS: task ids grouped by level
+  uint32_t* level_bar;        // LEVELS: one arrival counter per level boundary
+  int32_t* status;            // int32[4]
+  const float* rope_cos;      // [cap, D/2]
+  const float* rope_sin;
+  uint64_t* trace;            // 4 x uint64 per task, or null
+  uint64_t timeout_ns;
+  uint32_t epoch;             // 1-based step counter (counter target = epoch * deps)
+  int32_t mode;               // MK_MODE_MEGA / PER_OP / LEVELS
+  int32_t first_task;         // PER_OP: first task of the launched group
+  int32_t num_levels;         // LEVELS
+  int32_t nstages;            // ring slots in use
+  int32_t rope_half;          // D/2 of the tables
+};
+
+int smem_bytes_for(int nstages);
+
+}  // namespace mk

@@ -1,0 +1,946 @@
+// The persistent decode megakernel: an on-GPU interpreter of a static task DAG.
+//
+// One CTA per SM walks a static queue of 64-byte task descriptors.  Before a
+// task runs, one thread waits (acquire) until the task's counter reaches
+// epoch * remaining_deps; after it runs, one warp adds 1 (release) to the
+// counter of every dependent.  There is no grid-wide barrier between ops:
+// each tile starts when its own producers finish ("Megakernels",
+// runhoid.com, "Hoid's approach to megakernels" and Fig. 5; the edge array
+// and descriptor of "mega kernel initial", 1y33.com).  Because weights never
+// change during a step, a producer warp streams the weights (and the cached
+// KV rows) of the CTA's upcoming tasks into a shared-memory ring with bulk
+// async copies before their dependencies resolve ("Megakernels", the note
+// that managing dependencies by hand allows prefetching any input, and
+// Fig. 3 on overlapping one kernel's loads with another's compute).
+//
+// Warp roles: warps 0-7 consume (compute), warp 8 produces (bulk copies).
+// Task bodies:
+//   GEMV (B < 8 and B = 8 on CUDA cores): one output-column tile; epilogues
+//     RMS_NORM_INPUT, SILU_MUL, ADD_RESIDUAL, ARGMAX_EPI ("mega kernel
+//     initial": flags are epilogues, norm -> dot -> residual in one pass;
+//     the final norm fused into the lm_head GEMV).
+//   ATTENTION_APPEND: RoPE on k, bf16 k/v written at row pos (OpId table).
+//   ATTENTION_PARTIAL: online softmax over one KV chunk -> (m, l, o).
+//   ATTENTION_COMBINE: log-sum-exp merge of the partials -> O.
+//   MEMCPY: embedding row gather.   SAMPLE: argmax over the tile pairs.
+// Every wait is bounded by timeout_ns; on expiry the CTA records an error
+// in the status word, raises the abort flag that all CTAs poll, lets its
+// in-flight copies land and exits.  Nothing traps.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cfloat>
+#include <climits>
+
+#include "kernel.h"
+#include "ptx.cuh"
+
+namespace mk {
+
+using namespace ptx;
+
+// ------------------------------------------------------------------ status
+__device__ __forceinline__ bool aborted(const KParams& p) {
+  return ld_relaxed(p.status + kStatusAbort) != 0;
+}
+
+__device__ void raise_error(const KParams& p, int code, int task) {
+  if (atomicCAS(p.status + kStatusCode, 0, code) == 0) atomicExch(p.status + kStatusTask, task);
+  atomicExch(p.status + kStatusAbort, 1);
+}
+
+// Bounded wait on an mbarrier phase.  Returns false on abort or timeout
+// (and records the timeout); the caller then continues without the data.
+__device__ bool bar_wait(const KParams& p, uint64_t* bar, uint32_t parity, int task, bool honor_abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255u) == 0) {
+      if (honor_abort && aborted(p)) return false;
+      if (globaltimer() - t0 > p.timeout_ns) {
+        raise_error(p, MK_DEV_RING_TIMEOUT, task);
+        return false;
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------ task order
+struct Seq {
+  int i = 0, hi = 0, lvl = 0;
+};
+
+__device__ __forceinline__ void seq_init(Seq& s, const KParams& p) {
+  if (p.mode == MK_MODE_MEGA) {
+    s.i = p.queue_off[blockIdx.x];
+    s.hi = p.queue_off[blockIdx.x + 1];
+  } else if (p.mode == MK_MODE_LEVELS) {
+    s.lvl = 0;
+    s.i = p.level_off[0] + blockIdx.x;
+    s.hi = p.level_off[1];
+  } else {
+    s.i = 0;
+    s.hi = 1;
+  }
+}
+
+__device__ __forceinline__ bool seq_next(Seq& s, const KParams& p, int& task, int& lvl) {
+  if (p.mode == MK_MODE_MEGA) {
+    if (s.i >= s.hi) return false;
+    task = p.queue[s.i++];
+    lvl = 0;
+    return true;
+  }
+  if (p.mode == MK_MODE_LEVELS) {
+    while (s.i >= s.hi) {
+      if (++s.lvl >= p.num_levels) return false;
+      s.i = p.level_off[s.lvl] + blockIdx.x;
+      s.hi = p.level_off[s.lvl + 1];
+    }
+    task = p.level_tasks[s.i];
+    s.i += gridDim.x;
+    lvl = s.lvl;
+    return true;
+  }
+  if (s.i >= s.hi) return false;
+  s.i = s.hi;
+  task = p.first_task + blockIdx.x;
+  lvl = 0;
+  return true;
+}
+
+union DescWords {
+  uint4 w[4];
+  mk_task_descriptor d;
+};
+
+__device__ __forceinline__ mk_task_descriptor load_desc(const mk_task_descriptor* t) {
+  DescWords u;
+  const uint4* src = reinterpret_cast<const uint4*>(t);
+  u.w[0] = __ldg(src);
+  u.w[1] = __ldg(src + 1);
+  u.w[2] = __ldg(src + 2);
+  u.w[3] = __ldg(src + 3);
+  return u.d;
+}
+
+// ------------------------------------------------------------------ GEMV plan
+// A GEMV tile streams its weight rows [c0, c0+cn) (and the matching up rows
+// for SILU_MUL) in k-segments of KS columns.  A ring slot holds rs whole
+// row-segments.  Consumer warp w reads columns [wcol*KS/WCOL, ...) of rows
+// r = wrow (mod WROW) of each slot, with x in registers (B*NV*8 floats).
+struct GemvGeom {
+  int B, BT, K, n, c0, cn, seg, KS, nks, WCOL, WROW, NV, rs, RG;
+};
+
+__device__ __forceinline__ void gemv_geom(const mk_task_descriptor& d, GemvGeom& g) {
+  g.B = d.m;
+  g.BT = g.B == 1 ? 1 : g.B == 2 ? 2 : g.B <= 4 ? 4 : 8;  // instantiated batch width
+  g.K = d.k;
+  g.n = d.n;
+  g.c0 = (int)d.reserved[0];
+  g.cn = (int)d.reserved[1];
+  g.seg = (d.flags & MK_F_SILU_MUL) ? 2 : 1;
+  const int u = g.K / 256;
+  g.KS = 256; g.nks = u; g.WCOL = 1; g.WROW = 8; g.NV = 1;
+  for (int q = 1; q <= u; ++q) {
+    if (u % q) continue;
+    const int uk = u / q;
+    if (uk > 64) continue;
+    int wcol = 1;
+    while (wcol < 8 && (uk % (wcol * 2)) == 0) wcol *= 2;
+    const int nv = uk / wcol;
+    if (g.BT == 1 ? nv > 4 : nv > 1) continue;
+    g.KS = uk * 256; g.nks = q; g.WCOL = wcol; g.WROW = 8 / wcol; g.NV = nv;
+    break;
+  }
+  g.rs = kStageElems / g.KS;
+  int rg = kSlotFloats / (g.seg * g.BT * g.WCOL);
+  rg = min(rg, kAccFloats / (g.seg * g.BT));
+  g.RG = min(rg, g.cn);
+}
+
+// ------------------------------------------------------------------ PARTIAL plan
+struct PartGeom {
+  int s, g, Hkv, c, P, slot, D, Hq, G, cap, pos, j0, j1, jst, R, nstage;
+  bool has_new;
+  bool bad;
+};
+
+__device__ __forceinline__ void part_geom(const KParams& p, const mk_task_descriptor& d, PartGeom& q) {
+  q.s = (int)d.reserved[0];
+  q.g = (int)d.reserved[1];
+  q.Hkv = (int)d.reserved[2];
+  q.c = (int)(d.reserved[3] & 0xFFFFu);
+  q.P = (int)(d.reserved[3] >> 16);
+  q.slot = (int)d.reserved[4] + q.c;
+  q.D = d.n;
+  q.Hq = d.k;
+  q.G = q.Hq / q.Hkv;
+  q.cap = d.kv_len;
+  const int32_t* state = static_cast<const int32_t*>(p.bufs[MK_BUF_STATE]);
+  q.pos = ld_relaxed(state + 2 * q.s + 1);
+  q.bad = q.pos < 0 || q.pos >= q.cap;
+  if (q.bad) {
+    q.j0 = q.j1 = q.jst = 0;
+    q.nstage = 0;
+    q.R = 1;
+    q.has_new = false;
+    return;
+  }
+  const int L = q.pos + 1;
+  const int e = (L + q.P - 1) / q.P;
+  q.j0 = min(q.c * e, L);
+  q.j1 = min(q.j0 + e, L);
+  q.jst = min(q.j1, q.pos);
+  q.R = (kStageBytes / 4) / q.D;  // rows of K and of V per slot
+  const int nrows = max(0, q.jst - q.j0);
+  q.nstage = (nrows + q.R - 1) / q.R;
+  q.has_new = (q.j1 == L) && (q.j0 < q.j1);
+}
+
+// ------------------------------------------------------------------ producer
+// Claim the next ring slot once the consumers have freed it and announce the
+// bytes the coming copies will deliver.  Null on abort or timeout.
+__device__ __forceinline__ uint8_t* produce_slot(const KParams& p, uint8_t* ring, uint64_t* full, uint64_t* empty,
+                                                 uint32_t& stage, int task, uint32_t bytes) {
+  const int nst = p.nstages;
+  const uint32_t slot = stage % nst, ph = (stage / nst) & 1u;
+  if (!bar_wait(p, &empty[slot], ph ^ 1u, task, true)) return nullptr;
+  mbar_arrive_expect_tx(&full[slot], bytes);
+  ++stage;
+  return ring + (size_t)slot * kStageBytes;
+}
+
+__device__ void producer(const KParams& p, uint8_t* ring, uint64_t* full, uint64_t* empty) {
+  if ((threadIdx.x & 31) != 0) return;
+  const uint64_t pol = policy_evict_first();
+  const int nst = p.nstages;
+  uint32_t stage = 0;
+  bool stop = false;
+  Seq sq;
+  seq_init(sq, p);
+  int task, lvl;
+  while (!stop && seq_next(sq, p, task, lvl)) {
+    const mk_task_descriptor d = load_desc(p.tasks + task);
+    if (d.op_id == MK_OP_GEMV) {
+      GemvGeom G;
+      gemv_geom(d, G);
+      const uint16_t* W = static_cast<const uint16_t*>(p.bufs[d.in_buf[1]]);
+      for (int g0 = 0; g0 < G.cn && !stop; g0 += G.RG) {
+        const int rows_g = min(G.RG, G.cn - g0);
+        for (int ks = 0; ks < G.nks && !stop; ++ks)
+          for (int sg = 0; sg < G.seg && !stop; ++sg)
+            for (int r0 = 0; r0 < rows_g; r0 += G.rs) {
+              const int nr = min(G.rs, rows_g - r0);
+              const uint32_t bytes = (uint32_t)nr * G.KS * 2u;
+              uint8_t* dst = produce_slot(p, ring, full, empty, stage, task, bytes);
+              if (!dst) { stop = true; break; }
+              const int64_t row = (int64_t)(sg ? G.n : 0) + G.c0 + g0 + r0;
+              const uint16_t* src = W + row * G.K + (int64_t)ks * G.KS;
+              if (G.nks == 1) {
+                bulk_g2s(dst, src, bytes, &full[(stage - 1) % nst], pol);
+              } else {
+                for (int r = 0; r < nr; ++r)
+                  bulk_g2s(dst + (size_t)r * G.KS * 2, src + (int64_t)r * G.K, (uint32_t)G.KS * 2u,
+                           &full[(stage - 1) % nst], pol);
+              }
+            }
+      }
+    } else if (d.op_id == MK_OP_ATTENTION_PARTIAL) {
+      PartGeom q;
+      part_geom(p, d, q);
+      const uint16_t* Kc = static_cast<const uint16_t*>(p.bufs[d.in_buf[1]]);
+      const uint16_t* Vc = static_cast<const uint16_t*>(p.bufs[d.in_buf[2]]);
+      const int64_t rowbase = ((int64_t)q.s * q.Hkv + q.g) * q.cap;
+      for (int i = 0; i < q.nstage && !stop; ++i) {
+        const int j = q.j0 + i * q.R;
+        const int nr = min(q.R, q.jst - j);
+        const uint32_t bytes = (uint32_t)nr * q.D * 2u;
+        uint8_t* dst = produce_slot(p, ring, full, empty, stage, task, 2u * bytes);
+        if (!dst) { stop = true; break; }
+        uint64_t* fb = &full[(stage - 1) % nst];
+        bulk_g2s(dst, Kc + (rowbase + j) * q.D, bytes, fb, pol);
+        bulk_g2s(dst + kStageBytes / 2, Vc + (rowbase + j) * q.D, bytes, fb, pol);
+      }
+    }
+  }
+  // Let every copy still in flight land before the CTA can exit.
+  const uint32_t inflight = stage < (uint32_t)nst ? stage : (uint32_t)nst;
+  for (uint32_t k = 0; k < inflight; ++k) {
+    const uint32_t st = stage - 1 - k;
+    bar_wait(p, &full[st % nst], (st / nst) & 1u, -1, false);
+  }
+}
+
+// ------------------------------------------------------------------ consumer context
+struct Ctx {
+  const KParams* p;
+  uint8_t* ring;
+  uint64_t* full;
+  uint64_t* empty;
+  float* scratch;
+  uint32_t stage;
+  int nst;
+  int task;
+};
+
+// Lane 0 waits for the slot, the warp then reads it.
+__device__ __forceinline__ uint32_t consume_begin(Ctx& c) {
+  const uint32_t slot = c.stage % c.nst, ph = (c.stage / c.nst) & 1u;
+  if ((threadIdx.x & 31) == 0) bar_wait(*c.p, &c.full[slot], ph, c.task, true);
+  __syncwarp();
+  return slot;
+}
+
+__device__ __forceinline__ void consume_end(Ctx& c, uint32_t slot) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(&c.empty[slot]);
+  ++c.stage;
+}
+
+__device__ __forceinline__ void cbar() { named_bar_sync(1, kConsumerThreads); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// (value, index) max with ties to the lower index, across the 256 consumer
+// threads; result valid in thread 0.  red: 16 floats of shared scratch.
+__device__ void block_argmax(float& v, int& idx, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+    if (ov > v || (ov == v && oi < idx)) {
+      v = ov;
+      idx = oi;
+    }
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    red[warp] = v;
+    reinterpret_cast<int*>(red)[8 + warp] = idx;
+  }
+  cbar();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kConsumerWarps; ++w) {
+      const float ov = red[w];
+      const int oi = reinterpret_cast<int*>(red)[8 + w];
+      if (ov > v || (ov == v && oi < idx)) {
+        v = ov;
+        idx = oi;
+      }
+    }
+  }
+  cbar();
+}
+
+// ------------------------------------------------------------------ GEMV body
+// x (times gamma when normalising) for this lane's columns col0 + v*256 + [0,8).
+template <int B, int NV>
+__device__ __forceinline__ void gemv_load_x(float (&xr)[B][NV][8], const float* __restrict__ x,
+                                            const uint16_t* __restrict__ gamma, int K, int col0, int Bact) {
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+    const int col = col0 + v * 256;
+    float gm[8];
+    if (gamma) {
+      const uint4 gv = __ldg(reinterpret_cast<const uint4*>(gamma + col));
+      gm[0] = bf_lo(gv.x); gm[1] = bf_hi(gv.x); gm[2] = bf_lo(gv.y); gm[3] = bf_hi(gv.y);
+      gm[4] = bf_lo(gv.z); gm[5] = bf_hi(gv.z); gm[6] = bf_lo(gv.w); gm[7] = bf_hi(gv.w);
+    } else {
+#pragma unroll
+      for (int k = 0; k < 8; ++k) gm[k] = 1.f;
+    }
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), e = a;
+      if (b < Bact) {
+        a = __ldcg(reinterpret_cast<const float4*>(x + (size_t)b * K + col));
+        e = __ldcg(reinterpret_cast<const float4*>(x + (size_t)b * K + col + 4));
+      }
+      xr[b][v][0] = a.x * gm[0]; xr[b][v][1] = a.y * gm[1]; xr[b][v][2] = a.z * gm[2]; xr[b][v][3] = a.w * gm[3];
+      xr[b][v][4] = e.x * gm[4]; xr[b][v][5] = e.y * gm[5]; xr[b][v][6] = e.z * gm[6]; xr[b][v][7] = e.w * gm[7];
+    }
+  }
+}
+
+template <int B, int NV>
+__device__ void gemv_body(Ctx& c, const mk_task_descriptor& d, const GemvGeom& G) {
+  const KParams& p = *c.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const float* x = static_cast<const float*>(p.bufs[d.in_buf[0]]);
+  float* out = static_cast<float*>(p.bufs[d.out_buf]);
+  const bool rms = d.flags & MK_F_RMS_NORM_INPUT;
+  const bool silu = d.flags & MK_F_SILU_MUL;
+  const bool argmax = d.flags & MK_F_ARGMAX_EPI;
+  const uint16_t* gamma = rms ? static_cast<const uint16_t*>(p.bufs[d.in_buf[2]]) : nullptr;
+  const float* res = (d.flags & MK_F_ADD_RESIDUAL) ? static_cast<const float*>(p.bufs[d.in_buf[2]]) : nullptr;
+  float* slots = c.scratch;
+  float* acc = slots + kSlotFloats;
+  float* red = acc + kAccFloats;  // [0,64) sumsq partials, [64,72) inv_rms, [80,96) argmax, [96,112) tile best
+  const int K = G.K;
+  const int wcol = warp % G.WCOL, wrow = warp / G.WCOL;
+  const int colw = G.KS / G.WCOL;
+
+  // 1 / rms(x) per batch row (applied in the epilogue: W (x*gamma) * inv)
+  if (rms) {
+    float ss[B];
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      float a = 0.f;
+      if (b < G.B)
+        for (int i = tid * 4; i < K; i += kConsumerThreads * 4) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(x + (size_t)b * K + i));
+        a += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+      }
+      ss[b] = warp_sum(a);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int b = 0; b < B; ++b) red[warp * 8 + b] = ss[b];
+    }
+    cbar();
+    if (tid < G.B) {
+      float t = 0.f;
+      for (int w = 0; w < kConsumerWarps; ++w) t += red[w * 8 + tid];
+      const float eps = __uint_as_float(d.reserved[2]);
+      red[64 + tid] = 1.0f / sqrtf(t / (float)K + eps);
+    }
+  }
+  if (argmax && tid < G.B) {
+    red[96 + tid] = -FLT_MAX;
+    reinterpret_cast<int*>(red)[104 + tid] = INT_MAX;
+  }
+
+  float xr[B][NV][8];
+  const int xcol0 = wcol * colw + lane * 8;
+  if (G.nks == 1) gemv_load_x<B, NV>(xr, x, gamma, K, xcol0, G.B);
+
+  for (int g0 = 0; g0 < G.cn; g0 += G.RG) {
+    const int rows_g = min(G.RG, G.cn - g0);
+    for (int ks = 0; ks < G.nks; ++ks) {
+      if (G.nks > 1) gemv_load_x<B, NV>(xr, x, gamma, K, ks * G.KS + xcol0, G.B);
+      for (int sg = 0; sg < G.seg; ++sg) {
+        for (int r0 = 0; r0 < rows_g; r0 += G.rs) {
+          const int nr = min(G.rs, rows_g - r0);
+          const uint32_t slot = consume_begin(c);
+          const uint32_t base = smem_addr(c.ring + (size_t)slot * kStageBytes) + (wcol * colw + lane * 8) * 2;
+          for (int rho = wrow; rho < nr; rho += G.WROW) {
+            float part[B];
+#pragma unroll
+            for (int b = 0; b < B; ++b) part[b] = 0.f;
+            const uint32_t ra = base + (uint32_t)rho * G.KS * 2;
+#pragma unroll
+            for (int v = 0; v < NV; ++v) {
+              const uint4 w = lds128(ra + v * 512);
+              float wf[8];
+              wf[0] = bf_lo(w.x); wf[1] = bf_hi(w.x); wf[2] = bf_lo(w.y); wf[3] = bf_hi(w.y);
+              wf[4] = bf_lo(w.z); wf[5] = bf_hi(w.z); wf[6] = bf_lo(w.w); wf[7] = bf_hi(w.w);
+#pragma unroll
+              for (int b = 0; b < B; ++b)
+#pragma unroll
+                for (int k = 0; k < 8; ++k) part[b] = fmaf(wf[k], xr[b][v][k], part[b]);
+            }
+#pragma unroll
+            for (int b = 0; b < B; ++b) part[b] = warp_sum(part[b]);
+            if (lane == 0) {
+              const int row = sg * rows_g + r0 + rho;
+#pragma unroll
+              for (int b = 0; b < B; ++b) slots[(row * B + b) * G.WCOL + wcol] = part[b];
+            }
+          }
+          consume_end(c, slot);
+        }
+      }
+      // fold this k-segment's per-warp partials, in a fixed order
+      cbar();
+      for (int i = tid; i < G.seg * rows_g * B; i += kConsumerThreads) {
+        float s = 0.f;
+        for (int w = 0; w < G.WCOL; ++w) s += slots[i * G.WCOL + w];
+        acc[i] = (ks == 0) ? s : acc[i] + s;
+      }
+      cbar();
+    }
+    // epilogue: normalisation scale, SiLU*mul, residual, store, argmax
+    for (int b = 0; b < G.B; ++b) {
+      const float inv = rms ? red[64 + b] : 1.f;
+      float bv = -FLT_MAX;
+      int bi = INT_MAX;
+      for (int j = tid; j < rows_g; j += kConsumerThreads) {
+        float y = acc[j * B + b] * inv;
+        if (silu) {
+          const float u = acc[(rows_g + j) * B + b] * inv;
+          y = y / (1.0f + expf(-y)) * u;
+        }
+        const int col = G.c0 + g0 + j;
+        if (res) y += __ldcg(res + (size_t)b * G.n + col);
+        out[(size_t)b * G.n + col] = y;
+        if (y > bv) {
+          bv = y;
+          bi = col;
+        }
+      }
+      if (argmax) {
+        block_argmax(bv, bi, red + 80);
+        if (tid == 0) {
+          const float cv = red[96 + b];
+          const int ci = reinterpret_cast<int*>(red)[104 + b];
+          if (bv > cv || (bv == cv && bi < ci)) {
+            red[96 + b] = bv;
+            reinterpret_cast<int*>(red)[104 + b] = bi;
+          }
+        }
+      }
+    }
+    cbar();
+  }
+  if (argmax && tid < G.B) {
+    mk_argmax_pair* pairs = static_cast<mk_argmax_pair*>(p.bufs[d.reserved[3]]);
+    mk_argmax_pair pr;
+    pr.value = red[96 + tid];
+    pr.index = reinterpret_cast<int*>(red)[104 + tid];
+    pairs[(size_t)d.reserved[4] * G.B + tid] = pr;
+  }
+}
+
+// Batch class 0 serves B <= 2, class 1 serves 3 <= B <= 8; each class is its
+// own kernel so its register allocation is not shared with the other's.
+template <int BCLASS>
+__device__ void gemv_task(Ctx& c, const mk_task_descriptor& d) {
+  GemvGeom G;
+  gemv_geom(d, G);
+  if constexpr (BCLASS == 0) {
+    switch (G.BT * 16 + G.NV) {
+      case 16 + 1: gemv_body<1, 1>(c, d, G); break;
+      case 16 + 2: gemv_body<1, 2>(c, d, G); break;
+      case 16 + 3: gemv_body<1, 3>(c, d, G); break;
+      case 16 + 4: gemv_body<1, 4>(c, d, G); break;
+      case 32 + 1: gemv_body<2, 1>(c, d, G); break;
+    }
+  } else {
+    switch (G.BT * 16 + G.NV) {
+      case 64 + 1: gemv_body<4, 1>(c, d, G); break;
+      case 128 + 1: gemv_body<8, 1>(c, d, G); break;
+    }
+  }
+}
+
+// ------------------------------------------------------------------ attention bodies
+__device__ void append_task(Ctx& c, const mk_task_descriptor& d) {
+  const KParams& p = *c.p;
+  const int s = d.reserved[0], g = d.reserved[1], Hkv = d.reserved[2];
+  const int D = d.n, Hq = d.k, cap = d.kv_len, half = D / 2;
+  int32_t* state = static_cast<int32_t*>(p.bufs[MK_BUF_STATE]);
+  const int pos = ld_relaxed(state + 2 * s + 1);
+  if (pos < 0 || pos >= cap) {
+    if (threadIdx.x == 0) raise_error(p, MK_DEV_CAPACITY, c.task);
+    return;
+  }
+  const float* qkv = static_cast<const float*>(p.bufs[d.in_buf[0]]) + (size_t)s * (Hq + 2 * Hkv) * D;
+  __nv_bfloat16* Kc = static_cast<__nv_bfloat16*>(p.bufs[d.in_buf[1]]);
+  __nv_bfloat16* Vc = static_cast<__nv_bfloat16*>(p.bufs[d.in_buf[2]]);
+  const size_t row = (((size_t)s * Hkv + g) * cap + pos) * D;
+  const int t = threadIdx.x;
+  if (t < half) {
+    const float k1 = __ldcg(qkv + Hq * D + g * D + t);
+    const float k2 = __ldcg(qkv + Hq * D + g * D + t + half);
+    const float cs = p.rope_cos[(size_t)pos * p.rope_half + t];
+    const float sn = p.rope_sin[(size_t)pos * p.rope_half + t];
+    Kc[row + t] = __float2bfloat16_rn(k1 * cs - k2 * sn);
+    Kc[row + t + half] = __float2bfloat16_rn(k2 * cs + k1 * sn);
+  }
+  if (t < D) Vc[row + t] = __float2bfloat16_rn(__ldcg(qkv + (Hq + Hkv) * D + g * D + t));
+}
+
+// One key of the online softmax for the G heads of a KV group.
+template <int DPL, int MAXG>
+__device__ __forceinline__ void partial_step(const float (&qr)[MAXG][DPL], float (&o)[MAXG][DPL], float (&m)[MAXG],
+                                             float (&l)[MAXG], const float (&kf)[DPL], const float (&vf)[DPL],
+                                             int G) {
+#pragma unroll
+  for (int h = 0; h < MAXG; ++h) {
+    if (h < G) {
+      float sc = 0.f;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) sc = fmaf(qr[h][e], kf[e], sc);
+      sc = warp_sum(sc);
+      const float mn = fmaxf(m[h], sc);
+      const float a = exp2f(m[h] - mn);
+      const float pe = exp2f(sc - mn);
+      l[h] = l[h] * a + pe;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) o[h][e] = fmaf(o[h][e], a, pe * vf[e]);
+      m[h] = mn;
+    }
+  }
+}
+
+// Online softmax of G query heads over one KV chunk (log2 domain: scores
+// are scaled by log2(e)/sqrt(D) and exponentials taken base 2).  Writes
+// (m, l, o[D]) per head to the chunk's scratch slot.
+template <int DPL>  // dims per lane: D / 32
+__device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom& q) {
+  constexpr int D = DPL * 32;
+  constexpr int MAXG = 4;
+  const KParams& p = *c.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = q.G, half = D / 2;
+  float* qs = c.scratch;                    // [G][D]
+  float* mrg = c.scratch + MAXG * D;        // [8 warps][G][D + 2]
+  const float* qkv = static_cast<const float*>(p.bufs[d.in_buf[0]]) + (size_t)q.s * (q.Hq + 2 * q.Hkv) * D;
+  const float scale = 1.4426950408889634f / sqrtf((float)D);
+  // RoPE on the group's query heads at position pos
+  for (int i = tid; i < G * half; i += kConsumerThreads) {
+    const int h = i / half, j = i % half;
+    const float* qh = qkv + (size_t)(q.g * G + h) * D;
+    const float a = __ldcg(qh + j), b = __ldcg(qh + j + half);
+    const float cs = p.rope_cos[(size_t)q.pos * p.rope_half + j];
+    const float sn = p.rope_sin[(size_t)q.pos * p.rope_half + j];
+    qs[h * D + j] = (a * cs - b * sn) * scale;
+    qs[h * D + j + half] = (b * cs + a * sn) * scale;
+  }
+  cbar();
+  float qr[MAXG][DPL], o[MAXG][DPL], m[MAXG], l[MAXG];
+#pragma unroll
+  for (int h = 0; h < MAXG; ++h) {
+    m[h] = -INFINITY;
+    l[h] = 0.f;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) {
+      qr[h][e] = h < G ? qs[h * D + lane * DPL + e] : 0.f;
+      o[h][e] = 0.f;
+    }
+  }
+  const int kpw = q.R / kConsumerWarps;  // keys per warp per slot
+  for (int i = 0; i < q.nstage; ++i) {
+    const int nr = min(q.R, q.jst - (q.j0 + i * q.R));
+    const uint32_t slot = consume_begin(c);
+    const uint32_t kb = smem_addr(c.ring + (size_t)slot * kStageBytes);
+    const uint32_t vb = kb + kStageBytes / 2;
+    const int k0 = warp * kpw, k1 = min(nr, k0 + kpw);
+    for (int kk = k0; kk < k1; ++kk) {
+      float kf[DPL], vf[DPL];
+      const uint32_t off = (uint32_t)(kk * D + lane * DPL) * 2;
+      if constexpr (DPL == 4) {
+        const uint2 kv = lds64(kb + off), vv = lds64(vb + off);
+        kf[0] = bf_lo(kv.x); kf[1] = bf_hi(kv.x); kf[2] = bf_lo(kv.y); kf[3] = bf_hi(kv.y);
+        vf[0] = bf_lo(vv.x); vf[1] = bf_hi(vv.x); vf[2] = bf_lo(vv.y); vf[3] = bf_hi(vv.y);
+      } else {
+        const uint32_t kv = lds32(kb + off), vv = lds32(vb + off);
+        kf[0] = bf_lo(kv); kf[1] = bf_hi(kv);
+        vf[0] = bf_lo(vv); vf[1] = bf_hi(vv);
+      }
+      partial_step<DPL, MAXG>(qr, o, m, l, kf, vf, G);
+    }
+    consume_end(c, slot);
+  }
+  if (q.has_new && warp == kConsumerWarps - 1) {
+    // the row appended this step: generic (L2) loads after the dependency wait
+    const size_t row = (((size_t)q.s * q.Hkv + q.g) * q.cap + q.pos) * D + lane * DPL;
+    const uint16_t* Kc = static_cast<const uint16_t*>(p.bufs[d.in_buf[1]]);
+    const uint16_t* Vc = static_cast<const uint16_t*>(p.bufs[d.in_buf[2]]);
+    float kf[DPL], vf[DPL];
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) {
+      kf[e] = __uint_as_float((uint32_t)__ldcg(reinterpret_cast<const unsigned short*>(Kc + row + e)) << 16);
+      vf[e] = __uint_as_float((uint32_t)__ldcg(reinterpret_cast<const unsigned short*>(Vc + row + e)) << 16);
+    }
+    partial_step<DPL, MAXG>(qr, o, m, l, kf, vf, G);
+  }
+  // merge the 8 warps' states
+#pragma unroll
+  for (int h = 0; h < MAXG; ++h) {
+    if (h < G) {
+      float* r = mrg + (warp * MAXG + h) * (D + 2);
+      if (lane == 0) {
+        r[0] = m[h];
+        r[1] = l[h];
+      }
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) r[2 + lane * DPL + e] = o[h][e];
+    }
+  }
+  cbar();
+  float* scr = static_cast<float*>(p.bufs[d.out_buf]) + (size_t)q.slot * G * (D + 2);
+  for (int i = tid; i < G * D; i += kConsumerThreads) {
+    const int h = i / D, e = i % D;
+    float M = -INFINITY;
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mrg[(w * MAXG + h) * (D + 2)]);
+    float Ls = 0.f, O = 0.f;
+    if (M != -INFINITY) {
+      for (int w = 0; w < kConsumerWarps; ++w) {
+        const float* r = mrg + (w * MAXG + h) * (D + 2);
+        const float f = exp2f(r[0] - M);
+        Ls = fmaf(r[1], f, Ls);
+        O = fmaf(r[2 + e], f, O);
+      }
+    }
+    scr[h * (D + 2) + 2 + e] = O;
+    if (e == 0) {
+      scr[h * (D + 2)] = M;
+      scr[h * (D + 2) + 1] = Ls;
+    }
+  }
+}
+
+__device__ void partial_task(Ctx& c, const mk_task_descriptor& d) {
+  PartGeom q;
+  part_geom(*c.p, d, q);
+  if (q.bad) {
+    if (threadIdx.x == 0) raise_error(*c.p, MK_DEV_CAPACITY, c.task);
+    return;
+  }
+  if (q.D == 128) partial_body<4>(c, d, q);
+  else partial_body<2>(c, d, q);
+}
+
+__device__ void combine_task(Ctx& c, const mk_task_descriptor& d) {
+  const KParams& p = *c.p;
+  const int s = d.reserved[0], g = d.reserved[1], Hkv = d.reserved[2];
+  const int P = d.reserved[3], base = d.reserved[4];
+  const int D = d.n, Hq = d.k, G = Hq / Hkv;
+  const float* scr = static_cast<const float*>(p.bufs[d.in_buf[0]]);
+  float* out = static_cast<float*>(p.bufs[d.out_buf]);
+  for (int i = threadIdx.x; i < G * D; i += kConsumerThreads) {
+    const int h = i / D, e = i % D;
+    float M = -INFINITY;
+    for (int k = 0; k < P; ++k) M = fmaxf(M, __ldcg(scr + (size_t)(base + k) * G * (D + 2) + h * (D + 2)));
+    float Ls = 0.f, O = 0.f;
+    for (int k = 0; k < P; ++k) {
+      const float* r = scr + (size_t)(base + k) * G * (D + 2) + h * (D + 2);
+      const float f = exp2f(__ldcg(r) - M);
+      Ls = fmaf(__ldcg(r + 1), f, Ls);
+      O = fmaf(__ldcg(r + 2 + e), f, O);
+    }
+    out[(size_t)s * Hq * D + (size_t)(g * G + h) * D + e] = O / Ls;
+  }
+}
+
+__device__ void embed_task(Ctx& c, const mk_task_descriptor& d) {
+  const KParams& p = *c.p;
+  const int s = d.reserved[0], V = d.reserved[1], H = d.n;
+  const int32_t* state = static_cast<const int32_t*>(p.bufs[MK_BUF_STATE]);
+  const int tok = ld_relaxed(state + 2 * s);
+  if (tok < 0 || tok >= V) {
+    if (threadIdx.x == 0) raise_error(p, MK_DEV_BAD_INDEX, c.task);
+    return;
+  }
+  const uint16_t* E = static_cast<const uint16_t*>(p.bufs[d.in_buf[0]]) + (size_t)tok * H;
+  float* out = static_cast<float*>(p.bufs[d.out_buf]) + (size_t)s * H;
+  for (int i = threadIdx.x * 8; i < H; i += kConsumerThreads * 8) {
+    const uint4 v = __ldg(reinterpret_cast<const uint4*>(E + i));
+    float4 a = make_float4(bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y));
+    float4 b = make_float4(bf_lo(v.z), bf_hi(v.z), bf_lo(v.w), bf_hi(v.w));
+    *reinterpret_cast<float4*>(out + i) = a;
+    *reinterpret_cast<float4*>(out + i + 4) = b;
+  }
+}
+
+__device__ void sample_task(Ctx& c, const mk_task_descriptor& d) {
+  const KParams& p = *c.p;
+  const int s = d.reserved[0], B = d.m, T = d.k, cap = d.kv_len;
+  const mk_argmax_pair* pairs = static_cast<const mk_argmax_pair*>(p.bufs[d.in_buf[0]]);
+  float bv = -FLT_MAX;
+  int bi = INT_MAX;
+  for (int t = threadIdx.x; t < T; t += kConsumerThreads) {
+    const float2 pr = __ldcg(reinterpret_cast<const float2*>(pairs + (size_t)t * B + s));
+    const int idx = __float_as_int(pr.y);
+    if (pr.x > bv || (pr.x == bv && idx < bi)) {
+      bv = pr.x;
+      bi = idx;
+    }
+  }
+  block_argmax(bv, bi, c.scratch);
+  if (threadIdx.x == 0) {
+    int32_t* state = static_cast<int32_t*>(p.bufs[MK_BUF_STATE]);
+    int32_t* hist = static_cast<int32_t*>(p.bufs[d.out_buf]);
+    const int pos = ld_relaxed(state + 2 * s + 1);
+    if (pos < 0 || pos + 1 >= cap) {
+      raise_error(p, MK_DEV_CAPACITY, c.task);
+      return;
+    }
+    hist[(size_t)s * cap + pos + 1] = bi;
+    state[2 * s] = bi;
+    state[2 * s + 1] = pos + 1;
+  }
+}
+
+// ------------------------------------------------------------------ consumer loop
+__device__ bool wait_deps(const KParams& p, int task, int deps) {
+  if (aborted(p)) return false;
+  if (deps == 0) return true;
+  const uint32_t target = p.epoch * (uint32_t)deps;
+  const uint32_t* ctr = p.counters + task;
+  if (ld_acquire(ctr) >= target) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (ld_acquire(ctr) >= target) return true;
+    if ((it & 63u) == 0) {
+      if (aborted(p)) return false;
+      if (globaltimer() - t0 > p.timeout_ns) {
+        raise_error(p, MK_DEV_DEP_TIMEOUT, task);
+        return false;
+      }
+    }
+  }
+}
+
+// Grid barrier k of MK_MODE_LEVELS (consumer thread 0 of every CTA): one
+// counter per level boundary, so a CTA that has run out of work can arrive
+// at all remaining boundaries at once.
+__device__ bool level_barrier(const KParams& p, int k) {
+  red_release_add(p.level_bar + k, 1u);
+  const uint32_t target = gridDim.x;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    if (ld_acquire(p.level_bar + k) >= target) return true;
+    if ((it & 63u) == 0) {
+      if (aborted(p)) return false;
+      if (globaltimer() - t0 > p.timeout_ns) {
+        raise_error(p, MK_DEV_DEP_TIMEOUT, -1);
+        return false;
+      }
+    }
+  }
+}
+
+template <int BCLASS>
+__device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64_t* empty, float* scratch,
+                         volatile int* sflag) {
+  Ctx c{&p, ring, full, empty, scratch, 0u, p.nstages, -1};
+  Seq sq;
+  seq_init(sq, p);
+  int task, lvl, cur_lvl = 0;
+  const int tid = threadIdx.x;
+  while (seq_next(sq, p, task, lvl)) {
+    c.task = task;
+    const mk_task_descriptor d = load_desc(p.tasks + task);
+    uint64_t t_wait = 0, t_start = 0;
+    if (tid == 0) {
+      bool ok = true;
+      if (p.trace) t_wait = globaltimer();
+      if (p.mode == MK_MODE_MEGA) {
+        ok = wait_deps(p, task, d.remaining_deps);
+      } else if (p.mode == MK_MODE_LEVELS) {
+        while (ok && cur_lvl < lvl) ok = level_barrier(p, ++cur_lvl);
+        ok = ok && !aborted(p);
+      } else {
+        ok = !aborted(p);
+      }
+      if (p.trace) t_start = globaltimer();
+      *sflag = ok ? 1 : 0;
+    }
+    cbar();
+    if (!*sflag) return;
+    switch (d.op_id) {
+      case MK_OP_GEMV: gemv_task<BCLASS>(c, d); break;
+      case MK_OP_ATTENTION_APPEND: append_task(c, d); break;
+      case MK_OP_ATTENTION_PARTIAL: partial_task(c, d); break;
+      case MK_OP_ATTENTION_COMBINE: combine_task(c, d); break;
+      case MK_OP_MEMCPY: embed_task(c, d); break;
+      case MK_OP_SAMPLE: sample_task(c, d); break;
+      case MK_OP_NOP: break;
+      default:
+        if (tid == 0) raise_error(p, MK_DEV_BAD_OP, task);
+        break;
+    }
+    cbar();  // every output of the task is written
+    if (p.mode == MK_MODE_MEGA && tid < 32) {
+      const int nd = d.num_dependents;
+      const uint32_t* e = p.edges + d.dependents_offset;
+      for (int i = tid; i < nd; i += 32) red_release_add(p.counters + __ldg(e + i), 1u);
+    }
+    if (p.trace && tid == 0) {
+      uint64_t* r = p.trace + (size_t)task * 4;
+      r[0] = ((uint64_t)blockIdx.x << 32) | smid();
+      r[1] = t_wait;
+      r[2] = t_start;
+      r[3] = globaltimer();
+    }
+  }
+  // LEVELS: arrive at the barriers of the remaining levels so no CTA waits on us
+  if (p.mode == MK_MODE_LEVELS && tid == 0) {
+    for (int k = cur_lvl + 1; k < p.num_levels; ++k) red_release_add(p.level_bar + k, 1u);
+  }
+}
+
+int smem_bytes_for(int nstages) {
+  return nstages * kStageBytes + 2 * nstages * 8 + 16 + kScratchBytes;
+}
+
+template <int BCLASS>
+__global__ void __launch_bounds__(kThreads, 1) mk_interpreter_kernel(const __grid_constant__ KParams p) {
+  // 3 warpgroups: two consumer warpgroups and one producer warpgroup whose
+  // first warp issues the copies.  Registers move from the producer group to
+  // the consumers: 128 * kProducerRegs + 256 * kConsumerRegs equals
+  // 384 * kLaunchRegs, the allocation the CTA is launched with (the host
+  // refuses to launch if the compiled kernel's count differs).
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const int nst = p.nstages;
+  uint8_t* ring = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)nst * kStageBytes);
+  uint64_t* empty = full + nst;
+  volatile int* sflag = reinterpret_cast<volatile int*>(empty + nst);
+  float* scratch = reinterpret_cast<float*>(smem + (size_t)nst * kStageBytes + 2 * nst * 8 + 16);
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nst; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], kConsumerWarps);
+    }
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x >= kConsumerThreads) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
+    if (threadIdx.x < kConsumerThreads + 32) producer(p, ring, full, empty);
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
+    consumer<BCLASS>(p, ring, full, empty, scratch, sflag);
+  }
+}
+
+}  // namespace mk
+
+// Launch helpers used by the runtime (host side, same translation unit as the kernels).
+namespace mk {
+
+static const void* kernel_for(int batch) {
+  return batch <= 2 ? (const void*)mk_interpreter_kernel<0> : (const void*)mk_interpreter_kernel<1>;
+}
+
+cudaError_t configure_interpreter(int batch, int* num_regs) {
+  const void* fn = kernel_for(batch);
+  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_for(kMaxStages));
+  if (e != cudaSuccess) return e;
+  cudaFuncAttributes attr;
+  e = cudaFuncGetAttributes(&attr, fn);
+  if (e != cudaSuccess) return e;
+  *num_regs = attr.numRegs;
+  return cudaSuccess;
+}
+
+cudaError_t launch_interpreter(const KParams& p, int batch, int grid, bool cooperative, cudaStream_t stream) {
+  const int smem = smem_bytes_for(p.nstages);
+  const void* fn = kernel_for(batch);
+  void* args[] = {const_cast<KParams*>(&p)};
+  if (cooperative)
+    return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kThreads), args, (size_t)smem, stream);
+  return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, (size_t)smem, stream);
+}
+
+cudaError_t max_coresident_ctas(int batch, int nstages, int* per_sm) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, kernel_for(batch), kThreads, smem_bytes_for(nstages));
+}
+
+}  // namespace mk

@@ -1,0 +1,360 @@
+// Host runtime of libmk: upload of the lowered graph, launches, status.
+//
+// Upload follows "mega kernel initial" (1y33.com, buffer-table and upload
+// part): one contiguous device blob holding a 64-byte header, the task
+// array and the edge array, copied with a single cudaMemcpy, plus the
+// buffer pointer table.  Where the page keeps a pristine copy of the blob to
+// restore between runs, this runtime keeps the descriptors immutable and
+// makes dependency counters monotone: step e waits for counter >= e * deps,
+// so nothing has to be restored between steps.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "graph.h"
+#include "kernel.h"
+
+namespace mk {
+
+cudaError_t configure_interpreter(int batch, int* num_regs);
+cudaError_t launch_interpreter(const KParams& p, int batch, int grid, bool cooperative, cudaStream_t stream);
+cudaError_t max_coresident_ctas(int batch, int nstages, int* per_sm);
+
+struct DeviceState {
+  int device = -1;
+  void* blob = nullptr;
+  size_t blob_bytes = 0;
+  mk_task_descriptor* tasks = nullptr;
+  uint32_t* edges = nullptr;
+  void** bufs = nullptr;
+  uint32_t* counters = nullptr;
+  int32_t* queue_off = nullptr;
+  int32_t* queue = nullptr;
+  int32_t* level_off = nullptr;
+  int32_t* level_tasks = nullptr;
+  uint32_t* level_bar = nullptr;
+  int32_t* status = nullptr;
+  float* rope_cos = nullptr;
+  float* rope_sin = nullptr;
+  uint64_t* trace = nullptr;
+  uint32_t epoch = 0;
+  int nstages = kMaxStages;
+  cudaGraphExec_t per_op_exec = nullptr;
+  cudaGraph_t per_op_graph = nullptr;
+};
+
+}  // namespace mk
+
+using namespace mk;
+
+#define CUDA_TRY(call)                                                                       \
+  do {                                                                                       \
+    cudaError_t e__ = (call);                                                                \
+    if (e__ != cudaSuccess)                                                                  \
+      return fail(MK_ERR_CUDA, std::string(#call) + ": " + cudaGetErrorString(e__));         \
+  } while (0)
+
+int mk::query_sm_count(int* out) {
+  int dev = 0, n = 0;
+  CUDA_TRY(cudaGetDevice(&dev));
+  CUDA_TRY(cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev));
+  *out = n;
+  return MK_OK;
+}
+
+namespace {
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+void free_device(DeviceState* d) {
+  if (!d) return;
+  if (d->per_op_exec) cudaGraphExecDestroy(d->per_op_exec);
+  if (d->per_op_graph) cudaGraphDestroy(d->per_op_graph);
+  if (d->blob) cudaFree(d->blob);
+  delete d;
+}
+
+KParams base_params(const mk_graph* g) {
+  const DeviceState* d = g->dev;
+  KParams p{};
+  p.tasks = d->tasks;
+  p.edges = d->edges;
+  p.bufs = d->bufs;
+  p.counters = d->counters;
+  p.queue_off = d->queue_off;
+  p.queue = d->queue;
+  p.level_off = d->level_off;
+  p.level_tasks = d->level_tasks;
+  p.level_bar = d->level_bar;
+  p.status = d->status;
+  p.rope_cos = d->rope_cos;
+  p.rope_sin = d->rope_sin;
+  p.trace = nullptr;
+  p.timeout_ns = (uint64_t)g->timeout_us * 1000ull;
+  p.epoch = d->epoch;
+  p.mode = MK_MODE_MEGA;
+  p.first_task = 0;
+  p.num_levels = (int)g->level_off.size() - 1;
+  p.nstages = d->nstages;
+  p.rope_half = g->rope_D / 2;
+  return p;
+}
+
+int launch_per_op(mk_graph* g, cudaStream_t stream, uint64_t* trace) {
+  KParams p = base_params(g);
+  p.mode = MK_MODE_PER_OP;
+  p.trace = trace;
+  for (size_t i = 0; i + 1 < g->group_off.size(); ++i) {
+    p.first_task = g->group_off[i];
+    const int n = g->group_off[i + 1] - g->group_off[i];
+    if (n <= 0) continue;
+    CUDA_TRY(launch_interpreter(p, g->B, n, false, stream));
+  }
+  return MK_OK;
+}
+
+}  // namespace
+
+extern "C" int mk_upload(mk_graph* g, void* stream_) {
+  if (!g) return fail(MK_ERR_ARG, "mk_upload: null graph");
+  if (!g->lowered) return fail(MK_ERR_STATE, "mk_upload: call mk_lower first");
+  if (g->uploaded) return fail(MK_ERR_STATE, "mk_upload: already uploaded");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  auto* d = new (std::nothrow) DeviceState();
+  if (!d) return fail(MK_ERR_NOMEM, "mk_upload: out of memory");
+  int rc = MK_OK;
+  do {
+    if (cudaGetDevice(&d->device) != cudaSuccess) { rc = fail(MK_ERR_CUDA, "mk_upload: no device"); break; }
+    // ring depth from the opt-in shared-memory limit, then co-residency check
+    int optin = 0;
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d->device);
+    d->nstages = kMaxStages;
+    while (d->nstages > 2 && smem_bytes_for(d->nstages) > optin) --d->nstages;
+    int regs = 0;
+    if (configure_interpreter(g->B, &regs) != cudaSuccess) {
+      rc = fail(MK_ERR_CUDA, "mk_upload: cannot configure the interpreter kernel");
+      break;
+    }
+    if (regs != kLaunchRegs) {
+      // the producer/consumer register split assumes this launch allocation
+      rc = fail(MK_ERR_CUDA, "mk_upload: interpreter kernel compiled with " + std::to_string(regs) +
+                                 " registers per thread, expected " + std::to_string(kLaunchRegs));
+      break;
+    }
+    int per_sm = 0, sms = 0;
+    if (max_coresident_ctas(g->B, d->nstages, &per_sm) != cudaSuccess || per_sm < 1) {
+      rc = fail(MK_ERR_CUDA, "mk_upload: the interpreter kernel cannot be resident");
+      break;
+    }
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d->device);
+    if (g->num_ctas > per_sm * sms) {
+      rc = fail(MK_ERR_LIMIT, "mk_upload: num_ctas " + std::to_string(g->num_ctas) + " exceeds co-resident CTAs " +
+                                  std::to_string(per_sm * sms));
+      break;
+    }
+    const size_t N = g->tasks.size(), E = g->edges.size(), NB = g->bufs.size();
+    const int half = g->rope_D / 2, cap = g->rope_cap;
+    // blob layout: header | tasks | edges | queue_off | queue | level_off | level_tasks | bufs | cos | sin
+    //              then (zeroed) counters | status | level_bar | trace
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+      size_t o = off;
+      off = align_up(off + bytes, 256);
+      return o;
+    };
+    const size_t o_hdr = take(64), o_tasks = take(N * 64), o_edges = take(E * 4),
+                 o_qoff = take(g->queue_off.size() * 4), o_q = take(g->queue.size() * 4),
+                 o_loff = take(g->level_off.size() * 4), o_lt = take(g->level_tasks.size() * 4),
+                 o_bufs = take(NB * 8), o_cos = take((size_t)cap * half * 4), o_sin = take((size_t)cap * half * 4);
+    const size_t static_bytes = off;
+    const size_t o_ctr = take(N * 4), o_status = take(16), o_lbar = take(g->level_off.size() * 4),
+                 o_trace = take(N * 32);
+    d->blob_bytes = off;
+    if (cudaMalloc(&d->blob, d->blob_bytes) != cudaSuccess) {
+      rc = fail(MK_ERR_NOMEM, "mk_upload: cudaMalloc of " + std::to_string(d->blob_bytes) + " bytes failed");
+      break;
+    }
+    std::vector<uint8_t> img(static_bytes, 0);
+    uint32_t hdr[16] = {0x31474B4Du /* "MKG1" */, MK_ABI_VERSION, (uint32_t)N, (uint32_t)E, (uint32_t)NB,
+                        (uint32_t)g->num_ctas, (uint32_t)(g->level_off.size() - 1), 64u};
+    std::memcpy(img.data() + o_hdr, hdr, 64);
+    std::memcpy(img.data() + o_tasks, g->tasks.data(), N * 64);
+    std::memcpy(img.data() + o_edges, g->edges.data(), E * 4);
+    std::memcpy(img.data() + o_qoff, g->queue_off.data(), g->queue_off.size() * 4);
+    std::memcpy(img.data() + o_q, g->queue.data(), g->queue.size() * 4);
+    std::memcpy(img.data() + o_loff, g->level_off.data(), g->level_off.size() * 4);
+    std::memcpy(img.data() + o_lt, g->level_tasks.data(), g->level_tasks.size() * 4);
+    char* base = static_cast<char*>(d->blob);
+    std::vector<void*> ptrs(NB);
+    for (size_t i = 0; i < NB; ++i) ptrs[i] = g->bufs[i].ptr;
+    ptrs[MK_BUF_ROPE_COS] = base + o_cos;
+    ptrs[MK_BUF_ROPE_SIN] = base + o_sin;
+    std::memcpy(img.data() + o_bufs, ptrs.data(), NB * 8);
+    // RoPE tables: angle = pos * theta^(-2i/D), evaluated in double, stored as float
+    {
+      float* cs = reinterpret_cast<float*>(img.data() + o_cos);
+      float* sn = reinterpret_cast<float*>(img.data() + o_sin);
+      for (int i = 0; i < half; ++i) {
+        const double inv = std::pow(g->rope_theta, -2.0 * i / (double)g->rope_D);
+        for (int pos = 0; pos < cap; ++pos) {
+          const double a = (double)pos * inv;
+          cs[(size_t)pos * half + i] = (float)std::cos(a);
+          sn[(size_t)pos * half + i] = (float)std::sin(a);
+        }
+      }
+    }
+    if (cudaMemcpy(d->blob, img.data(), static_bytes, cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemset(base + o_ctr, 0, d->blob_bytes - o_ctr) != cudaSuccess) {
+      rc = fail(MK_ERR_CUDA, "mk_upload: copy to device failed");
+      break;
+    }
+    d->tasks = reinterpret_cast<mk_task_descriptor*>(base + o_tasks);
+    d->edges = reinterpret_cast<uint32_t*>(base + o_edges);
+    d->queue_off = reinterpret_cast<int32_t*>(base + o_qoff);
+    d->queue = reinterpret_cast<int32_t*>(base + o_q);
+    d->level_off = reinterpret_cast<int32_t*>(base + o_loff);
+    d->level_tasks = reinterpret_cast<int32_t*>(base + o_lt);
+    d->bufs = reinterpret_cast<void**>(base + o_bufs);
+    d->rope_cos = reinterpret_cast<float*>(base + o_cos);
+    d->rope_sin = reinterpret_cast<float*>(base + o_sin);
+    d->counters = reinterpret_cast<uint32_t*>(base + o_ctr);
+    d->status = reinterpret_cast<int32_t*>(base + o_status);
+    d->level_bar = reinterpret_cast<uint32_t*>(base + o_lbar);
+    d->trace = reinterpret_cast<uint64_t*>(base + o_trace);
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+      rc = fail(MK_ERR_CUDA, "mk_upload: stream synchronisation failed");
+      break;
+    }
+  } while (0);
+  if (rc != MK_OK) {
+    free_device(d);
+    return rc;
+  }
+  g->dev = d;
+  g->uploaded = true;
+  return MK_OK;
+}
+
+extern "C" int mk_decode_step_ex(mk_graph* g, void* stream_, int mode, uint32_t trace) {
+  if (!g) return fail(MK_ERR_ARG, "mk_decode_step: null graph");
+  if (!g->uploaded) return fail(MK_ERR_STATE, "mk_decode_step: call mk_upload first");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  DeviceState* d = g->dev;
+  uint64_t* tr = trace ? d->trace : nullptr;
+  switch (mode) {
+    case MK_MODE_MEGA: {
+      KParams p = base_params(g);
+      p.epoch = d->epoch + 1;
+      p.trace = tr;
+      CUDA_TRY(launch_interpreter(p, g->B, g->num_ctas, true, stream));
+      d->epoch += 1;
+      return MK_OK;
+    }
+    case MK_MODE_LEVELS: {
+      KParams p = base_params(g);
+      p.mode = MK_MODE_LEVELS;
+      p.trace = tr;
+      CUDA_TRY(cudaMemsetAsync(d->level_bar, 0, g->level_off.size() * 4, stream));
+      CUDA_TRY(launch_interpreter(p, g->B, g->num_ctas, true, stream));
+      return MK_OK;
+    }
+    case MK_MODE_PER_OP:
+      return launch_per_op(g, stream, tr);
+    case MK_MODE_PER_OP_GRAPH: {
+      if (trace) return fail(MK_ERR_ARG, "mk_decode_step_ex: tracing is not available in graph mode");
+      if (!d->per_op_exec) {
+        cudaStream_t cs;
+        CUDA_TRY(cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking));
+        int rc = MK_OK;
+        if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+          rc = fail(MK_ERR_CUDA, "mk_decode_step_ex: begin capture failed");
+        } else {
+          rc = launch_per_op(g, cs, nullptr);
+          cudaGraph_t graph = nullptr;
+          cudaError_t e = cudaStreamEndCapture(cs, &graph);
+          if (rc == MK_OK && e != cudaSuccess) rc = fail(MK_ERR_CUDA, "mk_decode_step_ex: end capture failed");
+          if (rc == MK_OK) {
+            if (cudaGraphInstantiate(&d->per_op_exec, graph, 0) != cudaSuccess) {
+              rc = fail(MK_ERR_CUDA, "mk_decode_step_ex: graph instantiation failed");
+              cudaGraphDestroy(graph);
+            } else {
+              d->per_op_graph = graph;
+            }
+          } else if (graph) {
+            cudaGraphDestroy(graph);
+          }
+        }
+        cudaStreamDestroy(cs);
+        if (rc != MK_OK) return rc;
+      }
+      CUDA_TRY(cudaGraphLaunch(d->per_op_exec, stream));
+      return MK_OK;
+    }
+    default:
+      return fail(MK_ERR_ARG, "mk_decode_step_ex: unknown mode " + std::to_string(mode));
+  }
+}
+
+extern "C" int mk_decode_step(mk_graph* g, void* stream) { return mk_decode_step_ex(g, stream, MK_MODE_MEGA, 0); }
+
+extern "C" int mk_decode_step_host(mk_graph* g, void* stream_, const int32_t* state_in, int32_t* tokens_out) {
+  if (!g) return fail(MK_ERR_ARG, "mk_decode_step_host: null graph");
+  if (!g->uploaded) return fail(MK_ERR_STATE, "mk_decode_step_host: call mk_upload first");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  void* state = g->bufs[MK_BUF_STATE].ptr;
+  if (state_in) CUDA_TRY(cudaMemcpyAsync(state, state_in, (size_t)g->B * 8, cudaMemcpyHostToDevice, stream));
+  int rc = mk_decode_step_ex(g, stream_, MK_MODE_MEGA, 0);
+  if (rc != MK_OK) return rc;
+  if (tokens_out)
+    CUDA_TRY(cudaMemcpy2DAsync(tokens_out, 4, state, 8, 4, (size_t)g->B, cudaMemcpyDeviceToHost, stream));
+  return MK_OK;
+}
+
+extern "C" int mk_status(mk_graph* g, void* stream_, int* dev_code, int32_t* task_id) {
+  if (!g || !dev_code || !task_id) return fail(MK_ERR_ARG, "mk_status: null argument");
+  if (!g->uploaded) return fail(MK_ERR_STATE, "mk_status: call mk_upload first");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  DeviceState* d = g->dev;
+  CUDA_TRY(cudaStreamSynchronize(stream));
+  int32_t st[4] = {0, 0, 0, 0};
+  CUDA_TRY(cudaMemcpy(st, d->status, 16, cudaMemcpyDeviceToHost));
+  *dev_code = st[kStatusCode];
+  *task_id = st[kStatusCode] ? st[kStatusTask] : -1;
+  if (st[kStatusCode] || st[kStatusAbort]) {
+    // A failed step leaves counters part-way; start the epochs afresh.
+    CUDA_TRY(cudaMemsetAsync(d->counters, 0, g->tasks.size() * 4, stream));
+    CUDA_TRY(cudaMemsetAsync(d->status, 0, 16, stream));
+    CUDA_TRY(cudaStreamSynchronize(stream));
+    d->epoch = 0;
+  }
+  return MK_OK;
+}
+
+extern "C" int mk_get_trace(mk_graph* g, const uint64_t** records, size_t* count) {
+  if (!g || !records || !count) return fail(MK_ERR_ARG, "mk_get_trace: null argument");
+  if (!g->uploaded) return fail(MK_ERR_STATE, "mk_get_trace: call mk_upload first");
+  CUDA_TRY(cudaDeviceSynchronize());
+  g->trace_host.resize(g->tasks.size() * 4);
+  CUDA_TRY(cudaMemcpy(g->trace_host.data(), g->dev->trace, g->trace_host.size() * 8, cudaMemcpyDeviceToHost));
+  *records = g->trace_host.data();
+  *count = g->tasks.size();
+  return MK_OK;
+}
+
+extern "C" int mk_kernel_info(const mk_graph* g, int* smem_bytes, int* threads, int* stages) {
+  if (!g || !smem_bytes || !threads || !stages) return fail(MK_ERR_ARG, "mk_kernel_info: null argument");
+  const int nst = g->dev ? g->dev->nstages : kMaxStages;
+  *smem_bytes = smem_bytes_for(nst);
+  *threads = kThreads;
+  *stages = nst;
+  return MK_OK;
+}
+
+extern "C" void mk_destroy(mk_graph* g) {
+  if (!g) return;
+  free_device(g->dev);
+  delete g;
+}

@@ -1,0 +1,206 @@
+"""Host-side tests of the C ABI (no GPU): symbols, lowering parity, errors.
+
+The C++ lowering must emit exactly the bytes of the oracle's independent
+lowering for every workload; nothing here dereferences a registered pointer,
+so fake 256-byte-aligned addresses stand in for device memory.
+"""
+import re
+import os
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import lowering as ol
+from oracle.graph import llama_decode_spec
+from oracle.validate import validate
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def L():
+    from task_graph_interpreter_gb300 import build as _b
+    _b()
+    from task_graph_interpreter_gb300 import _lib
+    _lib.lib()
+    return _lib
+
+
+def test_library_exports_every_declared_symbol(L):
+    hdr = open(os.path.join(ROOT, "include", "mk.h")).read()
+    hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
+    declared = set(re.findall(r"\b(mk_[a-z_]+)\s*\(", hdr))
+    assert declared == set(L.EXPORTS)
+    lib = L.lib()
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def _replay(L, spec, B):
+    """Feed an oracle graph spec to libmk through the C ABI (fake pointers)."""
+    g = L.mk_graph_create(num_ctas=spec["num_ctas"], tiles_target=spec["tiles_target"],
+                          col_align=spec["col_align"])
+    base = 1 << 40
+    L.mk_set_state(g, base, B)
+    for i, (dt, rows, cols) in enumerate(spec["buffers"][3:], start=3):
+        idx = L.mk_add_buffer(g, base + i * (1 << 24), dt, rows, cols)
+        assert idx == i
+    for op in spec["ops"]:
+        k = op["kind"]
+        if k == "embed":
+            L.mk_add_embed(g, op["table"], op["out"], op["B"], op["H"])
+        elif k == "matmul":
+            L.mk_add_matmul(g, op["x"], op["w"], op["out"], op["aux"], op["pairs"], op["flags"],
+                            op["m"], op["n"], op["k"], op["eps"])
+        elif k == "attention":
+            L.mk_add_attention(g, op["qkv"], op["k"], op["v"], op["out"], op["scratch"], op["B"],
+                               op["Hq"], op["Hkv"], op["D"], op["capacity"], op["len0"], op["chunk"], 5e5)
+        elif k == "sample":
+            L.mk_add_sample(g, op["pairs"], op["history"], op["B"], op["V"], op["capacity"])
+    L.mk_lower(g)
+    return g
+
+
+@pytest.mark.parametrize("name", synth.WORKLOADS)
+@pytest.mark.parametrize("num_ctas", [152, 37])
+def test_cpp_lowering_is_byte_identical_to_oracle(L, name, num_ctas):
+    w = synth.workload(name)
+    spec = llama_decode_spec(w.model, w.B, w.kv_len, w.capacity, w.chunk, num_ctas)
+    tasks, edges = ol.lower(spec)
+    g = _replay(L, spec, w.B)
+    try:
+        got = L.mk_get_tasks(g)
+        assert len(got) == tasks.nbytes
+        if got != tasks.tobytes():
+            gt = np.frombuffer(got, dtype=ol.TASK_DTYPE)
+            bad = int(np.nonzero(gt != tasks)[0][0])
+            pytest.fail(f"descriptor {bad} differs:\n lib    {gt[bad]}\n oracle {tasks[bad]}")
+        assert np.array_equal(L.mk_get_edges(g), edges)
+        off, q = L.mk_get_queues(g)
+        assert len(off) == num_ctas + 1 and off[0] == 0 and off[-1] == len(tasks)
+        assert np.array_equal(np.sort(q), np.arange(len(tasks)))
+        for c in range(num_ctas):
+            qq = q[off[c]:off[c + 1]]
+            assert np.all(np.diff(qq) > 0), "each CTA queue must be in topological order"
+    finally:
+        L.mk_destroy(g)
+
+
+def test_cpp_lowering_validates(L):
+    w = synth.workload("1b")
+    spec = llama_decode_spec(w.model, w.B, w.kv_len, w.capacity, w.chunk, 152)
+    g = _replay(L, spec, w.B)
+    try:
+        tasks = np.frombuffer(L.mk_get_tasks(g), dtype=ol.TASK_DTYPE)
+        validate(tasks, L.mk_get_edges(g))
+    finally:
+        L.mk_destroy(g)
+
+
+def test_worked_example_through_the_library(L):
+    # "qkv with 3072 output columns and 8 tiles becomes 8 GEMV tasks of 384"
+    g = L.mk_graph_create(num_ctas=8, tiles_target=8, col_align=16)
+    try:
+        assert L.mk_gemv_tiles(g, 3072) == 8
+        L.mk_set_state(g, 1 << 40, 1)
+        x = L.mk_add_buffer(g, (1 << 40) + (1 << 24), L.MK_F32, 1, 2048)
+        wq = L.mk_add_buffer(g, (1 << 40) + (2 << 24), L.MK_BF16, 3072, 2048)
+        y = L.mk_add_buffer(g, (1 << 40) + (3 << 24), L.MK_F32, 1, 3072)
+        L.mk_add_matmul(g, x, wq, y, L.MK_NO_BUF, L.MK_NO_BUF, 0, 1, 3072, 2048, 0.0)
+        L.mk_lower(g)
+        t = np.frombuffer(L.mk_get_tasks(g), dtype=ol.TASK_DTYPE)
+        assert len(t) == 8
+        assert list(t["reserved"][:, 0]) == [384 * i for i in range(8)]
+        assert set(t["reserved"][:, 1]) == {384}
+    finally:
+        L.mk_destroy(g)
+
+
+def test_errors_are_reported(L):
+    with pytest.raises(L.MkError) as e:
+        L.mk_graph_create(num_ctas=4, abi_version=99)
+    assert e.value.code == L.MK_ERR_ABI
+    g = L.mk_graph_create(num_ctas=4)
+    try:
+        with pytest.raises(L.MkError) as e:
+            L.mk_add_buffer(g, 1 << 40, L.MK_F32, 1, 1)     # before the state
+        assert e.value.code == L.MK_ERR_STATE
+        L.mk_set_state(g, 1 << 40, 1)
+        with pytest.raises(L.MkError) as e:
+            L.mk_add_buffer(g, (1 << 40) + 8, L.MK_F32, 1, 1)  # misaligned
+        assert e.value.code == L.MK_ERR_ARG
+        x = L.mk_add_buffer(g, (1 << 40) + (1 << 24), L.MK_F32, 1, 256)
+        w = L.mk_add_buffer(g, (1 << 40) + (2 << 24), L.MK_BF16, 64, 256)
+        y = L.mk_add_buffer(g, (1 << 40) + (3 << 24), L.MK_F32, 1, 64)
+        gm = L.mk_add_buffer(g, (1 << 40) + (4 << 24), L.MK_BF16, 1, 256)
+        with pytest.raises(L.MkError) as e:   # both norm and residual: one aux slot
+            L.mk_add_matmul(g, x, w, y, gm, L.MK_NO_BUF, L.MK_F_RMS_NORM_INPUT | L.MK_F_ADD_RESIDUAL,
+                            1, 64, 256, 1e-5)
+        assert e.value.code == L.MK_ERR_ARG
+        with pytest.raises(L.MkError) as e:   # K mismatch with x
+            L.mk_add_matmul(g, x, w, y, L.MK_NO_BUF, L.MK_NO_BUF, 0, 1, 64, 512, 0.0)
+        assert e.value.code == L.MK_ERR_ARG
+        with pytest.raises(L.MkError) as e:   # bad buffer index
+            L.mk_add_matmul(g, 77, w, y, L.MK_NO_BUF, L.MK_NO_BUF, 0, 1, 64, 256, 0.0)
+        assert e.value.code == L.MK_ERR_ARG
+        with pytest.raises(L.MkError) as e:   # nothing to lower yet
+            L.mk_lower(g)
+        assert e.value.code == L.MK_ERR_STATE
+        L.mk_add_matmul(g, x, w, y, gm, L.MK_NO_BUF, L.MK_F_RMS_NORM_INPUT, 1, 64, 256, 1e-5)
+        with pytest.raises(L.MkError) as e:   # step before upload
+            L.mk_decode_step(g, 0)
+        assert e.value.code == L.MK_ERR_STATE
+        L.mk_lower(g)
+        with pytest.raises(L.MkError) as e:   # add after lower
+            L.mk_add_matmul(g, x, w, y, gm, L.MK_NO_BUF, L.MK_F_RMS_NORM_INPUT, 1, 64, 256, 1e-5)
+        assert e.value.code == L.MK_ERR_STATE
+    finally:
+        L.mk_destroy(g)
+
+
+class _FakeTensor:
+    """Stands in for a large device tensor when only its address and shape matter."""
+    _next = 1 << 44
+
+    def __init__(self, *shape, dtype=None):
+        import torch
+        self.shape = tuple(shape)
+        self.dtype = dtype or torch.bfloat16
+        n = int(np.prod(shape))
+        self._ptr = _FakeTensor._next
+        _FakeTensor._next += ((n * 4 + 4095) // 4096) * 4096 + 4096
+
+    def numel(self):
+        return int(np.prod(self.shape))
+
+    def dim(self):
+        return len(self.shape)
+
+    def is_contiguous(self):
+        return True
+
+    def data_ptr(self):
+        return self._ptr
+
+
+@pytest.mark.parametrize("name", ["tiny", "8b", "8b_b8"])
+def test_product_builder_matches_oracle_graph(L, name):
+    """The package's Llama builder registers buffers and ops in the same order
+    as the oracle's graph spec, so its lowered bytes equal the oracle's."""
+    import torch
+    from task_graph_interpreter_gb300.llama import build_llama_decode
+    w = synth.workload(name)
+    m = w.model
+    weights = {n: _FakeTensor(*shape) for (n, shape, _, _) in synth.weight_names(m)}
+    kc = [_FakeTensor(w.B, m.Hkv, w.capacity, m.D) for _ in range(m.L)]
+    vc = [_FakeTensor(w.B, m.Hkv, w.capacity, m.D) for _ in range(m.L)]
+    hist = torch.zeros(w.B, w.capacity, dtype=torch.int32)
+    dec = build_llama_decode(m, w.B, w.kv_len, w.capacity, weights, kc, vc, hist, chunk=w.chunk,
+                             device="cpu", num_ctas=152)
+    dec.graph.lower()
+    spec = llama_decode_spec(m, w.B, w.kv_len, w.capacity, w.chunk, 152)
+    tasks, edges = ol.lower(spec)
+    assert dec.graph.tasks_bytes() == tasks.tobytes()
+    assert np.array_equal(dec.graph.edges(), edges)
+    dec.graph.close()

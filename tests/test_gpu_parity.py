@@ -1,0 +1,108 @@
+"""CUDA path vs the float64 oracle, element by element, through the C ABI.
+
+Sizes: the tiny model (several tiles per op and a short last tile), a
+ragged batch with empty and one-key chunks (the batch-3 kernel class), and
+the 1B-shaped model at full size in the launch configuration the benchmark
+uses (one CTA per SM).
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import forward as of
+from tests.common import NpWeights, oracle_state
+from tests.gpu_common import build_gpu, compare_step, compare_cache_rows
+
+pytestmark = pytest.mark.gpu
+
+MODES = {"mega": 0, "per_op": 1, "per_op_graph": 2, "levels": 3}
+
+
+def _run_and_compare(w, steps, mode="mega", num_ctas=0, seed=0, check_cache=True):
+    from task_graph_interpreter_gb300 import _lib as L
+    dec = build_gpu(w, seed, num_ctas)
+    W = NpWeights(w.model, seed)
+    st = oracle_state(w, seed)
+    clear_steps = 0
+    try:
+        for i in range(steps):
+            pos_before = [int(p) for p in st.pos]
+            dec.graph.step(MODES[mode])
+            code, task = dec.graph.status()
+            assert code == 0, f"device status {code} at task {task}"
+            res = of.decode_step(w.model, W, st)
+            dmax, clear = compare_step(dec, res, st)
+            if check_cache:
+                compare_cache_rows(dec, st, pos_before)
+            hist = dec.history.tensor.cpu().numpy()
+            for s in range(w.B):
+                assert hist[s, pos_before[s] + 1] == dec.graph.state[s, 0].item()
+            if not clear:
+                break                   # a near-tie: later inputs may differ legitimately
+            clear_steps += 1
+    finally:
+        dec.graph.close()
+    return clear_steps
+
+
+def test_tiny_one_step_megakernel():
+    assert _run_and_compare(synth.workload("tiny"), 1) == 1
+
+
+def test_capacity_is_reported_not_overrun():
+    # the tiny workload has room for exactly one generated token
+    dec = build_gpu(synth.workload("tiny"))
+    try:
+        dec.graph.step()
+        assert dec.graph.status()[0] == 0
+        dec.graph.step()
+        from task_graph_interpreter_gb300 import _lib as L
+        code, task = dec.graph.status()
+        assert code == L.MK_DEV_CAPACITY
+    finally:
+        dec.graph.close()
+
+
+@pytest.mark.parametrize("mode", ["per_op", "per_op_graph", "levels"])
+def test_tiny_other_modes(mode):
+    w = synth.custom(synth.TINY, 1, [128], 2, name="tiny2")
+    assert _run_and_compare(w, 2, mode) >= 1
+
+
+def test_tiny_multi_step_greedy_tokens():
+    w = synth.custom(synth.TINY, 1, [128], 8, name="tiny8")
+    assert _run_and_compare(w, 8) >= 6
+
+
+def test_ragged_batch_with_empty_and_single_key_chunks():
+    # B = 3 uses the batch-3..8 kernel; kv lengths 0, 4 and 70 with one-key
+    # chunks give P = 1, 4, 70 partials, some of them empty as keys grow
+    w = synth.custom(synth.TINY, 3, [0, 4, 70], 3, chunk=1, name="tiny_ragged")
+    assert _run_and_compare(w, 3) >= 2
+
+
+def test_batch_two_and_few_ctas():
+    w = synth.custom(synth.TINY, 2, [33, 128], 2, name="tiny_b2")
+    assert _run_and_compare(w, 2, num_ctas=7) >= 1
+
+
+def test_modes_are_bitwise_identical_and_deterministic():
+    w = synth.workload("tiny")
+    outs = []
+    for mode in ("mega", "mega", "per_op", "levels"):
+        dec = build_gpu(w)
+        dec.graph.step(MODES[mode])
+        assert dec.graph.status()[0] == 0
+        outs.append((dec.logits.tensor.cpu().clone(), [h.tensor.cpu().clone() for h in dec.hidden]))
+        dec.graph.close()
+    for o in outs[1:]:
+        assert torch.equal(o[0], outs[0][0])
+        for a, b in zip(o[1], outs[0][1]):
+            assert torch.equal(a, b)
+
+
+@pytest.mark.slow
+def test_1b_full_size_two_steps():
+    w = synth.custom(synth.LLAMA_1B, 1, [1024], 2, name="1b2")
+    assert _run_and_compare(w, 2, check_cache=False) >= 1
