@@ -856,17 +856,19 @@ __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
         break;
     }
     cbar();  // every output of the task is written
-    if (p.mode == MK_MODE_MEGA && tid < 32) {
-      const int nd = d.num_dependents;
-      const uint32_t* e = p.edges + d.dependents_offset;
-      for (int i = tid; i < nd; i += 32) red_release_add(p.counters + __ldg(e + i), 1u);
-    }
     if (p.trace && tid == 0) {
+      // end stamp taken before the dependents are released, so a child's
+      // start stamp is never earlier than its parents' end stamps
       uint64_t* r = p.trace + (size_t)task * 4;
       r[0] = ((uint64_t)blockIdx.x << 32) | smid();
       r[1] = t_wait;
       r[2] = t_start;
       r[3] = globaltimer();
+    }
+    if (p.mode == MK_MODE_MEGA && tid < 32) {
+      const int nd = d.num_dependents;
+      const uint32_t* e = p.edges + d.dependents_offset;
+      for (int i = tid; i < nd; i += 32) red_release_add(p.counters + __ldg(e + i), 1u);
     }
   }
   // LEVELS: arrive at the barriers of the remaining levels so no CTA waits on us
