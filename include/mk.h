@@ -270,6 +270,32 @@ int mk_get_trace(mk_graph* g, const uint64_t** records, size_t* count);
 /* Bytes of shared memory the kernel uses per CTA and its thread count. */
 int mk_kernel_info(const mk_graph* g, int* smem_bytes, int* threads, int* stages);
 
+/* Decode attention that allocates nothing.  No counterpart in the paper:
+ * this entry point exists for callers that cannot call cudaMalloc once they
+ * run -- servers and plugins that give all of HBM to their own pool at start
+ * up and forbid later device allocations, and latency-critical loops where
+ * an allocation could synchronise the device.  It runs one step of the
+ * attention op on device pointers the caller passes: the new k (rotate-half
+ * RoPE, base rope_theta) and v rows of qkv f32 [B, (Hq + 2 Hkv) D] are
+ * stored as bf16 at row pos[s] of kcache / vcache bf16 [B, Hkv, capacity, D],
+ * and out f32 [B, Hq D] receives softmax(q K^T / sqrt(D)) V over keys
+ * 0..pos[s], computed as split-KV partials (chunk count from len0 and chunk
+ * as in mk_add_attention; chunk 0 uses the device's SM count) merged by a
+ * log-sum-exp combine.  pos and len0 are host arrays [B].  Same limits as
+ * mk_add_attention (B <= 8, D in {64, 128}, Hq/Hkv <= 4).
+ * The partial scratch lives in a file-scope device array of
+ * MK_NOALLOC_SCRATCH_FLOATS floats (4 MiB) that every GPU loading the
+ * library holds until the process exits; a call needing more returns
+ * MK_ERR_LIMIT.  No cudaMalloc, cudaFree or other allocation happens here.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture.  All
+ * calls share the array: calls whose kernels overlap on the GPU race.
+ * Enqueued on `stream`; errors: MK_ERR_ARG, MK_ERR_LIMIT, MK_ERR_CUDA. */
+#define MK_NOALLOC_SCRATCH_FLOATS (1 << 20)
+int mk_attention_decode_noalloc(void* stream, const float* qkv, void* kcache, void* vcache, float* out,
+                                int B, int Hq, int Hkv, int D, int capacity, const int32_t* pos,
+                                const int32_t* len0, int chunk, double rope_theta);
+
 /* Release everything the library allocated.  Safe on NULL. */
 void mk_destroy(mk_graph* g);
 

@@ -31,6 +31,7 @@ EXPORTS = [
     "mk_lower", "mk_get_tasks", "mk_get_edges", "mk_get_queues", "mk_upload",
     "mk_decode_step", "mk_decode_step_ex", "mk_decode_step_host", "mk_status",
     "mk_get_trace", "mk_kernel_info", "mk_destroy", "mk_last_error", "mk_debug_patch_task",
+    "mk_attention_decode_noalloc",
 ]
 
 
@@ -82,6 +83,9 @@ def lib():
         "mk_kernel_info": (c_int, [G, POINTER(c_int), POINTER(c_int), POINTER(c_int)]),
         "mk_destroy": (None, [G]),
         "mk_debug_patch_task": (c_int, [G, c_int, c_void_p]),
+        "mk_attention_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
+                                                c_int, c_int, c_int, POINTER(c_int32), POINTER(c_int32), c_int,
+                                                c_double]),
         "mk_last_error": (c_char_p, []),
     }
     for name, (res, args) in sig.items():
@@ -217,6 +221,16 @@ def mk_debug_patch_task(g, task: int, desc: bytes):
     assert len(desc) == 64
     buf = ctypes.create_string_buffer(desc, 64)
     check(lib().mk_debug_patch_task(g, task, buf), "mk_debug_patch_task")
+
+
+def mk_attention_decode_noalloc(stream: int, qkv: int, kcache: int, vcache: int, out: int, B: int, Hq: int,
+                                Hkv: int, D: int, capacity: int, pos, len0, chunk: int, theta: float):
+    """Device pointers as ints; pos and len0 are sequences of B ints (host)."""
+    pa = (c_int32 * B)(*[int(v) for v in pos])
+    la = (c_int32 * B)(*[int(v) for v in len0])
+    check(lib().mk_attention_decode_noalloc(c_void_p(stream), c_void_p(qkv), c_void_p(kcache), c_void_p(vcache),
+                                            c_void_p(out), B, Hq, Hkv, D, capacity, pa, la, chunk, float(theta)),
+          "mk_attention_decode_noalloc")
 
 
 def mk_last_error() -> str:

@@ -18,7 +18,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libmk.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["graph.cpp", "runtime.cu", "megakernel.cu"]
+SOURCES = ["graph.cpp", "runtime.cu", "megakernel.cu", "noalloc.cu"]
 
 
 def nvcc() -> str:
