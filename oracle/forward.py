@@ -4,16 +4,12 @@ TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and
 ``bench.py``'s CPU-baseline leg may import this module.  It shares no code
 with the CUDA path and never calls it.
 
-What is computed.  The decode megakernel ("mega kernel initial", 1y33.com)
-lowers one decoder layer, written on its graph object as
-
-    qkv = matmul(residual, W_qkv, gamma=attn_norm)     RMSNorm fused on input
-    att = attention(qkv, kcache, vcache)               RoPE-append + split-KV
-    h   = matmul(att, W_o, residual=residual)          residual epilogue
-    gu  = matmul(h, W_gate_up, gamma=mlp_norm, silu_mul=True)
-    out = matmul(gu, W_down, residual=h)
-
-(the decoder-layer listing in its "building the graph" part), with the final
+What is computed.  The decode megakernel ("mega kernel initial", 1y33.com,
+its graph-building part) writes a decoder layer as five graph ops: a qkv
+projection of the RMS-normalised residual stream, attention over the KV
+cache (RoPE, append, split-KV), an output projection added to the residual,
+a gate/up projection of the normalised stream with SiLU(gate) * up, and a
+down projection added to the residual; the final
 RMSNorm fused into the lm_head GEMV and a SAMPLE task taking the argmax over
 the vocabulary (its OpId table).  Split-KV flash decoding, the fused
 epilogues and the column tiling reach exactly (up to floating-point

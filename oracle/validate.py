@@ -6,7 +6,7 @@ Checks the properties that "mega kernel initial" (1y33.com) states for its
 lowered graph and that the interpreter's correctness rests on:
 
 * tasks are in topological order: every edge points to a later task
-  (the edge-array part: "a task can never depend on one emitted after it");
+  (the edge-array part: no task depends on a later one);
 * each task's dependency count equals its number of parents, and the edge
   array is the flattened, offset-indexed dependents lists;
 * a task's level is 1 + the max level of its parents, and two tasks of the

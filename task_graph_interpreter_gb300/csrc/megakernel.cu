@@ -17,8 +17,8 @@
 // Task bodies:
 //   GEMV (B < 8 and B = 8 on CUDA cores): one output-column tile; epilogues
 //     RMS_NORM_INPUT, SILU_MUL, ADD_RESIDUAL, ARGMAX_EPI ("mega kernel
-//     initial": flags are epilogues, norm -> dot -> residual in one pass;
-//     the final norm fused into the lm_head GEMV).
+//     initial", lowering part: the fusions are epilogue flags of one GEMV
+//     pass, and the final norm is fused into the lm_head GEMV).
 //   ATTENTION_APPEND: RoPE on k, bf16 k/v written at row pos (OpId table).
 //   ATTENTION_PARTIAL: online softmax over one KV chunk -> (m, l, o).
 //   ATTENTION_COMBINE: log-sum-exp merge of the partials -> O.

@@ -1,11 +1,8 @@
-"""Graph builder over libmk: ops on a graph object, as in "mega kernel initial"
-(1y33.com, the graph-building part):
-
-    qkv = g.matmul(residual, w_qkv, gamma=attn_norm)
-    att = g.attention(qkv, kcache, vcache, ...)
-    h   = g.matmul(att, w_o, residual=residual)
-    gu  = g.matmul(h, w_gate_up, gamma=mlp_norm, silu_mul=True)
-    out = g.matmul(gu, w_down, residual=h)
+"""Graph builder over libmk: a model is composed by calling ops on a graph
+object ("mega kernel initial", 1y33.com, the graph-building part).  matmul
+takes the fusions as keywords -- gamma (RMSNorm of its input), residual
+(added to its output), silu_mul (SiLU of the gate half times the up half) --
+and attention takes the fused qkv activations and the two caches.
 
 Each call registers its output tensor (allocated with PyTorch on the graph's
 device) in libmk's append-only buffer table and adds the op; every step of

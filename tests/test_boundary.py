@@ -99,7 +99,7 @@ def test_cpp_lowering_validates(L):
 
 
 def test_worked_example_through_the_library(L):
-    # "qkv with 3072 output columns and 8 tiles becomes 8 GEMV tasks of 384"
+    # the page's worked example: 3072 qkv columns over 8 tiles, 384 columns each
     g = L.mk_graph_create(num_ctas=8, tiles_target=8, col_align=16)
     try:
         assert L.mk_gemv_tiles(g, 3072) == 8
