@@ -213,7 +213,8 @@ def run_reference(args, workload):
 
 
 def config_dict(args, w):
-    return {"workload": WORKLOAD_NAMES[args.config], "B": w.B, "kv_len_start": list(w.kv_len)[:8],
+    name = WORKLOAD_NAMES[args.config] + (f", truncated to {w.model.L} layers" if args.layers else "")
+    return {"workload": name, "B": w.B, "kv_len_start": list(w.kv_len)[:8],
             "layers": w.model.L, "hidden": w.model.H, "ffn": w.model.F, "vocab": w.model.V,
             "heads_q_kv": [w.model.Hq, w.model.Hkv], "head_dim": w.model.D,
             "l2": "inputs larger than L2 (weights streamed every step exceed the 129 MB L2)",
@@ -229,10 +230,15 @@ def main():
     ap.add_argument("--impl", default="mk", choices=["mk", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-modes", action="store_true")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="truncate the model to this many layers (small cases for profiling)")
     args = ap.parse_args()
 
+    import dataclasses
     import synth
     base = synth.workload(args.config)
+    if args.layers:
+        base = dataclasses.replace(base, model=dataclasses.replace(base.model, L=args.layers))
     if args.impl == "reference":
         run_reference(args, base)
         return

@@ -184,7 +184,8 @@ int mk_add_matmul(mk_graph* g, uint16_t x, uint16_t w, uint16_t out, uint16_t au
  *  kcache / vcache bf16 [B * Hkv, capacity * D] (= [B, Hkv, capacity, D]).
  *  out  f32 [B, Hq D].     scratch f32 [mk_attention_scratch_rows, G (D + 2)].
  *  len0[B]: cached keys per sequence when the graph is built (fixes the chunk
- *  count).  chunk: keys per chunk, 0 = automatic.  D in {64, 128}; Hq/Hkv <= 4.
+ *  count).  chunk: keys per chunk, 0 = automatic.  D in {64, 128}; Hq/Hkv <= 4;
+ *  at most 2048 / (Hq/Hkv) chunks per sequence (MK_ERR_LIMIT beyond).
  * APPEND applies rotate-half RoPE (base rope_theta) to k at position pos and
  * stores bf16 k, v at row pos; PARTIAL applies RoPE to q and runs an online
  * softmax (scale 1/sqrt(D)) over its chunk of the pos + 1 keys. */
@@ -214,7 +215,8 @@ int mk_gemv_tiles(const mk_graph* g, int n, int32_t* tiles);
  *  APPEND   in={qkv,K,V} out=K m=B n=D k=Hq kv_len=capacity reserved={s,g,Hkv,0,0}
  *  PARTIAL  in={qkv,K,V} out=scratch, same m/n/k/kv_len,
  *           reserved={s,g,Hkv, c | (P_s << 16), first slot of (s,g)}
- *  COMBINE  in={scratch} out=att, same m/n/k/kv_len, reserved={s,g,Hkv,P_s,first slot}
+ *  COMBINE  in={scratch,K,V} out=att, same m/n/k/kv_len, reserved={s,g,Hkv,P_s,first slot}
+ *           (K and V order the append before the attention output)
  *  MEMCPY   in={table} out=h m=B n=H reserved={s, rows of the table}
  *  SAMPLE   in={pairs} out=history m=B n=V k=T kv_len=capacity reserved={s}
  * Errors: MK_ERR_STATE (already lowered or no ops). */
@@ -263,8 +265,12 @@ int mk_decode_step_host(mk_graph* g, void* stream, const int32_t* state_in,
  * *dev_code = MK_DEV_* and *task_id = the failing task (or -1). */
 int mk_status(mk_graph* g, void* stream, int* dev_code, int32_t* task_id);
 
-/* Trace records of the last traced step: uint64[count * 4] as
- * (cta << 32 | smid, t_wait_begin_ns, t_start_ns, t_end_ns) per task. */
+/* Trace records of the last traced step: uint64[count * 8] per task as
+ * (cta << 32 | smid, t_wait_begin, t_start, t_end, mark0, mark1, mark2, 0),
+ * %globaltimer nanoseconds: the dependency wait began / ended, the task's
+ * outputs were complete (before its dependents are released), and marks
+ * inside the body (GEMV and PARTIAL: first ring slot ready, all slots
+ * consumed, epilogue or merge done; 0 where unused). */
 int mk_get_trace(mk_graph* g, const uint64_t** records, size_t* count);
 
 /* Bytes of shared memory the kernel uses per CTA and its thread count. */

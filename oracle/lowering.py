@@ -29,7 +29,15 @@ row gather as a MEMCPY task carrying the table's row count in reserved[1];
 the per-tile (max, index) pairs stored tile-major ([T, B]); field maps per
 op as in ``lower`` below.
 Access ranges are tracked as row x column rectangles of each buffer's 2-D
-view, so per-sequence writes (embedding, combine) do not alias.
+view, so per-sequence writes (embedding, combine) do not alias.  In a KV
+cache block, columns [0, cap*D) stand for the rows of earlier steps and
+[cap*D, cap*D + D) for the row this step appends: APPEND writes only the
+latter, PARTIAL reads only the former (it takes the appended key and value
+from qkv, rotated and rounded as APPEND stores them), so the partials do not
+wait for the append.  COMBINE takes the appended row as an input (its
+in_buf[1..2] are the caches), so the append is complete before the
+attention output is and every reader of the decode state stays an
+ancestor of SAMPLE, which advances it.
 """
 from __future__ import annotations
 
@@ -74,11 +82,11 @@ def tiles(n: int, tiles_target: int, col_align: int):
 def partials_per_sequence(len0, Hkv: int, chunk: int, num_ctas: int):
     """Split-KV chunk count P_s per sequence (fixed at lowering time).
     chunk > 0: ceil(len0_s / chunk).  chunk == 0: chunks of about
-    E = max(256, ceil(Hkv * sum(len0) / num_ctas)) keys, so the partial tasks
+    E = max(128, ceil(Hkv * sum(len0) / num_ctas)) keys, so the partial tasks
     of a ragged batch carry about the same bytes and number about one per SM."""
     if chunk > 0:
         return [max(1, ceil_div(int(l), chunk)) for l in len0]
-    E = max(256, ceil_div(Hkv * sum(int(l) for l in len0), num_ctas))
+    E = max(128, ceil_div(Hkv * sum(int(l) for l in len0), num_ctas))
     return [max(1, ceil_div(int(l), E)) for l in len0]
 
 
@@ -178,8 +186,8 @@ def lower(spec: dict):
                          reads=[(qkv, s, s + 1, kcol, kcol + D),
                                 (qkv, s, s + 1, vcol, vcol + D),
                                 (BUF_STATE, s, s + 1, 0, 2)],
-                         writes=[(kc, row, row + 1, 0, cap * D),
-                                 (vc, row, row + 1, 0, cap * D)])
+                         writes=[(kc, row, row + 1, cap * D, cap * D + D),
+                                 (vc, row, row + 1, cap * D, cap * D + D)])
             for s in range(B):
                 for g in range(Hkv):
                     row = s * Hkv + g
@@ -190,16 +198,21 @@ def lower(spec: dict):
                                   reserved=(s, g, Hkv, c | (P[s] << 16), base[s][g]),
                                   **common),
                              reads=[(qkv, s, s + 1, g * G * D, (g + 1) * G * D),
+                                    (qkv, s, s + 1, Hq * D + g * D, Hq * D + (g + 1) * D),
+                                    (qkv, s, s + 1, (Hq + Hkv) * D + g * D, (Hq + Hkv) * D + (g + 1) * D),
                                     (kc, row, row + 1, 0, cap * D),
                                     (vc, row, row + 1, 0, cap * D),
                                     (BUF_STATE, s, s + 1, 0, 2)],
                              writes=[(scr, slot, slot + 1, 0, G * (D + 2))])
             for s in range(B):
                 for g in range(Hkv):
+                    row = s * Hkv + g
                     emit(dict(op_id=OP_ATT_COMBINE, config_id=cfg,
-                              in_buf=(scr, NO_BUF, NO_BUF), out_buf=out,
+                              in_buf=(scr, kc, vc), out_buf=out,
                               reserved=(s, g, Hkv, P[s], base[s][g]), **common),
-                         reads=[(scr, base[s][g], base[s][g] + P[s], 0, G * (D + 2))],
+                         reads=[(scr, base[s][g], base[s][g] + P[s], 0, G * (D + 2)),
+                                (kc, row, row + 1, cap * D, cap * D + D),
+                                (vc, row, row + 1, cap * D, cap * D + D)],
                          writes=[(out, s, s + 1, g * G * D, (g + 1) * G * D)])
         elif kind == "sample":
             B, V, cap = op["B"], op["V"], op["capacity"]

@@ -14,8 +14,9 @@ lowered graph and that the interpreter's correctness rests on:
 * every pair of tasks touching overlapping data, at least one writing, is
   ordered by a path in the DAG (no read/write or write/write race);
 * every read of a buffer that the graph writes is covered by earlier writes,
-  except reads of the decode state (carried in from the previous step) and
-  reads of buffers whose writers all come later.
+  except reads of data carried in from the previous step (the decode state,
+  the KV rows of earlier steps) and reads of buffers whose writers all come
+  later.
 
 Access rectangles are decoded from the descriptor fields alone, by code
 separate from the lowering that produced them.
@@ -64,18 +65,24 @@ def task_accesses(d) -> tuple:
             R += [(ib[0], s, s + 1, Hq * D + g * D, Hq * D + (g + 1) * D),
                   (ib[0], s, s + 1, (Hq + Hkv) * D + g * D, (Hq + Hkv) * D + (g + 1) * D),
                   (BUF_STATE, s, s + 1, 0, 2)]
-            Wr += [(ib[1], row, row + 1, 0, cap * D), (ib[2], row, row + 1, 0, cap * D)]
+            # the appended row: columns [cap*D, cap*D + D) of the (s, g) block
+            Wr += [(ib[1], row, row + 1, cap * D, cap * D + D), (ib[2], row, row + 1, cap * D, cap * D + D)]
         elif op == OP_ATT_PARTIAL:
             c, P = rs[3] & 0xFFFF, rs[3] >> 16
             assert c < P
             slot = rs[4] + c
+            # q, k and v of the group from qkv; the cache rows of earlier
+            # steps (columns [0, cap*D)), carried in from the previous step
             R += [(ib[0], s, s + 1, g * G * D, (g + 1) * G * D),
-                  (ib[1], row, row + 1, 0, cap * D), (ib[2], row, row + 1, 0, cap * D),
+                  (ib[0], s, s + 1, Hq * D + g * D, Hq * D + (g + 1) * D),
+                  (ib[0], s, s + 1, (Hq + Hkv) * D + g * D, (Hq + Hkv) * D + (g + 1) * D),
+                  (ib[1], row, row + 1, 0, cap * D, True), (ib[2], row, row + 1, 0, cap * D, True),
                   (BUF_STATE, s, s + 1, 0, 2)]
             Wr.append((ob, slot, slot + 1, 0, G * (D + 2)))
         else:
             P, base = rs[3], rs[4]
             R.append((ib[0], base, base + P, 0, G * (D + 2)))
+            R += [(ib[1], row, row + 1, cap * D, cap * D + D), (ib[2], row, row + 1, cap * D, cap * D + D)]
             Wr.append((ob, s, s + 1, g * G * D, (g + 1) * G * D))
     elif op == OP_SAMPLE:
         s = rs[0]
@@ -134,10 +141,12 @@ def validate(tasks: np.ndarray, edges: np.ndarray, check_hazards: bool = True) -
         for (b, r0, r1, c0, c1) in acc[t][1]:
             writes_by_buf[b].append((t, r0, r1, c0, c1))
     for t in range(N):
-        for (b, r0, r1, c0, c1) in acc[t][0]:
+        for rd in acc[t][0]:
+            b, r0, r1, c0, c1 = rd[:5]
+            carried = len(rd) > 5 and rd[5]
             ws = writes_by_buf.get(b)
-            if b == BUF_STATE or not ws or min(w[0] for w in ws) >= t:
-                continue      # carried in from the previous step (state) or external
+            if carried or b == BUF_STATE or not ws or min(w[0] for w in ws) >= t:
+                continue      # carried in from the previous step (state, old KV rows) or external
             for r in range(r0, r1):
                 iv = [(a0, a1) for (wt, q0, q1, a0, a1) in ws if wt < t and q0 <= r < q1]
                 if not _covered(iv, c0, c1):
@@ -161,7 +170,8 @@ def validate(tasks: np.ndarray, edges: np.ndarray, check_hazards: bool = True) -
 
     by_buf = defaultdict(list)
     for t in range(N):
-        for (b, r0, r1, c0, c1) in acc[t][0]:
+        for rd in acc[t][0]:
+            b, r0, r1, c0, c1 = rd[:5]
             by_buf[b].append((t, r0, r1, c0, c1, False))
         for (b, r0, r1, c0, c1) in acc[t][1]:
             by_buf[b].append((t, r0, r1, c0, c1, True))

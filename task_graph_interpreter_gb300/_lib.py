@@ -204,7 +204,7 @@ def mk_get_trace(g):
     import numpy as np
     p, n = c_void_p(), c_size_t()
     check(lib().mk_get_trace(g, ctypes.byref(p), ctypes.byref(n)), "mk_get_trace")
-    return np.frombuffer(ctypes.string_at(p, n.value * 32), dtype=np.uint64).reshape(-1, 4).copy()
+    return np.frombuffer(ctypes.string_at(p, n.value * 64), dtype=np.uint64).reshape(-1, 8).copy()
 
 
 def mk_kernel_info(g):

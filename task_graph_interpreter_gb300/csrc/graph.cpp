@@ -13,6 +13,13 @@
 //    topological order (the edge-array part);
 //  * levels: level = 1 + max parent level (the levels part), kept for the
 //    level-synchronous ablation mode.
+// In a KV cache block, columns [0, cap*D) stand for the rows of earlier steps
+// and [cap*D, cap*D + D) for the row appended this step: APPEND writes only
+// the latter and PARTIAL reads only the former (it takes the new key/value
+// from qkv), so partials do not wait for the append.  COMBINE takes the
+// appended row as an input, so the append completes before the attention
+// output does and every reader of the decode state stays an ancestor of
+// SAMPLE, which advances it.
 #include <algorithm>
 #include <cmath>
 #include <cstring>
@@ -45,7 +52,7 @@ int tile_count(int n, int tiles_target, int col_align) {
 
 // Split-KV chunk count per sequence, fixed at lowering time.  chunk > 0:
 // ceil(len0 / chunk).  chunk == 0: chunks of about
-// E = max(256, ceil(Hkv * sum(len0) / num_ctas)) keys, so that the partials
+// E = max(128, ceil(Hkv * sum(len0) / num_ctas)) keys, so that the partials
 // of a ragged batch carry similar bytes and number about one per SM.
 std::vector<int> partials_per_sequence(const std::vector<int32_t>& len0, int Hkv, int chunk,
                                        int num_ctas) {
@@ -56,7 +63,7 @@ std::vector<int> partials_per_sequence(const std::vector<int32_t>& len0, int Hkv
   }
   int64_t tot = 0;
   for (int32_t l : len0) tot += l;
-  int64_t E = std::max<int64_t>(256, cdiv((int64_t)Hkv * tot, num_ctas));
+  int64_t E = std::max<int64_t>(128, cdiv((int64_t)Hkv * tot, num_ctas));
   for (size_t s = 0; s < len0.size(); ++s) P[s] = (int)std::max<int64_t>(1, cdiv(len0[s], E));
   return P;
 }
@@ -237,6 +244,13 @@ extern "C" int mk_add_attention(mk_graph* g, uint16_t qkv, uint16_t kcache, uint
   CHECK(check_buf(g, kcache, MK_BF16, (int64_t)B * Hkv, (int64_t)capacity * D, "mk_add_attention kcache"));
   CHECK(check_buf(g, vcache, MK_BF16, (int64_t)B * Hkv, (int64_t)capacity * D, "mk_add_attention vcache"));
   CHECK(check_buf(g, out, MK_F32, B, (int64_t)Hq * D, "mk_add_attention out"));
+  {
+    // a combine task stages 3 floats per (partial, head) in its shared scratch
+    std::vector<int32_t> l(len0, len0 + B);
+    for (int P : partials_per_sequence(l, Hkv, chunk, g->num_ctas))
+      if ((int64_t)P * G > 2048)
+        return fail(MK_ERR_LIMIT, "mk_add_attention: more than 2048 / (Hq/Hkv) chunks per sequence");
+  }
   int64_t need = 0;
   CHECK(mk_attention_scratch_rows(g, B, Hkv, len0, chunk, &need));
   CHECK(check_buf(g, scratch, MK_F32, -1, (int64_t)G * (D + 2), "mk_add_attention scratch"));
@@ -410,7 +424,8 @@ extern "C" int mk_lower(mk_graph* g) {
             L.emit(d,
                    {{qkv, s, s + 1, kcol, kcol + D}, {qkv, s, s + 1, vcol, vcol + D},
                     {(int)MK_BUF_STATE, s, s + 1, 0, 2}},
-                   {{kc, row, row + 1, 0, cacheCols}, {vc, row, row + 1, 0, cacheCols}}, kTaskOverhead);
+                   {{kc, row, row + 1, cacheCols, cacheCols + D}, {vc, row, row + 1, cacheCols, cacheCols + D}},
+                   kTaskOverhead);
           }
         g->group_off.push_back((int)g->tasks.size());
         for (int s = 0; s < B; ++s)
@@ -428,6 +443,8 @@ extern "C" int mk_lower(mk_graph* g) {
               const int64_t slot = base[s * Hkv + gg] + c;
               L.emit(d,
                      {{qkv, s, s + 1, (int64_t)gg * G * D, (int64_t)(gg + 1) * G * D},
+                      {qkv, s, s + 1, (int64_t)Hq * D + gg * D, (int64_t)Hq * D + (gg + 1) * D},
+                      {qkv, s, s + 1, (int64_t)(Hq + Hkv) * D + gg * D, (int64_t)(Hq + Hkv) * D + (gg + 1) * D},
                       {kc, row, row + 1, 0, cacheCols}, {vc, row, row + 1, 0, cacheCols},
                       {(int)MK_BUF_STATE, s, s + 1, 0, 2}},
                      {{scr, slot, slot + 1, 0, (int64_t)G * (D + 2)}},
@@ -440,12 +457,18 @@ extern "C" int mk_lower(mk_graph* g) {
             mk_task_descriptor d = blank(MK_OP_ATTENTION_COMBINE);
             common(d);
             d.in_buf[0] = scr;
+            d.in_buf[1] = kc;
+            d.in_buf[2] = vc;
             d.out_buf = out;
             d.reserved[0] = s; d.reserved[1] = gg; d.reserved[2] = Hkv;
             d.reserved[3] = P[s];
             d.reserved[4] = base[s * Hkv + gg];
             const int64_t b0 = base[s * Hkv + gg];
-            L.emit(d, {{scr, b0, b0 + P[s], 0, (int64_t)G * (D + 2)}},
+            const int64_t row = (int64_t)s * Hkv + gg;
+            L.emit(d,
+                   {{scr, b0, b0 + P[s], 0, (int64_t)G * (D + 2)},
+                    {kc, row, row + 1, cacheCols, cacheCols + D},
+                    {vc, row, row + 1, cacheCols, cacheCols + D}},
                    {{out, s, s + 1, (int64_t)gg * G * D, (int64_t)(gg + 1) * G * D}}, kTaskOverhead);
           }
         break;

@@ -39,7 +39,7 @@ struct KParams {
   int32_t* status;            // int32[4]
   const float* rope_cos;      // [cap, D/2]
   const float* rope_sin;
-  uint64_t* trace;            // 4 x uint64 per task, or null
+  uint64_t* trace;            // 8 x uint64 per task, or null
   uint64_t timeout_ns;
   uint32_t epoch;             // 1-based step counter (counter target = epoch * deps)
   int32_t mode;               // MK_MODE_MEGA / PER_OP / LEVELS

@@ -151,7 +151,7 @@ __device__ __forceinline__ void gemv_geom(const mk_task_descriptor& d, GemvGeom&
     int wcol = 1;
     while (wcol < 8 && (uk % (wcol * 2)) == 0) wcol *= 2;
     const int nv = uk / wcol;
-    if (g.BT == 1 ? nv > 4 : nv > 1) continue;
+    if (g.BT == 1 ? (nv == 3 || nv == 5 || nv == 6 || nv > 7) : nv > 1) continue;
     g.KS = uk * 256; g.nks = q; g.WCOL = wcol; g.WROW = 8 / wcol; g.NV = nv;
     break;
   }
@@ -281,14 +281,23 @@ struct Ctx {
   uint64_t* full;
   uint64_t* empty;
   float* scratch;
-  uint32_t stage;
+  uint32_t stage;     // next ring slot to wait for (consume_begin)
+  uint32_t released;  // next ring slot to hand back (consume_end)
   int nst;
   int task;
+  uint64_t mark[3];  // optional trace marks inside a task body (thread 0)
 };
 
+__device__ __forceinline__ void trace_mark(Ctx& c, int i) {
+  if (c.p->trace && threadIdx.x == 0) c.mark[i] = globaltimer();
+}
+
 // Lane 0 waits for the slot, the warp then reads it.
+// Slots are waited for and handed back in order; a consumer may wait for
+// the next slot before handing back the current one.
 __device__ __forceinline__ uint32_t consume_begin(Ctx& c) {
   const uint32_t slot = c.stage % c.nst, ph = (c.stage / c.nst) & 1u;
+  ++c.stage;
   if ((threadIdx.x & 31) == 0) bar_wait(*c.p, &c.full[slot], ph, c.task, true);
   __syncwarp();
   return slot;
@@ -297,7 +306,7 @@ __device__ __forceinline__ uint32_t consume_begin(Ctx& c) {
 __device__ __forceinline__ void consume_end(Ctx& c, uint32_t slot) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(&c.empty[slot]);
-  ++c.stage;
+  ++c.released;
 }
 
 __device__ __forceinline__ void cbar() { named_bar_sync(1, kConsumerThreads); }
@@ -346,10 +355,21 @@ __device__ void block_argmax(float& v, int& idx, float* red) {
 }
 
 // ------------------------------------------------------------------ GEMV body
-// x (times gamma when normalising) for this lane's columns col0 + v*256 + [0,8).
+// Shared-memory scratch of a GEMV task: per-(row, batch, warp column) slots,
+// per-(row, batch) accumulators, then a small reduction area:
+//   red[0,64) sum-of-squares partials, red[64,72) 1/rms per batch row,
+//   red[80,96) argmax scratch, red[96,104) tile max, red[104,112) tile argmax.
+__device__ __forceinline__ float* gemv_slots(Ctx& c) { return c.scratch; }
+__device__ __forceinline__ float* gemv_acc(Ctx& c) { return c.scratch + kSlotFloats; }
+__device__ __forceinline__ float* gemv_red(Ctx& c) { return c.scratch + kSlotFloats + kAccFloats; }
+
+// x (times gamma when normalising) for this lane's columns col0 + v*256 + [0,8),
+// and the sum of squares of the raw x values loaded (for the RMS norm).
 template <int B, int NV>
-__device__ __forceinline__ void gemv_load_x(float (&xr)[B][NV][8], const float* __restrict__ x,
+__device__ __forceinline__ void gemv_load_x(float (&xr)[B][NV][8], float (&ss)[B], const float* __restrict__ x,
                                             const uint16_t* __restrict__ gamma, int K, int col0, int Bact) {
+#pragma unroll
+  for (int b = 0; b < B; ++b) ss[b] = 0.f;
 #pragma unroll
   for (int v = 0; v < NV; ++v) {
     const int col = col0 + v * 256;
@@ -369,170 +389,252 @@ __device__ __forceinline__ void gemv_load_x(float (&xr)[B][NV][8], const float* 
         a = __ldcg(reinterpret_cast<const float4*>(x + (size_t)b * K + col));
         e = __ldcg(reinterpret_cast<const float4*>(x + (size_t)b * K + col + 4));
       }
+      ss[b] += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + e.x * e.x + e.y * e.y + e.z * e.z + e.w * e.w;
       xr[b][v][0] = a.x * gm[0]; xr[b][v][1] = a.y * gm[1]; xr[b][v][2] = a.z * gm[2]; xr[b][v][3] = a.w * gm[3];
       xr[b][v][4] = e.x * gm[4]; xr[b][v][5] = e.y * gm[5]; xr[b][v][6] = e.z * gm[6]; xr[b][v][7] = e.w * gm[7];
     }
   }
 }
 
-template <int B, int NV>
-__device__ void gemv_body(Ctx& c, const mk_task_descriptor& d, const GemvGeom& G) {
-  const KParams& p = *c.p;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const float* x = static_cast<const float*>(p.bufs[d.in_buf[0]]);
-  float* out = static_cast<float*>(p.bufs[d.out_buf]);
-  const bool rms = d.flags & MK_F_RMS_NORM_INPUT;
-  const bool silu = d.flags & MK_F_SILU_MUL;
-  const bool argmax = d.flags & MK_F_ARGMAX_EPI;
-  const uint16_t* gamma = rms ? static_cast<const uint16_t*>(p.bufs[d.in_buf[2]]) : nullptr;
-  const float* res = (d.flags & MK_F_ADD_RESIDUAL) ? static_cast<const float*>(p.bufs[d.in_buf[2]]) : nullptr;
-  float* slots = c.scratch;
-  float* acc = slots + kSlotFloats;
-  float* red = acc + kAccFloats;  // [0,64) sumsq partials, [64,72) inv_rms, [80,96) argmax, [96,112) tile best
-  const int K = G.K;
-  const int wcol = warp % G.WCOL, wrow = warp / G.WCOL;
-  const int colw = G.KS / G.WCOL;
-
-  // 1 / rms(x) per batch row (applied in the epilogue: W (x*gamma) * inv)
-  if (rms) {
-    float ss[B];
-#pragma unroll
-    for (int b = 0; b < B; ++b) {
-      float a = 0.f;
-      if (b < G.B)
-        for (int i = tid * 4; i < K; i += kConsumerThreads * 4) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(x + (size_t)b * K + i));
-        a += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-      }
-      ss[b] = warp_sum(a);
-    }
-    if (lane == 0) {
-#pragma unroll
-      for (int b = 0; b < B; ++b) red[warp * 8 + b] = ss[b];
-    }
-    cbar();
-    if (tid < G.B) {
-      float t = 0.f;
-      for (int w = 0; w < kConsumerWarps; ++w) t += red[w * 8 + tid];
-      const float eps = __uint_as_float(d.reserved[2]);
-      red[64 + tid] = 1.0f / sqrtf(t / (float)K + eps);
-    }
-  }
-  if (argmax && tid < G.B) {
+// The tile's running argmax, and 1/rms = 1 when the input is not
+// normalised (a normalised input gets it from gemv_fold).  Once per task.
+__device__ __noinline__ void gemv_prologue(const mk_task_descriptor& d, const GemvGeom& G, float* red) {
+  const int tid = threadIdx.x;
+  if (!(d.flags & MK_F_RMS_NORM_INPUT) && tid < G.B) red[64 + tid] = 1.f;
+  if ((d.flags & MK_F_ARGMAX_EPI) && tid < G.B) {
     red[96 + tid] = -FLT_MAX;
     reinterpret_cast<int*>(red)[104 + tid] = INT_MAX;
   }
+}
 
-  float xr[B][NV][8];
-  const int xcol0 = wcol * colw + lane * 8;
-  if (G.nks == 1) gemv_load_x<B, NV>(xr, x, gamma, K, xcol0, G.B);
-
-  for (int g0 = 0; g0 < G.cn; g0 += G.RG) {
-    const int rows_g = min(G.RG, G.cn - g0);
-    for (int ks = 0; ks < G.nks; ++ks) {
-      if (G.nks > 1) gemv_load_x<B, NV>(xr, x, gamma, K, ks * G.KS + xcol0, G.B);
-      for (int sg = 0; sg < G.seg; ++sg) {
-        for (int r0 = 0; r0 < rows_g; r0 += G.rs) {
-          const int nr = min(G.rs, rows_g - r0);
-          const uint32_t slot = consume_begin(c);
-          const uint32_t base = smem_addr(c.ring + (size_t)slot * kStageBytes) + (wcol * colw + lane * 8) * 2;
-          for (int rho = wrow; rho < nr; rho += G.WROW) {
-            float part[B];
+// Sum N values (N a power of two, at most 32) across the warp.  Afterwards
+// lane l holds the warp-wide sum of value l >> (5 - log2 N); the first
+// log2 N steps halve the values each lane carries, the rest are butterflies.
+template <int N>
+__device__ __forceinline__ float transpose_reduce(float (&v)[N], int lane) {
+  static_assert(N >= 1 && N <= 32 && (N & (N - 1)) == 0, "N must be a power of two <= 32");
 #pragma unroll
-            for (int b = 0; b < B; ++b) part[b] = 0.f;
-            const uint32_t ra = base + (uint32_t)rho * G.KS * 2;
+  for (int t = 0; t < 5; ++t) {
+    const int o = 16 >> t;
+    const int n = N >> t;  // values each lane still carries (a constant once unrolled)
+    if (n > 1) {
+      const bool up = (lane & o) != 0;
 #pragma unroll
-            for (int v = 0; v < NV; ++v) {
-              const uint4 w = lds128(ra + v * 512);
-              float wf[8];
-              wf[0] = bf_lo(w.x); wf[1] = bf_hi(w.x); wf[2] = bf_lo(w.y); wf[3] = bf_hi(w.y);
-              wf[4] = bf_lo(w.z); wf[5] = bf_hi(w.z); wf[6] = bf_lo(w.w); wf[7] = bf_hi(w.w);
-#pragma unroll
-              for (int b = 0; b < B; ++b)
-#pragma unroll
-                for (int k = 0; k < 8; ++k) part[b] = fmaf(wf[k], xr[b][v][k], part[b]);
-            }
-#pragma unroll
-            for (int b = 0; b < B; ++b) part[b] = warp_sum(part[b]);
-            if (lane == 0) {
-              const int row = sg * rows_g + r0 + rho;
-#pragma unroll
-              for (int b = 0; b < B; ++b) slots[(row * B + b) * G.WCOL + wcol] = part[b];
-            }
-          }
-          consume_end(c, slot);
-        }
+      for (int i = 0; i < n / 2; ++i) {
+        const float send = up ? v[i] : v[i + n / 2];
+        const float keep = up ? v[i + n / 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
       }
-      // fold this k-segment's per-warp partials, in a fixed order
-      cbar();
-      for (int i = tid; i < G.seg * rows_g * B; i += kConsumerThreads) {
-        float s = 0.f;
-        for (int w = 0; w < G.WCOL; ++w) s += slots[i * G.WCOL + w];
-        acc[i] = (ks == 0) ? s : acc[i] + s;
-      }
-      cbar();
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
     }
-    // epilogue: normalisation scale, SiLU*mul, residual, store, argmax
-    for (int b = 0; b < G.B; ++b) {
-      const float inv = rms ? red[64 + b] : 1.f;
-      float bv = -FLT_MAX;
-      int bi = INT_MAX;
-      for (int j = tid; j < rows_g; j += kConsumerThreads) {
-        float y = acc[j * B + b] * inv;
-        if (silu) {
-          const float u = acc[(rows_g + j) * B + b] * inv;
-          y = y / (1.0f + expf(-y)) * u;
-        }
-        const int col = G.c0 + g0 + j;
-        if (res) y += __ldcg(res + (size_t)b * G.n + col);
-        out[(size_t)b * G.n + col] = y;
-        if (y > bv) {
-          bv = y;
-          bi = col;
-        }
-      }
-      if (argmax) {
-        block_argmax(bv, bi, red + 80);
-        if (tid == 0) {
-          const float cv = red[96 + b];
-          const int ci = reinterpret_cast<int*>(red)[104 + b];
-          if (bv > cv || (bv == cv && bi < ci)) {
-            red[96 + b] = bv;
-            reinterpret_cast<int*>(red)[104 + b] = bi;
-          }
-        }
-      }
-    }
-    cbar();
   }
-  if (argmax && tid < G.B) {
-    mk_argmax_pair* pairs = static_cast<mk_argmax_pair*>(p.bufs[d.reserved[3]]);
-    mk_argmax_pair pr;
-    pr.value = red[96 + tid];
-    pr.index = reinterpret_cast<int*>(red)[104 + tid];
-    pairs[(size_t)d.reserved[4] * G.B + tid] = pr;
+  return v[0];
+}
+
+// bf16 weights of one slot for this lane: rows wrow + r * WROW (r < RWM),
+// vectors v < NV of 8 elements.
+template <int RWM, int NV>
+__device__ __forceinline__ void gemv_load_slot(uint4 (&w)[RWM][NV], uint32_t base, int rw, int WROW, int KS) {
+#pragma unroll
+  for (int r = 0; r < RWM; ++r) {
+    const uint32_t ra = base + (uint32_t)(r * WROW) * KS * 2;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) w[r][v] = r < rw ? lds128(ra + v * 512) : make_uint4(0u, 0u, 0u, 0u);
   }
 }
 
-// Batch class 0 serves B <= 2, class 1 serves 3 <= B <= 8; each class is its
-// own kernel so its register allocation is not shared with the other's.
+// Segment and first row of slot sidx, and the rows of it this warp takes.
+__device__ __forceinline__ int gemv_slot_rows(int sidx, int nstg, int rs, int rows_g, int wrow, int WROW, int& sg,
+                                              int& r0) {
+  sg = sidx / nstg;
+  r0 = (sidx - sg * nstg) * rs;
+  const int nr = min(rs, rows_g - r0);
+  return nr > wrow ? (nr - wrow + WROW - 1) / WROW : 0;
+}
+
+// Every ring slot of one (row group, k-segment).  A warp takes rows
+// wrow, wrow + WROW, ... of each slot over its column block, with x in
+// registers: all shared loads of a slot first, independent FMA chains per
+// row, then one transposed reduction of the slot's (row, batch) sums.
+// Results go to slots[(row, b, warp column)].
+template <int B, int NV>
+__device__ __forceinline__ void gemv_stages(Ctx& c, const mk_task_descriptor& d, const GemvGeom& G, int rows_g,
+                                            int ks, bool first_group) {
+  const KParams& p = *c.p;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int wcol = warp % G.WCOL, wrow = warp / G.WCOL;
+  const int colw = G.KS / G.WCOL;
+  const float* x = static_cast<const float*>(p.bufs[d.in_buf[0]]);
+  const uint16_t* gamma =
+      (d.flags & MK_F_RMS_NORM_INPUT) ? static_cast<const uint16_t*>(p.bufs[d.in_buf[2]]) : nullptr;
+  float* slots = gemv_slots(c);
+  float xr[B][NV][8], ss[B];
+  gemv_load_x<B, NV>(xr, ss, x, gamma, G.K, ks * G.KS + wcol * colw + lane * 8, G.B);
+  if (gamma && first_group) {
+    // sum of squares of x over this warp's columns; warps of the first warp
+    // row cover every column once (the others contribute zero)
+    float* red = gemv_red(c);
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      const float t = warp_sum(wrow == 0 ? ss[b] : 0.f);
+      if (lane == 0 && b < 8) red[warp * 8 + b] = (ks == 0 ? 0.f : red[warp * 8 + b]) + t;
+    }
+  }
+  constexpr int RWM = 8 / NV;                // most rows a warp takes from one full slot
+  constexpr int VPS = RWM * B;               // (row, batch) sums per slot
+  constexpr int NR = VPS > 32 ? 32 : VPS;    // values per transposed reduction
+  constexpr int SH = NR >= 32 ? 0 : (NR >= 16 ? 1 : (NR >= 8 ? 2 : (NR >= 4 ? 3 : (NR >= 2 ? 4 : 5))));
+  for (int sg = 0; sg < G.seg; ++sg) {
+    for (int r0 = 0; r0 < rows_g; r0 += G.rs) {
+      const int nr = min(G.rs, rows_g - r0);
+      const uint32_t slot = consume_begin(c);
+      if (first_group && ks == 0 && sg == 0 && r0 == 0) trace_mark(c, 0);
+      const uint32_t base = smem_addr(c.ring + (size_t)slot * kStageBytes) + (wcol * colw + lane * 8) * 2;
+      const int rw = nr > wrow ? (nr - wrow + G.WROW - 1) / G.WROW : 0;
+      uint4 w[RWM][NV];
+#pragma unroll
+      for (int r = 0; r < RWM; ++r) {
+        const uint32_t ra = base + (uint32_t)(wrow + r * G.WROW) * G.KS * 2;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) w[r][v] = r < rw ? lds128(ra + v * 512) : make_uint4(0u, 0u, 0u, 0u);
+      }
+      float acc[VPS];
+#pragma unroll
+      for (int i = 0; i < VPS; ++i) acc[i] = 0.f;
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+#pragma unroll
+        for (int k2 = 0; k2 < 4; ++k2) {
+#pragma unroll
+          for (int r = 0; r < RWM; ++r) {
+            const uint32_t u = k2 == 0 ? w[r][v].x : k2 == 1 ? w[r][v].y : k2 == 2 ? w[r][v].z : w[r][v].w;
+            const float lo = bf_lo(u), hi = bf_hi(u);
+#pragma unroll
+            for (int b = 0; b < B; ++b) {
+              acc[r * B + b] = fmaf(lo, xr[b][v][2 * k2], acc[r * B + b]);
+              acc[r * B + b] = fmaf(hi, xr[b][v][2 * k2 + 1], acc[r * B + b]);
+            }
+          }
+        }
+      }
+      consume_end(c, slot);
+#pragma unroll
+      for (int h = 0; h < VPS / NR; ++h) {
+        float vv[NR];
+#pragma unroll
+        for (int i = 0; i < NR; ++i) vv[i] = acc[h * NR + i];
+        const float tot = transpose_reduce<NR>(vv, lane);
+        if ((lane & ((1 << SH) - 1)) == 0) {
+          const int i = h * NR + (lane >> SH);
+          const int r = i / B, b = i % B;
+          if (r < rw) {
+            const int row = sg * rows_g + r0 + wrow + r * G.WROW;
+            slots[(row * B + b) * G.WCOL + wcol] = tot;
+          }
+        }
+      }
+    }
+  }
+}
+
+// Fold one k-segment's per-warp partials into the accumulators, in a fixed
+// order (deterministic; no float atomics).
+__device__ __noinline__ void gemv_fold(const mk_task_descriptor& d, const GemvGeom& G, int rows_g, int ks,
+                                       bool first_group, float* slots, float* acc, float* red) {
+  cbar();
+  for (int i = threadIdx.x; i < G.seg * rows_g * G.BT; i += kConsumerThreads) {
+    float s = 0.f;
+    for (int w = 0; w < G.WCOL; ++w) s += slots[i * G.WCOL + w];
+    acc[i] = (ks == 0) ? s : acc[i] + s;
+  }
+  if ((d.flags & MK_F_RMS_NORM_INPUT) && first_group && ks == G.nks - 1 && threadIdx.x < G.B) {
+    float t = 0.f;
+    for (int w = 0; w < kConsumerWarps; ++w) t += red[w * 8 + threadIdx.x];
+    red[64 + threadIdx.x] = 1.0f / sqrtf(t / (float)G.K + __uint_as_float(d.reserved[2]));
+  }
+  cbar();
+}
+
+// Epilogue of one row group: normalisation scale, SiLU*mul, residual,
+// store, and the tile's running argmax.
+__device__ __noinline__ void gemv_epilogue(const KParams& p, const mk_task_descriptor& d, const GemvGeom& G,
+                                           int g0, int rows_g, const float* acc, float* red) {
+  const int tid = threadIdx.x;
+  float* out = static_cast<float*>(p.bufs[d.out_buf]);
+  const bool silu = d.flags & MK_F_SILU_MUL;
+  const bool argmax = d.flags & MK_F_ARGMAX_EPI;
+  const float* res = (d.flags & MK_F_ADD_RESIDUAL) ? static_cast<const float*>(p.bufs[d.in_buf[2]]) : nullptr;
+  const int BT = G.BT;
+  for (int b = 0; b < G.B; ++b) {
+    const float inv = red[64 + b];
+    float bv = -FLT_MAX;
+    int bi = INT_MAX;
+    for (int j = tid; j < rows_g; j += kConsumerThreads) {
+      float y = acc[j * BT + b] * inv;
+      if (silu) {
+        const float u = acc[(rows_g + j) * BT + b] * inv;
+        y = y / (1.0f + expf(-y)) * u;
+      }
+      const int col = G.c0 + g0 + j;
+      if (res) y += __ldcg(res + (size_t)b * G.n + col);
+      out[(size_t)b * G.n + col] = y;
+      if (y > bv) {
+        bv = y;
+        bi = col;
+      }
+    }
+    if (argmax) {
+      block_argmax(bv, bi, red + 80);
+      if (tid == 0) {
+        const float cv = red[96 + b];
+        const int ci = reinterpret_cast<int*>(red)[104 + b];
+        if (bv > cv || (bv == cv && bi < ci)) {
+          red[96 + b] = bv;
+          reinterpret_cast<int*>(red)[104 + b] = bi;
+        }
+      }
+    }
+  }
+  cbar();
+}
+
+// Batch class 0 serves B <= 2, class 1 serves B <= 4, class 2 serves B <= 8;
+// each class is its own kernel so register allocations are not shared.
 template <int BCLASS>
 __device__ void gemv_task(Ctx& c, const mk_task_descriptor& d) {
   GemvGeom G;
   gemv_geom(d, G);
-  if constexpr (BCLASS == 0) {
-    switch (G.BT * 16 + G.NV) {
-      case 16 + 1: gemv_body<1, 1>(c, d, G); break;
-      case 16 + 2: gemv_body<1, 2>(c, d, G); break;
-      case 16 + 3: gemv_body<1, 3>(c, d, G); break;
-      case 16 + 4: gemv_body<1, 4>(c, d, G); break;
-      case 32 + 1: gemv_body<2, 1>(c, d, G); break;
+  float* red = gemv_red(c);
+  gemv_prologue(d, G, red);
+  for (int g0 = 0; g0 < G.cn; g0 += G.RG) {
+    const int rows_g = min(G.RG, G.cn - g0);
+    for (int ks = 0; ks < G.nks; ++ks) {
+      if constexpr (BCLASS == 0) {
+        switch (G.BT * 16 + G.NV) {
+          case 16 + 1: gemv_stages<1, 1>(c, d, G, rows_g, ks, g0 == 0); break;
+          case 16 + 2: gemv_stages<1, 2>(c, d, G, rows_g, ks, g0 == 0); break;
+          case 16 + 4: gemv_stages<1, 4>(c, d, G, rows_g, ks, g0 == 0); break;
+          case 16 + 7: gemv_stages<1, 7>(c, d, G, rows_g, ks, g0 == 0); break;
+          default: gemv_stages<2, 1>(c, d, G, rows_g, ks, g0 == 0); break;
+        }
+      } else if constexpr (BCLASS == 1) {
+        gemv_stages<4, 1>(c, d, G, rows_g, ks, g0 == 0);
+      } else {
+        gemv_stages<8, 1>(c, d, G, rows_g, ks, g0 == 0);
+      }
+      gemv_fold(d, G, rows_g, ks, g0 == 0, gemv_slots(c), gemv_acc(c), red);
     }
-  } else {
-    switch (G.BT * 16 + G.NV) {
-      case 64 + 1: gemv_body<4, 1>(c, d, G); break;
-      case 128 + 1: gemv_body<8, 1>(c, d, G); break;
-    }
+    trace_mark(c, 1);
+    gemv_epilogue(*c.p, d, G, g0, rows_g, gemv_acc(c), red);
+    trace_mark(c, 2);
+  }
+  if ((d.flags & MK_F_ARGMAX_EPI) && threadIdx.x < G.B) {
+    mk_argmax_pair* pairs = static_cast<mk_argmax_pair*>(c.p->bufs[d.reserved[3]]);
+    mk_argmax_pair pr;
+    pr.value = red[96 + threadIdx.x];
+    pr.index = reinterpret_cast<int*>(red)[104 + threadIdx.x];
+    pairs[(size_t)d.reserved[4] * G.B + threadIdx.x] = pr;
   }
 }
 
@@ -563,25 +665,67 @@ __device__ void append_task(Ctx& c, const mk_task_descriptor& d) {
   if (t < D) Vc[row + t] = __float2bfloat16_rn(__ldcg(qkv + (Hq + Hkv) * D + g * D + t));
 }
 
-// One key of the online softmax for the G heads of a KV group.
-template <int DPL, int MAXG>
-__device__ __forceinline__ void partial_step(const float (&qr)[MAXG][DPL], float (&o)[MAXG][DPL], float (&m)[MAXG],
-                                             float (&l)[MAXG], const float (&kf)[DPL], const float (&vf)[DPL],
-                                             int G) {
+// Sum 32 per-lane values across the warp, transposed: afterwards lane l
+// holds the warp-wide sum of value l (31 shuffles instead of 32 x 5).
+__device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
 #pragma unroll
-  for (int h = 0; h < MAXG; ++h) {
-    if (h < G) {
+  for (int o = 16; o > 0; o >>= 1) {
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = up ? v[i] : v[i + o];
+      const float keep = up ? v[i + o] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  return v[0];
+}
+
+// Eight keys of the online softmax for the (up to 4) query heads of a KV
+// group, base 2.  kf/vf: this lane's DPL dims of each key and value; nvalid
+// keys are real.  m/l/o are kept identical in every lane of the warp.
+template <int DPL>
+__device__ __forceinline__ void partial_group(const float (&qr)[4][DPL], float (&o)[4][DPL], float (&m)[4],
+                                              float (&l)[4], const float (&kf)[8][DPL], const float (&vf)[8][DPL],
+                                              int nvalid, int G, int lane) {
+  float v[32];
+#pragma unroll
+  for (int h = 0; h < 4; ++h)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
       float sc = 0.f;
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) sc = fmaf(qr[h][e], kf[e], sc);
-      sc = warp_sum(sc);
-      const float mn = fmaxf(m[h], sc);
-      const float a = exp2f(m[h] - mn);
-      const float pe = exp2f(sc - mn);
-      l[h] = l[h] * a + pe;
+      for (int e = 0; e < DPL; ++e) sc = fmaf(qr[h][e], kf[j][e], sc);
+      v[h * 8 + j] = sc;
+    }
+  const int hl = lane >> 3, jl = lane & 7;  // this lane's (head, key) after the reduce
+  float val = transpose_reduce32(v, lane);
+  const bool live = jl < nvalid && hl < G;
+  float gmax = live ? val : -INFINITY;
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) o[h][e] = fmaf(o[h][e], a, pe * vf[e]);
-      m[h] = mn;
+  for (int off = 1; off < 8; off <<= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, off));
+  const float mold = hl == 0 ? m[0] : hl == 1 ? m[1] : hl == 2 ? m[2] : m[3];
+  const float mnew = fmaxf(mold, gmax);
+  const float pr = live ? exp2f(val - mnew) : 0.f;
+  float psum = pr;
+#pragma unroll
+  for (int off = 1; off < 8; off <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    if (h < G) {
+      const float mh = __shfl_sync(0xffffffffu, mnew, h * 8);
+      const float ph = __shfl_sync(0xffffffffu, psum, h * 8);
+      const float a = exp2f(m[h] - mh);
+      l[h] = fmaf(l[h], a, ph);
+      m[h] = mh;
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) o[h][e] *= a;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float pj = __shfl_sync(0xffffffffu, pr, h * 8 + j);
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) o[h][e] = fmaf(pj, vf[j][e], o[h][e]);
+      }
     }
   }
 }
@@ -622,42 +766,61 @@ __device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom
       o[h][e] = 0.f;
     }
   }
-  const int kpw = q.R / kConsumerWarps;  // keys per warp per slot
+  const int kpw = q.R / kConsumerWarps;  // keys per warp per slot (a multiple of 8)
   for (int i = 0; i < q.nstage; ++i) {
     const int nr = min(q.R, q.jst - (q.j0 + i * q.R));
     const uint32_t slot = consume_begin(c);
+    if (i == 0) trace_mark(c, 0);
     const uint32_t kb = smem_addr(c.ring + (size_t)slot * kStageBytes);
     const uint32_t vb = kb + kStageBytes / 2;
-    const int k0 = warp * kpw, k1 = min(nr, k0 + kpw);
-    for (int kk = k0; kk < k1; ++kk) {
-      float kf[DPL], vf[DPL];
-      const uint32_t off = (uint32_t)(kk * D + lane * DPL) * 2;
-      if constexpr (DPL == 4) {
-        const uint2 kv = lds64(kb + off), vv = lds64(vb + off);
-        kf[0] = bf_lo(kv.x); kf[1] = bf_hi(kv.x); kf[2] = bf_lo(kv.y); kf[3] = bf_hi(kv.y);
-        vf[0] = bf_lo(vv.x); vf[1] = bf_hi(vv.x); vf[2] = bf_lo(vv.y); vf[3] = bf_hi(vv.y);
-      } else {
-        const uint32_t kv = lds32(kb + off), vv = lds32(vb + off);
-        kf[0] = bf_lo(kv); kf[1] = bf_hi(kv);
-        vf[0] = bf_lo(vv); vf[1] = bf_hi(vv);
+    for (int k0 = warp * kpw; k0 < min(nr, (warp + 1) * kpw); k0 += 8) {
+      const int nvalid = min(8, nr - k0);
+      float kf[8][DPL], vf[8][DPL];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t off = (uint32_t)((k0 + (j < nvalid ? j : 0)) * D + lane * DPL) * 2;
+        if constexpr (DPL == 4) {
+          const uint2 kv = lds64(kb + off), vv = lds64(vb + off);
+          kf[j][0] = bf_lo(kv.x); kf[j][1] = bf_hi(kv.x); kf[j][2] = bf_lo(kv.y); kf[j][3] = bf_hi(kv.y);
+          vf[j][0] = bf_lo(vv.x); vf[j][1] = bf_hi(vv.x); vf[j][2] = bf_lo(vv.y); vf[j][3] = bf_hi(vv.y);
+        } else {
+          const uint32_t kv = lds32(kb + off), vv = lds32(vb + off);
+          kf[j][0] = bf_lo(kv); kf[j][1] = bf_hi(kv);
+          vf[j][0] = bf_lo(vv); vf[j][1] = bf_hi(vv);
+        }
       }
-      partial_step<DPL, MAXG>(qr, o, m, l, kf, vf, G);
+      partial_group<DPL>(qr, o, m, l, kf, vf, nvalid, G, lane);
     }
     consume_end(c, slot);
   }
   if (q.has_new && warp == kConsumerWarps - 1) {
-    // the row appended this step: generic (L2) loads after the dependency wait
-    const size_t row = (((size_t)q.s * q.Hkv + q.g) * q.cap + q.pos) * D + lane * DPL;
-    const uint16_t* Kc = static_cast<const uint16_t*>(p.bufs[d.in_buf[1]]);
-    const uint16_t* Vc = static_cast<const uint16_t*>(p.bufs[d.in_buf[2]]);
-    float kf[DPL], vf[DPL];
+    // the key/value of the token at pos come straight from qkv, rotated and
+    // rounded to bf16 exactly as ATTENTION_APPEND stores them, so this task
+    // does not wait for the append
+    const float* kq = qkv + (size_t)q.Hq * D + (size_t)q.g * D;
+    const float* vq = qkv + (size_t)(q.Hq + q.Hkv) * D + (size_t)q.g * D;
+    float kf[8][DPL], vf[8][DPL];
 #pragma unroll
     for (int e = 0; e < DPL; ++e) {
-      kf[e] = __uint_as_float((uint32_t)__ldcg(reinterpret_cast<const unsigned short*>(Kc + row + e)) << 16);
-      vf[e] = __uint_as_float((uint32_t)__ldcg(reinterpret_cast<const unsigned short*>(Vc + row + e)) << 16);
+      const int dd = lane * DPL + e;
+      const int jj = dd < half ? dd : dd - half;
+      const float cs = p.rope_cos[(size_t)q.pos * p.rope_half + jj];
+      const float sn = p.rope_sin[(size_t)q.pos * p.rope_half + jj];
+      const float k1 = __ldcg(kq + jj), k2 = __ldcg(kq + jj + half);
+      const float kr = dd < half ? k1 * cs - k2 * sn : k2 * cs + k1 * sn;
+      kf[0][e] = __bfloat162float(__float2bfloat16_rn(kr));
+      vf[0][e] = __bfloat162float(__float2bfloat16_rn(__ldcg(vq + dd)));
     }
-    partial_step<DPL, MAXG>(qr, o, m, l, kf, vf, G);
+#pragma unroll
+    for (int j = 1; j < 8; ++j)
+#pragma unroll
+      for (int e = 0; e < DPL; ++e) {
+        kf[j][e] = kf[0][e];
+        vf[j][e] = vf[0][e];
+      }
+    partial_group<DPL>(qr, o, m, l, kf, vf, 1, G, lane);
   }
+  trace_mark(c, 1);
   // merge the 8 warps' states
 #pragma unroll
   for (int h = 0; h < MAXG; ++h) {
@@ -705,23 +868,42 @@ __device__ void partial_task(Ctx& c, const mk_task_descriptor& d) {
   else partial_body<2>(c, d, q);
 }
 
+// Log-sum-exp merge of the P partials of one (sequence, kv head), as a
+// running merge: every partial's (m, l, o) is loaded up front (independent
+// loads, one L2 round trip) and folded in with a running maximum.  Empty
+// partials (m = -inf) contribute nothing.
 __device__ void combine_task(Ctx& c, const mk_task_descriptor& d) {
   const KParams& p = *c.p;
   const int s = d.reserved[0], g = d.reserved[1], Hkv = d.reserved[2];
   const int P = d.reserved[3], base = d.reserved[4];
   const int D = d.n, Hq = d.k, G = Hq / Hkv;
-  const float* scr = static_cast<const float*>(p.bufs[d.in_buf[0]]);
+  const int rec = G * (D + 2);
+  const float* scr = static_cast<const float*>(p.bufs[d.in_buf[0]]) + (size_t)base * rec;
   float* out = static_cast<float*>(p.bufs[d.out_buf]);
   for (int i = threadIdx.x; i < G * D; i += kConsumerThreads) {
     const int h = i / D, e = i % D;
-    float M = -INFINITY;
-    for (int k = 0; k < P; ++k) M = fmaxf(M, __ldcg(scr + (size_t)(base + k) * G * (D + 2) + h * (D + 2)));
-    float Ls = 0.f, O = 0.f;
-    for (int k = 0; k < P; ++k) {
-      const float* r = scr + (size_t)(base + k) * G * (D + 2) + h * (D + 2);
-      const float f = exp2f(__ldcg(r) - M);
-      Ls = fmaf(__ldcg(r + 1), f, Ls);
-      O = fmaf(__ldcg(r + 2 + e), f, O);
+    const float* r = scr + h * (D + 2);
+    float M = -INFINITY, Ls = 0.f, O = 0.f;
+    for (int k0 = 0; k0 < P; k0 += 4) {
+      float mv[4], lv[4], ov[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const bool ok = k0 + j < P;
+        const float* rr = r + (size_t)(k0 + j) * rec;
+        mv[j] = ok ? __ldcg(rr) : -INFINITY;
+        lv[j] = ok ? __ldcg(rr + 1) : 0.f;
+        ov[j] = ok ? __ldcg(rr + 2 + e) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (mv[j] != -INFINITY) {
+          const float Mn = fmaxf(M, mv[j]);
+          const float a = exp2f(M - Mn), b = exp2f(mv[j] - Mn);
+          Ls = fmaf(Ls, a, lv[j] * b);
+          O = fmaf(O, a, ov[j] * b);
+          M = Mn;
+        }
+      }
     }
     out[(size_t)s * Hq * D + (size_t)(g * G + h) * D + e] = O / Ls;
   }
@@ -818,13 +1000,14 @@ __device__ bool level_barrier(const KParams& p, int k) {
 template <int BCLASS>
 __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64_t* empty, float* scratch,
                          volatile int* sflag) {
-  Ctx c{&p, ring, full, empty, scratch, 0u, p.nstages, -1};
+  Ctx c{&p, ring, full, empty, scratch, 0u, 0u, p.nstages, -1, {0, 0, 0}};
   Seq sq;
   seq_init(sq, p);
   int task, lvl, cur_lvl = 0;
   const int tid = threadIdx.x;
   while (seq_next(sq, p, task, lvl)) {
     c.task = task;
+    c.mark[0] = c.mark[1] = c.mark[2] = 0;
     const mk_task_descriptor d = load_desc(p.tasks + task);
     uint64_t t_wait = 0, t_start = 0;
     if (tid == 0) {
@@ -859,16 +1042,24 @@ __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
     if (p.trace && tid == 0) {
       // end stamp taken before the dependents are released, so a child's
       // start stamp is never earlier than its parents' end stamps
-      uint64_t* r = p.trace + (size_t)task * 4;
+      uint64_t* r = p.trace + (size_t)task * 8;
       r[0] = ((uint64_t)blockIdx.x << 32) | smid();
       r[1] = t_wait;
       r[2] = t_start;
       r[3] = globaltimer();
+      r[4] = c.mark[0];
+      r[5] = c.mark[1];
+      r[6] = c.mark[2];
+      r[7] = 0;
     }
     if (p.mode == MK_MODE_MEGA && tid < 32) {
+      // release: one gpu-scope fence per signalling lane (covering, through
+      // the barrier above, every consumer thread's output writes), then
+      // relaxed adds that the dependents' acquire loads synchronise with
       const int nd = d.num_dependents;
       const uint32_t* e = p.edges + d.dependents_offset;
-      for (int i = tid; i < nd; i += 32) red_release_add(p.counters + __ldg(e + i), 1u);
+      if (tid < nd) fence_acq_rel_gpu();
+      for (int i = tid; i < nd; i += 32) red_relaxed_add(p.counters + __ldg(e + i), 1u);
     }
   }
   // LEVELS: arrive at the barriers of the remaining levels so no CTA waits on us
@@ -918,7 +1109,8 @@ __global__ void __launch_bounds__(kThreads, 1) mk_interpreter_kernel(const __gri
 namespace mk {
 
 static const void* kernel_for(int batch) {
-  return batch <= 2 ? (const void*)mk_interpreter_kernel<0> : (const void*)mk_interpreter_kernel<1>;
+  return batch <= 2 ? (const void*)mk_interpreter_kernel<0>
+                    : batch <= 4 ? (const void*)mk_interpreter_kernel<1> : (const void*)mk_interpreter_kernel<2>;
 }
 
 cudaError_t configure_interpreter(int batch, int* num_regs) {

@@ -171,7 +171,7 @@ extern "C" int mk_upload(mk_graph* g, void* stream_) {
                  o_bufs = take(NB * 8), o_cos = take((size_t)cap * half * 4), o_sin = take((size_t)cap * half * 4);
     const size_t static_bytes = off;
     const size_t o_ctr = take(N * 4), o_status = take(16), o_lbar = take(g->level_off.size() * 4),
-                 o_trace = take(N * 32);
+                 o_trace = take(N * 64);
     d->blob_bytes = off;
     if (cudaMalloc(&d->blob, d->blob_bytes) != cudaSuccess) {
       rc = fail(MK_ERR_NOMEM, "mk_upload: cudaMalloc of " + std::to_string(d->blob_bytes) + " bytes failed");
@@ -337,7 +337,7 @@ extern "C" int mk_get_trace(mk_graph* g, const uint64_t** records, size_t* count
   if (!g || !records || !count) return fail(MK_ERR_ARG, "mk_get_trace: null argument");
   if (!g->uploaded) return fail(MK_ERR_STATE, "mk_get_trace: call mk_upload first");
   CUDA_TRY(cudaDeviceSynchronize());
-  g->trace_host.resize(g->tasks.size() * 4);
+  g->trace_host.resize(g->tasks.size() * 8);
   CUDA_TRY(cudaMemcpy(g->trace_host.data(), g->dev->trace, g->trace_host.size() * 8, cudaMemcpyDeviceToHost));
   *records = g->trace_host.data();
   *count = g->tasks.size();

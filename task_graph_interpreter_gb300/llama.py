@@ -32,7 +32,7 @@ class LlamaDecode:
 
 def build_llama_decode(model, B: int, len0, capacity: int, weights: dict, kcache: list, vcache: list,
                        history: torch.Tensor, chunk: int = 0, device="cuda", num_ctas: int = 0,
-                       tiles_target: int = 0, col_align: int = 16, wait_timeout_us: int = 0) -> LlamaDecode:
+                       tiles_target: int = 0, col_align: int = 4, wait_timeout_us: int = 0) -> LlamaDecode:
     """weights: name -> bf16 tensor (names of synth.weight_names);
     kcache/vcache: per layer bf16 [B, Hkv, capacity, D]; history int32 [B, capacity]."""
     m = model

@@ -63,10 +63,10 @@ def _replay(L, spec, B):
 
 
 @pytest.mark.parametrize("name", synth.WORKLOADS)
-@pytest.mark.parametrize("num_ctas", [152, 37])
-def test_cpp_lowering_is_byte_identical_to_oracle(L, name, num_ctas):
+@pytest.mark.parametrize("num_ctas,col_align", [(152, 16), (37, 16), (152, 4), (148, 1)])
+def test_cpp_lowering_is_byte_identical_to_oracle(L, name, num_ctas, col_align):
     w = synth.workload(name)
-    spec = llama_decode_spec(w.model, w.B, w.kv_len, w.capacity, w.chunk, num_ctas)
+    spec = llama_decode_spec(w.model, w.B, w.kv_len, w.capacity, w.chunk, num_ctas, col_align=col_align)
     tasks, edges = ol.lower(spec)
     g = _replay(L, spec, w.B)
     try:
@@ -199,7 +199,7 @@ def test_product_builder_matches_oracle_graph(L, name):
     dec = build_llama_decode(m, w.B, w.kv_len, w.capacity, weights, kc, vc, hist, chunk=w.chunk,
                              device="cpu", num_ctas=152)
     dec.graph.lower()
-    spec = llama_decode_spec(m, w.B, w.kv_len, w.capacity, w.chunk, 152)
+    spec = llama_decode_spec(m, w.B, w.kv_len, w.capacity, w.chunk, 152, col_align=4)
     tasks, edges = ol.lower(spec)
     assert dec.graph.tasks_bytes() == tasks.tobytes()
     assert np.array_equal(dec.graph.edges(), edges)
