@@ -228,6 +228,8 @@ __device__ void producer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
       GemvGeom G;
       gemv_geom(d, G);
       const uint16_t* W = static_cast<const uint16_t*>(p.bufs[d.in_buf[1]]);
+      // the norm gain is read right after the dependency wait: warm the L2
+      if (d.flags & MK_F_RMS_NORM_INPUT) prefetch_l2(p.bufs[d.in_buf[2]], (uint32_t)G.K * 2u);
       for (int g0 = 0; g0 < G.cn && !stop; g0 += G.RG) {
         const int rows_g = min(G.RG, G.cn - g0);
         for (int ks = 0; ks < G.nks && !stop; ++ks)
@@ -254,6 +256,10 @@ __device__ void producer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
       const uint16_t* Kc = static_cast<const uint16_t*>(p.bufs[d.in_buf[1]]);
       const uint16_t* Vc = static_cast<const uint16_t*>(p.bufs[d.in_buf[2]]);
       const int64_t rowbase = ((int64_t)q.s * q.Hkv + q.g) * q.cap;
+      if (!q.bad && (p.rope_half * 4) % 16 == 0) {  // the RoPE rows of pos
+        prefetch_l2(p.rope_cos + (size_t)q.pos * p.rope_half, (uint32_t)p.rope_half * 4u);
+        prefetch_l2(p.rope_sin + (size_t)q.pos * p.rope_half, (uint32_t)p.rope_half * 4u);
+      }
       for (int i = 0; i < q.nstage && !stop; ++i) {
         const int j = q.j0 + i * q.R;
         const int nr = min(q.R, q.jst - j);
@@ -559,7 +565,8 @@ __device__ __noinline__ void gemv_fold(const mk_task_descriptor& d, const GemvGe
 // Epilogue of one row group: normalisation scale, SiLU*mul, residual,
 // store, and the tile's running argmax.
 __device__ __noinline__ void gemv_epilogue(const KParams& p, const mk_task_descriptor& d, const GemvGeom& G,
-                                           int g0, int rows_g, const float* acc, float* red) {
+                                           int g0, int rows_g, const float* acc, float* red,
+                                           const float* staged_res) {
   const int tid = threadIdx.x;
   float* out = static_cast<float*>(p.bufs[d.out_buf]);
   const bool silu = d.flags & MK_F_SILU_MUL;
@@ -577,7 +584,8 @@ __device__ __noinline__ void gemv_epilogue(const KParams& p, const mk_task_descr
         y = y / (1.0f + expf(-y)) * u;
       }
       const int col = G.c0 + g0 + j;
-      if (res) y += __ldcg(res + (size_t)b * G.n + col);
+      if (staged_res) y += staged_res[j * BT + b];
+      else if (res) y += __ldcg(res + (size_t)b * G.n + col);
       out[(size_t)b * G.n + col] = y;
       if (y > bv) {
         bv = y;
@@ -607,6 +615,15 @@ __device__ void gemv_task(Ctx& c, const mk_task_descriptor& d) {
   gemv_geom(d, G);
   float* red = gemv_red(c);
   gemv_prologue(d, G, red);
+  // A residual read by the epilogue is loaded now, so its latency hides
+  // behind the slots; it is parked in the (then free) slot area afterwards.
+  const bool stage_res = (d.flags & MK_F_ADD_RESIDUAL) && G.cn <= kConsumerThreads && G.RG >= G.cn;
+  float rv[8];
+  if (stage_res && threadIdx.x < G.cn) {
+    const float* res = static_cast<const float*>(c.p->bufs[d.in_buf[2]]);
+#pragma unroll
+    for (int b = 0; b < 8; ++b) rv[b] = b < G.B ? __ldcg(res + (size_t)b * G.n + G.c0 + threadIdx.x) : 0.f;
+  }
   for (int g0 = 0; g0 < G.cn; g0 += G.RG) {
     const int rows_g = min(G.RG, G.cn - g0);
     for (int ks = 0; ks < G.nks; ++ks) {
@@ -626,7 +643,16 @@ __device__ void gemv_task(Ctx& c, const mk_task_descriptor& d) {
       gemv_fold(d, G, rows_g, ks, g0 == 0, gemv_slots(c), gemv_acc(c), red);
     }
     trace_mark(c, 1);
-    gemv_epilogue(*c.p, d, G, g0, rows_g, gemv_acc(c), red);
+    float* staged = nullptr;
+    if (stage_res) {  // the fold's closing barrier has freed the slot area
+      staged = gemv_slots(c);
+      if (threadIdx.x < G.cn) {
+#pragma unroll
+        for (int b = 0; b < 8; ++b)
+          if (b < G.B) staged[threadIdx.x * G.BT + b] = rv[b];
+      }
+    }
+    gemv_epilogue(*c.p, d, G, g0, rows_g, gemv_acc(c), red, staged);
     trace_mark(c, 2);
   }
   if ((d.flags & MK_F_ARGMAX_EPI) && threadIdx.x < G.B) {
@@ -869,9 +895,21 @@ __device__ void partial_task(Ctx& c, const mk_task_descriptor& d) {
 }
 
 // Log-sum-exp merge of the P partials of one (sequence, kv head), as a
-// running merge: every partial's (m, l, o) is loaded up front (independent
-// loads, one L2 round trip) and folded in with a running maximum.  Empty
-// partials (m = -inf) contribute nothing.
+// running merge with a running maximum; empty partials (m = -inf) add
+// nothing.  Up to 32 partials a thread issues every load it needs at once
+// (one L2 round trip); more partials go through a loop.
+__device__ __forceinline__ void lse_fold(float& M, float& Ls, float& O0, float& O1, float m, float l, float o0,
+                                         float o1) {
+  if (m != -INFINITY) {
+    const float Mn = fmaxf(M, m);
+    const float a = exp2f(M - Mn), b = exp2f(m - Mn);
+    Ls = fmaf(Ls, a, l * b);
+    O0 = fmaf(O0, a, o0 * b);
+    O1 = fmaf(O1, a, o1 * b);
+    M = Mn;
+  }
+}
+
 __device__ void combine_task(Ctx& c, const mk_task_descriptor& d) {
   const KParams& p = *c.p;
   const int s = d.reserved[0], g = d.reserved[1], Hkv = d.reserved[2];
@@ -880,32 +918,34 @@ __device__ void combine_task(Ctx& c, const mk_task_descriptor& d) {
   const int rec = G * (D + 2);
   const float* scr = static_cast<const float*>(p.bufs[d.in_buf[0]]) + (size_t)base * rec;
   float* out = static_cast<float*>(p.bufs[d.out_buf]);
-  for (int i = threadIdx.x; i < G * D; i += kConsumerThreads) {
-    const int h = i / D, e = i % D;
+  // each thread produces two adjacent outputs (e, e + 1) of one head
+  for (int i = threadIdx.x; i < G * D / 2; i += kConsumerThreads) {
+    const int h = (2 * i) / D, e = (2 * i) % D;
     const float* r = scr + h * (D + 2);
-    float M = -INFINITY, Ls = 0.f, O = 0.f;
-    for (int k0 = 0; k0 < P; k0 += 4) {
-      float mv[4], lv[4], ov[4];
+    float M = -INFINITY, Ls = 0.f, O0 = 0.f, O1 = 0.f;
+    if (P <= 32) {
+      float mv[32], lv[32], o0[32], o1[32];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const bool ok = k0 + j < P;
-        const float* rr = r + (size_t)(k0 + j) * rec;
-        mv[j] = ok ? __ldcg(rr) : -INFINITY;
-        lv[j] = ok ? __ldcg(rr + 1) : 0.f;
-        ov[j] = ok ? __ldcg(rr + 2 + e) : 0.f;
+      for (int k = 0; k < 32; ++k) {
+        const bool ok = k < P;
+        const float* rr = r + (size_t)k * rec;
+        mv[k] = ok ? __ldcg(rr) : -INFINITY;
+        lv[k] = ok ? __ldcg(rr + 1) : 0.f;
+        const float2 ov = ok ? __ldcg(reinterpret_cast<const float2*>(rr + 2 + e)) : make_float2(0.f, 0.f);
+        o0[k] = ov.x;
+        o1[k] = ov.y;
       }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        if (mv[j] != -INFINITY) {
-          const float Mn = fmaxf(M, mv[j]);
-          const float a = exp2f(M - Mn), b = exp2f(mv[j] - Mn);
-          Ls = fmaf(Ls, a, lv[j] * b);
-          O = fmaf(O, a, ov[j] * b);
-          M = Mn;
-        }
+      for (int k = 0; k < 32; ++k) lse_fold(M, Ls, O0, O1, mv[k], lv[k], o0[k], o1[k]);
+    } else {
+      for (int k = 0; k < P; ++k) {
+        const float* rr = r + (size_t)k * rec;
+        const float2 ov = __ldcg(reinterpret_cast<const float2*>(rr + 2 + e));
+        lse_fold(M, Ls, O0, O1, __ldcg(rr), __ldcg(rr + 1), ov.x, ov.y);
       }
     }
-    out[(size_t)s * Hq * D + (size_t)(g * G + h) * D + e] = O / Ls;
+    const float inv = 1.f / Ls;
+    *reinterpret_cast<float2*>(out + (size_t)s * Hq * D + (size_t)(g * G + h) * D + e) = make_float2(O0 * inv, O1 * inv);
   }
 }
 
