@@ -234,6 +234,21 @@ int mk_get_edges(const mk_graph* g, const uint32_t** edges, size_t* count);
  * Errors: MK_ERR_STATE (not lowered, or already uploaded), MK_ERR_ARG. */
 int mk_debug_patch_task(mk_graph* g, int task, const mk_task_descriptor* d);
 
+/* The dependency-counter plan the persistent kernel follows (a runtime
+ * detail; descriptors and edges are not changed by it).  Task t waits until
+ * counter[wait[2i]] >= epoch * wait[2i+1] for every i in
+ * [wait_off[t], wait_off[t+1]) and, when done, adds 1 to counter[sig[j]]
+ * for every j in [sig_off[t], sig_off[t+1]).  Parents that make up a whole
+ * launch group (all GEMV tiles of one op, all partials of one attention op,
+ * ...) are waited for through that group's one shared counter; the other
+ * parents through one counter shared by every task with the same remaining
+ * parents (its index is the first such task's); counter_words is the size
+ * of the counter array.  Arrays: wait_off and sig_off uint32[N + 1],
+ * wait uint32[2 * wait_off[N]], sig uint32[sig_off[N]]; they belong to the
+ * graph.  Errors: MK_ERR_STATE (not lowered), MK_ERR_ARG. */
+int mk_get_sync_plan(const mk_graph* g, const uint32_t** wait_off, const uint32_t** wait,
+                     const uint32_t** sig_off, const uint32_t** sig, uint32_t* counter_words);
+
 /* Per-CTA task queues: offsets int32[num_ctas + 1] into tasks int32[]. */
 int mk_get_queues(const mk_graph* g, const int32_t** offsets, const int32_t** tasks,
                   int* num_ctas);

@@ -28,7 +28,7 @@ MK_NO_BUF = 0xFFFF
 EXPORTS = [
     "mk_graph_create", "mk_set_state", "mk_add_buffer", "mk_add_embed", "mk_add_matmul",
     "mk_add_attention", "mk_add_sample", "mk_attention_scratch_rows", "mk_gemv_tiles",
-    "mk_lower", "mk_get_tasks", "mk_get_edges", "mk_get_queues", "mk_upload",
+    "mk_lower", "mk_get_tasks", "mk_get_edges", "mk_get_sync_plan", "mk_get_queues", "mk_upload",
     "mk_decode_step", "mk_decode_step_ex", "mk_decode_step_host", "mk_status",
     "mk_get_trace", "mk_kernel_info", "mk_destroy", "mk_last_error", "mk_debug_patch_task",
     "mk_attention_decode_noalloc",
@@ -74,6 +74,8 @@ def lib():
         "mk_get_tasks": (c_int, [G, POINTER(c_void_p), POINTER(c_size_t)]),
         "mk_get_edges": (c_int, [G, POINTER(c_void_p), POINTER(c_size_t)]),
         "mk_get_queues": (c_int, [G, POINTER(c_void_p), POINTER(c_void_p), POINTER(c_int)]),
+        "mk_get_sync_plan": (c_int, [G, POINTER(c_void_p), POINTER(c_void_p), POINTER(c_void_p),
+                                     POINTER(c_void_p), POINTER(c_uint32)]),
         "mk_upload": (c_int, [G, c_void_p]),
         "mk_decode_step": (c_int, [G, c_void_p]),
         "mk_decode_step_ex": (c_int, [G, c_void_p, c_int, c_uint32]),
@@ -166,6 +168,21 @@ def mk_get_edges(g):
     p, n = c_void_p(), c_size_t()
     check(lib().mk_get_edges(g, ctypes.byref(p), ctypes.byref(n)), "mk_get_edges")
     return np.frombuffer(ctypes.string_at(p, n.value * 4), dtype=np.uint32).copy()
+
+
+def mk_get_sync_plan(g, num_tasks: int):
+    """(wait_off, wait[:, 2], sig_off, sig, counter_words) as numpy arrays."""
+    import numpy as np
+    wo, w, so, sg, cw = c_void_p(), c_void_p(), c_void_p(), c_void_p(), c_uint32()
+    check(lib().mk_get_sync_plan(g, ctypes.byref(wo), ctypes.byref(w), ctypes.byref(so), ctypes.byref(sg),
+                                 ctypes.byref(cw)), "mk_get_sync_plan")
+    u32 = lambda ptr, n: np.frombuffer(ctypes.string_at(ptr, n * 4), dtype=np.uint32).copy() if n else \
+        np.zeros(0, np.uint32)
+    wait_off = u32(wo, num_tasks + 1)
+    sig_off = u32(so, num_tasks + 1)
+    wait = u32(w, 2 * int(wait_off[-1])).reshape(-1, 2)
+    sig = u32(sg, int(sig_off[-1]))
+    return wait_off, wait, sig_off, sig, int(cw.value)
 
 
 def mk_get_queues(g):

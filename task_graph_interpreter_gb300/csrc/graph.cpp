@@ -21,6 +21,7 @@
 // output does and every reader of the decode state stays an ancestor of
 // SAMPLE, which advances it.
 #include <algorithm>
+#include <map>
 #include <cmath>
 #include <cstring>
 #include <limits>
@@ -511,6 +512,8 @@ extern "C" int mk_lower(mk_graph* g) {
     off += (uint32_t)children[t].size();
   }
 
+  if (int rc = build_sync_plan(g)) return rc;
+
   // topological levels
   std::vector<int> level(N, 0);
   int nlev = 0;
@@ -563,6 +566,108 @@ extern "C" int mk_lower(mk_graph* g) {
   return MK_OK;
 }
 
+// Dependency-counter plan.  With one counter per task, a B = 1 GEMV tile
+// whose ~150 children each need every tile of its op sends ~150 atomics,
+// and one op hand-off puts ~150^2 atomics on a few cache lines of
+// neighbouring counters.  Here a task whose parents include a whole launch
+// group waits on that group's one counter (each group member adds 1 to it
+// once).  The remaining parents signal one counter per distinct remaining
+// set (the partials of one KV-head group share theirs), indexed by the
+// first task with that set.  Group counters sit 128 bytes apart after the
+// per-task counters.  The plan follows the descriptors' remaining_deps: the
+// set counter is expected to reach remaining_deps minus the parents covered
+// by group counters, so a descriptor patched to one dependency too many
+// still times out.
+int mk::build_sync_plan(mk_graph* g) {
+  const int N = (int)g->tasks.size();
+  const int NG = (int)g->group_off.size() - 1;
+  std::vector<int> group_of(N, 0);
+  for (int k = 0; k < NG; ++k)
+    for (int t = g->group_off[k]; t < g->group_off[k + 1]; ++t) group_of[t] = k;
+  std::vector<std::vector<int>> parents(N);
+  for (int p = 0; p < N; ++p) {
+    const mk_task_descriptor& d = g->tasks[p];
+    if ((uint64_t)d.dependents_offset + (uint64_t)d.num_dependents > g->edges.size())
+      return fail(MK_ERR_ARG, "sync plan: dependents range of task " + std::to_string(p) + " outside the edges");
+    for (int i = 0; i < d.num_dependents; ++i) {
+      const uint32_t c = g->edges[d.dependents_offset + i];
+      if ((int)c <= p || (int)c >= N)
+        return fail(MK_ERR_ARG, "sync plan: edge " + std::to_string(p) + "->" + std::to_string(c) +
+                                    " does not point forward");
+      parents[c].push_back(p);
+    }
+  }
+  const uint32_t npad = (uint32_t)((N + 31) / 32 * 32);
+  auto group_size = [&](int k) { return g->group_off[k + 1] - g->group_off[k]; };
+  auto group_counter = [&](int k) { return npad + 32u * (uint32_t)k; };
+  std::vector<char> group_used(NG, 0);
+  std::vector<std::vector<int>> whole(N);    // groups task t waits on as a whole
+  std::vector<int> own(N, 0);                // count task t expects on its set counter
+  std::vector<int> own_ctr(N, 0);            // that counter: the first task with the same set
+  std::vector<std::vector<uint32_t>> own_sig(N);  // set counters parent p signals
+  std::map<std::vector<int>, int> set_ctr;   // remaining-parent set -> its counter
+  std::vector<int> cnt(NG, 0);
+  for (int t = 0; t < N; ++t) {
+    for (int p : parents[t]) cnt[group_of[p]]++;
+    int covered = 0;
+    for (int p : parents[t]) {
+      const int k = group_of[p];
+      if (group_size(k) > 1 && cnt[k] == group_size(k)) {
+        whole[t].push_back(k);
+        group_used[k] = 1;
+        covered += group_size(k);
+        cnt[k] = -1;  // marks the group as waited on whole
+      }
+    }
+    std::vector<int> rest;
+    for (int p : parents[t])
+      if (cnt[group_of[p]] != -1) rest.push_back(p);
+    for (int p : parents[t]) cnt[group_of[p]] = 0;
+    own[t] = std::max(g->tasks[t].remaining_deps - covered, 0);
+    own_ctr[t] = t;
+    if (!rest.empty()) {  // tasks with the same remaining parents share one counter
+      auto it = set_ctr.emplace(rest, t).first;
+      own_ctr[t] = it->second;
+      if (it->second == t)
+        for (int p : rest) own_sig[p].push_back((uint32_t)t);
+    }
+  }
+  g->wait_off.assign(N + 1, 0);
+  g->wait.clear();
+  g->sig_off.assign(N + 1, 0);
+  g->sig.clear();
+  for (int t = 0; t < N; ++t) {
+    std::sort(whole[t].begin(), whole[t].end());
+    for (int k : whole[t]) {
+      g->wait.push_back(group_counter(k));
+      g->wait.push_back((uint32_t)group_size(k));
+    }
+    if (own[t] > 0) {
+      g->wait.push_back((uint32_t)own_ctr[t]);
+      g->wait.push_back((uint32_t)own[t]);
+    }
+    g->wait_off[t + 1] = (uint32_t)(g->wait.size() / 2);
+    if (group_used[group_of[t]]) g->sig.push_back(group_counter(group_of[t]));
+    for (uint32_t c : own_sig[t]) g->sig.push_back(c);  // ascending: children come in order
+    g->sig_off[t + 1] = (uint32_t)g->sig.size();
+  }
+  g->counter_words = npad + 32u * (uint32_t)NG;
+  return MK_OK;
+}
+
+extern "C" int mk_get_sync_plan(const mk_graph* g, const uint32_t** wait_off, const uint32_t** wait,
+                                const uint32_t** sig_off, const uint32_t** sig, uint32_t* counter_words) {
+  if (!g || !wait_off || !wait || !sig_off || !sig || !counter_words)
+    return fail(MK_ERR_ARG, "mk_get_sync_plan: null argument");
+  if (!g->lowered) return fail(MK_ERR_STATE, "mk_get_sync_plan: not lowered");
+  *wait_off = g->wait_off.data();
+  *wait = g->wait.data();
+  *sig_off = g->sig_off.data();
+  *sig = g->sig.data();
+  *counter_words = g->counter_words;
+  return MK_OK;
+}
+
 extern "C" int mk_get_tasks(const mk_graph* g, const void** bytes, size_t* nbytes) {
   if (!g || !bytes || !nbytes) return fail(MK_ERR_ARG, "mk_get_tasks: null argument");
   if (!g->lowered) return fail(MK_ERR_STATE, "mk_get_tasks: not lowered");
@@ -584,7 +689,7 @@ extern "C" int mk_debug_patch_task(mk_graph* g, int task, const mk_task_descript
   if (!g->lowered || g->uploaded) return fail(MK_ERR_STATE, "mk_debug_patch_task: needs a lowered, not uploaded graph");
   if (task < 0 || task >= (int)g->tasks.size()) return fail(MK_ERR_ARG, "mk_debug_patch_task: bad task index");
   g->tasks[task] = *d;
-  return MK_OK;
+  return build_sync_plan(g);
 }
 
 extern "C" int mk_get_queues(const mk_graph* g, const int32_t** offsets, const int32_t** tasks,

@@ -56,6 +56,12 @@ struct mk_graph {
   std::vector<int32_t> queue_off, queue;       // per-CTA static queues
   std::vector<int32_t> level_off, level_tasks;  // topological levels
   std::vector<int32_t> group_off;               // per-op launch groups (task ranges)
+  // dependency-counter plan (runtime only; descriptors and edges unchanged):
+  // task t waits until counter[wait[i].first] >= epoch * wait[i].second for
+  // every i in [wait_off[t], wait_off[t+1]), and when done adds 1 to
+  // counter[sig[j]] for every j in [sig_off[t], sig_off[t+1]).
+  std::vector<uint32_t> wait_off, wait, sig_off, sig;  // wait holds (counter, count) pairs
+  uint32_t counter_words = 0;
   // kernel geometry
   int max_m = 1;
   mk::DeviceState* dev = nullptr;
@@ -66,6 +72,7 @@ namespace mk {
 int query_sm_count(int* out);  // runtime.cu
 int tile_width(int n, int tiles_target, int col_align);
 int tile_count(int n, int tiles_target, int col_align);
+int build_sync_plan(mk_graph* g);  // graph.cpp; from the descriptors and edges
 std::vector<int> partials_per_sequence(const std::vector<int32_t>& len0, int Hkv, int chunk,
                                        int num_ctas);
 }  // namespace mk

@@ -4,6 +4,8 @@
 
 #include <cstdint>
 
+#include <vector_types.h>
+
 #include "mk.h"
 
 namespace mk {
@@ -30,7 +32,11 @@ struct KParams {
   const mk_task_descriptor* tasks;
   const uint32_t* edges;
   void* const* bufs;          // buffer table (device pointers by index)
-  uint32_t* counters;         // per-task dependency counters (monotone)
+  uint32_t* counters;         // dependency counters (monotone): per task, then per launch group
+  const uint32_t* wait_off;   // MEGA: task t waits on wait[wait_off[t] .. wait_off[t+1])
+  const uint2* wait;          //   (counter index, count): counter >= epoch * count
+  const uint32_t* sig_off;    // MEGA: task t then adds 1 to counters sig[sig_off[t] .. sig_off[t+1])
+  const uint32_t* sig;
   const int32_t* queue_off;   // MEGA: per-CTA queue offsets
   const int32_t* queue;       // MEGA: task ids
   const int32_t* level_off;   // LEVELS: task range of each level

@@ -999,23 +999,38 @@ __device__ void sample_task(Ctx& c, const mk_task_descriptor& d) {
 }
 
 // ------------------------------------------------------------------ consumer loop
-__device__ bool wait_deps(const KParams& p, int task, int deps) {
+// Wait (consumer warp 0) until every counter the task's plan names reaches
+// epoch * count.  Lane i polls entry i with acquire loads; entries are
+// usually one (a whole-group counter or the task's own) or two.
+__device__ bool wait_deps(const KParams& p, int task) {
   if (aborted(p)) return false;
-  if (deps == 0) return true;
-  const uint32_t target = p.epoch * (uint32_t)deps;
-  const uint32_t* ctr = p.counters + task;
-  if (ld_acquire(ctr) >= target) return true;
-  const uint64_t t0 = globaltimer();
-  for (uint32_t it = 1;; ++it) {
-    if (ld_acquire(ctr) >= target) return true;
-    if ((it & 63u) == 0) {
-      if (aborted(p)) return false;
-      if (globaltimer() - t0 > p.timeout_ns) {
-        raise_error(p, MK_DEV_DEP_TIMEOUT, task);
-        return false;
+  const int lane = threadIdx.x & 31;
+  const uint32_t w0 = __ldg(p.wait_off + task), nw = __ldg(p.wait_off + task + 1) - w0;
+  for (uint32_t base = 0; base < nw; base += 32) {
+    const bool mine = base + lane < nw;
+    const uint32_t* ctr = p.counters;
+    uint32_t target = 0;
+    if (mine) {
+      const uint2 e = __ldg(p.wait + w0 + base + lane);
+      ctr = p.counters + e.x;
+      target = p.epoch * e.y;
+    }
+    bool done = !mine || ld_acquire(ctr) >= target;
+    if (__all_sync(0xffffffffu, done)) continue;
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1;; ++it) {
+      if (!done) done = ld_acquire(ctr) >= target;
+      if (__all_sync(0xffffffffu, done)) break;
+      if ((it & 63u) == 0) {
+        if (aborted(p)) return false;
+        if (globaltimer() - t0 > p.timeout_ns) {
+          if (lane == 0) raise_error(p, MK_DEV_DEP_TIMEOUT, task);
+          return false;
+        }
       }
     }
   }
+  return true;
 }
 
 // Grid barrier k of MK_MODE_LEVELS (consumer thread 0 of every CTA): one
@@ -1050,19 +1065,19 @@ __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
     c.mark[0] = c.mark[1] = c.mark[2] = 0;
     const mk_task_descriptor d = load_desc(p.tasks + task);
     uint64_t t_wait = 0, t_start = 0;
-    if (tid == 0) {
+    if (tid < 32) {  // warp 0 waits (MEGA: all lanes; other modes: thread 0)
       bool ok = true;
       if (p.trace) t_wait = globaltimer();
       if (p.mode == MK_MODE_MEGA) {
-        ok = wait_deps(p, task, d.remaining_deps);
-      } else if (p.mode == MK_MODE_LEVELS) {
+        ok = wait_deps(p, task);
+      } else if (tid == 0 && p.mode == MK_MODE_LEVELS) {
         while (ok && cur_lvl < lvl) ok = level_barrier(p, ++cur_lvl);
         ok = ok && !aborted(p);
-      } else {
+      } else if (tid == 0) {
         ok = !aborted(p);
       }
       if (p.trace) t_start = globaltimer();
-      *sflag = ok ? 1 : 0;
+      if (tid == 0) *sflag = ok ? 1 : 0;
     }
     cbar();
     if (!*sflag) return;
@@ -1096,10 +1111,9 @@ __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
       // release: one gpu-scope fence per signalling lane (covering, through
       // the barrier above, every consumer thread's output writes), then
       // relaxed adds that the dependents' acquire loads synchronise with
-      const int nd = d.num_dependents;
-      const uint32_t* e = p.edges + d.dependents_offset;
-      if (tid < nd) fence_acq_rel_gpu();
-      for (int i = tid; i < nd; i += 32) red_relaxed_add(p.counters + __ldg(e + i), 1u);
+      const uint32_t s0 = __ldg(p.sig_off + task), ns = __ldg(p.sig_off + task + 1) - s0;
+      if ((uint32_t)tid < ns) fence_acq_rel_gpu();
+      for (uint32_t i = tid; i < ns; i += 32) red_relaxed_add(p.counters + __ldg(p.sig + s0 + i), 1u);
     }
   }
   // LEVELS: arrive at the barriers of the remaining levels so no CTA waits on us

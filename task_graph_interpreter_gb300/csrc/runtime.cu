@@ -31,6 +31,11 @@ struct DeviceState {
   uint32_t* edges = nullptr;
   void** bufs = nullptr;
   uint32_t* counters = nullptr;
+  uint32_t* wait_off = nullptr;
+  uint2* wait = nullptr;
+  uint32_t* sig_off = nullptr;
+  uint32_t* sig = nullptr;
+  size_t counter_words = 0;
   int32_t* queue_off = nullptr;
   int32_t* queue = nullptr;
   int32_t* level_off = nullptr;
@@ -84,6 +89,10 @@ KParams base_params(const mk_graph* g) {
   p.edges = d->edges;
   p.bufs = d->bufs;
   p.counters = d->counters;
+  p.wait_off = d->wait_off;
+  p.wait = d->wait;
+  p.sig_off = d->sig_off;
+  p.sig = d->sig;
   p.queue_off = d->queue_off;
   p.queue = d->queue;
   p.level_off = d->level_off;
@@ -157,8 +166,8 @@ extern "C" int mk_upload(mk_graph* g, void* stream_) {
     }
     const size_t N = g->tasks.size(), E = g->edges.size(), NB = g->bufs.size();
     const int half = g->rope_D / 2, cap = g->rope_cap;
-    // blob layout: header | tasks | edges | queue_off | queue | level_off | level_tasks | bufs | cos | sin
-    //              then (zeroed) counters | status | level_bar | trace
+    // blob layout: header | tasks | edges | queue_off | queue | level_off | level_tasks | bufs | cos | sin |
+    //              wait_off | wait | sig_off | sig, then (zeroed) counters | status | level_bar | trace
     size_t off = 0;
     auto take = [&](size_t bytes) {
       size_t o = off;
@@ -168,9 +177,11 @@ extern "C" int mk_upload(mk_graph* g, void* stream_) {
     const size_t o_hdr = take(64), o_tasks = take(N * 64), o_edges = take(E * 4),
                  o_qoff = take(g->queue_off.size() * 4), o_q = take(g->queue.size() * 4),
                  o_loff = take(g->level_off.size() * 4), o_lt = take(g->level_tasks.size() * 4),
-                 o_bufs = take(NB * 8), o_cos = take((size_t)cap * half * 4), o_sin = take((size_t)cap * half * 4);
+                 o_bufs = take(NB * 8), o_cos = take((size_t)cap * half * 4), o_sin = take((size_t)cap * half * 4),
+                 o_woff = take(g->wait_off.size() * 4), o_wait = take(g->wait.size() * 4),
+                 o_soff = take(g->sig_off.size() * 4), o_sig = take(g->sig.size() * 4);
     const size_t static_bytes = off;
-    const size_t o_ctr = take(N * 4), o_status = take(16), o_lbar = take(g->level_off.size() * 4),
+    const size_t o_ctr = take((size_t)g->counter_words * 4), o_status = take(16), o_lbar = take(g->level_off.size() * 4),
                  o_trace = take(N * 64);
     d->blob_bytes = off;
     if (cudaMalloc(&d->blob, d->blob_bytes) != cudaSuccess) {
@@ -187,6 +198,10 @@ extern "C" int mk_upload(mk_graph* g, void* stream_) {
     std::memcpy(img.data() + o_q, g->queue.data(), g->queue.size() * 4);
     std::memcpy(img.data() + o_loff, g->level_off.data(), g->level_off.size() * 4);
     std::memcpy(img.data() + o_lt, g->level_tasks.data(), g->level_tasks.size() * 4);
+    std::memcpy(img.data() + o_woff, g->wait_off.data(), g->wait_off.size() * 4);
+    std::memcpy(img.data() + o_wait, g->wait.data(), g->wait.size() * 4);
+    std::memcpy(img.data() + o_soff, g->sig_off.data(), g->sig_off.size() * 4);
+    std::memcpy(img.data() + o_sig, g->sig.data(), g->sig.size() * 4);
     char* base = static_cast<char*>(d->blob);
     std::vector<void*> ptrs(NB);
     for (size_t i = 0; i < NB; ++i) ptrs[i] = g->bufs[i].ptr;
@@ -221,6 +236,11 @@ extern "C" int mk_upload(mk_graph* g, void* stream_) {
     d->rope_cos = reinterpret_cast<float*>(base + o_cos);
     d->rope_sin = reinterpret_cast<float*>(base + o_sin);
     d->counters = reinterpret_cast<uint32_t*>(base + o_ctr);
+    d->counter_words = g->counter_words;
+    d->wait_off = reinterpret_cast<uint32_t*>(base + o_woff);
+    d->wait = reinterpret_cast<uint2*>(base + o_wait);
+    d->sig_off = reinterpret_cast<uint32_t*>(base + o_soff);
+    d->sig = reinterpret_cast<uint32_t*>(base + o_sig);
     d->status = reinterpret_cast<int32_t*>(base + o_status);
     d->level_bar = reinterpret_cast<uint32_t*>(base + o_lbar);
     d->trace = reinterpret_cast<uint64_t*>(base + o_trace);
@@ -325,7 +345,7 @@ extern "C" int mk_status(mk_graph* g, void* stream_, int* dev_code, int32_t* tas
   *task_id = st[kStatusCode] ? st[kStatusTask] : -1;
   if (st[kStatusCode] || st[kStatusAbort]) {
     // A failed step leaves counters part-way; start the epochs afresh.
-    CUDA_TRY(cudaMemsetAsync(d->counters, 0, g->tasks.size() * 4, stream));
+    CUDA_TRY(cudaMemsetAsync(d->counters, 0, d->counter_words * 4, stream));
     CUDA_TRY(cudaMemsetAsync(d->status, 0, 16, stream));
     CUDA_TRY(cudaStreamSynchronize(stream));
     d->epoch = 0;

@@ -204,3 +204,73 @@ def test_product_builder_matches_oracle_graph(L, name):
     assert dec.graph.tasks_bytes() == tasks.tobytes()
     assert np.array_equal(dec.graph.edges(), edges)
     dec.graph.close()
+
+
+def _check_sync_plan(tasks, edges, plan):
+    """When every wait of a task is satisfied, every parent of the task has
+    signalled, and no wait can be satisfied without all its signallers."""
+    wait_off, wait, sig_off, sig, words = plan
+    N = len(tasks)
+    parents = [set() for _ in range(N)]
+    for p in range(N):
+        o, n = int(tasks["dependents_offset"][p]), int(tasks["num_dependents"][p])
+        for c in edges[o:o + n]:
+            parents[int(c)].add(p)
+    signallers = {}
+    for p in range(N):
+        got = [int(x) for x in sig[sig_off[p]:sig_off[p + 1]]]
+        assert len(got) == len(set(got)), f"task {p} signals a counter twice"
+        for c in got:
+            assert c < words
+            signallers.setdefault(c, set()).add(p)
+    for t in range(N):
+        covered = set()
+        entries = wait[wait_off[t]:wait_off[t + 1]]
+        assert len({int(c) for c, _ in entries}) == len(entries)
+        for c, n in entries:
+            c, n = int(c), int(n)
+            assert c < words
+            if c < N:
+                assert c <= t, f"task {t} waits on the set counter of a later task {c}"
+            who = signallers.get(c, set())
+            assert len(who) == n, f"task {t}: counter {c} expects {n}, has {len(who)} signallers"
+            assert who <= parents[t], f"task {t}: counter {c} is signalled by a non-parent"
+            assert not (who & covered)
+            covered |= who
+        assert covered == parents[t], f"task {t}: waits cover {len(covered)} of {len(parents[t])} parents"
+        assert sum(int(n) for _, n in entries) == int(tasks["remaining_deps"][t])
+
+
+@pytest.mark.parametrize("name", synth.WORKLOADS)
+def test_sync_plan_is_equivalent_to_the_edges(L, name):
+    w = synth.workload(name)
+    spec = llama_decode_spec(w.model, w.B, w.kv_len, w.capacity, w.chunk, 152, col_align=4)
+    g = _replay(L, spec, w.B)
+    try:
+        tasks = np.frombuffer(L.mk_get_tasks(g), dtype=ol.TASK_DTYPE)
+        plan = L.mk_get_sync_plan(g, len(tasks))
+        _check_sync_plan(tasks, L.mk_get_edges(g), plan)
+        # a B = 1 hand-off between GEMVs costs one atomic per tile, not one per edge
+        if w.B == 1 and name != "tiny":
+            assert len(plan[3]) < len(L.mk_get_edges(g)) / 20
+    finally:
+        L.mk_destroy(g)
+
+
+def test_sync_plan_follows_a_patched_dependency_count(L):
+    w = synth.workload("tiny")
+    spec = llama_decode_spec(w.model, w.B, w.kv_len, w.capacity, w.chunk, 16, col_align=4)
+    g = _replay(L, spec, w.B)
+    try:
+        tasks = np.frombuffer(L.mk_get_tasks(g), dtype=ol.TASK_DTYPE).copy()
+        victim = int(np.nonzero(tasks["op_id"] == ol.OP_GEMV)[0][10])
+        t = tasks[victim].copy()
+        t["remaining_deps"] += 1
+        L.mk_debug_patch_task(g, victim, t.tobytes())
+        wait_off, wait, _, sig, _ = L.mk_get_sync_plan(g, len(tasks))
+        entries = wait[wait_off[victim]:wait_off[victim + 1]]
+        assert sum(int(n) for _, n in entries) == int(t["remaining_deps"])
+        own = [(int(c), int(n)) for c, n in entries if int(c) < len(tasks)]
+        assert own and own[0][1] > np.count_nonzero(sig == own[0][0]), "the extra dependency can never be met"
+    finally:
+        L.mk_destroy(g)
