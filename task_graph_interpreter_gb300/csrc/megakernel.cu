@@ -131,7 +131,7 @@ __device__ __forceinline__ mk_task_descriptor load_desc(const mk_task_descriptor
 // row-segments.  Consumer warp w reads columns [wcol*KS/WCOL, ...) of rows
 // r = wrow (mod WROW) of each slot, with x in registers (B*NV*8 floats).
 struct GemvGeom {
-  int B, BT, K, n, c0, cn, seg, KS, nks, WCOL, WROW, NV, rs, RG;
+  int B, BT, K, n, c0, cn, seg, KS, nks, WCOL, WROW, lgW, NV, rs, RG;
 };
 
 __device__ __forceinline__ void gemv_geom(const mk_task_descriptor& d, GemvGeom& g) {
@@ -155,6 +155,7 @@ __device__ __forceinline__ void gemv_geom(const mk_task_descriptor& d, GemvGeom&
     g.KS = uk * 256; g.nks = q; g.WCOL = wcol; g.WROW = 8 / wcol; g.NV = nv;
     break;
   }
+  g.lgW = g.WROW == 8 ? 3 : g.WROW == 4 ? 2 : g.WROW == 2 ? 1 : 0;
   g.rs = kStageElems / g.KS;
   int rg = kSlotFloats / (g.seg * g.BT * g.WCOL);
   rg = min(rg, kAccFloats / (g.seg * g.BT));
@@ -200,16 +201,32 @@ __device__ __forceinline__ void part_geom(const KParams& p, const mk_task_descri
   q.has_new = (q.j1 == L) && (q.j0 < q.j1);
 }
 
+// ------------------------------------------------------------------ ring position
+// Slot index and mbarrier phase parity of the next ring use, advanced
+// without division (this runs once per slot in every warp).
+struct RingPos {
+  uint32_t slot = 0, phase = 0;
+  __device__ __forceinline__ void advance(int nst) {
+    if (++slot == (uint32_t)nst) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 // ------------------------------------------------------------------ producer
 // Claim the next ring slot once the consumers have freed it and announce the
-// bytes the coming copies will deliver.  Null on abort or timeout.
+// bytes the coming copies will deliver; *fb receives the slot's full
+// barrier.  Null on abort or timeout.
 __device__ __forceinline__ uint8_t* produce_slot(const KParams& p, uint8_t* ring, uint64_t* full, uint64_t* empty,
-                                                 uint32_t& stage, int task, uint32_t bytes) {
-  const int nst = p.nstages;
-  const uint32_t slot = stage % nst, ph = (stage / nst) & 1u;
-  if (!bar_wait(p, &empty[slot], ph ^ 1u, task, true)) return nullptr;
+                                                 RingPos& rp, uint32_t& issued, int task, uint32_t bytes,
+                                                 uint64_t** fb) {
+  const uint32_t slot = rp.slot;
+  if (!bar_wait(p, &empty[slot], rp.phase ^ 1u, task, true)) return nullptr;
   mbar_arrive_expect_tx(&full[slot], bytes);
-  ++stage;
+  rp.advance(p.nstages);
+  ++issued;
+  *fb = &full[slot];
   return ring + (size_t)slot * kStageBytes;
 }
 
@@ -217,7 +234,8 @@ __device__ void producer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
   if ((threadIdx.x & 31) != 0) return;
   const uint64_t pol = policy_evict_first();
   const int nst = p.nstages;
-  uint32_t stage = 0;
+  RingPos rp;
+  uint32_t issued = 0;
   bool stop = false;
   Seq sq;
   seq_init(sq, p);
@@ -237,16 +255,16 @@ __device__ void producer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
             for (int r0 = 0; r0 < rows_g; r0 += G.rs) {
               const int nr = min(G.rs, rows_g - r0);
               const uint32_t bytes = (uint32_t)nr * G.KS * 2u;
-              uint8_t* dst = produce_slot(p, ring, full, empty, stage, task, bytes);
+              uint64_t* fb;
+              uint8_t* dst = produce_slot(p, ring, full, empty, rp, issued, task, bytes, &fb);
               if (!dst) { stop = true; break; }
               const int64_t row = (int64_t)(sg ? G.n : 0) + G.c0 + g0 + r0;
               const uint16_t* src = W + row * G.K + (int64_t)ks * G.KS;
               if (G.nks == 1) {
-                bulk_g2s(dst, src, bytes, &full[(stage - 1) % nst], pol);
+                bulk_g2s(dst, src, bytes, fb, pol);
               } else {
                 for (int r = 0; r < nr; ++r)
-                  bulk_g2s(dst + (size_t)r * G.KS * 2, src + (int64_t)r * G.K, (uint32_t)G.KS * 2u,
-                           &full[(stage - 1) % nst], pol);
+                  bulk_g2s(dst + (size_t)r * G.KS * 2, src + (int64_t)r * G.K, (uint32_t)G.KS * 2u, fb, pol);
               }
             }
       }
@@ -264,18 +282,18 @@ __device__ void producer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
         const int j = q.j0 + i * q.R;
         const int nr = min(q.R, q.jst - j);
         const uint32_t bytes = (uint32_t)nr * q.D * 2u;
-        uint8_t* dst = produce_slot(p, ring, full, empty, stage, task, 2u * bytes);
+        uint64_t* fb;
+        uint8_t* dst = produce_slot(p, ring, full, empty, rp, issued, task, 2u * bytes, &fb);
         if (!dst) { stop = true; break; }
-        uint64_t* fb = &full[(stage - 1) % nst];
         bulk_g2s(dst, Kc + (rowbase + j) * q.D, bytes, fb, pol);
         bulk_g2s(dst + kStageBytes / 2, Vc + (rowbase + j) * q.D, bytes, fb, pol);
       }
     }
   }
   // Let every copy still in flight land before the CTA can exit.
-  const uint32_t inflight = stage < (uint32_t)nst ? stage : (uint32_t)nst;
+  const uint32_t inflight = issued < (uint32_t)nst ? issued : (uint32_t)nst;
   for (uint32_t k = 0; k < inflight; ++k) {
-    const uint32_t st = stage - 1 - k;
+    const uint32_t st = issued - 1 - k;
     bar_wait(p, &full[st % nst], (st / nst) & 1u, -1, false);
   }
 }
@@ -287,8 +305,7 @@ struct Ctx {
   uint64_t* full;
   uint64_t* empty;
   float* scratch;
-  uint32_t stage;     // next ring slot to wait for (consume_begin)
-  uint32_t released;  // next ring slot to hand back (consume_end)
+  RingPos rp;  // next ring slot to wait for (consume_begin)
   int nst;
   int task;
   uint64_t mark[3];  // optional trace marks inside a task body (thread 0)
@@ -302,8 +319,8 @@ __device__ __forceinline__ void trace_mark(Ctx& c, int i) {
 // Slots are waited for and handed back in order; a consumer may wait for
 // the next slot before handing back the current one.
 __device__ __forceinline__ uint32_t consume_begin(Ctx& c) {
-  const uint32_t slot = c.stage % c.nst, ph = (c.stage / c.nst) & 1u;
-  ++c.stage;
+  const uint32_t slot = c.rp.slot, ph = c.rp.phase;
+  c.rp.advance(c.nst);
   if ((threadIdx.x & 31) == 0) bar_wait(*c.p, &c.full[slot], ph, c.task, true);
   __syncwarp();
   return slot;
@@ -312,7 +329,6 @@ __device__ __forceinline__ uint32_t consume_begin(Ctx& c) {
 __device__ __forceinline__ void consume_end(Ctx& c, uint32_t slot) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(&c.empty[slot]);
-  ++c.released;
 }
 
 __device__ __forceinline__ void cbar() { named_bar_sync(1, kConsumerThreads); }
@@ -438,27 +454,6 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[N], int lane) {
   return v[0];
 }
 
-// bf16 weights of one slot for this lane: rows wrow + r * WROW (r < RWM),
-// vectors v < NV of 8 elements.
-template <int RWM, int NV>
-__device__ __forceinline__ void gemv_load_slot(uint4 (&w)[RWM][NV], uint32_t base, int rw, int WROW, int KS) {
-#pragma unroll
-  for (int r = 0; r < RWM; ++r) {
-    const uint32_t ra = base + (uint32_t)(r * WROW) * KS * 2;
-#pragma unroll
-    for (int v = 0; v < NV; ++v) w[r][v] = r < rw ? lds128(ra + v * 512) : make_uint4(0u, 0u, 0u, 0u);
-  }
-}
-
-// Segment and first row of slot sidx, and the rows of it this warp takes.
-__device__ __forceinline__ int gemv_slot_rows(int sidx, int nstg, int rs, int rows_g, int wrow, int WROW, int& sg,
-                                              int& r0) {
-  sg = sidx / nstg;
-  r0 = (sidx - sg * nstg) * rs;
-  const int nr = min(rs, rows_g - r0);
-  return nr > wrow ? (nr - wrow + WROW - 1) / WROW : 0;
-}
-
 // Every ring slot of one (row group, k-segment).  A warp takes rows
 // wrow, wrow + WROW, ... of each slot over its column block, with x in
 // registers: all shared loads of a slot first, independent FMA chains per
@@ -497,7 +492,7 @@ __device__ __forceinline__ void gemv_stages(Ctx& c, const mk_task_descriptor& d,
       const uint32_t slot = consume_begin(c);
       if (first_group && ks == 0 && sg == 0 && r0 == 0) trace_mark(c, 0);
       const uint32_t base = smem_addr(c.ring + (size_t)slot * kStageBytes) + (wcol * colw + lane * 8) * 2;
-      const int rw = nr > wrow ? (nr - wrow + G.WROW - 1) / G.WROW : 0;
+      const int rw = nr > wrow ? (nr - wrow + G.WROW - 1) >> G.lgW : 0;
       uint4 w[RWM][NV];
 #pragma unroll
       for (int r = 0; r < RWM; ++r) {
@@ -1055,7 +1050,7 @@ __device__ bool level_barrier(const KParams& p, int k) {
 template <int BCLASS>
 __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64_t* empty, float* scratch,
                          volatile int* sflag) {
-  Ctx c{&p, ring, full, empty, scratch, 0u, 0u, p.nstages, -1, {0, 0, 0}};
+  Ctx c{&p, ring, full, empty, scratch, RingPos{}, p.nstages, -1, {0, 0, 0}};
   Seq sq;
   seq_init(sq, p);
   int task, lvl, cur_lvl = 0;
