@@ -281,11 +281,13 @@ int mk_decode_step_host(mk_graph* g, void* stream, const int32_t* state_in,
 int mk_status(mk_graph* g, void* stream, int* dev_code, int32_t* task_id);
 
 /* Trace records of the last traced step: uint64[count * 8] per task as
- * (cta << 32 | smid, t_wait_begin, t_start, t_end, mark0, mark1, mark2, 0),
- * %globaltimer nanoseconds: the dependency wait began / ended, the task's
- * outputs were complete (before its dependents are released), and marks
- * inside the body (GEMV and PARTIAL: first ring slot ready, all slots
- * consumed, epilogue or merge done; 0 where unused). */
+ * (cta << 32 | smid, t_wait_begin, t_start, t_end, mark0, mark1, mark2,
+ * ring_waits), %globaltimer nanoseconds: the dependency wait began /
+ * ended, the task's outputs were complete (before its dependents are
+ * released), and marks inside the body (GEMV and PARTIAL: first ring slot
+ * ready, all slots consumed, epilogue or merge done; 0 where unused);
+ * ring_waits counts the task's ring slots whose copies had not landed when
+ * the consumers reached them. */
 int mk_get_trace(mk_graph* g, const uint64_t** records, size_t* count);
 
 /* Bytes of shared memory the kernel uses per CTA and its thread count. */

@@ -309,6 +309,7 @@ struct Ctx {
   int nst;
   int task;
   uint64_t mark[3];  // optional trace marks inside a task body (thread 0)
+  uint32_t ring_waits;  // traced: ring slots thread 0 found not yet landed
 };
 
 __device__ __forceinline__ void trace_mark(Ctx& c, int i) {
@@ -321,7 +322,10 @@ __device__ __forceinline__ void trace_mark(Ctx& c, int i) {
 __device__ __forceinline__ uint32_t consume_begin(Ctx& c) {
   const uint32_t slot = c.rp.slot, ph = c.rp.phase;
   c.rp.advance(c.nst);
-  if ((threadIdx.x & 31) == 0) bar_wait(*c.p, &c.full[slot], ph, c.task, true);
+  if ((threadIdx.x & 31) == 0) {
+    if (c.p->trace && threadIdx.x == 0 && !mbar_try_wait(&c.full[slot], ph)) ++c.ring_waits;
+    bar_wait(*c.p, &c.full[slot], ph, c.task, true);
+  }
   __syncwarp();
   return slot;
 }
@@ -420,7 +424,7 @@ __device__ __forceinline__ void gemv_load_x(float (&xr)[B][NV][8], float (&ss)[B
 
 // The tile's running argmax, and 1/rms = 1 when the input is not
 // normalised (a normalised input gets it from gemv_fold).  Once per task.
-__device__ __noinline__ void gemv_prologue(const mk_task_descriptor& d, const GemvGeom& G, float* red) {
+__device__ __forceinline__ void gemv_prologue(const mk_task_descriptor& d, const GemvGeom& G, float* red) {
   const int tid = threadIdx.x;
   if (!(d.flags & MK_F_RMS_NORM_INPUT) && tid < G.B) red[64 + tid] = 1.f;
   if ((d.flags & MK_F_ARGMAX_EPI) && tid < G.B) {
@@ -541,7 +545,7 @@ __device__ __forceinline__ void gemv_stages(Ctx& c, const mk_task_descriptor& d,
 
 // Fold one k-segment's per-warp partials into the accumulators, in a fixed
 // order (deterministic; no float atomics).
-__device__ __noinline__ void gemv_fold(const mk_task_descriptor& d, const GemvGeom& G, int rows_g, int ks,
+__device__ __forceinline__ void gemv_fold(const mk_task_descriptor& d, const GemvGeom& G, int rows_g, int ks,
                                        bool first_group, float* slots, float* acc, float* red) {
   cbar();
   for (int i = threadIdx.x; i < G.seg * rows_g * G.BT; i += kConsumerThreads) {
@@ -559,7 +563,7 @@ __device__ __noinline__ void gemv_fold(const mk_task_descriptor& d, const GemvGe
 
 // Epilogue of one row group: normalisation scale, SiLU*mul, residual,
 // store, and the tile's running argmax.
-__device__ __noinline__ void gemv_epilogue(const KParams& p, const mk_task_descriptor& d, const GemvGeom& G,
+__device__ __forceinline__ void gemv_epilogue(const KParams& p, const mk_task_descriptor& d, const GemvGeom& G,
                                            int g0, int rows_g, const float* acc, float* red,
                                            const float* staged_res) {
   const int tid = threadIdx.x;
@@ -1050,7 +1054,7 @@ __device__ bool level_barrier(const KParams& p, int k) {
 template <int BCLASS>
 __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64_t* empty, float* scratch,
                          volatile int* sflag) {
-  Ctx c{&p, ring, full, empty, scratch, RingPos{}, p.nstages, -1, {0, 0, 0}};
+  Ctx c{&p, ring, full, empty, scratch, RingPos{}, p.nstages, -1, {0, 0, 0}, 0u};
   Seq sq;
   seq_init(sq, p);
   int task, lvl, cur_lvl = 0;
@@ -1058,6 +1062,7 @@ __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
   while (seq_next(sq, p, task, lvl)) {
     c.task = task;
     c.mark[0] = c.mark[1] = c.mark[2] = 0;
+    c.ring_waits = 0;
     const mk_task_descriptor d = load_desc(p.tasks + task);
     uint64_t t_wait = 0, t_start = 0;
     if (tid < 32) {  // warp 0 waits (MEGA: all lanes; other modes: thread 0)
@@ -1100,7 +1105,7 @@ __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
       r[4] = c.mark[0];
       r[5] = c.mark[1];
       r[6] = c.mark[2];
-      r[7] = 0;
+      r[7] = c.ring_waits;
     }
     if (p.mode == MK_MODE_MEGA && tid < 32) {
       // release: one gpu-scope fence per signalling lane (covering, through
