@@ -212,6 +212,24 @@ def run_reference(args, workload):
     print(json.dumps(line), flush=True)
 
 
+def reduce_max(x, ws, device=None):
+    """Max over ranks of a float (the slowest replica sets the time); the
+    value itself at world size 1."""
+    if ws == 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(B, steps, seconds, ws):
+    """Whole-job tokens/s: every replica decodes B sequences per step, the
+    job takes as long as its slowest replica."""
+    return B * steps / seconds * ws
+
+
 def config_dict(args, w):
     name = WORKLOAD_NAMES[args.config] + (f", truncated to {w.model.L} layers" if args.layers else "")
     return {"workload": name, "B": w.B, "kv_len_start": list(w.kv_len)[:8],
@@ -298,13 +316,9 @@ def main():
     with ClockSampler(lr) as clk:
         ms, nbytes = timed(L.MK_MODE_MEGA, args.steps, args.warmup)
     clocks = clk.summary()
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = reduce_max(ms, ws, dev)
     ms_step = ms / args.steps
-    tok_s = w.B * args.steps / (ms / 1000.0) * ws
+    tok_s = job_throughput(w.B, args.steps, ms / 1000.0, ws)
     hbm_peak, peak_kind = measured_peaks()
     achieved = nbytes / args.steps / (ms_step / 1000.0) / 1e9
 
@@ -321,8 +335,8 @@ def main():
         cur[:, 0] = tok_h
         cur[:, 1] += 1
     barrier()
-    e2e_s = time.perf_counter() - t0
-    e2e = {"value": w.B * args.steps / e2e_s * ws, "unit": "tokens/s", "h2d_bytes_per_step": 8 * w.B,
+    e2e_s = reduce_max(time.perf_counter() - t0, ws, dev)
+    e2e = {"value": job_throughput(w.B, args.steps, e2e_s, ws), "unit": "tokens/s", "h2d_bytes_per_step": 8 * w.B,
            "d2h_bytes_per_step": 4 * w.B, "ms_per_step": 1000.0 * e2e_s / args.steps}
 
     modes = {}
@@ -339,7 +353,7 @@ def main():
         return
 
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and ws == 1:  # the oracle baseline is timed at N=1 only
         cpu = oracle_sample(base, repeats=2)
         cpu.pop("seconds_per_step", None)
 
