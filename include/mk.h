@@ -259,6 +259,16 @@ int mk_get_queues(const mk_graph* g, const int32_t** offsets, const int32_t** ta
  * Errors: MK_ERR_STATE (not lowered), MK_ERR_CUDA, MK_ERR_NOMEM. */
 int mk_upload(mk_graph* g, void* stream);
 
+/* Number of GEMV tiles of an uploaded graph that run on the tensor-core
+ * path: tiles of batch-8 ops (config_id 1) whose K is a multiple of 64.
+ * Their weights stream through TMA tensor copies (a tensor map per weight
+ * buffer, built by mk_upload) and multiply on tcgen05 tensor cores with
+ * f32 accumulators in tensor memory; the activations enter as three
+ * bf16 parts (hi + mid + lo), which carry x to about f32 precision.
+ * Other tiles run on CUDA cores.  Errors: MK_ERR_STATE (not uploaded),
+ * MK_ERR_ARG. */
+int mk_gemv_tensor_core_tiles(const mk_graph* g, int* tiles);
+
 /* One decode step with the persistent kernel (MK_MODE_MEGA). */
 int mk_decode_step(mk_graph* g, void* stream);
 

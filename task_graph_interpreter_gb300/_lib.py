@@ -31,7 +31,7 @@ EXPORTS = [
     "mk_lower", "mk_get_tasks", "mk_get_edges", "mk_get_sync_plan", "mk_get_queues", "mk_upload",
     "mk_decode_step", "mk_decode_step_ex", "mk_decode_step_host", "mk_status",
     "mk_get_trace", "mk_kernel_info", "mk_destroy", "mk_last_error", "mk_debug_patch_task",
-    "mk_attention_decode_noalloc",
+    "mk_attention_decode_noalloc", "mk_gemv_tensor_core_tiles",
 ]
 
 
@@ -85,6 +85,7 @@ def lib():
         "mk_kernel_info": (c_int, [G, POINTER(c_int), POINTER(c_int), POINTER(c_int)]),
         "mk_destroy": (None, [G]),
         "mk_debug_patch_task": (c_int, [G, c_int, c_void_p]),
+        "mk_gemv_tensor_core_tiles": (c_int, [G, POINTER(c_int)]),
         "mk_attention_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
                                                 c_int, c_int, c_int, POINTER(c_int32), POINTER(c_int32), c_int,
                                                 c_double]),
@@ -232,6 +233,12 @@ def mk_kernel_info(g):
 
 def mk_destroy(g):
     lib().mk_destroy(g)
+
+
+def mk_gemv_tensor_core_tiles(g) -> int:
+    n = c_int()
+    check(lib().mk_gemv_tensor_core_tiles(g, ctypes.byref(n)), "mk_gemv_tensor_core_tiles")
+    return n.value
 
 
 def mk_debug_patch_task(g, task: int, desc: bytes):

@@ -22,6 +22,9 @@ constexpr int kStageBytes = 32768;               // one ring slot
 constexpr int kStageElems = kStageBytes / 2;     // bf16 elements per slot
 constexpr int kMaxStages = 6;
 constexpr int kScratchBytes = 24576;             // per-task shared scratch
+constexpr int kXbufBytes = 24576;                // B >= 8 kernel: two 12 KB activation staging tiles
+constexpr int kTmemCols = 256;                   // B >= 8 kernel: tensor-memory accumulator columns
+constexpr int kTmapBytes = 128;                  // one CUtensorMap
 constexpr int kSlotFloats = 4096;                // GEMV per-warp partial slots
 constexpr int kAccFloats = 1024;                 // GEMV per-row accumulators
 
@@ -43,6 +46,8 @@ struct KParams {
   const int32_t* level_tasks; // LEVELS: task ids grouped by level
   uint32_t* level_bar;        // LEVELS: one arrival counter per level boundary
   int32_t* status;            // int32[4]
+  const uint8_t* tmaps;       // CUtensorMap per buffer index (tensor-core weights), kTmapBytes each
+  const int32_t* tm_rows;     // per buffer index: rows of its tensor map's box, 0 = no map
   const float* rope_cos;      // [cap, D/2]
   const float* rope_sin;
   uint64_t* trace;            // 8 x uint64 per task, or null
@@ -55,6 +60,6 @@ struct KParams {
   int32_t rope_half;          // D/2 of the tables
 };
 
-int smem_bytes_for(int nstages);
+int smem_bytes_for(int nstages, int batch);
 
 }  // namespace mk

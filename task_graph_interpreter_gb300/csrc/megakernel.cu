@@ -162,6 +162,23 @@ __device__ __forceinline__ void gemv_geom(const mk_task_descriptor& d, GemvGeom&
   g.RG = min(rg, g.cn);
 }
 
+// Tensor-core tile plan (B = 8): row groups of RG rows (the TMA box), N =
+// RG rounded up to 16, nkb K blocks of 64 columns per ring slot.
+struct TcGeom {
+  int RG, Nr, nkb, nkr, seg, K;
+};
+
+__device__ __forceinline__ void tc_geom(const KParams& p, const mk_task_descriptor& d, TcGeom& t) {
+  t.RG = p.tm_rows[d.in_buf[1]];
+  t.Nr = (t.RG + 15) & ~15;
+  t.seg = (d.flags & MK_F_SILU_MUL) ? 2 : 1;
+  t.K = d.k;
+  const int nkbt = d.k / 64;
+  t.nkb = 4;  // K blocks per slot: the staged activations of 4 blocks fill one 12 KB tile
+  while (t.nkb > 1 && (t.nkb * t.Nr * 128 > kStageBytes || nkbt % t.nkb)) t.nkb >>= 1;
+  t.nkr = nkbt / t.nkb;
+}
+
 // ------------------------------------------------------------------ PARTIAL plan
 struct PartGeom {
   int s, g, Hkv, c, P, slot, D, Hq, G, cap, pos, j0, j1, jst, R, nstage;
@@ -242,6 +259,27 @@ __device__ void producer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
   int task, lvl;
   while (!stop && seq_next(sq, p, task, lvl)) {
     const mk_task_descriptor d = load_desc(p.tasks + task);
+    if (d.op_id == MK_OP_GEMV && d.config_id == 1 && p.tm_rows[d.in_buf[1]] > 0) {
+      // tensor-core tile: per K range and segment one slot of nkb K blocks,
+      // each a TMA box of 64 columns x RG rows in the 128-byte swizzle
+      TcGeom T;
+      tc_geom(p, d, T);
+      const uint8_t* tmap = p.tmaps + (size_t)d.in_buf[1] * kTmapBytes;
+      const int c0 = (int)d.reserved[0], cn = (int)d.reserved[1];
+      if (d.flags & MK_F_RMS_NORM_INPUT) prefetch_l2(p.bufs[d.in_buf[2]], (uint32_t)d.k * 2u);
+      for (int g0 = 0; g0 < cn && !stop; g0 += T.RG)
+        for (int kr = 0; kr < T.nkr && !stop; ++kr)
+          for (int sg = 0; sg < T.seg; ++sg) {
+            uint64_t* fb;
+            uint8_t* dst =
+                produce_slot(p, ring, full, empty, rp, issued, task, (uint32_t)(T.nkb * T.RG * 128), &fb);
+            if (!dst) { stop = true; break; }
+            const int row = (sg ? d.n : 0) + c0 + g0;
+            for (int kb = 0; kb < T.nkb; ++kb)
+              tma_load_2d(dst + (size_t)kb * T.Nr * 128, tmap, (kr * T.nkb + kb) * 64, row, fb, pol);
+          }
+      continue;
+    }
     if (d.op_id == MK_OP_GEMV) {
       GemvGeom G;
       gemv_geom(d, G);
@@ -310,6 +348,10 @@ struct Ctx {
   int task;
   uint64_t mark[3];  // optional trace marks inside a task body (thread 0)
   uint32_t ring_waits;  // traced: ring slots thread 0 found not yet landed
+  uint8_t* xbuf;        // B >= 8 kernel: activation staging tiles (tensor-core A operand)
+  uint64_t* mma_bar;    // two mbarriers the tensor-core commits arrive on
+  uint32_t taddr;       // tensor-memory accumulator base
+  uint32_t mma_done;    // thread 0: completed phases seen on mma_bar[0] (bit 0) and [1] (bit 1)
 };
 
 __device__ __forceinline__ void trace_mark(Ctx& c, int i) {
@@ -656,6 +698,177 @@ __device__ void gemv_task(Ctx& c, const mk_task_descriptor& d) {
   }
   if ((d.flags & MK_F_ARGMAX_EPI) && threadIdx.x < G.B) {
     mk_argmax_pair* pairs = static_cast<mk_argmax_pair*>(c.p->bufs[d.reserved[3]]);
+    mk_argmax_pair pr;
+    pr.value = red[96 + threadIdx.x];
+    pr.index = reinterpret_cast<int*>(red)[104 + threadIdx.x];
+    pairs[(size_t)d.reserved[4] * G.B + threadIdx.x] = pr;
+  }
+}
+
+// ------------------------------------------------------------------ GEMV on tensor cores (B = 8)
+// At batch 8 a tile is a real dense contraction (8 columns of x against the
+// tile's weight rows), so it runs on the 5th-generation tensor cores:
+// D[128 x N] (+)= A[128 x K] * B[K x N] with
+//   B = the tile's weight rows (N = rows rounded up to 16), K-major, brought
+//       in by TMA tensor copies in the 128-byte-swizzled layout, 64 K per row;
+//   A = the activations, split into three bf16 parts hi + mid + lo that
+//       carry x to about f32 precision (A rows 0-7, 8-15, 16-23 hold the
+//       parts of batch rows 0-7; the other 104 rows read whatever follows
+//       and are never used);
+//   D = f32 accumulators in tensor memory, y[b] = D[b] + D[8+b] + D[16+b].
+// One thread issues the MMAs; a commit per K range arrives on an mbarrier,
+// which releases that range's ring slots and staging tile.
+// This thread's share of one K range of x: batch row = warp, kpt = 2 * nkb
+// consecutive columns from k0 (rows past the batch read as zero).
+__device__ __forceinline__ void tc_load_x(float (&xv)[16], const float* x, int K, int b, int Bact, int k0,
+                                          int kpt) {
+#pragma unroll
+  for (int e = 0; e < 16; e += 2) {
+    float2 v = make_float2(0.f, 0.f);
+    if (e < kpt && b < Bact) v = __ldcg(reinterpret_cast<const float2*>(x + (size_t)b * K + k0 + e));
+    xv[e] = v.x;
+    xv[e + 1] = v.y;
+  }
+}
+
+__device__ void tc_gemv_task(Ctx& c, const mk_task_descriptor& d) {
+  const KParams& p = *c.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  GemvGeom G;
+  gemv_geom(d, G);
+  TcGeom T;
+  tc_geom(p, d, T);
+  float* red = gemv_red(c);
+  float* acc = c.scratch;  // [seg * rows][8] results (the GEMV slot area is unused here)
+  gemv_prologue(d, G, red);
+  const float* x = static_cast<const float*>(p.bufs[d.in_buf[0]]);
+  const uint16_t* gamma =
+      (d.flags & MK_F_RMS_NORM_INPUT) ? static_cast<const uint16_t*>(p.bufs[d.in_buf[2]]) : nullptr;
+  const int kpt = 2 * T.nkb;  // columns of x per lane and K range
+  const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)T.Nr);
+  const uint32_t xb0 = smem_addr(c.xbuf);
+  float ss = 0.f;  // sum of squares of this lane's raw x (first row group)
+  RingPos rel = c.rp;  // thread 0: next ring slot to hand back
+  bool ok = true;      // thread 0: every wait so far succeeded
+  for (int g0 = 0; g0 < G.cn; g0 += T.RG) {
+    const int rows_g = min(T.RG, G.cn - g0);
+    float xn[16];
+    tc_load_x(xn, x, T.K, warp, G.B, lane * kpt, kpt);
+    for (int kr = 0; kr < T.nkr; ++kr) {
+      float xc[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) xc[e] = xn[e];
+      const int k0 = kr * T.nkb * 64 + lane * kpt;  // this lane's first column
+      if (kr + 1 < T.nkr) tc_load_x(xn, x, T.K, warp, G.B, k0 + T.nkb * 64, kpt);
+      // the MMAs of the previous K range are done: its slots go back to the
+      // producer and its staging tile (two ranges ago) is free
+      if (tid == 0 && kr > 0) {
+        const int j = (kr - 1) & 1;
+        if (!bar_wait(p, &c.mma_bar[j], (c.mma_done >> j) & 1u, c.task, false)) ok = false;
+        c.mma_done ^= 1u << j;
+        for (int sg = 0; sg < T.seg; ++sg) {
+          mbar_arrive_cnt(&c.empty[rel.slot], kConsumerWarps);
+          rel.advance(c.nst);
+        }
+      }
+      cbar();
+      // stage x (times the gain) as bf16 hi / lo rows of the A tile
+      const uint32_t xt = xb0 + (uint32_t)(kr & 1) * (kXbufBytes / 2);  // K block b at xt + b * 3072
+#pragma unroll
+      for (int e = 0; e < 16; e += 2) {
+        if (e < kpt) {
+          const int kl = lane * kpt + e;  // column within the K range
+          const int kb = kl >> 6, kk = kl & 63;
+          float v0 = xc[e], v1 = xc[e + 1];
+          if (g0 == 0) ss += v0 * v0 + v1 * v1;
+          if (gamma) {
+            const uint32_t gw = __ldg(reinterpret_cast<const uint32_t*>(gamma + k0 + e));
+            v0 *= bf_lo(gw);
+            v1 *= bf_hi(gw);
+          }
+          // exact three-part split: each part is the bf16 rounding of what
+          // the previous parts leave (f32 subtractions of nearby values)
+          uint32_t part[3];
+#pragma unroll
+          for (int q = 0; q < 3; ++q) {
+            const __nv_bfloat16 a0 = __float2bfloat16_rn(v0), a1 = __float2bfloat16_rn(v1);
+            part[q] = (uint32_t)__bfloat16_as_ushort(a0) | ((uint32_t)__bfloat16_as_ushort(a1) << 16);
+            v0 -= __bfloat162float(a0);
+            v1 -= __bfloat162float(a1);
+          }
+          // row r of a K block sits at r * 128 bytes; its 16-byte chunk c is
+          // stored at chunk c ^ (row within the 1024-byte group), as the
+          // 128-byte swizzle reads it
+          const uint32_t ch = (uint32_t)(kk >> 3), cb = (uint32_t)(kk & 7) * 2u;
+#pragma unroll
+          for (int q = 0; q < 3; ++q) {
+            const uint32_t ra = xt + (uint32_t)kb * 3072u + (uint32_t)q * 1024u + (uint32_t)warp * 128u;
+            sts32(ra + ((ch ^ ((ra >> 7) & 7u)) << 4) + cb, part[q]);
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      cbar();
+      if (tid == 0) {
+        for (int sg = 0; sg < T.seg; ++sg) {
+          const uint32_t slot = c.rp.slot, ph = c.rp.phase;
+          if (ok && !bar_wait(p, &c.full[slot], ph, c.task, true)) ok = false;
+          tc_fence_after();
+          if (ok) {
+            const uint32_t wb = smem_addr(c.ring + (size_t)slot * kStageBytes);
+            const uint32_t dcol = c.taddr + (uint32_t)(sg * T.Nr);
+            for (int kb = 0; kb < T.nkb; ++kb)
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) {
+                const uint64_t ad = smem_desc_sw128(xt + (uint32_t)kb * 3072u + (uint32_t)ks * 32u, 1024u);
+                const uint64_t bd =
+                    smem_desc_sw128(wb + (uint32_t)(kb * T.Nr * 128) + (uint32_t)ks * 32u, 1024u);
+                tc_mma_bf16(dcol, ad, bd, idesc, (kr | kb | ks) != 0 ? 1u : 0u);
+              }
+          }
+          c.rp.advance(c.nst);
+        }
+        tc_commit(&c.mma_bar[kr & 1]);  // arrives once the MMAs issued so far are done
+      } else {
+        for (int sg = 0; sg < T.seg; ++sg) c.rp.advance(c.nst);
+      }
+    }
+    // last K range: wait for its MMAs, hand back its slots
+    if (tid == 0) {
+      const int j = (T.nkr - 1) & 1;
+      if (!bar_wait(p, &c.mma_bar[j], (c.mma_done >> j) & 1u, c.task, false)) ok = false;
+      c.mma_done ^= 1u << j;
+      for (int sg = 0; sg < T.seg; ++sg) {
+        mbar_arrive_cnt(&c.empty[rel.slot], kConsumerWarps);
+        rel.advance(c.nst);
+      }
+    }
+    if (g0 == 0 && gamma) {  // 1/rms per batch row (warp b holds row b's columns)
+      const float t = warp_sum(ss);
+      if (lane == 0) red[64 + warp] = 1.0f / sqrtf(t / (float)T.K + __uint_as_float(d.reserved[2]));
+    }
+    tc_fence_before();
+    cbar();
+    if (warp == 0) {  // TMEM lanes 0-31 = A rows: the batch's hi, mid, lo parts in 0-7, 8-15, 16-23
+      tc_fence_after();
+      for (int sg = 0; sg < T.seg; ++sg)
+        for (int j0 = 0; j0 < rows_g; j0 += 16) {
+          float v[16];
+          tmem_ld16(c.taddr + (uint32_t)(sg * T.Nr + j0), v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float mid = __shfl_down_sync(0xffffffffu, v[i], 8);
+            const float lo = __shfl_down_sync(0xffffffffu, v[i], 16);
+            if (lane < 8 && j0 + i < rows_g) acc[(sg * rows_g + j0 + i) * 8 + lane] = v[i] + mid + lo;
+          }
+        }
+      tc_fence_before();
+    }
+    cbar();
+    gemv_epilogue(p, d, G, g0, rows_g, acc, red, nullptr);
+  }
+  if ((d.flags & MK_F_ARGMAX_EPI) && threadIdx.x < G.B) {
+    mk_argmax_pair* pairs = static_cast<mk_argmax_pair*>(p.bufs[d.reserved[3]]);
     mk_argmax_pair pr;
     pr.value = red[96 + threadIdx.x];
     pr.index = reinterpret_cast<int*>(red)[104 + threadIdx.x];
@@ -1053,8 +1266,8 @@ __device__ bool level_barrier(const KParams& p, int k) {
 
 template <int BCLASS>
 __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64_t* empty, float* scratch,
-                         volatile int* sflag) {
-  Ctx c{&p, ring, full, empty, scratch, RingPos{}, p.nstages, -1, {0, 0, 0}, 0u};
+                         volatile int* sflag, uint8_t* xbuf, uint64_t* mma_bar, uint32_t taddr) {
+  Ctx c{&p, ring, full, empty, scratch, RingPos{}, p.nstages, -1, {0, 0, 0}, 0u, xbuf, mma_bar, taddr, 0u};
   Seq sq;
   seq_init(sq, p);
   int task, lvl, cur_lvl = 0;
@@ -1082,7 +1295,15 @@ __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
     cbar();
     if (!*sflag) return;
     switch (d.op_id) {
-      case MK_OP_GEMV: gemv_task<BCLASS>(c, d); break;
+      case MK_OP_GEMV:
+        if constexpr (BCLASS == 2) {
+          if (d.config_id == 1 && p.tm_rows[d.in_buf[1]] > 0) {
+            tc_gemv_task(c, d);
+            break;
+          }
+        }
+        gemv_task<BCLASS>(c, d);
+        break;
       case MK_OP_ATTENTION_APPEND: append_task(c, d); break;
       case MK_OP_ATTENTION_PARTIAL: partial_task(c, d); break;
       case MK_OP_ATTENTION_COMBINE: combine_task(c, d); break;
@@ -1122,8 +1343,11 @@ __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
   }
 }
 
-int smem_bytes_for(int nstages) {
-  return nstages * kStageBytes + 2 * nstages * 8 + 16 + kScratchBytes;
+// Shared memory: [activation staging (B >= 8 kernel)] [ring] [full, empty
+// mbarriers] [32-byte control: run flag, TMEM address, two MMA mbarriers]
+// [scratch].
+int smem_bytes_for(int nstages, int batch) {
+  return (batch > 4 ? kXbufBytes : 0) + nstages * kStageBytes + 2 * nstages * 8 + 32 + kScratchBytes;
 }
 
 template <int BCLASS>
@@ -1135,25 +1359,52 @@ __global__ void __launch_bounds__(kThreads, 1) mk_interpreter_kernel(const __gri
   // refuses to launch if the compiled kernel's count differs).
   extern __shared__ __align__(1024) uint8_t smem[];
   const int nst = p.nstages;
-  uint8_t* ring = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)nst * kStageBytes);
+  constexpr int xbytes = BCLASS == 2 ? kXbufBytes : 0;
+  uint8_t* xbuf = smem;
+  uint8_t* ring = smem + xbytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)nst * kStageBytes);
   uint64_t* empty = full + nst;
   volatile int* sflag = reinterpret_cast<volatile int*>(empty + nst);
-  float* scratch = reinterpret_cast<float*>(smem + (size_t)nst * kStageBytes + 2 * nst * 8 + 16);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty + nst) + 1;
+  uint64_t* mma_bar = empty + nst + 2;
+  float* scratch = reinterpret_cast<float*>(ring + (size_t)nst * kStageBytes + 2 * nst * 8 + 32);
+  // the swizzled operand layouts assume 1024-byte aligned tiles
+  const bool aligned = (smem_addr(smem) & 1023u) == 0;
   if (threadIdx.x == 0) {
     for (int i = 0; i < nst; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
     }
+    mbar_init(&mma_bar[0], 1);
+    mbar_init(&mma_bar[1], 1);
     fence_mbar_init();
+    if (BCLASS == 2 && !aligned) raise_error(p, MK_DEV_BAD_OP, -1);
+  }
+  if constexpr (BCLASS == 2) {
+    if (threadIdx.x < 32) {  // one warp allocates the accumulator columns
+      tmem_alloc(tmem_slot, kTmemCols);
+      tmem_relinquish();
+    }
+    tc_fence_before();
   }
   __syncthreads();
+  if constexpr (BCLASS == 2) tc_fence_after();
+  const uint32_t taddr = BCLASS == 2 ? *tmem_slot : 0u;
   if (threadIdx.x >= kConsumerThreads) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
     if (threadIdx.x < kConsumerThreads + 32) producer(p, ring, full, empty);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
-    consumer<BCLASS>(p, ring, full, empty, scratch, sflag);
+    if (BCLASS != 2 || aligned) consumer<BCLASS>(p, ring, full, empty, scratch, sflag, xbuf, mma_bar, taddr);
+    if (BCLASS == 2) {
+      // every tensor-core operation this CTA issued has completed (each
+      // tensor task waits for its commits); free the columns
+      named_bar_sync(1, kConsumerThreads);
+      if (threadIdx.x < 32) {
+        tc_fence_after();
+        tmem_dealloc(taddr, kTmemCols);
+      }
+    }
   }
 }
 
@@ -1167,9 +1418,10 @@ static const void* kernel_for(int batch) {
                     : batch <= 4 ? (const void*)mk_interpreter_kernel<1> : (const void*)mk_interpreter_kernel<2>;
 }
 
-cudaError_t configure_interpreter(int batch, int* num_regs) {
+cudaError_t configure_interpreter(int batch, int nstages, int* num_regs) {
   const void* fn = kernel_for(batch);
-  cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_for(kMaxStages));
+  cudaError_t e =
+      cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes_for(nstages, batch));
   if (e != cudaSuccess) return e;
   cudaFuncAttributes attr;
   e = cudaFuncGetAttributes(&attr, fn);
@@ -1179,7 +1431,7 @@ cudaError_t configure_interpreter(int batch, int* num_regs) {
 }
 
 cudaError_t launch_interpreter(const KParams& p, int batch, int grid, bool cooperative, cudaStream_t stream) {
-  const int smem = smem_bytes_for(p.nstages);
+  const int smem = smem_bytes_for(p.nstages, batch);
   const void* fn = kernel_for(batch);
   void* args[] = {const_cast<KParams*>(&p)};
   if (cooperative)
@@ -1188,7 +1440,8 @@ cudaError_t launch_interpreter(const KParams& p, int batch, int grid, bool coope
 }
 
 cudaError_t max_coresident_ctas(int batch, int nstages, int* per_sm) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, kernel_for(batch), kThreads, smem_bytes_for(nstages));
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, kernel_for(batch), kThreads,
+                                                       smem_bytes_for(nstages, batch));
 }
 
 }  // namespace mk

@@ -7,6 +7,7 @@
 // restore between runs, this runtime keeps the descriptors immutable and
 // makes dependency counters monotone: step e waits for counter >= e * deps,
 // so nothing has to be restored between steps.
+#include <cuda.h>  // CUtensorMap types; the encoder is fetched through the runtime
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -19,7 +20,7 @@
 
 namespace mk {
 
-cudaError_t configure_interpreter(int batch, int* num_regs);
+cudaError_t configure_interpreter(int batch, int nstages, int* num_regs);
 cudaError_t launch_interpreter(const KParams& p, int batch, int grid, bool cooperative, cudaStream_t stream);
 cudaError_t max_coresident_ctas(int batch, int nstages, int* per_sm);
 
@@ -36,6 +37,9 @@ struct DeviceState {
   uint32_t* sig_off = nullptr;
   uint32_t* sig = nullptr;
   size_t counter_words = 0;
+  uint8_t* tmaps = nullptr;
+  int32_t* tm_rows = nullptr;
+  int tc_tiles = 0;  // GEMV tiles on the tensor-core path
   int32_t* queue_off = nullptr;
   int32_t* queue = nullptr;
   int32_t* level_off = nullptr;
@@ -93,6 +97,8 @@ KParams base_params(const mk_graph* g) {
   p.wait = d->wait;
   p.sig_off = d->sig_off;
   p.sig = d->sig;
+  p.tmaps = d->tmaps;
+  p.tm_rows = d->tm_rows;
   p.queue_off = d->queue_off;
   p.queue = d->queue;
   p.level_off = d->level_off;
@@ -110,6 +116,62 @@ KParams base_params(const mk_graph* g) {
   p.nstages = d->nstages;
   p.rope_half = g->rope_D / 2;
   return p;
+}
+
+// Tensor maps of the weights that B >= 8 GEMV tiles stream through the
+// tensor-core path: a 2-D bf16 view [rows, K] with a box of 64 columns x RG
+// rows in the 128-byte swizzle.  RG splits the op's tile width into row
+// groups of at most 256 rows (128 per segment for SILU_MUL: gate and up
+// share the 256 accumulator columns).  Ops with K not a multiple of 64 stay
+// on the CUDA-core path (tm_rows 0).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int build_tensor_maps(const mk_graph* g, std::vector<uint8_t>& maps, std::vector<int32_t>& rows) {
+  const size_t NB = g->bufs.size();
+  maps.assign(NB * kTmapBytes, 0);
+  rows.assign(NB, 0);
+  EncodeTiledFn enc = nullptr;
+  for (const OpRec& op : g->ops) {
+    if (op.kind != K_MATMUL || op.B < 8 || op.k % 64 != 0) continue;
+    const int seg = (op.flags & MK_F_SILU_MUL) ? 2 : 1;
+    const int cw = tile_width(op.n, g->tiles_target, g->col_align);
+    const int rgmax = seg == 2 ? 128 : 256;
+    const int ng = (cw + rgmax - 1) / rgmax;
+    const int rg = (cw + ng - 1) / ng;
+    const int w = op.a[1];
+    if (rows[w] != 0) {
+      if (rows[w] != rg) return fail(MK_ERR_ARG, "mk_upload: weight buffer " + std::to_string(w) +
+                                                   " used by B >= 8 GEMVs with different tile widths");
+      continue;
+    }
+    if (!enc) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return fail(MK_ERR_CUDA, "mk_upload: cuTensorMapEncodeTiled is not available");
+      enc = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    const BufferRec& b = g->bufs[w];
+    CUtensorMap m;
+    const cuuint64_t gdim[2] = {(cuuint64_t)op.k, (cuuint64_t)b.rows};
+    const cuuint64_t gstride[1] = {(cuuint64_t)op.k * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)rg};
+    const cuuint32_t estride[2] = {1u, 1u};
+    const CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, b.ptr, gdim, gstride, box, estride,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return fail(MK_ERR_CUDA, "mk_upload: tensor map of buffer " + std::to_string(w) + " failed (" +
+                                   std::to_string((int)r) + ")");
+    static_assert(sizeof(CUtensorMap) == kTmapBytes, "tensor map size");
+    std::memcpy(maps.data() + (size_t)w * kTmapBytes, &m, kTmapBytes);
+    rows[w] = rg;
+  }
+  return MK_OK;
 }
 
 int launch_per_op(mk_graph* g, cudaStream_t stream, uint64_t* trace) {
@@ -141,9 +203,9 @@ extern "C" int mk_upload(mk_graph* g, void* stream_) {
     int optin = 0;
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d->device);
     d->nstages = kMaxStages;
-    while (d->nstages > 2 && smem_bytes_for(d->nstages) > optin) --d->nstages;
+    while (d->nstages > 2 && smem_bytes_for(d->nstages, g->B) > optin) --d->nstages;
     int regs = 0;
-    if (configure_interpreter(g->B, &regs) != cudaSuccess) {
+    if (configure_interpreter(g->B, d->nstages, &regs) != cudaSuccess) {
       rc = fail(MK_ERR_CUDA, "mk_upload: cannot configure the interpreter kernel");
       break;
     }
@@ -166,6 +228,9 @@ extern "C" int mk_upload(mk_graph* g, void* stream_) {
     }
     const size_t N = g->tasks.size(), E = g->edges.size(), NB = g->bufs.size();
     const int half = g->rope_D / 2, cap = g->rope_cap;
+    std::vector<uint8_t> tmaps;
+    std::vector<int32_t> tm_rows;
+    if ((rc = build_tensor_maps(g, tmaps, tm_rows)) != MK_OK) break;
     // blob layout: header | tasks | edges | queue_off | queue | level_off | level_tasks | bufs | cos | sin |
     //              wait_off | wait | sig_off | sig, then (zeroed) counters | status | level_bar | trace
     size_t off = 0;
@@ -179,7 +244,8 @@ extern "C" int mk_upload(mk_graph* g, void* stream_) {
                  o_loff = take(g->level_off.size() * 4), o_lt = take(g->level_tasks.size() * 4),
                  o_bufs = take(NB * 8), o_cos = take((size_t)cap * half * 4), o_sin = take((size_t)cap * half * 4),
                  o_woff = take(g->wait_off.size() * 4), o_wait = take(g->wait.size() * 4),
-                 o_soff = take(g->sig_off.size() * 4), o_sig = take(g->sig.size() * 4);
+                 o_soff = take(g->sig_off.size() * 4), o_sig = take(g->sig.size() * 4),
+                 o_tmap = take(tmaps.size()), o_tmr = take(tm_rows.size() * 4);
     const size_t static_bytes = off;
     const size_t o_ctr = take((size_t)g->counter_words * 4), o_status = take(16), o_lbar = take(g->level_off.size() * 4),
                  o_trace = take(N * 64);
@@ -202,6 +268,8 @@ extern "C" int mk_upload(mk_graph* g, void* stream_) {
     std::memcpy(img.data() + o_wait, g->wait.data(), g->wait.size() * 4);
     std::memcpy(img.data() + o_soff, g->sig_off.data(), g->sig_off.size() * 4);
     std::memcpy(img.data() + o_sig, g->sig.data(), g->sig.size() * 4);
+    std::memcpy(img.data() + o_tmap, tmaps.data(), tmaps.size());
+    std::memcpy(img.data() + o_tmr, tm_rows.data(), tm_rows.size() * 4);
     char* base = static_cast<char*>(d->blob);
     std::vector<void*> ptrs(NB);
     for (size_t i = 0; i < NB; ++i) ptrs[i] = g->bufs[i].ptr;
@@ -241,6 +309,10 @@ extern "C" int mk_upload(mk_graph* g, void* stream_) {
     d->wait = reinterpret_cast<uint2*>(base + o_wait);
     d->sig_off = reinterpret_cast<uint32_t*>(base + o_soff);
     d->sig = reinterpret_cast<uint32_t*>(base + o_sig);
+    d->tmaps = reinterpret_cast<uint8_t*>(base + o_tmap);
+    d->tm_rows = reinterpret_cast<int32_t*>(base + o_tmr);
+    for (const mk_task_descriptor& t : g->tasks)
+      if (t.op_id == MK_OP_GEMV && t.config_id == 1 && g->B > 4 && tm_rows[t.in_buf[1]] > 0) ++d->tc_tiles;
     d->status = reinterpret_cast<int32_t*>(base + o_status);
     d->level_bar = reinterpret_cast<uint32_t*>(base + o_lbar);
     d->trace = reinterpret_cast<uint64_t*>(base + o_trace);
@@ -367,9 +439,16 @@ extern "C" int mk_get_trace(mk_graph* g, const uint64_t** records, size_t* count
 extern "C" int mk_kernel_info(const mk_graph* g, int* smem_bytes, int* threads, int* stages) {
   if (!g || !smem_bytes || !threads || !stages) return fail(MK_ERR_ARG, "mk_kernel_info: null argument");
   const int nst = g->dev ? g->dev->nstages : kMaxStages;
-  *smem_bytes = smem_bytes_for(nst);
+  *smem_bytes = smem_bytes_for(nst, g->B);
   *threads = kThreads;
   *stages = nst;
+  return MK_OK;
+}
+
+extern "C" int mk_gemv_tensor_core_tiles(const mk_graph* g, int* tiles) {
+  if (!g || !tiles) return fail(MK_ERR_ARG, "mk_gemv_tensor_core_tiles: null argument");
+  if (!g->uploaded) return fail(MK_ERR_STATE, "mk_gemv_tensor_core_tiles: call mk_upload first");
+  *tiles = g->dev->tc_tiles;
   return MK_OK;
 }
 

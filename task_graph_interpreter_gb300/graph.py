@@ -139,6 +139,10 @@ class Graph:
     def trace(self):
         return L.mk_get_trace(self.h)
 
+    def tensor_core_tiles(self) -> int:
+        """GEMV tiles that run on the tensor-core path (batch-8 ops)."""
+        return L.mk_gemv_tensor_core_tiles(self.h)
+
     def kernel_info(self):
         return L.mk_kernel_info(self.h)
 

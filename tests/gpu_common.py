@@ -67,12 +67,23 @@ def compare_step(dec, res, st_oracle, check_hidden=True):
 
 
 def compare_cache_rows(dec, st_oracle, pos_before):
-    """The rows appended this step match the oracle's within one bf16 ulp."""
+    """The rows appended this step match the oracle's within one bf16 ulp of
+    each element plus 2^-8 of the row's RMS.  The rows are bf16 roundings of
+    f32 values whose inputs carry the error accumulated over the layers
+    before (bounded for the hidden states by 1e-2 relative L2); elements far
+    below the row's magnitude can then round a few bf16 steps away, most of
+    all under the tensor cores' truncating f32 accumulation.  2^-8 of the
+    RMS stays well inside the hidden-state bound and far below the O(RMS)
+    errors of a wrong head, position or rotation."""
     for l in range(len(dec.kcache)):
         for which, bufs, ref in (("k", dec.kcache, st_oracle.kcache), ("v", dec.vcache, st_oracle.vcache)):
             t = bufs[l].tensor
             for s, p in enumerate(pos_before):
                 got = t[s, :, p, :].float().cpu().numpy().astype(np.float64)
                 want = of.bf16_to_f64(ref[l][s, :, p, :])
-                tol = np.abs(want) * 2.0 ** -7 + 1e-30
-                assert np.all(np.abs(got - want) <= tol), f"layer {l} {which} row {p} seq {s}"
+                tol = np.abs(want) * 2.0 ** -7 + 2.0 ** -8 * np.sqrt(np.mean(want ** 2)) + 1e-30
+                err = np.abs(got - want)
+                i = np.unravel_index(np.argmax(err - tol), err.shape)
+                assert np.all(err <= tol), (f"layer {l} {which} row {p} seq {s}: |err| {err[i]:.3g} at {i}, "
+                                            f"want {want[i]:.6g} got {got[i]:.6g}, row rms "
+                                            f"{np.sqrt(np.mean(want ** 2)):.3g}, max |err| {err.max():.3g}")
