@@ -18,6 +18,11 @@ constexpr int kProducerRegs = 40;   // after setmaxnreg.dec in the producer warp
 constexpr int kConsumerRegs = 232;  // after setmaxnreg.inc in the consumer warpgroups
 static_assert(128 * kProducerRegs + 2 * 128 * kConsumerRegs <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
+// The B >= 8 kernel's producer warpgroup also runs the MMA warp.
+constexpr int kProducerRegsTc = 56;
+constexpr int kConsumerRegsTc = 224;
+static_assert(128 * kProducerRegsTc + 2 * 128 * kConsumerRegsTc <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr int kStageBytes = 32768;               // one ring slot
 constexpr int kStageElems = kStageBytes / 2;     // bf16 elements per slot
 constexpr int kMaxStages = 6;

@@ -218,6 +218,24 @@ __device__ __forceinline__ void part_geom(const KParams& p, const mk_task_descri
   q.has_new = (q.j1 == L) && (q.j0 < q.j1);
 }
 
+// ------------------------------------------------------------------ control block
+// Shared-memory words and mbarriers after the ring's full/empty barriers.
+struct TcCtl {
+  volatile int32_t run;            // consumers: 1 while the current task may run
+  uint32_t tmem;                   // B >= 8 kernel: tensor-memory base address
+  volatile int32_t mb_task;        // mailbox to the MMA warp: task index, -1 = no more tasks
+  volatile uint32_t mb_slot;       //   ring slot and phase parity of its first weight slot
+  volatile uint32_t mb_phase;
+  uint32_t pad[3];
+  uint64_t mma_bar[2];             // commit of each K range (alternating)
+  uint64_t x_full[2];              // a K range's activations are staged (one arrival per consumer warp)
+  uint64_t acc_full;               // commit after a row group's last MMA
+  uint64_t acc_empty;              // the consumers have read the accumulators
+  uint64_t task_go;                // the mailbox holds a task
+};
+static_assert(sizeof(TcCtl) == 88, "control block layout");
+constexpr int kCtlBytes = 96;
+
 // ------------------------------------------------------------------ ring position
 // Slot index and mbarrier phase parity of the next ring use, advanced
 // without division (this runs once per slot in every warp).
@@ -349,9 +367,9 @@ struct Ctx {
   uint64_t mark[3];  // optional trace marks inside a task body (thread 0)
   uint32_t ring_waits;  // traced: ring slots thread 0 found not yet landed
   uint8_t* xbuf;        // B >= 8 kernel: activation staging tiles (tensor-core A operand)
-  uint64_t* mma_bar;    // two mbarriers the tensor-core commits arrive on
+  TcCtl* ctl;
   uint32_t taddr;       // tensor-memory accumulator base
-  uint32_t mma_done;    // thread 0: completed phases seen on mma_bar[0] (bit 0) and [1] (bit 1)
+  uint32_t tc_ph;       // completed phases seen: mma_bar[0] (bit 0), mma_bar[1] (bit 1), acc_full (bit 2)
 };
 
 __device__ __forceinline__ void trace_mark(Ctx& c, int i) {
@@ -720,10 +738,10 @@ __device__ void gemv_task(Ctx& c, const mk_task_descriptor& d) {
 // which releases that range's ring slots and staging tile.
 // This thread's share of one K range of x: batch row = warp, kpt = 2 * nkb
 // consecutive columns from k0 (rows past the batch read as zero).
-__device__ __forceinline__ void tc_load_x(float (&xv)[16], const float* x, int K, int b, int Bact, int k0,
+__device__ __forceinline__ void tc_load_x(float (&xv)[8], const float* x, int K, int b, int Bact, int k0,
                                           int kpt) {
 #pragma unroll
-  for (int e = 0; e < 16; e += 2) {
+  for (int e = 0; e < 8; e += 2) {
     float2 v = make_float2(0.f, 0.f);
     if (e < kpt && b < Bact) v = __ldcg(reinterpret_cast<const float2*>(x + (size_t)b * K + k0 + e));
     xv[e] = v.x;
@@ -731,9 +749,15 @@ __device__ __forceinline__ void tc_load_x(float (&xv)[16], const float* x, int K
   }
 }
 
+// Consumer side of a tensor-core tile: hand the task to the MMA warp, stage
+// each K range's activations (three bf16 parts, 128-byte swizzle) into one
+// of two staging tiles, read the accumulators from tensor memory at the
+// end of each row group, run the usual epilogue.  No CTA-wide barrier per K
+// range: the staging tile of range kr waits only for the MMAs of kr - 2.
 __device__ void tc_gemv_task(Ctx& c, const mk_task_descriptor& d) {
   const KParams& p = *c.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  TcCtl* ctl = c.ctl;
   GemvGeom G;
   gemv_geom(d, G);
   TcGeom T;
@@ -745,37 +769,38 @@ __device__ void tc_gemv_task(Ctx& c, const mk_task_descriptor& d) {
   const uint16_t* gamma =
       (d.flags & MK_F_RMS_NORM_INPUT) ? static_cast<const uint16_t*>(p.bufs[d.in_buf[2]]) : nullptr;
   const int kpt = 2 * T.nkb;  // columns of x per lane and K range
-  const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)T.Nr);
   const uint32_t xb0 = smem_addr(c.xbuf);
+  if (tid == 0) {  // the mbarrier arrive publishes the mailbox (release)
+    ctl->mb_task = c.task;
+    ctl->mb_slot = c.rp.slot;
+    ctl->mb_phase = c.rp.phase;
+    mbar_arrive(&ctl->task_go);
+  }
   float ss = 0.f;  // sum of squares of this lane's raw x (first row group)
-  RingPos rel = c.rp;  // thread 0: next ring slot to hand back
-  bool ok = true;      // thread 0: every wait so far succeeded
   for (int g0 = 0; g0 < G.cn; g0 += T.RG) {
     const int rows_g = min(T.RG, G.cn - g0);
-    float xn[16];
-    tc_load_x(xn, x, T.K, warp, G.B, lane * kpt, kpt);
+    // x of the next two K ranges is in flight while a range is staged
+    float xa[8], xb[8];
+    tc_load_x(xa, x, T.K, warp, G.B, lane * kpt, kpt);
+    if (T.nkr > 1) tc_load_x(xb, x, T.K, warp, G.B, T.nkb * 64 + lane * kpt, kpt);
     for (int kr = 0; kr < T.nkr; ++kr) {
-      float xc[16];
+      float xc[8];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) xc[e] = xn[e];
-      const int k0 = kr * T.nkb * 64 + lane * kpt;  // this lane's first column
-      if (kr + 1 < T.nkr) tc_load_x(xn, x, T.K, warp, G.B, k0 + T.nkb * 64, kpt);
-      // the MMAs of the previous K range are done: its slots go back to the
-      // producer and its staging tile (two ranges ago) is free
-      if (tid == 0 && kr > 0) {
-        const int j = (kr - 1) & 1;
-        if (!bar_wait(p, &c.mma_bar[j], (c.mma_done >> j) & 1u, c.task, false)) ok = false;
-        c.mma_done ^= 1u << j;
-        for (int sg = 0; sg < T.seg; ++sg) {
-          mbar_arrive_cnt(&c.empty[rel.slot], kConsumerWarps);
-          rel.advance(c.nst);
-        }
+      for (int e = 0; e < 8; ++e) {
+        xc[e] = xa[e];
+        xa[e] = xb[e];
       }
-      cbar();
-      // stage x (times the gain) as bf16 hi / lo rows of the A tile
-      const uint32_t xt = xb0 + (uint32_t)(kr & 1) * (kXbufBytes / 2);  // K block b at xt + b * 3072
+      const int k0 = kr * T.nkb * 64 + lane * kpt;  // this lane's first column
+      if (kr + 2 < T.nkr) tc_load_x(xb, x, T.K, warp, G.B, k0 + 2 * T.nkb * 64, kpt);
+      const int j = kr & 1;
+      if (kr >= 2) {  // the MMAs of kr - 2 have read this staging tile
+        if (lane == 0) bar_wait(p, &ctl->mma_bar[j], (c.tc_ph >> j) & 1u, c.task, false);
+        __syncwarp();
+        c.tc_ph ^= 1u << j;
+      }
+      const uint32_t xt = xb0 + (uint32_t)j * (kXbufBytes / 2);  // K block b at xt + b * 3072
 #pragma unroll
-      for (int e = 0; e < 16; e += 2) {
+      for (int e = 0; e < 8; e += 2) {
         if (e < kpt) {
           const int kl = lane * kpt + e;  // column within the K range
           const int kb = kl >> 6, kk = kl & 63;
@@ -791,10 +816,10 @@ __device__ void tc_gemv_task(Ctx& c, const mk_task_descriptor& d) {
           uint32_t part[3];
 #pragma unroll
           for (int q = 0; q < 3; ++q) {
-            const __nv_bfloat16 a0 = __float2bfloat16_rn(v0), a1 = __float2bfloat16_rn(v1);
-            part[q] = (uint32_t)__bfloat16_as_ushort(a0) | ((uint32_t)__bfloat16_as_ushort(a1) << 16);
-            v0 -= __bfloat162float(a0);
-            v1 -= __bfloat162float(a1);
+            const __nv_bfloat162 a = __float22bfloat162_rn(make_float2(v0, v1));
+            part[q] = *reinterpret_cast<const uint32_t*>(&a);
+            v0 -= bf_lo(part[q]);
+            v1 -= bf_hi(part[q]);
           }
           // row r of a K block sits at r * 128 bytes; its 16-byte chunk c is
           // stored at chunk c ^ (row within the 1024-byte group), as the
@@ -808,47 +833,19 @@ __device__ void tc_gemv_task(Ctx& c, const mk_task_descriptor& d) {
         }
       }
       fence_proxy_async_smem();
-      cbar();
-      if (tid == 0) {
-        for (int sg = 0; sg < T.seg; ++sg) {
-          const uint32_t slot = c.rp.slot, ph = c.rp.phase;
-          if (ok && !bar_wait(p, &c.full[slot], ph, c.task, true)) ok = false;
-          tc_fence_after();
-          if (ok) {
-            const uint32_t wb = smem_addr(c.ring + (size_t)slot * kStageBytes);
-            const uint32_t dcol = c.taddr + (uint32_t)(sg * T.Nr);
-            for (int kb = 0; kb < T.nkb; ++kb)
-#pragma unroll
-              for (int ks = 0; ks < 4; ++ks) {
-                const uint64_t ad = smem_desc_sw128(xt + (uint32_t)kb * 3072u + (uint32_t)ks * 32u, 1024u);
-                const uint64_t bd =
-                    smem_desc_sw128(wb + (uint32_t)(kb * T.Nr * 128) + (uint32_t)ks * 32u, 1024u);
-                tc_mma_bf16(dcol, ad, bd, idesc, (kr | kb | ks) != 0 ? 1u : 0u);
-              }
-          }
-          c.rp.advance(c.nst);
-        }
-        tc_commit(&c.mma_bar[kr & 1]);  // arrives once the MMAs issued so far are done
-      } else {
-        for (int sg = 0; sg < T.seg; ++sg) c.rp.advance(c.nst);
-      }
-    }
-    // last K range: wait for its MMAs, hand back its slots
-    if (tid == 0) {
-      const int j = (T.nkr - 1) & 1;
-      if (!bar_wait(p, &c.mma_bar[j], (c.mma_done >> j) & 1u, c.task, false)) ok = false;
-      c.mma_done ^= 1u << j;
-      for (int sg = 0; sg < T.seg; ++sg) {
-        mbar_arrive_cnt(&c.empty[rel.slot], kConsumerWarps);
-        rel.advance(c.nst);
-      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->x_full[j]);
     }
     if (g0 == 0 && gamma) {  // 1/rms per batch row (warp b holds row b's columns)
       const float t = warp_sum(ss);
       if (lane == 0) red[64 + warp] = 1.0f / sqrtf(t / (float)T.K + __uint_as_float(d.reserved[2]));
     }
-    tc_fence_before();
-    cbar();
+    // the row group's MMAs are done (acc_full follows every earlier commit)
+    if (lane == 0) bar_wait(p, &ctl->acc_full, (c.tc_ph >> 2) & 1u, c.task, false);
+    __syncwarp();
+    c.tc_ph ^= 4u;
+    for (int kr = max(T.nkr - 2, 0); kr < T.nkr; ++kr)
+      c.tc_ph ^= 1u << (kr & 1);  // the last two ranges' commits (only the MMA warp waited on them)
     if (warp == 0) {  // TMEM lanes 0-31 = A rows: the batch's hi, mid, lo parts in 0-7, 8-15, 16-23
       tc_fence_after();
       for (int sg = 0; sg < T.seg; ++sg)
@@ -865,14 +862,106 @@ __device__ void tc_gemv_task(Ctx& c, const mk_task_descriptor& d) {
       tc_fence_before();
     }
     cbar();
+    if (tid == 0) mbar_arrive(&ctl->acc_empty);  // tensor memory is free for the next row group
     gemv_epilogue(p, d, G, g0, rows_g, acc, red, nullptr);
   }
+  for (int g0 = 0; g0 < G.cn; g0 += T.RG)
+    for (int i = 0; i < T.nkr * T.seg; ++i) c.rp.advance(c.nst);
   if ((d.flags & MK_F_ARGMAX_EPI) && threadIdx.x < G.B) {
     mk_argmax_pair* pairs = static_cast<mk_argmax_pair*>(p.bufs[d.reserved[3]]);
     mk_argmax_pair pr;
     pr.value = red[96 + threadIdx.x];
     pr.index = reinterpret_cast<int*>(red)[104 + threadIdx.x];
     pairs[(size_t)d.reserved[4] * G.B + threadIdx.x] = pr;
+  }
+}
+
+// MMA warp of the B >= 8 kernel (lane 0 of the producer warpgroup's second
+// warp): takes tensor-core tiles from the mailbox in the consumers' order;
+// per K range it waits for the staged activations and the landed weight
+// slots, issues the MMAs and commits; the commit of range kr - 2 hands that
+// range's ring slots back to the producer.  Every wait is bounded; after a
+// failed wait no more MMAs are issued but every commit still is, so the
+// consumers' waits end.
+__device__ void tc_mma_warp(const KParams& p, uint8_t* ring, uint64_t* full, uint64_t* empty, TcCtl* ctl,
+                            uint32_t xb0, uint32_t taddr) {
+  if ((threadIdx.x & 31) != 0) return;
+  const int nst = p.nstages;
+  uint32_t ph = 0;  // completed phases seen: task_go 0, x_full 1-2, mma_bar 3-4, acc_empty 5
+  bool first = true, ok = true;
+  const uint64_t t0 = globaltimer();
+  for (;;) {
+    // next task (or the end); idle waits are long, so only abort or a very
+    // long silence end them
+    for (uint32_t it = 0; !mbar_try_wait(&ctl->task_go, ph & 1u); ++it) {
+      __nanosleep(256);
+      if ((it & 255u) == 0 && (aborted(p) || globaltimer() - t0 > 64ull * p.timeout_ns)) return;
+    }
+    ph ^= 1u;
+    const int task = ctl->mb_task;
+    if (task < 0) return;
+    RingPos rp, rel;
+    rp.slot = rel.slot = ctl->mb_slot;
+    rp.phase = rel.phase = ctl->mb_phase;
+    // only the fields the schedule needs (this warp runs on few registers)
+    const mk_task_descriptor* td = p.tasks + task;
+    const int K = __ldg(&td->k), cn = (int)__ldg(&td->reserved[1]);
+    const int seg = (__ldg(&td->flags) & MK_F_SILU_MUL) ? 2 : 1;
+    const int RG = p.tm_rows[__ldg(&td->in_buf[1])], Nr = (RG + 15) & ~15;
+    int nkb = 4;
+    while (nkb > 1 && (nkb * Nr * 128 > kStageBytes || (K / 64) % nkb)) nkb >>= 1;
+    const int nkr = K / 64 / nkb;
+    const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)Nr);
+    const uint32_t bstep = (uint32_t)(Nr * 128) >> 4;  // one K block of the weight tile, in 16 bytes
+    for (int g0 = 0; g0 < cn; g0 += RG) {
+      if (!first) {  // the consumers have read the previous accumulators
+        if (!bar_wait(p, &ctl->acc_empty, (ph >> 5) & 1u, task, false)) ok = false;
+        ph ^= 1u << 5;
+      }
+      first = false;
+      for (int kr = 0; kr < nkr; ++kr) {
+        const int j = kr & 1;
+        if (!bar_wait(p, &ctl->x_full[j], (ph >> (1 + j)) & 1u, task, false)) ok = false;
+        ph ^= 1u << (1 + j);
+        if (kr >= 2) {  // range kr - 2 is done: its slots go back to the producer
+          if (!bar_wait(p, &ctl->mma_bar[j], (ph >> (3 + j)) & 1u, task, false)) ok = false;
+          ph ^= 1u << (3 + j);
+          for (int sg = 0; sg < seg; ++sg) {
+            mbar_arrive_cnt(&empty[rel.slot], kConsumerWarps);
+            rel.advance(nst);
+          }
+        }
+        tc_fence_after();
+        const uint64_t ad0 = smem_desc_sw128(xb0 + (uint32_t)j * (kXbufBytes / 2), 1024u);
+        for (int sg = 0; sg < seg; ++sg) {
+          if (ok && !bar_wait(p, &full[rp.slot], rp.phase, task, true)) ok = false;
+          if (ok) {
+            // descriptors of the first K step; later steps add their byte
+            // offset / 16 to the start-address field (no carry: < 256 KB)
+            const uint64_t bd0 = smem_desc_sw128(smem_addr(ring + (size_t)rp.slot * kStageBytes), 1024u);
+            const uint32_t dcol = taddr + (uint32_t)(sg * Nr);
+#pragma unroll 1
+            for (int q = 0; q < nkb * 4; ++q) {  // K block q / 4, K step q % 4
+              const uint32_t kb = (uint32_t)q >> 2, ks = (uint32_t)q & 3u;
+              tc_mma_bf16(dcol, ad0 + (uint64_t)(kb * (3072u >> 4) + ks * 2u), bd0 + (uint64_t)(kb * bstep + ks * 2u),
+                          idesc, (kr | q) != 0 ? 1u : 0u);
+            }
+          }
+          rp.advance(nst);
+        }
+        tc_commit(&ctl->mma_bar[j]);
+      }
+      tc_commit(&ctl->acc_full);
+      for (int kr = max(nkr - 2, 0); kr < nkr; ++kr) {  // the last ranges' slots
+        const int j = kr & 1;
+        if (!bar_wait(p, &ctl->mma_bar[j], (ph >> (3 + j)) & 1u, task, false)) ok = false;
+        ph ^= 1u << (3 + j);
+        for (int sg = 0; sg < seg; ++sg) {
+          mbar_arrive_cnt(&empty[rel.slot], kConsumerWarps);
+          rel.advance(nst);
+        }
+      }
+    }
   }
 }
 
@@ -1266,8 +1355,8 @@ __device__ bool level_barrier(const KParams& p, int k) {
 
 template <int BCLASS>
 __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64_t* empty, float* scratch,
-                         volatile int* sflag, uint8_t* xbuf, uint64_t* mma_bar, uint32_t taddr) {
-  Ctx c{&p, ring, full, empty, scratch, RingPos{}, p.nstages, -1, {0, 0, 0}, 0u, xbuf, mma_bar, taddr, 0u};
+                         volatile int* sflag, uint8_t* xbuf, TcCtl* ctl, uint32_t taddr) {
+  Ctx c{&p, ring, full, empty, scratch, RingPos{}, p.nstages, -1, {0, 0, 0}, 0u, xbuf, ctl, taddr, 0u};
   Seq sq;
   seq_init(sq, p);
   int task, lvl, cur_lvl = 0;
@@ -1344,10 +1433,9 @@ __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
 }
 
 // Shared memory: [activation staging (B >= 8 kernel)] [ring] [full, empty
-// mbarriers] [32-byte control: run flag, TMEM address, two MMA mbarriers]
-// [scratch].
+// mbarriers] [control block] [scratch].
 int smem_bytes_for(int nstages, int batch) {
-  return (batch > 4 ? kXbufBytes : 0) + nstages * kStageBytes + 2 * nstages * 8 + 32 + kScratchBytes;
+  return (batch > 4 ? kXbufBytes : 0) + nstages * kStageBytes + 2 * nstages * 8 + kCtlBytes + kScratchBytes;
 }
 
 template <int BCLASS>
@@ -1364,10 +1452,9 @@ __global__ void __launch_bounds__(kThreads, 1) mk_interpreter_kernel(const __gri
   uint8_t* ring = smem + xbytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(ring + (size_t)nst * kStageBytes);
   uint64_t* empty = full + nst;
-  volatile int* sflag = reinterpret_cast<volatile int*>(empty + nst);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(empty + nst) + 1;
-  uint64_t* mma_bar = empty + nst + 2;
-  float* scratch = reinterpret_cast<float*>(ring + (size_t)nst * kStageBytes + 2 * nst * 8 + 32);
+  TcCtl* ctl = reinterpret_cast<TcCtl*>(empty + nst);
+  volatile int* sflag = &ctl->run;
+  float* scratch = reinterpret_cast<float*>(ring + (size_t)nst * kStageBytes + 2 * nst * 8 + kCtlBytes);
   // the swizzled operand layouts assume 1024-byte aligned tiles
   const bool aligned = (smem_addr(smem) & 1023u) == 0;
   if (threadIdx.x == 0) {
@@ -1375,31 +1462,43 @@ __global__ void __launch_bounds__(kThreads, 1) mk_interpreter_kernel(const __gri
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], kConsumerWarps);
     }
-    mbar_init(&mma_bar[0], 1);
-    mbar_init(&mma_bar[1], 1);
+    mbar_init(&ctl->mma_bar[0], 1);
+    mbar_init(&ctl->mma_bar[1], 1);
+    mbar_init(&ctl->x_full[0], kConsumerWarps);
+    mbar_init(&ctl->x_full[1], kConsumerWarps);
+    mbar_init(&ctl->acc_full, 1);
+    mbar_init(&ctl->acc_empty, 1);
+    mbar_init(&ctl->task_go, 1);
     fence_mbar_init();
     if (BCLASS == 2 && !aligned) raise_error(p, MK_DEV_BAD_OP, -1);
   }
   if constexpr (BCLASS == 2) {
     if (threadIdx.x < 32) {  // one warp allocates the accumulator columns
-      tmem_alloc(tmem_slot, kTmemCols);
+      tmem_alloc(&ctl->tmem, kTmemCols);
       tmem_relinquish();
     }
     tc_fence_before();
   }
   __syncthreads();
   if constexpr (BCLASS == 2) tc_fence_after();
-  const uint32_t taddr = BCLASS == 2 ? *tmem_slot : 0u;
+  const uint32_t taddr = BCLASS == 2 ? ctl->tmem : 0u;
   if (threadIdx.x >= kConsumerThreads) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(BCLASS == 2 ? kProducerRegsTc : kProducerRegs));
     if (threadIdx.x < kConsumerThreads + 32) producer(p, ring, full, empty);
+    else if (BCLASS == 2 && threadIdx.x < kConsumerThreads + 64)
+      tc_mma_warp(p, ring, full, empty, ctl, smem_addr(xbuf), taddr);
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
-    if (BCLASS != 2 || aligned) consumer<BCLASS>(p, ring, full, empty, scratch, sflag, xbuf, mma_bar, taddr);
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(BCLASS == 2 ? kConsumerRegsTc : kConsumerRegs));
+    if (BCLASS != 2 || aligned) consumer<BCLASS>(p, ring, full, empty, scratch, sflag, xbuf, ctl, taddr);
     if (BCLASS == 2) {
-      // every tensor-core operation this CTA issued has completed (each
-      // tensor task waits for its commits); free the columns
+      // every tensor-core operation has completed (the consumers waited for
+      // each row group's last commit): tell the MMA warp to stop, free the
+      // columns
       named_bar_sync(1, kConsumerThreads);
+      if (threadIdx.x == 0) {
+        ctl->mb_task = -1;
+        mbar_arrive(&ctl->task_go);
+      }
       if (threadIdx.x < 32) {
         tc_fence_after();
         tmem_dealloc(taddr, kTmemCols);
