@@ -81,13 +81,31 @@ def tiles(n: int, tiles_target: int, col_align: int):
 
 def partials_per_sequence(len0, Hkv: int, chunk: int, num_ctas: int):
     """Split-KV chunk count P_s per sequence (fixed at lowering time).
-    chunk > 0: ceil(len0_s / chunk).  chunk == 0: chunks of about
-    E = max(128, ceil(Hkv * sum(len0) / num_ctas)) keys, so the partial tasks
-    of a ragged batch carry about the same bytes and number about one per SM."""
+    chunk > 0: ceil(len0_s / chunk).  chunk == 0: chunks of E keys, E the
+    smallest length of at least max(128, ceil(Hkv * sum(len0) / num_ctas))
+    for which Hkv * sum_s max(1, ceil(len0_s / E)) <= num_ctas (or the
+    longest sequence, when even one chunk per sequence is more than that):
+    the partial tasks of a ragged batch carry about the same bytes and fit
+    one wave of the CTAs."""
+    lens = [int(l) for l in len0]
     if chunk > 0:
-        return [max(1, ceil_div(int(l), chunk)) for l in len0]
-    E = max(128, ceil_div(Hkv * sum(int(l) for l in len0), num_ctas))
-    return [max(1, ceil_div(int(l), E)) for l in len0]
+        return [max(1, ceil_div(l, chunk)) for l in lens]
+
+    def count(E):
+        return Hkv * sum(max(1, ceil_div(l, E)) for l in lens)
+
+    lo = max(128, ceil_div(Hkv * sum(lens), num_ctas))
+    hi = max(lo, max(lens) if lens else lo)
+    if count(lo) > num_ctas:  # smallest E in (lo, hi] that fits, else hi
+        a, b = lo, hi
+        while b - a > 1:
+            m = (a + b) // 2
+            if count(m) <= num_ctas:
+                b = m
+            else:
+                a = m
+        lo = b
+    return [max(1, ceil_div(l, lo)) for l in lens]
 
 
 def f32_bits(x: float) -> int:

@@ -62,9 +62,28 @@ std::vector<int> partials_per_sequence(const std::vector<int32_t>& len0, int Hkv
     for (size_t s = 0; s < len0.size(); ++s) P[s] = (int)std::max<int64_t>(1, cdiv(len0[s], chunk));
     return P;
   }
-  int64_t tot = 0;
-  for (int32_t l : len0) tot += l;
+  // chunks of E keys: the smallest E >= max(128, Hkv * sum / num_ctas) whose
+  // chunk count Hkv * sum_s max(1, ceil(len_s / E)) fits one wave of CTAs
+  int64_t tot = 0, longest = 0;
+  for (int32_t l : len0) {
+    tot += l;
+    longest = std::max<int64_t>(longest, l);
+  }
+  auto count = [&](int64_t E) {
+    int64_t c = 0;
+    for (int32_t l : len0) c += std::max<int64_t>(1, cdiv(l, E));
+    return c * Hkv;
+  };
   int64_t E = std::max<int64_t>(128, cdiv((int64_t)Hkv * tot, num_ctas));
+  if (count(E) > num_ctas) {
+    int64_t a = E, b = std::max(E, longest);
+    while (b - a > 1) {
+      const int64_t m = (a + b) / 2;
+      if (count(m) <= num_ctas) b = m;
+      else a = m;
+    }
+    E = b;
+  }
   for (size_t s = 0; s < len0.size(); ++s) P[s] = (int)std::max<int64_t>(1, cdiv(len0[s], E));
   return P;
 }

@@ -317,3 +317,26 @@ def test_oracle_lowering_planted_tile_bug_is_caught():
         ol.tiles = orig
     with pytest.raises(ValidationError):
         validate(tasks, edges)
+
+
+def test_auto_chunking_fits_one_wave_with_the_smallest_chunk():
+    """Automatic split-KV chunking (our reading): the chunk count fits the
+    CTAs whenever one chunk per sequence does, with the smallest chunk
+    length that achieves it (never below max(128, average share))."""
+    import numpy as np
+    from oracle.lowering import partials_per_sequence, ceil_div
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        B = int(rng.integers(1, 9))
+        Hkv = int(rng.choice([1, 2, 8]))
+        ctas = int(rng.integers(8, 200))
+        lens = [int(x) for x in rng.integers(0, 9000, size=B)]
+        P = partials_per_sequence(lens, Hkv, 0, ctas)
+        assert all(p >= 1 for p in P)
+        floor = max(128, ceil_div(Hkv * sum(lens), ctas))
+        E = max(max(ceil_div(l, p) for l, p in zip(lens, P)), floor)
+        if Hkv * B <= ctas:
+            assert Hkv * sum(P) <= ctas
+            if E > floor:  # one key less per chunk would overflow the wave
+                assert Hkv * sum(max(1, ceil_div(l, E - 1)) for l in lens) > ctas
+        assert all(p == max(1, ceil_div(l, E)) or ceil_div(l, p) <= E for l, p in zip(lens, P))
