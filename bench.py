@@ -342,7 +342,7 @@ def main():
     modes = {}
     if not args.no_modes:
         for name, mode in (("per_op", L.MK_MODE_PER_OP), ("per_op_graph", L.MK_MODE_PER_OP_GRAPH),
-                           ("levels", L.MK_MODE_LEVELS)):
+                           ("per_op_pdl", L.MK_MODE_PER_OP_PDL), ("levels", L.MK_MODE_LEVELS)):
             k = max(4, args.steps // 4)
             mms, mb = timed(mode, k, 2)
             modes[name] = {"ms_per_step": mms / k, "tokens_per_s": w.B * k / (mms / 1000.0),

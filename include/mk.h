@@ -94,6 +94,8 @@ extern "C" {
 #define MK_MODE_PER_OP 1          /* one kernel launch per op, one CTA per task */
 #define MK_MODE_PER_OP_GRAPH 2    /* MK_MODE_PER_OP captured once into a CUDA graph */
 #define MK_MODE_LEVELS 3          /* persistent kernel, barrier per topological level */
+#define MK_MODE_PER_OP_PDL 4      /* MK_MODE_PER_OP with programmatic dependent launch: a kernel
+                                     starts streaming its weights while the previous one runs */
 
 #define MK_NO_BUF 0xFFFFu
 #define MK_BUF_STATE 0u           /* int32 [B, 2]: (next token, its position) */

@@ -22,7 +22,7 @@ MK_OP_NOP, MK_OP_MEMCPY, MK_OP_GEMV, MK_OP_RMSNORM, MK_OP_ATTENTION, MK_OP_MLP, 
 MK_OP_ATTENTION_APPEND, MK_OP_ATTENTION_PARTIAL, MK_OP_ATTENTION_COMBINE = 7, 8, 9
 MK_F_SILU_MUL, MK_F_ADD_RESIDUAL, MK_F_RMS_NORM_INPUT, MK_F_ARGMAX_EPI = 1, 2, 4, 8
 MK_BF16, MK_F32, MK_I32, MK_PAIR = 1, 2, 3, 4
-MK_MODE_MEGA, MK_MODE_PER_OP, MK_MODE_PER_OP_GRAPH, MK_MODE_LEVELS = 0, 1, 2, 3
+MK_MODE_MEGA, MK_MODE_PER_OP, MK_MODE_PER_OP_GRAPH, MK_MODE_LEVELS, MK_MODE_PER_OP_PDL = 0, 1, 2, 3, 4
 MK_NO_BUF = 0xFFFF
 
 EXPORTS = [

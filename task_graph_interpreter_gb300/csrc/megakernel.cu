@@ -1375,6 +1375,15 @@ __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
       } else if (tid == 0 && p.mode == MK_MODE_LEVELS) {
         while (ok && cur_lvl < lvl) ok = level_barrier(p, ++cur_lvl);
         ok = ok && !aborted(p);
+      } else if (p.mode == MK_MODE_PER_OP_PDL) {
+        // the previous op's kernel has completed and its writes are
+        // visible; only then may the next kernel launch (so its producer,
+        // which starts before its own wait, never runs ahead of two ops)
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (tid == 0) {
+          asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+          ok = !aborted(p);
+        }
       } else if (tid == 0) {
         ok = !aborted(p);
       }
@@ -1535,6 +1544,19 @@ cudaError_t launch_interpreter(const KParams& p, int batch, int grid, bool coope
   void* args[] = {const_cast<KParams*>(&p)};
   if (cooperative)
     return cudaLaunchCooperativeKernel(fn, dim3(grid), dim3(kThreads), args, (size_t)smem, stream);
+  if (p.mode == MK_MODE_PER_OP_PDL) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
+  }
   return cudaLaunchKernel(fn, dim3(grid), dim3(kThreads), args, (size_t)smem, stream);
 }
 

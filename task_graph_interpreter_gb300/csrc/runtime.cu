@@ -174,9 +174,9 @@ int build_tensor_maps(const mk_graph* g, std::vector<uint8_t>& maps, std::vector
   return MK_OK;
 }
 
-int launch_per_op(mk_graph* g, cudaStream_t stream, uint64_t* trace) {
+int launch_per_op(mk_graph* g, cudaStream_t stream, uint64_t* trace, int mode = MK_MODE_PER_OP) {
   KParams p = base_params(g);
-  p.mode = MK_MODE_PER_OP;
+  p.mode = mode;
   p.trace = trace;
   for (size_t i = 0; i + 1 < g->group_off.size(); ++i) {
     p.first_task = g->group_off[i];
@@ -355,6 +355,8 @@ extern "C" int mk_decode_step_ex(mk_graph* g, void* stream_, int mode, uint32_t 
     }
     case MK_MODE_PER_OP:
       return launch_per_op(g, stream, tr);
+    case MK_MODE_PER_OP_PDL:
+      return launch_per_op(g, stream, tr, MK_MODE_PER_OP_PDL);
     case MK_MODE_PER_OP_GRAPH: {
       if (trace) return fail(MK_ERR_ARG, "mk_decode_step_ex: tracing is not available in graph mode");
       if (!d->per_op_exec) {

@@ -16,7 +16,7 @@ from tests.gpu_common import build_gpu, compare_step, compare_cache_rows
 
 pytestmark = pytest.mark.gpu
 
-MODES = {"mega": 0, "per_op": 1, "per_op_graph": 2, "levels": 3}
+MODES = {"mega": 0, "per_op": 1, "per_op_graph": 2, "levels": 3, "per_op_pdl": 4}
 
 
 def _run_and_compare(w, steps, mode="mega", num_ctas=0, seed=0, check_cache=True):
@@ -64,7 +64,7 @@ def test_capacity_is_reported_not_overrun():
         dec.graph.close()
 
 
-@pytest.mark.parametrize("mode", ["per_op", "per_op_graph", "levels"])
+@pytest.mark.parametrize("mode", ["per_op", "per_op_graph", "levels", "per_op_pdl"])
 def test_tiny_other_modes(mode):
     w = synth.custom(synth.TINY, 1, [128], 2, name="tiny2")
     assert _run_and_compare(w, 2, mode) >= 1
@@ -90,7 +90,7 @@ def test_batch_two_and_few_ctas():
 def test_modes_are_bitwise_identical_and_deterministic():
     w = synth.workload("tiny")
     outs = []
-    for mode in ("mega", "mega", "per_op", "levels"):
+    for mode in ("mega", "mega", "per_op", "levels", "per_op_pdl"):
         dec = build_gpu(w)
         dec.graph.step(MODES[mode])
         assert dec.graph.status()[0] == 0
