@@ -162,6 +162,24 @@ int mk_add_buffer(mk_graph* g, void* dptr, int dtype, int64_t rows, int64_t cols
  * out f32 [B, H]. */
 int mk_add_embed(mk_graph* g, uint16_t table, uint16_t out, int B, int H);
 
+/* Standalone RMS norm, one RMSNORM task per sequence ("mega kernel
+ * initial", OpId table: usually fused into a GEMV, rarely standalone):
+ *   y = x (+ residual);  out[s, :] = y / sqrt(mean(y^2) + eps) * gamma.
+ * x, residual, out f32 [B, H]; gamma bf16 [1, H]; residual = MK_NO_BUF for
+ * none (with one, the task carries FUSED_RESIDUAL, flag bit 1; our reading:
+ * only the normalised sum is written).  H a multiple of 8, at most 16384.
+ * Errors: MK_ERR_ARG, MK_ERR_STATE. */
+int mk_add_rmsnorm(mk_graph* g, uint16_t x, uint16_t gamma, uint16_t residual, uint16_t out, int B,
+                   int H, float eps);
+
+/* Epilogue fusion pass, before mk_lower: every standalone RMS norm without a
+ * residual whose output is read only as the x input of GEMV ops that have
+ * no aux operand is folded into those GEMVs (they read the norm's input
+ * with RMS_NORM_INPUT, its gain and its eps) and removed; the norm's output
+ * buffer is then never written.  *fused receives the number of norms
+ * removed.  Errors: MK_ERR_STATE (already lowered), MK_ERR_ARG. */
+int mk_fuse_rmsnorm(mk_graph* g, int* fused);
+
 /* y = epilogue(W x) fanned out into one GEMV task per output-column tile
  * ("mega kernel initial", lowering part: one task per column tile, roughly
  * one per SM; RMSNorm, residual and SiLU*mul as epilogue flags).
@@ -211,6 +229,8 @@ int mk_gemv_tiles(const mk_graph* g, int n, int32_t* tiles);
 /* Lower every op to descriptors and edges and build the per-CTA queues;
  * freezes the graph.  Descriptor fields by op (unused in_buf = MK_NO_BUF,
  * unused fields 0):
+ *  RMSNORM  in={x,gamma,residual} out=out m=B n=H flags=FUSED_RESIDUAL (bit 1)
+ *           with a residual; reserved={s, float bits of eps}
  *  GEMV     in={x,W,aux} out=y m=B n k; reserved={col_begin, col_count,
  *           float bits of eps (RMS_NORM_INPUT) or 0, pairs idx or 0,
  *           tile index (ARGMAX_EPI) or 0}

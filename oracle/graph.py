@@ -26,7 +26,11 @@ BF16, F32, I32, PAIR = 1, 2, 3, 4
 
 
 def llama_decode_spec(model, B: int, len0, cap: int, chunk: int, num_ctas: int,
-                      tiles_target: int = 0, col_align: int = 16) -> dict:
+                      tiles_target: int = 0, col_align: int = 16, norms: str = "fused") -> dict:
+    """norms: "fused" sets RMS_NORM_INPUT on the GEMVs that consume a norm;
+    "standalone" emits each norm as its own op (a fresh output buffer) read
+    by a plain GEMV."""
+    assert norms in ("fused", "standalone")
     m = model
     tt = tiles_target or num_ctas
     bufs = [(I32, B, 2), (F32, cap, m.D // 2), (F32, cap, m.D // 2)]
@@ -65,27 +69,77 @@ def llama_decode_spec(model, B: int, len0, cap: int, chunk: int, num_ctas: int,
                         flags=flags, m=B, n=n, k=k, eps=eps))
         return out
 
+    def normed(x, gamma, flags):
+        """(input, aux, flags) of a GEMV that reads RMSNorm(x) * gamma."""
+        if norms == "fused":
+            return x, gamma, flags | F_RMS_NORM_INPUT
+        xn = fresh(F32, B, m.H)
+        ops.append(dict(kind="rmsnorm", x=x, gamma=gamma, residual=NO_BUF, out=xn, B=B, H=m.H, eps=m.eps))
+        return xn, NO_BUF, flags
+
     h = fresh(F32, B, m.H)
     ops.append(dict(kind="embed", table=idx["embed"], out=h, B=B, H=m.H))
     G = m.Hq // m.Hkv
     P = partials_per_sequence(len0, m.Hkv, chunk, num_ctas)
     for l in range(m.L):
-        qkv = matmul(h, idx[f"layer{l}.wqkv"], m.n_qkv, m.H, aux=idx[f"layer{l}.attn_norm"],
-                     flags=F_RMS_NORM_INPUT, eps=m.eps)
+        x, a, f = normed(h, idx[f"layer{l}.attn_norm"], 0)
+        qkv = matmul(x, idx[f"layer{l}.wqkv"], m.n_qkv, m.H, aux=a, flags=f, eps=m.eps)
         scr = fresh(F32, B * m.Hkv * 0 + sum(P) * m.Hkv, G * (m.D + 2))
         att = fresh(F32, B, m.Hq * m.D)
         ops.append(dict(kind="attention", qkv=qkv, k=idx[f"layer{l}.k_cache"],
                         v=idx[f"layer{l}.v_cache"], out=att, scratch=scr, B=B, Hq=m.Hq,
                         Hkv=m.Hkv, D=m.D, capacity=cap, len0=list(len0), chunk=chunk))
         h1 = matmul(att, idx[f"layer{l}.wo"], m.H, m.Hq * m.D, aux=h, flags=F_ADD_RESIDUAL)
-        gu = matmul(h1, idx[f"layer{l}.wgu"], m.F, m.H, aux=idx[f"layer{l}.mlp_norm"],
-                    flags=F_RMS_NORM_INPUT | F_SILU_MUL, eps=m.eps)
+        x, a, f = normed(h1, idx[f"layer{l}.mlp_norm"], F_SILU_MUL)
+        gu = matmul(x, idx[f"layer{l}.wgu"], m.F, m.H, aux=a, flags=f, eps=m.eps)
         h = matmul(gu, idx[f"layer{l}.wd"], m.H, m.F, aux=h1, flags=F_ADD_RESIDUAL)
+    x, a, f = normed(h, idx["final_norm"], F_ARGMAX_EPI)
     T = len(tiles(m.V, tt, col_align))
     logits = fresh(F32, B, m.V)
     pairs = fresh(PAIR, T, B)
-    matmul(h, lm, m.V, m.H, aux=idx["final_norm"], flags=F_RMS_NORM_INPUT | F_ARGMAX_EPI,
-           eps=m.eps, pairs=pairs, out=logits)
+    matmul(x, lm, m.V, m.H, aux=a, flags=f, eps=m.eps, pairs=pairs, out=logits)
     ops.append(dict(kind="sample", pairs=pairs, history=hist, B=B, V=m.V, capacity=cap))
     return dict(num_ctas=num_ctas, tiles_target=tiles_target, col_align=col_align,
                 buffers=bufs, ops=ops, names=idx)
+
+
+def fuse_rmsnorm(spec: dict):
+    """Epilogue fusion on an op list: a norm without a residual whose output
+    is read only as the x of GEMVs without an aux operand is folded into
+    them (x = the norm's input, aux = its gain, RMS_NORM_INPUT, its eps) and
+    dropped.  Returns (new spec, number of norms folded)."""
+    import copy
+    ops = copy.deepcopy(spec["ops"])
+
+    def reads(op, b):
+        k = op["kind"]
+        if k == "embed":
+            return op["table"] == b
+        if k == "matmul":
+            return b in (op["x"], op["w"], op.get("aux", NO_BUF))
+        if k == "attention":
+            return b in (op["qkv"], op["k"], op["v"])
+        if k == "sample":
+            return op["pairs"] == b
+        if k == "rmsnorm":
+            return b in (op["x"], op["gamma"], op.get("residual", NO_BUF))
+        raise ValueError(k)
+
+    out, folded = [], 0
+    for i, op in enumerate(ops):
+        if op["kind"] == "rmsnorm" and op.get("residual", NO_BUF) == NO_BUF:
+            users = [j for j, r in enumerate(ops) if j != i and reads(r, op["out"])]
+            ok = bool(users) and all(
+                j > i and ops[j]["kind"] == "matmul" and ops[j]["x"] == op["out"] and ops[j]["w"] != op["out"]
+                and ops[j].get("aux", NO_BUF) == NO_BUF and not ops[j]["flags"] & (F_RMS_NORM_INPUT | F_ADD_RESIDUAL)
+                for j in users)
+            if ok:
+                for j in users:
+                    ops[j].update(x=op["x"], aux=op["gamma"], eps=op["eps"],
+                                  flags=ops[j]["flags"] | F_RMS_NORM_INPUT)
+                folded += 1
+                continue
+        out.append(op)
+    new = dict(spec)
+    new["ops"] = out
+    return new, folded

@@ -232,6 +232,19 @@ def lower(spec: dict):
                                 (kc, row, row + 1, cap * D, cap * D + D),
                                 (vc, row, row + 1, cap * D, cap * D + D)],
                          writes=[(out, s, s + 1, g * G * D, (g + 1) * G * D)])
+        elif kind == "rmsnorm":
+            # standalone RMS norm per sequence (OpId table: usually fused,
+            # rarely standalone); a residual makes it FUSED_RESIDUAL (bit 1)
+            B, H = op["B"], op["H"]
+            res = op.get("residual", NO_BUF)
+            for s in range(B):
+                reads = [(op["x"], s, s + 1, 0, H)]
+                if res != NO_BUF:
+                    reads.append((res, s, s + 1, 0, H))
+                emit(dict(op_id=OP_RMSNORM, flags=F_ADD_RESIDUAL if res != NO_BUF else 0,
+                          in_buf=(op["x"], op["gamma"], res), out_buf=op["out"], m=B, n=H,
+                          reserved=(s, f32_bits(op["eps"]), 0, 0, 0)),
+                     reads, writes=[(op["out"], s, s + 1, 0, H)])
         elif kind == "sample":
             B, V, cap = op["B"], op["V"], op["capacity"]
             T = len(tiles(V, tt, align))

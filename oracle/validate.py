@@ -27,7 +27,7 @@ from collections import defaultdict
 
 import numpy as np
 
-from .lowering import (OP_MEMCPY, OP_GEMV, OP_SAMPLE, OP_ATT_APPEND, OP_ATT_PARTIAL,
+from .lowering import (OP_MEMCPY, OP_GEMV, OP_RMSNORM, OP_SAMPLE, OP_ATT_APPEND, OP_ATT_PARTIAL,
                        OP_ATT_COMBINE, F_ADD_RESIDUAL, F_ARGMAX_EPI, NO_BUF, BUF_STATE)
 
 
@@ -46,6 +46,12 @@ def task_accesses(d) -> tuple:
     if op == OP_MEMCPY:
         s = rs[0]
         R.append((BUF_STATE, s, s + 1, 0, 2))
+        Wr.append((ob, s, s + 1, 0, n))
+    elif op == OP_RMSNORM:
+        s = rs[0]
+        R.append((ib[0], s, s + 1, 0, n))
+        if int(d["flags"]) & F_ADD_RESIDUAL:
+            R.append((ib[2], s, s + 1, 0, n))
         Wr.append((ob, s, s + 1, 0, n))
     elif op == OP_GEMV:
         c0, cn = rs[0], rs[1]

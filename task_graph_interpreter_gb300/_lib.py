@@ -26,7 +26,8 @@ MK_MODE_MEGA, MK_MODE_PER_OP, MK_MODE_PER_OP_GRAPH, MK_MODE_LEVELS, MK_MODE_PER_
 MK_NO_BUF = 0xFFFF
 
 EXPORTS = [
-    "mk_graph_create", "mk_set_state", "mk_add_buffer", "mk_add_embed", "mk_add_matmul",
+    "mk_graph_create", "mk_set_state", "mk_add_buffer", "mk_add_embed", "mk_add_rmsnorm", "mk_fuse_rmsnorm",
+    "mk_add_matmul",
     "mk_add_attention", "mk_add_sample", "mk_attention_scratch_rows", "mk_gemv_tiles",
     "mk_lower", "mk_get_tasks", "mk_get_edges", "mk_get_sync_plan", "mk_get_queues", "mk_upload",
     "mk_decode_step", "mk_decode_step_ex", "mk_decode_step_host", "mk_status",
@@ -85,6 +86,8 @@ def lib():
         "mk_kernel_info": (c_int, [G, POINTER(c_int), POINTER(c_int), POINTER(c_int)]),
         "mk_destroy": (None, [G]),
         "mk_debug_patch_task": (c_int, [G, c_int, c_void_p]),
+        "mk_add_rmsnorm": (c_int, [G, c_uint16, c_uint16, c_uint16, c_uint16, c_int, c_int, c_float]),
+        "mk_fuse_rmsnorm": (c_int, [G, POINTER(c_int)]),
         "mk_gemv_tensor_core_tiles": (c_int, [G, POINTER(c_int)]),
         "mk_attention_decode_noalloc": (c_int, [c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_int,
                                                 c_int, c_int, c_int, POINTER(c_int32), POINTER(c_int32), c_int,
@@ -125,6 +128,16 @@ def mk_add_buffer(g, dptr: int, dtype: int, rows: int, cols: int) -> int:
 
 def mk_add_embed(g, table: int, out: int, B: int, H: int):
     check(lib().mk_add_embed(g, table, out, B, H), "mk_add_embed")
+
+
+def mk_add_rmsnorm(g, x, gamma, residual, out, B, H, eps):
+    check(lib().mk_add_rmsnorm(g, x, gamma, residual, out, B, H, eps), "mk_add_rmsnorm")
+
+
+def mk_fuse_rmsnorm(g) -> int:
+    n = c_int()
+    check(lib().mk_fuse_rmsnorm(g, ctypes.byref(n)), "mk_fuse_rmsnorm")
+    return n.value
 
 
 def mk_add_matmul(g, x, w, out, aux, pairs, flags, m, n, k, eps):

@@ -187,6 +187,80 @@ extern "C" int mk_add_embed(mk_graph* g, uint16_t table, uint16_t out, int B, in
   return MK_OK;
 }
 
+extern "C" int mk_add_rmsnorm(mk_graph* g, uint16_t x, uint16_t gamma, uint16_t residual, uint16_t out, int B,
+                              int H, float eps) {
+  CHECK(add_common(g, "mk_add_rmsnorm"));
+  if (B != g->B || H <= 0 || H % 8 || H > 16384)
+    return fail(MK_ERR_ARG, "mk_add_rmsnorm: B must equal the state's B, H a multiple of 8 up to 16384");
+  if (!std::isfinite(eps) || eps < 0.f) return fail(MK_ERR_ARG, "mk_add_rmsnorm: eps must be finite and >= 0");
+  CHECK(check_buf(g, x, MK_F32, B, H, "mk_add_rmsnorm x"));
+  CHECK(check_buf(g, gamma, MK_BF16, 1, H, "mk_add_rmsnorm gamma"));
+  CHECK(check_buf(g, out, MK_F32, B, H, "mk_add_rmsnorm out"));
+  if (residual != MK_NO_BUF) CHECK(check_buf(g, residual, MK_F32, B, H, "mk_add_rmsnorm residual"));
+  if (out == x || out == residual) return fail(MK_ERR_ARG, "mk_add_rmsnorm: out must not alias an input");
+  OpRec op{K_RMSNORM};
+  op.a[0] = x;
+  op.a[1] = gamma;
+  op.a[2] = out;
+  op.a[3] = residual;
+  op.B = B;
+  op.H = H;
+  op.eps = eps;
+  op.flags = residual != MK_NO_BUF ? MK_F_ADD_RESIDUAL : 0u;
+  g->ops.push_back(op);
+  return MK_OK;
+}
+
+// Which ops read buffer b (any operand position).
+static bool op_reads(const OpRec& op, uint16_t b) {
+  switch (op.kind) {
+    case K_EMBED: return op.a[0] == b;
+    case K_MATMUL: return op.a[0] == b || op.a[1] == b || op.a[3] == b;
+    case K_ATTENTION: return op.a[0] == b || op.a[1] == b || op.a[2] == b;
+    case K_SAMPLE: return op.a[0] == b;
+    case K_RMSNORM: return op.a[0] == b || op.a[1] == b || op.a[3] == b;
+  }
+  return false;
+}
+
+extern "C" int mk_fuse_rmsnorm(mk_graph* g, int* fused) {
+  if (!g || !fused) return fail(MK_ERR_ARG, "mk_fuse_rmsnorm: null argument");
+  if (g->lowered) return fail(MK_ERR_STATE, "mk_fuse_rmsnorm: graph already lowered");
+  *fused = 0;
+  std::vector<OpRec> kept;
+  for (size_t i = 0; i < g->ops.size(); ++i) {
+    const OpRec& nrm = g->ops[i];
+    bool fuse = nrm.kind == K_RMSNORM && nrm.a[3] == MK_NO_BUF;
+    int readers = 0;
+    for (size_t j = 0; fuse && j < g->ops.size(); ++j) {
+      if (j == i || !op_reads(g->ops[j], nrm.a[2])) continue;
+      const OpRec& r = g->ops[j];
+      // only as the x of a GEMV that has no aux operand, after the norm
+      if (j < i || r.kind != K_MATMUL || r.a[0] != nrm.a[2] || r.a[1] == nrm.a[2] || r.a[3] != MK_NO_BUF ||
+          (r.flags & (MK_F_RMS_NORM_INPUT | MK_F_ADD_RESIDUAL)))
+        fuse = false;
+      else
+        ++readers;
+    }
+    if (!fuse || readers == 0) {
+      kept.push_back(nrm);
+      continue;
+    }
+    for (size_t j = i + 1; j < g->ops.size(); ++j) {
+      OpRec& r = g->ops[j];
+      if (r.kind == K_MATMUL && r.a[0] == nrm.a[2]) {
+        r.a[0] = nrm.a[0];
+        r.a[3] = nrm.a[1];
+        r.flags |= MK_F_RMS_NORM_INPUT;
+        r.eps = nrm.eps;
+      }
+    }
+    ++*fused;
+  }
+  g->ops.swap(kept);
+  return MK_OK;
+}
+
 extern "C" int mk_add_matmul(mk_graph* g, uint16_t x, uint16_t w, uint16_t out, uint16_t aux,
                              uint16_t pairs, uint32_t flags, int m, int n, int k, float eps) {
   CHECK(add_common(g, "mk_add_matmul"));
@@ -491,6 +565,25 @@ extern "C" int mk_lower(mk_graph* g) {
                     {vc, row, row + 1, cacheCols, cacheCols + D}},
                    {{out, s, s + 1, (int64_t)gg * G * D, (int64_t)(gg + 1) * G * D}}, kTaskOverhead);
           }
+        break;
+      }
+      case K_RMSNORM: {
+        g->group_off.push_back((int)g->tasks.size());
+        for (int s = 0; s < op.B; ++s) {
+          mk_task_descriptor d = blank(MK_OP_RMSNORM);
+          d.flags = (uint16_t)op.flags;
+          d.in_buf[0] = op.a[0];
+          d.in_buf[1] = op.a[1];
+          d.in_buf[2] = op.a[3];
+          d.out_buf = op.a[2];
+          d.m = op.B;
+          d.n = op.H;
+          d.reserved[0] = s;
+          d.reserved[1] = f32_bits(op.eps);
+          std::vector<Rect> rd{{op.a[0], s, s + 1, 0, op.H}};
+          if (op.a[3] != MK_NO_BUF) rd.push_back({op.a[3], s, s + 1, 0, op.H});
+          L.emit(d, rd, {{op.a[2], s, s + 1, 0, op.H}}, op.H * 4.0 + kTaskOverhead);
+        }
         break;
       }
       case K_SAMPLE: {

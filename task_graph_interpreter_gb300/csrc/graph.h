@@ -18,7 +18,7 @@ struct BufferRec {
   int64_t rows = 0, cols = 0;
 };
 
-enum OpKind { K_EMBED, K_MATMUL, K_ATTENTION, K_SAMPLE };
+enum OpKind { K_EMBED, K_MATMUL, K_ATTENTION, K_SAMPLE, K_RMSNORM };
 
 struct OpRec {
   OpKind kind;
@@ -26,6 +26,7 @@ struct OpRec {
   // matmul: a0=x a1=w a2=out a3=aux a4=pairs
   // attention: a0=qkv a1=k a2=v a3=out a4=scratch
   // sample: a0=pairs a1=history
+  // rmsnorm: a0=x a1=gamma a2=out a3=residual
   uint16_t a[5] = {MK_NO_BUF, MK_NO_BUF, MK_NO_BUF, MK_NO_BUF, MK_NO_BUF};
   int B = 0, n = 0, k = 0, H = 0;
   int Hq = 0, Hkv = 0, D = 0, cap = 0, chunk = 0, V = 0;

@@ -1270,6 +1270,42 @@ __device__ void embed_task(Ctx& c, const mk_task_descriptor& d) {
   }
 }
 
+// Standalone RMS norm of one sequence's row ("mega kernel initial", OpId
+// table): y = x (+ residual with FUSED_RESIDUAL); out = y / sqrt(mean(y^2)
+// + eps) * gamma.  A rare op: two plain passes over the row (the second
+// reads it again from L2), kept small.
+__device__ void rmsnorm_task(Ctx& c, const mk_task_descriptor& d) {
+  const KParams& p = *c.p;
+  const int s = (int)d.reserved[0], H = d.n, tid = threadIdx.x;
+  const float* x = static_cast<const float*>(p.bufs[d.in_buf[0]]) + (size_t)s * H;
+  const uint16_t* gamma = static_cast<const uint16_t*>(p.bufs[d.in_buf[1]]);
+  const float* res =
+      (d.flags & MK_F_ADD_RESIDUAL) ? static_cast<const float*>(p.bufs[d.in_buf[2]]) + (size_t)s * H : nullptr;
+  float* out = static_cast<float*>(p.bufs[d.out_buf]) + (size_t)s * H;
+  float* red = c.scratch;
+  float ss = 0.f;
+#pragma unroll 1
+  for (int i = tid; i < H; i += kConsumerThreads) {
+    const float y = __ldcg(x + i) + (res ? __ldcg(res + i) : 0.f);
+    ss = fmaf(y, y, ss);
+  }
+  const float t = warp_sum(ss);
+  if ((tid & 31) == 0) red[tid >> 5] = t;
+  cbar();
+  if (tid == 0) {
+    float tot = 0.f;
+    for (int w = 0; w < kConsumerWarps; ++w) tot += red[w];
+    red[kConsumerWarps] = 1.0f / sqrtf(tot / (float)H + __uint_as_float(d.reserved[1]));
+  }
+  cbar();
+  const float inv = red[kConsumerWarps];
+#pragma unroll 1
+  for (int i = tid; i < H; i += kConsumerThreads) {
+    const float y = __ldcg(x + i) + (res ? __ldcg(res + i) : 0.f);
+    out[i] = y * inv * __uint_as_float((uint32_t)__ldg(gamma + i) << 16);
+  }
+}
+
 __device__ void sample_task(Ctx& c, const mk_task_descriptor& d) {
   const KParams& p = *c.p;
   const int s = d.reserved[0], B = d.m, T = d.k, cap = d.kv_len;
@@ -1406,6 +1442,7 @@ __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
       case MK_OP_ATTENTION_PARTIAL: partial_task(c, d); break;
       case MK_OP_ATTENTION_COMBINE: combine_task(c, d); break;
       case MK_OP_MEMCPY: embed_task(c, d); break;
+      case MK_OP_RMSNORM: rmsnorm_task(c, d); break;
       case MK_OP_SAMPLE: sample_task(c, d); break;
       case MK_OP_NOP: break;
       default:

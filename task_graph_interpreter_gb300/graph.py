@@ -61,6 +61,19 @@ class Graph:
         self.ops.append(("embed", table.idx, out.idx))
         return out
 
+    def rmsnorm(self, x: Buf, gamma: Buf, residual: Buf = None, eps: float = 1e-5) -> Buf:
+        """Standalone RMS norm (one task per sequence): RMSNorm(x [+ residual]) * gamma."""
+        B, H = x.tensor.shape
+        out = self._fresh(B, H)
+        L.mk_add_rmsnorm(self.h, x.idx, gamma.idx, residual.idx if residual is not None else L.MK_NO_BUF,
+                         out.idx, B, H, eps)
+        self.ops.append(("rmsnorm", x.idx, gamma.idx, out.idx))
+        return out
+
+    def fuse_rmsnorm(self) -> int:
+        """Fold standalone norms into the GEMVs that consume them (before lower)."""
+        return L.mk_fuse_rmsnorm(self.h)
+
     def matmul(self, x: Buf, w: Buf, gamma: Buf = None, residual: Buf = None, silu_mul: bool = False,
                eps: float = 1e-5, argmax: bool = False, out: Buf = None):
         """y = epilogue(W x) tiled over output columns; with argmax=True also

@@ -28,13 +28,18 @@ class LlamaDecode:
     history: Buf = None
     kcache: list = field(default_factory=list)
     vcache: list = field(default_factory=list)
+    fused_norms: int = 0                        # norms folded by the fusion pass
 
 
 def build_llama_decode(model, B: int, len0, capacity: int, weights: dict, kcache: list, vcache: list,
                        history: torch.Tensor, chunk: int = 0, device="cuda", num_ctas: int = 0,
-                       tiles_target: int = 0, col_align: int = 4, wait_timeout_us: int = 0) -> LlamaDecode:
+                       tiles_target: int = 0, col_align: int = 4, wait_timeout_us: int = 0,
+                       norms: str = "fused") -> LlamaDecode:
     """weights: name -> bf16 tensor (names of synth.weight_names);
-    kcache/vcache: per layer bf16 [B, Hkv, capacity, D]; history int32 [B, capacity]."""
+    kcache/vcache: per layer bf16 [B, Hkv, capacity, D]; history int32 [B, capacity].
+    norms: "fused" (RMS_NORM_INPUT on the consuming GEMVs), "standalone"
+    (RMSNORM tasks), or "fuse_pass" (standalone norms folded by the fusion pass)."""
+    assert norms in ("fused", "standalone", "fuse_pass")
     m = model
     g = Graph(B, device=device, num_ctas=num_ctas, tiles_target=tiles_target, col_align=col_align,
               wait_timeout_us=wait_timeout_us)
@@ -58,15 +63,26 @@ def build_llama_decode(model, B: int, len0, capacity: int, weights: dict, kcache
         out.vcache.append(reg(f"layer{l}.v_cache", vcache[l], B * m.Hkv, capacity * m.D))
     out.history = reg("history", history)
 
+    def normed(x, gamma):
+        """(input, gamma kwarg) of a GEMV that reads RMSNorm(x) * gamma."""
+        if norms == "fused":
+            return x, gamma
+        return g.rmsnorm(x, gamma, eps=m.eps), None
+
     h = g.embed(W["embed"])
     for l in range(m.L):
-        qkv = g.matmul(h, W[f"layer{l}.wqkv"], gamma=W[f"layer{l}.attn_norm"], eps=m.eps)
+        x, gm = normed(h, W[f"layer{l}.attn_norm"])
+        qkv = g.matmul(x, W[f"layer{l}.wqkv"], gamma=gm, eps=m.eps)
         att = g.attention(qkv, out.kcache[l], out.vcache[l], m.Hq, m.Hkv, m.D, capacity, len0, chunk,
                           m.theta)
         h1 = g.matmul(att, W[f"layer{l}.wo"], residual=h)
-        gu = g.matmul(h1, W[f"layer{l}.wgu"], gamma=W[f"layer{l}.mlp_norm"], silu_mul=True, eps=m.eps)
+        x, gm = normed(h1, W[f"layer{l}.mlp_norm"])
+        gu = g.matmul(x, W[f"layer{l}.wgu"], gamma=gm, silu_mul=True, eps=m.eps)
         h = g.matmul(gu, W[f"layer{l}.wd"], residual=h1)
         out.hidden.append(h)
-    out.logits, out.pairs = g.matmul(h, lm, gamma=W["final_norm"], eps=m.eps, argmax=True)
+    x, gm = normed(h, W["final_norm"])
+    out.logits, out.pairs = g.matmul(x, lm, gamma=gm, eps=m.eps, argmax=True)
     g.sample(out.pairs, out.history, m.V, capacity)
+    if norms == "fuse_pass":
+        out.fused_norms = g.fuse_rmsnorm()
     return out

@@ -19,11 +19,11 @@ LOGIT_COS = 0.9999
 HIDDEN_RTOL = 1e-2
 
 
-def build_gpu(w, seed=0, mode_ctas=0, layers_keep_hidden=True, wait_timeout_us=0):
+def build_gpu(w, seed=0, mode_ctas=0, layers_keep_hidden=True, wait_timeout_us=0, norms="fused"):
     from task_graph_interpreter_gb300.llama import build_llama_decode
     weights, kc, vc, hist, state = synth.device_inputs(w, seed, "cuda")
     dec = build_llama_decode(w.model, w.B, w.kv_len, w.capacity, weights, kc, vc, hist, chunk=w.chunk,
-                             device="cuda", num_ctas=mode_ctas, wait_timeout_us=wait_timeout_us)
+                             device="cuda", num_ctas=mode_ctas, wait_timeout_us=wait_timeout_us, norms=norms)
     dec.graph.state.copy_(state)
     dec.graph.lower()
     dec.graph.upload()

@@ -37,8 +37,9 @@ def test_library_exports_every_declared_symbol(L):
         assert hasattr(lib, name), name
 
 
-def _replay(L, spec, B):
-    """Feed an oracle graph spec to libmk through the C ABI (fake pointers)."""
+def _replay(L, spec, B, fuse=False, g_fused=[0]):
+    """Feed an oracle graph spec to libmk through the C ABI (fake pointers);
+    with fuse, run the library's RMS-norm fusion pass before lowering."""
     g = L.mk_graph_create(num_ctas=spec["num_ctas"], tiles_target=spec["tiles_target"],
                           col_align=spec["col_align"])
     base = 1 << 40
@@ -58,6 +59,10 @@ def _replay(L, spec, B):
                                op["Hq"], op["Hkv"], op["D"], op["capacity"], op["len0"], op["chunk"], 5e5)
         elif k == "sample":
             L.mk_add_sample(g, op["pairs"], op["history"], op["B"], op["V"], op["capacity"])
+        elif k == "rmsnorm":
+            L.mk_add_rmsnorm(g, op["x"], op["gamma"], op["residual"], op["out"], op["B"], op["H"], op["eps"])
+    if fuse:
+        g_fused[0] = L.mk_fuse_rmsnorm(g)
     L.mk_lower(g)
     return g
 
@@ -272,5 +277,70 @@ def test_sync_plan_follows_a_patched_dependency_count(L):
         assert sum(int(n) for _, n in entries) == int(t["remaining_deps"])
         own = [(int(c), int(n)) for c, n in entries if int(c) < len(tasks)]
         assert own and own[0][1] > np.count_nonzero(sig == own[0][0]), "the extra dependency can never be met"
+    finally:
+        L.mk_destroy(g)
+
+
+
+@pytest.mark.parametrize("name", ["tiny", "1b", "8b_b8"])
+def test_standalone_rmsnorm_lowering_is_byte_identical(L, name):
+    w = synth.workload(name)
+    spec = llama_decode_spec(w.model, w.B, w.kv_len, w.capacity, w.chunk, 152, col_align=4, norms="standalone")
+    tasks, edges = ol.lower(spec)
+    validate(tasks, edges)
+    assert np.count_nonzero(tasks["op_id"] == ol.OP_RMSNORM) == w.B * (2 * w.model.L + 1)
+    g = _replay(L, spec, w.B)
+    try:
+        assert L.mk_get_tasks(g) == tasks.tobytes()
+        assert np.array_equal(L.mk_get_edges(g), edges)
+    finally:
+        L.mk_destroy(g)
+
+
+@pytest.mark.parametrize("name", ["tiny", "8b"])
+def test_fusion_pass_matches_oracle_fusion_and_hand_flags(L, name):
+    from oracle.graph import fuse_rmsnorm
+    w = synth.workload(name)
+    spec = llama_decode_spec(w.model, w.B, w.kv_len, w.capacity, w.chunk, 152, col_align=4, norms="standalone")
+    fused, n = fuse_rmsnorm(spec)
+    assert n == 2 * w.model.L + 1
+    tasks, edges = ol.lower(fused)
+    count = [0]
+    g = _replay(L, spec, w.B, fuse=True, g_fused=count)
+    try:
+        assert count[0] == n
+        assert L.mk_get_tasks(g) == tasks.tobytes()
+        assert np.array_equal(L.mk_get_edges(g), edges)
+    finally:
+        L.mk_destroy(g)
+    # the folded graph is the hand-flagged one up to buffer numbering
+    hand, hedges = ol.lower(llama_decode_spec(w.model, w.B, w.kv_len, w.capacity, w.chunk, 152, col_align=4))
+    assert len(hand) == len(tasks) and np.array_equal(hedges, edges)
+    for f in ("op_id", "config_id", "flags", "remaining_deps", "num_dependents", "dependents_offset", "m", "n",
+              "k", "kv_len"):
+        assert np.array_equal(hand[f], tasks[f]), f
+    gemv = hand["op_id"] == ol.OP_GEMV
+    assert np.array_equal(hand["reserved"][gemv][:, [0, 1, 2, 4]], tasks["reserved"][gemv][:, [0, 1, 2, 4]])
+
+
+def test_fusion_pass_leaves_norms_with_other_readers(L):
+    """A norm whose output is also a residual (or that carries a residual)
+    stays standalone."""
+    g = L.mk_graph_create(num_ctas=8, tiles_target=8, col_align=16)
+    try:
+        base = 1 << 40
+        L.mk_set_state(g, base, 1)
+        nb = iter(range(1, 100))
+        add = lambda dt, r, c: L.mk_add_buffer(g, base + next(nb) * (1 << 24), dt, r, c)
+        x, gm = add(L.MK_F32, 1, 256), add(L.MK_BF16, 1, 256)
+        xn, w = add(L.MK_F32, 1, 256), add(L.MK_BF16, 256, 256)
+        y, z = add(L.MK_F32, 1, 256), add(L.MK_F32, 1, 256)
+        L.mk_add_rmsnorm(g, x, gm, L.MK_NO_BUF, xn, 1, 256, 1e-5)
+        L.mk_add_matmul(g, xn, w, y, L.MK_NO_BUF, L.MK_NO_BUF, 0, 1, 256, 256, 0.0)
+        L.mk_add_matmul(g, y, w, z, xn, L.MK_NO_BUF, L.MK_F_ADD_RESIDUAL, 1, 256, 256, 0.0)
+        assert L.mk_fuse_rmsnorm(g) == 0
+        L.mk_lower(g)
+        t = np.frombuffer(L.mk_get_tasks(g), dtype=ol.TASK_DTYPE)
+        assert (t["op_id"] == ol.OP_RMSNORM).sum() == 1
     finally:
         L.mk_destroy(g)

@@ -19,9 +19,11 @@ pytestmark = pytest.mark.gpu
 MODES = {"mega": 0, "per_op": 1, "per_op_graph": 2, "levels": 3, "per_op_pdl": 4}
 
 
-def _run_and_compare(w, steps, mode="mega", num_ctas=0, seed=0, check_cache=True):
+def _run_and_compare(w, steps, mode="mega", num_ctas=0, seed=0, check_cache=True, norms="fused"):
     from task_graph_interpreter_gb300 import _lib as L
-    dec = build_gpu(w, seed, num_ctas)
+    dec = build_gpu(w, seed, num_ctas, norms=norms)
+    if norms == "fuse_pass":
+        assert dec.fused_norms == 2 * w.model.L + 1
     W = NpWeights(w.model, seed)
     st = oracle_state(w, seed)
     clear_steps = 0
@@ -106,3 +108,11 @@ def test_modes_are_bitwise_identical_and_deterministic():
 def test_1b_full_size_two_steps():
     w = synth.custom(synth.LLAMA_1B, 1, [1024], 2, name="1b2")
     assert _run_and_compare(w, 2, check_cache=False) >= 1
+
+
+@pytest.mark.parametrize("norms", ["standalone", "fuse_pass"])
+def test_standalone_and_pass_fused_rmsnorm(norms):
+    # standalone RMSNORM tasks (one per sequence, batch 2) and the same graph
+    # after the fusion pass both match the oracle
+    w = synth.custom(synth.TINY, 2, [40, 128], 3, name="tiny_norms")
+    assert _run_and_compare(w, 3, norms=norms) >= 2
