@@ -29,7 +29,8 @@ EXPORTS = [
     "mk_graph_create", "mk_set_state", "mk_add_buffer", "mk_add_embed", "mk_add_rmsnorm", "mk_fuse_rmsnorm",
     "mk_add_matmul",
     "mk_add_attention", "mk_add_sample", "mk_attention_scratch_rows", "mk_gemv_tiles",
-    "mk_lower", "mk_get_tasks", "mk_get_edges", "mk_get_sync_plan", "mk_get_queues", "mk_upload",
+    "mk_lower", "mk_get_tasks", "mk_get_edges", "mk_get_sync_plan", "mk_get_ll_plan", "mk_get_queues",
+    "mk_upload",
     "mk_decode_step", "mk_decode_step_ex", "mk_decode_step_host", "mk_status",
     "mk_get_trace", "mk_kernel_info", "mk_destroy", "mk_last_error", "mk_debug_patch_task",
     "mk_attention_decode_noalloc", "mk_gemv_tensor_core_tiles",
@@ -77,6 +78,7 @@ def lib():
         "mk_get_queues": (c_int, [G, POINTER(c_void_p), POINTER(c_void_p), POINTER(c_int)]),
         "mk_get_sync_plan": (c_int, [G, POINTER(c_void_p), POINTER(c_void_p), POINTER(c_void_p),
                                      POINTER(c_void_p), POINTER(c_uint32)]),
+        "mk_get_ll_plan": (c_int, [G, POINTER(c_void_p), POINTER(c_void_p)]),
         "mk_upload": (c_int, [G, c_void_p]),
         "mk_decode_step": (c_int, [G, c_void_p]),
         "mk_decode_step_ex": (c_int, [G, c_void_p, c_int, c_uint32]),
@@ -197,6 +199,16 @@ def mk_get_sync_plan(g, num_tasks: int):
     wait = u32(w, 2 * int(wait_off[-1])).reshape(-1, 2)
     sig = u32(sg, int(sig_off[-1]))
     return wait_off, wait, sig_off, sig, int(cw.value)
+
+
+def mk_get_ll_plan(g, num_tasks: int, num_bufs: int):
+    """(task_ll, buf_ll) as numpy uint8 arrays: the GEMV tasks that read
+    tagged pairs, and the buffers whose producers write them."""
+    import numpy as np
+    tl, bl = c_void_p(), c_void_p()
+    check(lib().mk_get_ll_plan(g, ctypes.byref(tl), ctypes.byref(bl)), "mk_get_ll_plan")
+    u8 = lambda ptr, n: np.frombuffer(ctypes.string_at(ptr, n), dtype=np.uint8).copy() if n else np.zeros(0, np.uint8)
+    return u8(tl, num_tasks), u8(bl, num_bufs)
 
 
 def mk_get_queues(g):

@@ -624,6 +624,31 @@ extern "C" int mk_lower(mk_graph* g) {
     off += (uint32_t)children[t].size();
   }
 
+  {
+    // buffers written exactly once per step: by one op, whose tasks' write
+    // rectangles tile the whole buffer without overlap
+    const size_t NB = g->bufs.size();
+    std::vector<int> group_of(N, 0);
+    for (size_t k = 0; k + 1 < g->group_off.size(); ++k)
+      for (int t = g->group_off[k]; t < g->group_off[k + 1]; ++t) group_of[t] = (int)k;
+    std::vector<uint8_t> once(NB, 0);
+    for (size_t b = 0; b < NB; ++b) {
+      const std::vector<Writer>& ws = L.writes[b];
+      if (ws.empty()) continue;
+      bool ok = true;
+      int64_t area = 0;
+      for (size_t i = 0; i < ws.size() && ok; ++i) {
+        const Writer& w = ws[i];
+        ok = group_of[w.task] == group_of[ws[0].task] && w.r0 >= 0 && w.c0 >= 0 && w.r1 <= g->bufs[b].rows &&
+             w.c1 <= g->bufs[b].cols;
+        area += (w.r1 - w.r0) * (w.c1 - w.c0);
+        for (size_t j = 0; j < i && ok; ++j)
+          ok = !(ws[j].r0 < w.r1 && w.r0 < ws[j].r1 && ws[j].c0 < w.c1 && w.c0 < ws[j].c1);
+      }
+      once[b] = ok && area == g->bufs[b].rows * g->bufs[b].cols;
+    }
+    build_ll_plan(g, L.parents, once);
+  }
   if (int rc = build_sync_plan(g)) return rc;
 
   // topological levels
@@ -678,6 +703,56 @@ extern "C" int mk_lower(mk_graph* g) {
   return MK_OK;
 }
 
+// Tagged hand-offs.  At B <= 4 the activations a GEMV reads (its x, and
+// its residual) are also written by their producers as (value, step tag)
+// pairs into a library-owned mirror.  Such a GEMV polls its inputs' tags
+// instead of waiting on counters: the data and the news that it is ready
+// arrive in one round trip, where a counter costs the producer's fence,
+// the counter's round trip and then the data's.  A buffer qualifies when
+// it is f32, written exactly once per step (once[b]) and only by GEMV,
+// COMBINE, embedding MEMCPY or RMSNORM tasks (the bodies that write the
+// pairs); a GEMV qualifies when its x and residual do and every one of its
+// parents writes one of them (weights and gamma have no writers).
+void mk::build_ll_plan(mk_graph* g, const std::vector<std::vector<int>>& parents,
+                       const std::vector<uint8_t>& once) {
+  const size_t NB = g->bufs.size(), N = g->tasks.size();
+  g->ll_buf.assign(NB, 0);
+  g->ll_task.assign(N, 0);
+  if (g->B > 4) return;
+  std::vector<uint8_t> read_as_input(NB, 0), bad_writer(NB, 0);
+  for (const mk_task_descriptor& d : g->tasks) {
+    if (d.op_id == MK_OP_GEMV) {
+      read_as_input[d.in_buf[0]] = 1;
+      if (d.flags & MK_F_ADD_RESIDUAL) read_as_input[d.in_buf[2]] = 1;
+    }
+    if (d.out_buf >= NB) continue;
+    const bool ok = d.op_id == MK_OP_GEMV || d.op_id == MK_OP_ATTENTION_COMBINE || d.op_id == MK_OP_MEMCPY ||
+                    d.op_id == MK_OP_RMSNORM;
+    if (!ok) bad_writer[d.out_buf] = 1;
+  }
+  for (size_t b = MK_BUF_ROPE_SIN + 1; b < NB; ++b)
+    g->ll_buf[b] = read_as_input[b] && once[b] && !bad_writer[b] && g->bufs[b].dtype == MK_F32;
+  for (size_t t = 0; t < N; ++t) {
+    const mk_task_descriptor& d = g->tasks[t];
+    if (d.op_id != MK_OP_GEMV) continue;
+    const bool res = d.flags & MK_F_ADD_RESIDUAL;
+    bool ok = g->ll_buf[d.in_buf[0]] && (!res || g->ll_buf[d.in_buf[2]]);
+    for (int q : parents[t]) {
+      const uint16_t o = g->tasks[q].out_buf;
+      ok = ok && (o == d.in_buf[0] || (res && o == d.in_buf[2]));
+    }
+    g->ll_task[t] = ok;
+  }
+}
+
+extern "C" int mk_get_ll_plan(const mk_graph* g, const uint8_t** task_ll, const uint8_t** buf_ll) {
+  if (!g || !task_ll || !buf_ll) return fail(MK_ERR_ARG, "mk_get_ll_plan: null argument");
+  if (!g->lowered) return fail(MK_ERR_STATE, "mk_get_ll_plan: not lowered");
+  *task_ll = g->ll_task.data();
+  *buf_ll = g->ll_buf.data();
+  return MK_OK;
+}
+
 // Dependency-counter plan.  With one counter per task, a B = 1 GEMV tile
 // whose ~150 children each need every tile of its op sends ~150 atomics,
 // and one op hand-off puts ~150^2 atomics on a few cache lines of
@@ -719,7 +794,15 @@ int mk::build_sync_plan(mk_graph* g) {
   std::vector<std::vector<uint32_t>> own_sig(N);  // set counters parent p signals
   std::map<std::vector<int>, int> set_ctr;   // remaining-parent set -> its counter
   std::vector<int> cnt(NG, 0);
+  const bool have_ll = g->ll_task.size() == (size_t)N;
   for (int t = 0; t < N; ++t) {
+    if (have_ll && g->ll_task[t]) {
+      // reads every parent's output as tagged pairs: no counter, except a
+      // surplus in a patched descriptor (which then can never be met)
+      own[t] = std::max(g->tasks[t].remaining_deps - (int)parents[t].size(), 0);
+      own_ctr[t] = t;
+      continue;
+    }
     for (int p : parents[t]) cnt[group_of[p]]++;
     int covered = 0;
     for (int p : parents[t]) {

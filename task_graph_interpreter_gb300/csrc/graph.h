@@ -63,6 +63,10 @@ struct mk_graph {
   // counter[sig[j]] for every j in [sig_off[t], sig_off[t+1]).
   std::vector<uint32_t> wait_off, wait, sig_off, sig;  // wait holds (counter, count) pairs
   uint32_t counter_words = 0;
+  // tagged hand-offs (B <= 4): buffers whose values are also written as
+  // (value, step tag) pairs, and the GEMV tasks that read all their inputs
+  // from such pairs instead of waiting on counters
+  std::vector<uint8_t> ll_buf, ll_task;
   // kernel geometry
   int max_m = 1;
   mk::DeviceState* dev = nullptr;
@@ -74,6 +78,8 @@ int query_sm_count(int* out);  // runtime.cu
 int tile_width(int n, int tiles_target, int col_align);
 int tile_count(int n, int tiles_target, int col_align);
 int build_sync_plan(mk_graph* g);  // graph.cpp; from the descriptors and edges
+void build_ll_plan(mk_graph* g, const std::vector<std::vector<int>>& parents,
+                   const std::vector<uint8_t>& once);  // graph.cpp; before build_sync_plan
 std::vector<int> partials_per_sequence(const std::vector<int32_t>& len0, int Hkv, int chunk,
                                        int num_ctas);
 }  // namespace mk

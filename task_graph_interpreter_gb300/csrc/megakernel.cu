@@ -440,6 +440,100 @@ __device__ void block_argmax(float& v, int& idx, float* red) {
   cbar();
 }
 
+// ------------------------------------------------------------------ tagged hand-offs
+// At B <= 4 the activations that GEMVs read also travel as (value, step
+// tag) pairs in mirrors of their buffers (MEGA mode only; every launch has
+// a new tag, so pairs of earlier steps never match).  A GEMV whose inputs
+// all have mirrors waits on no counter: it loads its pairs and polls those
+// whose tag is not yet this step's.
+__device__ __forceinline__ uint64_t ll_pack(float v, uint32_t tag) {
+  return ((uint64_t)tag << 32) | __float_as_uint(v);
+}
+
+__device__ __forceinline__ bool ll_ready(uint64_t v, uint32_t tag) { return (uint32_t)(v >> 32) == tag; }
+
+// Poll the pair at m (found stale) until it carries this step's tag, and
+// return it; on abort or timeout (raised here) return the stale pair, and
+// the caller carries on with it as after any failed wait.
+__device__ uint64_t ll_wait(const KParams& p, const uint64_t* m, int task) {
+  const uint64_t t0 = globaltimer();
+  for (uint32_t it = 1;; ++it) {
+    __nanosleep(32);
+    const uint64_t v = ld_relaxed_u64(m);
+    if (ll_ready(v, p.tag)) return v;
+    if ((it & 15u) == 0) {
+      if (aborted(p)) return v;
+      if (globaltimer() - t0 > p.timeout_ns) {
+        raise_error(p, MK_DEV_DEP_TIMEOUT, task);
+        return v;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ float ll_load1(const KParams& p, const uint64_t* m, int task) {
+  uint64_t v = ld_relaxed_u64(m);
+  if (!ll_ready(v, p.tag)) v = ll_wait(p, m, task);
+  return __uint_as_float((uint32_t)v);
+}
+
+// Eight consecutive pairs into o; returns the mask of those already tagged.
+__device__ __forceinline__ uint32_t ll_piece(const uint64_t* m, uint32_t tag, float (&o)[8]) {
+  const ulonglong2 a = ld_relaxed_v2u64(m), b = ld_relaxed_v2u64(m + 2), e = ld_relaxed_v2u64(m + 4),
+                   f = ld_relaxed_v2u64(m + 6);
+  const uint64_t q[8] = {a.x, a.y, b.x, b.y, e.x, e.y, f.x, f.y};
+  uint32_t ok = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    o[k] = __uint_as_float((uint32_t)q[k]);
+    ok |= (ll_ready(q[k], tag) ? 1u : 0u) << k;
+  }
+  return ok;
+}
+
+// x for this lane's pieces (b, v) of 8 columns from the mirror xm: all
+// pieces are loaded at once; while some hold stale pairs, wait for one
+// stale pair to turn, then reload the pieces still pending.
+template <int B, int NV>
+__device__ __forceinline__ void ll_load_x(const KParams& p, int task, float (&xr)[B][NV][8], const uint64_t* xm,
+                                          int K, int col0, int Bact) {
+  uint32_t pend = 0;
+  const uint64_t* probe = nullptr;
+#pragma unroll
+  for (int v = 0; v < NV; ++v) {
+#pragma unroll
+    for (int b = 0; b < B; ++b) {
+      if (b < Bact) {
+        const uint64_t* m = xm + (size_t)b * K + col0 + v * 256;
+        const uint32_t ok = ll_piece(m, p.tag, xr[b][v]);
+        if (ok != 0xFFu) {
+          pend |= 1u << (v * B + b);
+          if (!probe) probe = m + (__ffs(~ok) - 1);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) xr[b][v][k] = 0.f;
+      }
+    }
+  }
+  while (pend) {
+    if (!ll_ready(ll_wait(p, probe, task), p.tag)) break;
+    probe = nullptr;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        if (pend & (1u << (v * B + b))) {
+          const uint64_t* m = xm + (size_t)b * K + col0 + v * 256;
+          const uint32_t ok = ll_piece(m, p.tag, xr[b][v]);
+          if (ok == 0xFFu) pend &= ~(1u << (v * B + b));
+          else if (!probe) probe = m + (__ffs(~ok) - 1);
+        }
+      }
+    }
+  }
+}
+
 // ------------------------------------------------------------------ GEMV body
 // Shared-memory scratch of a GEMV task: per-(row, batch, warp column) slots,
 // per-(row, batch) accumulators, then a small reduction area:
@@ -450,10 +544,29 @@ __device__ __forceinline__ float* gemv_acc(Ctx& c) { return c.scratch + kSlotFlo
 __device__ __forceinline__ float* gemv_red(Ctx& c) { return c.scratch + kSlotFloats + kAccFloats; }
 
 // x (times gamma when normalising) for this lane's columns col0 + v*256 + [0,8),
-// and the sum of squares of the raw x values loaded (for the RMS norm).
+// and the sum of squares of the raw x values loaded (for the RMS norm); from
+// the mirror xm when the task reads tagged pairs.
 template <int B, int NV>
-__device__ __forceinline__ void gemv_load_x(float (&xr)[B][NV][8], float (&ss)[B], const float* __restrict__ x,
+__device__ __forceinline__ void gemv_load_x(const KParams& p, int task, float (&xr)[B][NV][8], float (&ss)[B],
+                                            const float* __restrict__ x, const uint64_t* xm,
                                             const uint16_t* __restrict__ gamma, int K, int col0, int Bact) {
+  if (xm) {
+    ll_load_x<B, NV>(p, task, xr, xm, K, col0, Bact);
+  } else {
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+#pragma unroll
+      for (int b = 0; b < B; ++b) {
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), e = a;
+        if (b < Bact) {
+          a = __ldcg(reinterpret_cast<const float4*>(x + (size_t)b * K + col0 + v * 256));
+          e = __ldcg(reinterpret_cast<const float4*>(x + (size_t)b * K + col0 + v * 256 + 4));
+        }
+        xr[b][v][0] = a.x; xr[b][v][1] = a.y; xr[b][v][2] = a.z; xr[b][v][3] = a.w;
+        xr[b][v][4] = e.x; xr[b][v][5] = e.y; xr[b][v][6] = e.z; xr[b][v][7] = e.w;
+      }
+    }
+  }
 #pragma unroll
   for (int b = 0; b < B; ++b) ss[b] = 0.f;
 #pragma unroll
@@ -470,14 +583,11 @@ __device__ __forceinline__ void gemv_load_x(float (&xr)[B][NV][8], float (&ss)[B
     }
 #pragma unroll
     for (int b = 0; b < B; ++b) {
-      float4 a = make_float4(0.f, 0.f, 0.f, 0.f), e = a;
-      if (b < Bact) {
-        a = __ldcg(reinterpret_cast<const float4*>(x + (size_t)b * K + col));
-        e = __ldcg(reinterpret_cast<const float4*>(x + (size_t)b * K + col + 4));
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        ss[b] = fmaf(xr[b][v][k], xr[b][v][k], ss[b]);
+        xr[b][v][k] *= gm[k];
       }
-      ss[b] += a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + e.x * e.x + e.y * e.y + e.z * e.z + e.w * e.w;
-      xr[b][v][0] = a.x * gm[0]; xr[b][v][1] = a.y * gm[1]; xr[b][v][2] = a.z * gm[2]; xr[b][v][3] = a.w * gm[3];
-      xr[b][v][4] = e.x * gm[4]; xr[b][v][5] = e.y * gm[5]; xr[b][v][6] = e.z * gm[6]; xr[b][v][7] = e.w * gm[7];
     }
   }
 }
@@ -525,7 +635,7 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[N], int lane) {
 // Results go to slots[(row, b, warp column)].
 template <int B, int NV>
 __device__ __forceinline__ void gemv_stages(Ctx& c, const mk_task_descriptor& d, const GemvGeom& G, int rows_g,
-                                            int ks, bool first_group) {
+                                            int ks, bool first_group, const uint64_t* xm) {
   const KParams& p = *c.p;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wcol = warp % G.WCOL, wrow = warp / G.WCOL;
@@ -535,7 +645,7 @@ __device__ __forceinline__ void gemv_stages(Ctx& c, const mk_task_descriptor& d,
       (d.flags & MK_F_RMS_NORM_INPUT) ? static_cast<const uint16_t*>(p.bufs[d.in_buf[2]]) : nullptr;
   float* slots = gemv_slots(c);
   float xr[B][NV][8], ss[B];
-  gemv_load_x<B, NV>(xr, ss, x, gamma, G.K, ks * G.KS + wcol * colw + lane * 8, G.B);
+  gemv_load_x<B, NV>(p, c.task, xr, ss, x, xm, gamma, G.K, ks * G.KS + wcol * colw + lane * 8, G.B);
   if (gamma && first_group) {
     // sum of squares of x over this warp's columns; warps of the first warp
     // row cover every column once (the others contribute zero)
@@ -625,7 +735,7 @@ __device__ __forceinline__ void gemv_fold(const mk_task_descriptor& d, const Gem
 // store, and the tile's running argmax.
 __device__ __forceinline__ void gemv_epilogue(const KParams& p, const mk_task_descriptor& d, const GemvGeom& G,
                                            int g0, int rows_g, const float* acc, float* red,
-                                           const float* staged_res) {
+                                           const float* staged_res, const uint64_t* rm, uint64_t* om, int task) {
   const int tid = threadIdx.x;
   float* out = static_cast<float*>(p.bufs[d.out_buf]);
   const bool silu = d.flags & MK_F_SILU_MUL;
@@ -644,8 +754,10 @@ __device__ __forceinline__ void gemv_epilogue(const KParams& p, const mk_task_de
       }
       const int col = G.c0 + g0 + j;
       if (staged_res) y += staged_res[j * BT + b];
+      else if (rm) y += ll_load1(p, rm + (size_t)b * G.n + col, task);
       else if (res) y += __ldcg(res + (size_t)b * G.n + col);
       out[(size_t)b * G.n + col] = y;
+      if (om) st_relaxed_u64(om + (size_t)b * G.n + col, ll_pack(y, p.tag));
       if (y > bv) {
         bv = y;
         bi = col;
@@ -676,28 +788,53 @@ __device__ void gemv_task(Ctx& c, const mk_task_descriptor& d) {
   gemv_prologue(d, G, red);
   // A residual read by the epilogue is loaded now, so its latency hides
   // behind the slots; it is parked in the (then free) slot area afterwards.
+  // tagged pairs (B <= 4 only): the output's mirror, and the inputs' when
+  // both x and the residual have one (the task then waited on no counter)
+  const KParams& p = *c.p;
+  const uint64_t *xm = nullptr, *rm = nullptr;
+  uint64_t* om = nullptr;
+  if (BCLASS < 2 && p.mode == MK_MODE_MEGA) {
+    om = p.mirrors[d.out_buf];
+    xm = p.mirrors[d.in_buf[0]];
+    if (d.flags & MK_F_ADD_RESIDUAL) {
+      rm = p.mirrors[d.in_buf[2]];
+      if (!rm) xm = nullptr;
+    }
+    if (!xm) rm = nullptr;
+  }
   const bool stage_res = (d.flags & MK_F_ADD_RESIDUAL) && G.cn <= kConsumerThreads && G.RG >= G.cn;
   float rv[8];
   if (stage_res && threadIdx.x < G.cn) {
-    const float* res = static_cast<const float*>(c.p->bufs[d.in_buf[2]]);
+    const float* res = static_cast<const float*>(p.bufs[d.in_buf[2]]);
+    if (rm) {
+      uint64_t q[8];
 #pragma unroll
-    for (int b = 0; b < 8; ++b) rv[b] = b < G.B ? __ldcg(res + (size_t)b * G.n + G.c0 + threadIdx.x) : 0.f;
+      for (int b = 0; b < 8; ++b) q[b] = b < G.B ? ld_relaxed_u64(rm + (size_t)b * G.n + G.c0 + threadIdx.x) : 0u;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) {
+        if (b < G.B && !ll_ready(q[b], p.tag)) q[b] = ll_wait(p, rm + (size_t)b * G.n + G.c0 + threadIdx.x, c.task);
+        rv[b] = b < G.B ? __uint_as_float((uint32_t)q[b]) : 0.f;
+      }
+    } else {
+#pragma unroll
+      for (int b = 0; b < 8; ++b) rv[b] = b < G.B ? __ldcg(res + (size_t)b * G.n + G.c0 + threadIdx.x) : 0.f;
+    }
   }
   for (int g0 = 0; g0 < G.cn; g0 += G.RG) {
     const int rows_g = min(G.RG, G.cn - g0);
     for (int ks = 0; ks < G.nks; ++ks) {
       if constexpr (BCLASS == 0) {
         switch (G.BT * 16 + G.NV) {
-          case 16 + 1: gemv_stages<1, 1>(c, d, G, rows_g, ks, g0 == 0); break;
-          case 16 + 2: gemv_stages<1, 2>(c, d, G, rows_g, ks, g0 == 0); break;
-          case 16 + 4: gemv_stages<1, 4>(c, d, G, rows_g, ks, g0 == 0); break;
-          case 16 + 7: gemv_stages<1, 7>(c, d, G, rows_g, ks, g0 == 0); break;
-          default: gemv_stages<2, 1>(c, d, G, rows_g, ks, g0 == 0); break;
+          case 16 + 1: gemv_stages<1, 1>(c, d, G, rows_g, ks, g0 == 0, xm); break;
+          case 16 + 2: gemv_stages<1, 2>(c, d, G, rows_g, ks, g0 == 0, xm); break;
+          case 16 + 4: gemv_stages<1, 4>(c, d, G, rows_g, ks, g0 == 0, xm); break;
+          case 16 + 7: gemv_stages<1, 7>(c, d, G, rows_g, ks, g0 == 0, xm); break;
+          default: gemv_stages<2, 1>(c, d, G, rows_g, ks, g0 == 0, xm); break;
         }
       } else if constexpr (BCLASS == 1) {
-        gemv_stages<4, 1>(c, d, G, rows_g, ks, g0 == 0);
+        gemv_stages<4, 1>(c, d, G, rows_g, ks, g0 == 0, xm);
       } else {
-        gemv_stages<8, 1>(c, d, G, rows_g, ks, g0 == 0);
+        gemv_stages<8, 1>(c, d, G, rows_g, ks, g0 == 0, xm);
       }
       gemv_fold(d, G, rows_g, ks, g0 == 0, gemv_slots(c), gemv_acc(c), red);
     }
@@ -711,11 +848,11 @@ __device__ void gemv_task(Ctx& c, const mk_task_descriptor& d) {
           if (b < G.B) staged[threadIdx.x * G.BT + b] = rv[b];
       }
     }
-    gemv_epilogue(*c.p, d, G, g0, rows_g, gemv_acc(c), red, staged);
+    gemv_epilogue(p, d, G, g0, rows_g, gemv_acc(c), red, staged, rm, om, c.task);
     trace_mark(c, 2);
   }
   if ((d.flags & MK_F_ARGMAX_EPI) && threadIdx.x < G.B) {
-    mk_argmax_pair* pairs = static_cast<mk_argmax_pair*>(c.p->bufs[d.reserved[3]]);
+    mk_argmax_pair* pairs = static_cast<mk_argmax_pair*>(p.bufs[d.reserved[3]]);
     mk_argmax_pair pr;
     pr.value = red[96 + threadIdx.x];
     pr.index = reinterpret_cast<int*>(red)[104 + threadIdx.x];
@@ -863,7 +1000,7 @@ __device__ void tc_gemv_task(Ctx& c, const mk_task_descriptor& d) {
     }
     cbar();
     if (tid == 0) mbar_arrive(&ctl->acc_empty);  // tensor memory is free for the next row group
-    gemv_epilogue(p, d, G, g0, rows_g, acc, red, nullptr);
+    gemv_epilogue(p, d, G, g0, rows_g, acc, red, nullptr, nullptr, nullptr, c.task);
   }
   for (int g0 = 0; g0 < G.cn; g0 += T.RG)
     for (int i = 0; i < T.nkr * T.seg; ++i) c.rp.advance(c.nst);
@@ -1219,6 +1356,7 @@ __device__ void combine_task(Ctx& c, const mk_task_descriptor& d) {
   const int rec = G * (D + 2);
   const float* scr = static_cast<const float*>(p.bufs[d.in_buf[0]]) + (size_t)base * rec;
   float* out = static_cast<float*>(p.bufs[d.out_buf]);
+  uint64_t* om = p.mode == MK_MODE_MEGA ? p.mirrors[d.out_buf] : nullptr;
   // each thread produces two adjacent outputs (e, e + 1) of one head
   for (int i = threadIdx.x; i < G * D / 2; i += kConsumerThreads) {
     const int h = (2 * i) / D, e = (2 * i) % D;
@@ -1246,7 +1384,9 @@ __device__ void combine_task(Ctx& c, const mk_task_descriptor& d) {
       }
     }
     const float inv = 1.f / Ls;
-    *reinterpret_cast<float2*>(out + (size_t)s * Hq * D + (size_t)(g * G + h) * D + e) = make_float2(O0 * inv, O1 * inv);
+    const size_t o = (size_t)s * Hq * D + (size_t)(g * G + h) * D + e;
+    *reinterpret_cast<float2*>(out + o) = make_float2(O0 * inv, O1 * inv);
+    if (om) st_relaxed_v2u64(om + o, ll_pack(O0 * inv, p.tag), ll_pack(O1 * inv, p.tag));
   }
 }
 
@@ -1261,12 +1401,21 @@ __device__ void embed_task(Ctx& c, const mk_task_descriptor& d) {
   }
   const uint16_t* E = static_cast<const uint16_t*>(p.bufs[d.in_buf[0]]) + (size_t)tok * H;
   float* out = static_cast<float*>(p.bufs[d.out_buf]) + (size_t)s * H;
+  uint64_t* om = p.mode == MK_MODE_MEGA ? p.mirrors[d.out_buf] : nullptr;
   for (int i = threadIdx.x * 8; i < H; i += kConsumerThreads * 8) {
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(E + i));
     float4 a = make_float4(bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y));
     float4 b = make_float4(bf_lo(v.z), bf_hi(v.z), bf_lo(v.w), bf_hi(v.w));
     *reinterpret_cast<float4*>(out + i) = a;
     *reinterpret_cast<float4*>(out + i + 4) = b;
+    if (om) {
+      uint64_t* m = om + (size_t)s * H + i;
+      const uint32_t t = p.tag;
+      st_relaxed_v2u64(m, ll_pack(a.x, t), ll_pack(a.y, t));
+      st_relaxed_v2u64(m + 2, ll_pack(a.z, t), ll_pack(a.w, t));
+      st_relaxed_v2u64(m + 4, ll_pack(b.x, t), ll_pack(b.y, t));
+      st_relaxed_v2u64(m + 6, ll_pack(b.z, t), ll_pack(b.w, t));
+    }
   }
 }
 
@@ -1282,6 +1431,7 @@ __device__ void rmsnorm_task(Ctx& c, const mk_task_descriptor& d) {
   const float* res =
       (d.flags & MK_F_ADD_RESIDUAL) ? static_cast<const float*>(p.bufs[d.in_buf[2]]) + (size_t)s * H : nullptr;
   float* out = static_cast<float*>(p.bufs[d.out_buf]) + (size_t)s * H;
+  uint64_t* om = p.mode == MK_MODE_MEGA ? p.mirrors[d.out_buf] : nullptr;
   float* red = c.scratch;
   float ss = 0.f;
 #pragma unroll 1
@@ -1302,7 +1452,9 @@ __device__ void rmsnorm_task(Ctx& c, const mk_task_descriptor& d) {
 #pragma unroll 1
   for (int i = tid; i < H; i += kConsumerThreads) {
     const float y = __ldcg(x + i) + (res ? __ldcg(res + i) : 0.f);
-    out[i] = y * inv * __uint_as_float((uint32_t)__ldg(gamma + i) << 16);
+    const float o = y * inv * __uint_as_float((uint32_t)__ldg(gamma + i) << 16);
+    out[i] = o;
+    if (om) st_relaxed_u64(om + (size_t)s * H + i, ll_pack(o, p.tag));
   }
 }
 

@@ -40,6 +40,8 @@ struct DeviceState {
   uint8_t* tmaps = nullptr;
   int32_t* tm_rows = nullptr;
   int tc_tiles = 0;  // GEMV tiles on the tensor-core path
+  uint64_t** mirrors = nullptr;  // device table: per buffer, its tagged pairs or null
+  uint32_t tag = 0;              // last step tag (never reset, so stale pairs never match)
   int32_t* queue_off = nullptr;
   int32_t* queue = nullptr;
   int32_t* level_off = nullptr;
@@ -99,6 +101,8 @@ KParams base_params(const mk_graph* g) {
   p.sig = d->sig;
   p.tmaps = d->tmaps;
   p.tm_rows = d->tm_rows;
+  p.mirrors = d->mirrors;
+  p.tag = d->tag;
   p.queue_off = d->queue_off;
   p.queue = d->queue;
   p.level_off = d->level_off;
@@ -245,8 +249,11 @@ extern "C" int mk_upload(mk_graph* g, void* stream_) {
                  o_bufs = take(NB * 8), o_cos = take((size_t)cap * half * 4), o_sin = take((size_t)cap * half * 4),
                  o_woff = take(g->wait_off.size() * 4), o_wait = take(g->wait.size() * 4),
                  o_soff = take(g->sig_off.size() * 4), o_sig = take(g->sig.size() * 4),
-                 o_tmap = take(tmaps.size()), o_tmr = take(tm_rows.size() * 4);
+                 o_tmap = take(tmaps.size()), o_tmr = take(tm_rows.size() * 4), o_mtab = take(NB * 8);
     const size_t static_bytes = off;
+    std::vector<size_t> o_mir(NB, 0);  // tagged pairs of the buffers that carry them (zeroed)
+    for (size_t b = 0; b < NB; ++b)
+      if (b < g->ll_buf.size() && g->ll_buf[b]) o_mir[b] = take((size_t)g->bufs[b].rows * g->bufs[b].cols * 8);
     const size_t o_ctr = take((size_t)g->counter_words * 4), o_status = take(16), o_lbar = take(g->level_off.size() * 4),
                  o_trace = take(N * 64);
     d->blob_bytes = off;
@@ -270,6 +277,12 @@ extern "C" int mk_upload(mk_graph* g, void* stream_) {
     std::memcpy(img.data() + o_sig, g->sig.data(), g->sig.size() * 4);
     std::memcpy(img.data() + o_tmap, tmaps.data(), tmaps.size());
     std::memcpy(img.data() + o_tmr, tm_rows.data(), tm_rows.size() * 4);
+    {
+      std::vector<uint64_t*> mt(NB, nullptr);
+      for (size_t b = 0; b < NB; ++b)
+        if (o_mir[b]) mt[b] = reinterpret_cast<uint64_t*>(static_cast<char*>(d->blob) + o_mir[b]);
+      std::memcpy(img.data() + o_mtab, mt.data(), NB * 8);
+    }
     char* base = static_cast<char*>(d->blob);
     std::vector<void*> ptrs(NB);
     for (size_t i = 0; i < NB; ++i) ptrs[i] = g->bufs[i].ptr;
@@ -290,7 +303,7 @@ extern "C" int mk_upload(mk_graph* g, void* stream_) {
       }
     }
     if (cudaMemcpy(d->blob, img.data(), static_bytes, cudaMemcpyHostToDevice) != cudaSuccess ||
-        cudaMemset(base + o_ctr, 0, d->blob_bytes - o_ctr) != cudaSuccess) {
+        cudaMemset(base + static_bytes, 0, d->blob_bytes - static_bytes) != cudaSuccess) {
       rc = fail(MK_ERR_CUDA, "mk_upload: copy to device failed");
       break;
     }
@@ -311,6 +324,7 @@ extern "C" int mk_upload(mk_graph* g, void* stream_) {
     d->sig = reinterpret_cast<uint32_t*>(base + o_sig);
     d->tmaps = reinterpret_cast<uint8_t*>(base + o_tmap);
     d->tm_rows = reinterpret_cast<int32_t*>(base + o_tmr);
+    d->mirrors = reinterpret_cast<uint64_t**>(base + o_mtab);
     for (const mk_task_descriptor& t : g->tasks)
       if (t.op_id == MK_OP_GEMV && t.config_id == 1 && g->B > 4 && tm_rows[t.in_buf[1]] > 0) ++d->tc_tiles;
     d->status = reinterpret_cast<int32_t*>(base + o_status);
@@ -340,6 +354,7 @@ extern "C" int mk_decode_step_ex(mk_graph* g, void* stream_, int mode, uint32_t 
     case MK_MODE_MEGA: {
       KParams p = base_params(g);
       p.epoch = d->epoch + 1;
+      p.tag = ++d->tag;
       p.trace = tr;
       CUDA_TRY(launch_interpreter(p, g->B, g->num_ctas, true, stream));
       d->epoch += 1;

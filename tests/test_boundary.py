@@ -211,10 +211,14 @@ def test_product_builder_matches_oracle_graph(L, name):
     dec.graph.close()
 
 
-def _check_sync_plan(tasks, edges, plan):
+def _check_sync_plan(tasks, edges, plan, ll=None):
     """When every wait of a task is satisfied, every parent of the task has
-    signalled, and no wait can be satisfied without all its signallers."""
+    signalled, and no wait can be satisfied without all its signallers.
+    A task that reads tagged pairs (ll = (task_ll, buf_ll)) waits on no
+    counter; each of its parents then writes its x or its residual, and
+    that buffer carries pairs."""
     wait_off, wait, sig_off, sig, words = plan
+    task_ll, buf_ll = ll if ll is not None else (np.zeros(len(tasks), np.uint8), None)
     N = len(tasks)
     parents = [set() for _ in range(N)]
     for p in range(N):
@@ -231,6 +235,15 @@ def _check_sync_plan(tasks, edges, plan):
     for t in range(N):
         covered = set()
         entries = wait[wait_off[t]:wait_off[t + 1]]
+        if task_ll[t]:
+            assert int(tasks["op_id"][t]) == ol.OP_GEMV and len(entries) == 0
+            res = int(tasks["flags"][t]) & ol.F_ADD_RESIDUAL
+            x, aux = int(tasks["in_buf"][t][0]), int(tasks["in_buf"][t][2])
+            assert buf_ll[x] and (not res or buf_ll[aux])
+            for p in parents[t]:
+                assert int(tasks["out_buf"][p]) in ((x, aux) if res else (x,)), f"task {t}: parent {p}"
+            assert int(tasks["remaining_deps"][t]) == len(parents[t])
+            continue
         assert len({int(c) for c, _ in entries}) == len(entries)
         for c, n in entries:
             c, n = int(c), int(n)
@@ -254,7 +267,15 @@ def test_sync_plan_is_equivalent_to_the_edges(L, name):
     try:
         tasks = np.frombuffer(L.mk_get_tasks(g), dtype=ol.TASK_DTYPE)
         plan = L.mk_get_sync_plan(g, len(tasks))
-        _check_sync_plan(tasks, L.mk_get_edges(g), plan)
+        ll = L.mk_get_ll_plan(g, len(tasks), len(spec["buffers"]))
+        _check_sync_plan(tasks, L.mk_get_edges(g), plan, ll)
+        gemv = tasks["op_id"] == ol.OP_GEMV
+        if w.B <= 4:
+            # every GEMV reads tagged pairs (its inputs come from GEMV,
+            # COMBINE, embedding or norm tasks), and no other task does
+            assert np.all(ll[0][gemv] == 1) and np.all(ll[0][~gemv] == 0)
+        else:
+            assert not ll[0].any() and not ll[1].any()
         # a B = 1 hand-off between GEMVs costs one atomic per tile, not one per edge
         if w.B == 1 and name != "tiny":
             assert len(plan[3]) < len(L.mk_get_edges(g)) / 20
@@ -274,7 +295,10 @@ def test_sync_plan_follows_a_patched_dependency_count(L):
         L.mk_debug_patch_task(g, victim, t.tobytes())
         wait_off, wait, _, sig, _ = L.mk_get_sync_plan(g, len(tasks))
         entries = wait[wait_off[victim]:wait_off[victim + 1]]
-        assert sum(int(n) for _, n in entries) == int(t["remaining_deps"])
+        task_ll, _ = L.mk_get_ll_plan(g, len(tasks), len(spec["buffers"]))
+        # a task reading tagged pairs counts only the surplus on a counter
+        want = 1 if task_ll[victim] else int(t["remaining_deps"])
+        assert sum(int(n) for _, n in entries) == want
         own = [(int(c), int(n)) for c, n in entries if int(c) < len(tasks)]
         assert own and own[0][1] > np.count_nonzero(sig == own[0][0]), "the extra dependency can never be met"
     finally:

@@ -122,7 +122,16 @@ def test_trace_respects_every_dependency():
     cta = (tr[:, 0] >> 32).astype(np.int64)
     for c in range(len(off) - 1):
         assert np.all(cta[q[off[c]:off[c + 1]]] == c)
+    from task_graph_interpreter_gb300 import _lib as L
+    task_ll, _ = L.mk_get_ll_plan(dec.graph.h, N, len(dec.graph.bufs) + 3)
+    assert task_ll.any()
     for p in range(N):
         ch = edges[t["dependents_offset"][p]: t["dependents_offset"][p] + t["num_dependents"][p]]
-        assert np.all(tr[ch, 2] >= tr[p, 3]), f"a child of task {p} started before it ended"
+        # a child waiting on counters starts after its parents end; one that
+        # polls tagged pairs starts at once and ends only after its parents
+        # began (their output is written before their end stamp)
+        ctr = ch[task_ll[ch] == 0]
+        ll = ch[task_ll[ch] == 1]
+        assert np.all(tr[ctr, 2] >= tr[p, 3]), f"a child of task {p} started before it ended"
+        assert np.all(tr[ll, 3] >= tr[p, 2]), f"a tagged child of task {p} ended before it began"
     dec.graph.close()
