@@ -14,14 +14,11 @@ constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 128;  // + one producer warpgroup
 constexpr int kLaunchRegs = 168;    // registers per thread at launch (384 threads, 1 CTA/SM)
-constexpr int kProducerRegs = 40;   // after setmaxnreg.dec in the producer warpgroup
-constexpr int kConsumerRegs = 232;  // after setmaxnreg.inc in the consumer warpgroups
+// The producer warpgroup runs the copy thread, the task-record warp and (in
+// the B >= 8 kernel) the MMA warp.
+constexpr int kProducerRegs = 56;   // after setmaxnreg.dec in the producer warpgroup
+constexpr int kConsumerRegs = 224;  // after setmaxnreg.inc in the consumer warpgroups
 static_assert(128 * kProducerRegs + 2 * 128 * kConsumerRegs <= kThreads * kLaunchRegs,
-              "register split exceeds the launch allocation");
-// The B >= 8 kernel's producer warpgroup also runs the MMA warp.
-constexpr int kProducerRegsTc = 56;
-constexpr int kConsumerRegsTc = 224;
-static_assert(128 * kProducerRegsTc + 2 * 128 * kConsumerRegsTc <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr int kStageBytes = 32768;               // one ring slot
 constexpr int kStageElems = kStageBytes / 2;     // bf16 elements per slot
@@ -30,6 +27,8 @@ constexpr int kScratchBytes = 24576;             // per-task shared scratch
 constexpr int kXbufBytes = 24576;                // B >= 8 kernel: two 12 KB activation staging tiles
 constexpr int kTmemCols = 256;                   // B >= 8 kernel: tensor-memory accumulator columns
 constexpr int kTmapBytes = 128;                  // one CUtensorMap
+constexpr int kRecs = 8;                         // task-record FIFO entries (a power of two)
+constexpr int kRecBytes = 256;                   // one task record
 constexpr int kSlotFloats = 4096;                // GEMV per-warp partial slots
 constexpr int kAccFloats = 1024;                 // GEMV per-row accumulators
 
@@ -65,6 +64,7 @@ struct KParams {
   int32_t num_levels;         // LEVELS
   int32_t nstages;            // ring slots in use
   int32_t rope_half;          // D/2 of the tables
+  int32_t num_bufs;           // entries of bufs / mirrors / tm_rows
 };
 
 int smem_bytes_for(int nstages, int batch);

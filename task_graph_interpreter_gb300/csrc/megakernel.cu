@@ -110,21 +110,6 @@ __device__ __forceinline__ bool seq_next(Seq& s, const KParams& p, int& task, in
   return true;
 }
 
-union DescWords {
-  uint4 w[4];
-  mk_task_descriptor d;
-};
-
-__device__ __forceinline__ mk_task_descriptor load_desc(const mk_task_descriptor* t) {
-  DescWords u;
-  const uint4* src = reinterpret_cast<const uint4*>(t);
-  u.w[0] = __ldg(src);
-  u.w[1] = __ldg(src + 1);
-  u.w[2] = __ldg(src + 2);
-  u.w[3] = __ldg(src + 3);
-  return u.d;
-}
-
 // ------------------------------------------------------------------ GEMV plan
 // A GEMV tile streams its weight rows [c0, c0+cn) (and the matching up rows
 // for SILU_MUL) in k-segments of KS columns.  A ring slot holds rs whole
@@ -168,8 +153,8 @@ struct TcGeom {
   int RG, Nr, nkb, nkr, seg, K;
 };
 
-__device__ __forceinline__ void tc_geom(const KParams& p, const mk_task_descriptor& d, TcGeom& t) {
-  t.RG = p.tm_rows[d.in_buf[1]];
+__device__ __forceinline__ void tc_geom(int rows, const mk_task_descriptor& d, TcGeom& t) {
+  t.RG = rows;
   t.Nr = (t.RG + 15) & ~15;
   t.seg = (d.flags & MK_F_SILU_MUL) ? 2 : 1;
   t.K = d.k;
@@ -186,7 +171,7 @@ struct PartGeom {
   bool bad;
 };
 
-__device__ __forceinline__ void part_geom(const KParams& p, const mk_task_descriptor& d, PartGeom& q) {
+__device__ __forceinline__ void part_geom(const int32_t* state, const mk_task_descriptor& d, PartGeom& q) {
   q.s = (int)d.reserved[0];
   q.g = (int)d.reserved[1];
   q.Hkv = (int)d.reserved[2];
@@ -197,7 +182,6 @@ __device__ __forceinline__ void part_geom(const KParams& p, const mk_task_descri
   q.Hq = d.k;
   q.G = q.Hq / q.Hkv;
   q.cap = d.kv_len;
-  const int32_t* state = static_cast<const int32_t*>(p.bufs[MK_BUF_STATE]);
   q.pos = ld_relaxed(state + 2 * q.s + 1);
   q.bad = q.pos < 0 || q.pos >= q.cap;
   if (q.bad) {
@@ -236,6 +220,29 @@ struct TcCtl {
 static_assert(sizeof(TcCtl) == 88, "control block layout");
 constexpr int kCtlBytes = 96;
 
+// ------------------------------------------------------------------ task records
+// A warp of the producer group walks the CTA's task order ahead of the
+// consumers and leaves, per task, its descriptor with everything the
+// descriptor only names resolved: buffer pointers, mirrors, the dependency
+// plan's ranges and first entries.  The consumers then start a task from
+// shared memory instead of a chain of dependent global loads (queue entry,
+// descriptor, buffer table, plan offsets).  kRecs entries, each guarded by
+// a full and an empty mbarrier.
+enum { kPIn0 = 0, kPIn1 = 1, kPIn2 = 2, kPOut = 3, kMirX = 4, kMirAux = 5, kMirOut = 6, kPPairs = 7 };
+struct TaskRec {
+  mk_task_descriptor d;
+  uint64_t ptr[8];     // in_buf[0..2] and out_buf resolved; mirrors of in_buf[0], in_buf[2], out_buf;
+                       // the argmax pairs of a GEMV with ARGMAX_EPI (null where absent)
+  int32_t task, lvl;   // task index (-1: no more tasks), level (LEVELS)
+  uint32_t w0, nw;     // MEGA: wait entries [w0, w0 + nw)
+  uint32_t s0, ns;     //   and signal entries [s0, s0 + ns)
+  uint2 wi[4];         //   the first four wait entries
+  uint32_t si[4];      //   the first four signal entries
+  int32_t tm_rows;     // rows of in_buf[1]'s tensor map box (0: none)
+  uint32_t pad[13];
+};
+static_assert(sizeof(TaskRec) == kRecBytes, "task record layout");
+
 // ------------------------------------------------------------------ ring position
 // Slot index and mbarrier phase parity of the next ring use, advanced
 // without division (this runs once per slot in every warp).
@@ -265,26 +272,33 @@ __device__ __forceinline__ uint8_t* produce_slot(const KParams& p, uint8_t* ring
   return ring + (size_t)slot * kStageBytes;
 }
 
-__device__ void producer(const KParams& p, uint8_t* ring, uint64_t* full, uint64_t* empty) {
+// Producer (one thread): walks the task records and streams every task's
+// operand tiles into the ring, at most nstages slots ahead of the consumers.
+__device__ void producer(const KParams& p, uint8_t* ring, uint64_t* full, uint64_t* empty, const TaskRec* recs,
+                         uint64_t* rfull, uint64_t* rempty) {
   if ((threadIdx.x & 31) != 0) return;
   const uint64_t pol = policy_evict_first();
   const int nst = p.nstages;
   RingPos rp;
   uint32_t issued = 0;
   bool stop = false;
-  Seq sq;
-  seq_init(sq, p);
-  int task, lvl;
-  while (!stop && seq_next(sq, p, task, lvl)) {
-    const mk_task_descriptor d = load_desc(p.tasks + task);
-    if (d.op_id == MK_OP_GEMV && d.config_id == 1 && p.tm_rows[d.in_buf[1]] > 0) {
+  const int32_t* state = static_cast<const int32_t*>(p.bufs[MK_BUF_STATE]);
+  for (uint32_t k = 0; !stop; ++k) {
+    const uint32_t e = k & (kRecs - 1);
+    const TaskRec* r = recs + e;
+    if (!bar_wait(p, &rfull[e], (k / kRecs) & 1u, -1, true)) break;
+    const int task = r->task;
+    if (task < 0) break;
+    const mk_task_descriptor& d = r->d;
+    const int tmr = r->tm_rows;
+    if (d.op_id == MK_OP_GEMV && d.config_id == 1 && tmr > 0) {
       // tensor-core tile: per K range and segment one slot of nkb K blocks,
       // each a TMA box of 64 columns x RG rows in the 128-byte swizzle
       TcGeom T;
-      tc_geom(p, d, T);
+      tc_geom(tmr, d, T);
       const uint8_t* tmap = p.tmaps + (size_t)d.in_buf[1] * kTmapBytes;
       const int c0 = (int)d.reserved[0], cn = (int)d.reserved[1];
-      if (d.flags & MK_F_RMS_NORM_INPUT) prefetch_l2(p.bufs[d.in_buf[2]], (uint32_t)d.k * 2u);
+      if (d.flags & MK_F_RMS_NORM_INPUT) prefetch_l2(reinterpret_cast<const void*>(r->ptr[kPIn2]), (uint32_t)d.k * 2u);
       for (int g0 = 0; g0 < cn && !stop; g0 += T.RG)
         for (int kr = 0; kr < T.nkr && !stop; ++kr)
           for (int sg = 0; sg < T.seg; ++sg) {
@@ -296,14 +310,12 @@ __device__ void producer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
             for (int kb = 0; kb < T.nkb; ++kb)
               tma_load_2d(dst + (size_t)kb * T.Nr * 128, tmap, (kr * T.nkb + kb) * 64, row, fb, pol);
           }
-      continue;
-    }
-    if (d.op_id == MK_OP_GEMV) {
+    } else if (d.op_id == MK_OP_GEMV) {
       GemvGeom G;
       gemv_geom(d, G);
-      const uint16_t* W = static_cast<const uint16_t*>(p.bufs[d.in_buf[1]]);
+      const uint16_t* W = reinterpret_cast<const uint16_t*>(r->ptr[kPIn1]);
       // the norm gain is read right after the dependency wait: warm the L2
-      if (d.flags & MK_F_RMS_NORM_INPUT) prefetch_l2(p.bufs[d.in_buf[2]], (uint32_t)G.K * 2u);
+      if (d.flags & MK_F_RMS_NORM_INPUT) prefetch_l2(reinterpret_cast<const void*>(r->ptr[kPIn2]), (uint32_t)G.K * 2u);
       for (int g0 = 0; g0 < G.cn && !stop; g0 += G.RG) {
         const int rows_g = min(G.RG, G.cn - g0);
         for (int ks = 0; ks < G.nks && !stop; ++ks)
@@ -319,16 +331,16 @@ __device__ void producer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
               if (G.nks == 1) {
                 bulk_g2s(dst, src, bytes, fb, pol);
               } else {
-                for (int r = 0; r < nr; ++r)
-                  bulk_g2s(dst + (size_t)r * G.KS * 2, src + (int64_t)r * G.K, (uint32_t)G.KS * 2u, fb, pol);
+                for (int rr = 0; rr < nr; ++rr)
+                  bulk_g2s(dst + (size_t)rr * G.KS * 2, src + (int64_t)rr * G.K, (uint32_t)G.KS * 2u, fb, pol);
               }
             }
       }
     } else if (d.op_id == MK_OP_ATTENTION_PARTIAL) {
       PartGeom q;
-      part_geom(p, d, q);
-      const uint16_t* Kc = static_cast<const uint16_t*>(p.bufs[d.in_buf[1]]);
-      const uint16_t* Vc = static_cast<const uint16_t*>(p.bufs[d.in_buf[2]]);
+      part_geom(state, d, q);
+      const uint16_t* Kc = reinterpret_cast<const uint16_t*>(r->ptr[kPIn1]);
+      const uint16_t* Vc = reinterpret_cast<const uint16_t*>(r->ptr[kPIn2]);
       const int64_t rowbase = ((int64_t)q.s * q.Hkv + q.g) * q.cap;
       if (!q.bad && (p.rope_half * 4) % 16 == 0) {  // the RoPE rows of pos
         prefetch_l2(p.rope_cos + (size_t)q.pos * p.rope_half, (uint32_t)p.rope_half * 4u);
@@ -345,12 +357,75 @@ __device__ void producer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
         bulk_g2s(dst + kStageBytes / 2, Vc + (rowbase + j) * q.D, bytes, fb, pol);
       }
     }
+    mbar_arrive(&rempty[e]);  // done with the record (the consumers arrive too)
   }
   // Let every copy still in flight land before the CTA can exit.
   const uint32_t inflight = issued < (uint32_t)nst ? issued : (uint32_t)nst;
   for (uint32_t k = 0; k < inflight; ++k) {
     const uint32_t st = issued - 1 - k;
     bar_wait(p, &full[st % nst], (st / nst) & 1u, -1, false);
+  }
+}
+
+// The record warp: per task, lanes 0-15 copy the descriptor, lanes 0-7
+// resolve its pointers, lanes 8-11 read its plan ranges and lane 12 its
+// tensor-map rows; then the first plan entries.  Runs at most kRecs tasks
+// ahead of the producer and the consumers, which both release a record.
+__device__ void record_warp(const KParams& p, TaskRec* recs, uint64_t* rfull, uint64_t* rempty) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t all = 0xffffffffu;
+  Seq sq;
+  seq_init(sq, p);
+  int task = 0, lvl = 0;
+  for (uint32_t k = 0;; ++k) {
+    const uint32_t e = k & (kRecs - 1);
+    TaskRec* r = recs + e;
+    if (k >= (uint32_t)kRecs) {  // the consumers are done with this entry's previous task
+      int ok = 1;
+      if (lane == 0) ok = bar_wait(p, &rempty[e], ((k / kRecs) - 1) & 1u, -1, true) ? 1 : 0;
+      if (!__shfl_sync(all, ok, 0)) return;
+    }
+    if (!seq_next(sq, p, task, lvl)) {
+      if (lane == 0) {
+        r->task = -1;
+        mbar_arrive(&rfull[e]);
+      }
+      return;
+    }
+    if (lane < 16) reinterpret_cast<uint32_t*>(&r->d)[lane] = __ldg(reinterpret_cast<const uint32_t*>(p.tasks + task) + lane);
+    __syncwarp();
+    const bool mega = p.mode == MK_MODE_MEGA;
+    const mk_task_descriptor& d = r->d;
+    if (lane < 8) {
+      const bool argmax = d.op_id == MK_OP_GEMV && (d.flags & MK_F_ARGMAX_EPI);
+      const uint32_t idx = lane < 3 ? d.in_buf[lane] : lane == 3 ? d.out_buf : lane == 4 ? d.in_buf[0]
+                         : lane == 5 ? d.in_buf[2] : lane == 6 ? d.out_buf : argmax ? d.reserved[3] : (uint32_t)MK_NO_BUF;
+      uint64_t v = 0;
+      if (idx < (uint32_t)p.num_bufs) {
+        if (lane < 4 || lane == 7) v = reinterpret_cast<uint64_t>(p.bufs[idx]);
+        else if (mega) v = reinterpret_cast<uint64_t>(p.mirrors[idx]);
+      }
+      r->ptr[lane] = v;
+    } else if (lane < 12) {
+      const uint32_t ov = mega ? __ldg((lane < 10 ? p.wait_off : p.sig_off) + task + (lane & 1)) : 0u;
+      (&r->w0)[lane - 8] = ov;  // w0, nw, s0, ns hold the four offsets for now
+    } else if (lane == 12) {
+      const uint32_t in1 = d.in_buf[1];
+      r->tm_rows = (d.op_id == MK_OP_GEMV && d.config_id == 1 && in1 < (uint32_t)p.num_bufs) ? p.tm_rows[in1] : 0;
+    }
+    __syncwarp();
+    const uint32_t wb = r->w0, we = r->nw, sb = r->s0, se = r->ns;
+    __syncwarp();
+    if (lane == 0) {
+      r->task = task;
+      r->lvl = lvl;
+      r->nw = we - wb;
+      r->ns = se - sb;
+    }
+    if (lane < 4 && (uint32_t)lane < we - wb) r->wi[lane] = __ldg(p.wait + wb + lane);
+    if (lane >= 4 && lane < 8 && (uint32_t)(lane - 4) < se - sb) r->si[lane - 4] = __ldg(p.sig + sb + lane - 4);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&rfull[e]);  // release: publishes every lane's writes (ordered by the syncwarp)
   }
 }
 
@@ -370,7 +445,14 @@ struct Ctx {
   TcCtl* ctl;
   uint32_t taddr;       // tensor-memory accumulator base
   uint32_t tc_ph;       // completed phases seen: mma_bar[0] (bit 0), mma_bar[1] (bit 1), acc_full (bit 2)
+  const TaskRec* rec;   // the current task's record
+  int32_t* state;       // the decode state (token, position) per sequence
 };
+
+template <class T>
+__device__ __forceinline__ T* rec_ptr(const Ctx& c, int i) {
+  return reinterpret_cast<T*>(c.rec->ptr[i]);
+}
 
 __device__ __forceinline__ void trace_mark(Ctx& c, int i) {
   if (c.p->trace && threadIdx.x == 0) c.mark[i] = globaltimer();
@@ -640,9 +722,8 @@ __device__ __forceinline__ void gemv_stages(Ctx& c, const mk_task_descriptor& d,
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int wcol = warp % G.WCOL, wrow = warp / G.WCOL;
   const int colw = G.KS / G.WCOL;
-  const float* x = static_cast<const float*>(p.bufs[d.in_buf[0]]);
-  const uint16_t* gamma =
-      (d.flags & MK_F_RMS_NORM_INPUT) ? static_cast<const uint16_t*>(p.bufs[d.in_buf[2]]) : nullptr;
+  const float* x = rec_ptr<const float>(c, kPIn0);
+  const uint16_t* gamma = (d.flags & MK_F_RMS_NORM_INPUT) ? rec_ptr<const uint16_t>(c, kPIn2) : nullptr;
   float* slots = gemv_slots(c);
   float xr[B][NV][8], ss[B];
   gemv_load_x<B, NV>(p, c.task, xr, ss, x, xm, gamma, G.K, ks * G.KS + wcol * colw + lane * 8, G.B);
@@ -735,12 +816,11 @@ __device__ __forceinline__ void gemv_fold(const mk_task_descriptor& d, const Gem
 // store, and the tile's running argmax.
 __device__ __forceinline__ void gemv_epilogue(const KParams& p, const mk_task_descriptor& d, const GemvGeom& G,
                                            int g0, int rows_g, const float* acc, float* red,
-                                           const float* staged_res, const uint64_t* rm, uint64_t* om, int task) {
+                                           const float* staged_res, float* out, const float* res,
+                                           const uint64_t* rm, uint64_t* om, int task) {
   const int tid = threadIdx.x;
-  float* out = static_cast<float*>(p.bufs[d.out_buf]);
   const bool silu = d.flags & MK_F_SILU_MUL;
   const bool argmax = d.flags & MK_F_ARGMAX_EPI;
-  const float* res = (d.flags & MK_F_ADD_RESIDUAL) ? static_cast<const float*>(p.bufs[d.in_buf[2]]) : nullptr;
   const int BT = G.BT;
   for (int b = 0; b < G.B; ++b) {
     const float inv = red[64 + b];
@@ -793,19 +873,20 @@ __device__ void gemv_task(Ctx& c, const mk_task_descriptor& d) {
   const KParams& p = *c.p;
   const uint64_t *xm = nullptr, *rm = nullptr;
   uint64_t* om = nullptr;
-  if (BCLASS < 2 && p.mode == MK_MODE_MEGA) {
-    om = p.mirrors[d.out_buf];
-    xm = p.mirrors[d.in_buf[0]];
+  if (BCLASS < 2) {  // the record holds mirrors in MEGA mode only
+    om = rec_ptr<uint64_t>(c, kMirOut);
+    xm = rec_ptr<const uint64_t>(c, kMirX);
     if (d.flags & MK_F_ADD_RESIDUAL) {
-      rm = p.mirrors[d.in_buf[2]];
+      rm = rec_ptr<const uint64_t>(c, kMirAux);
       if (!rm) xm = nullptr;
     }
     if (!xm) rm = nullptr;
   }
+  float* out = rec_ptr<float>(c, kPOut);
+  const float* res = (d.flags & MK_F_ADD_RESIDUAL) ? rec_ptr<const float>(c, kPIn2) : nullptr;
   const bool stage_res = (d.flags & MK_F_ADD_RESIDUAL) && G.cn <= kConsumerThreads && G.RG >= G.cn;
   float rv[8];
   if (stage_res && threadIdx.x < G.cn) {
-    const float* res = static_cast<const float*>(p.bufs[d.in_buf[2]]);
     if (rm) {
       uint64_t q[8];
 #pragma unroll
@@ -848,11 +929,11 @@ __device__ void gemv_task(Ctx& c, const mk_task_descriptor& d) {
           if (b < G.B) staged[threadIdx.x * G.BT + b] = rv[b];
       }
     }
-    gemv_epilogue(p, d, G, g0, rows_g, gemv_acc(c), red, staged, rm, om, c.task);
+    gemv_epilogue(p, d, G, g0, rows_g, gemv_acc(c), red, staged, out, res, rm, om, c.task);
     trace_mark(c, 2);
   }
   if ((d.flags & MK_F_ARGMAX_EPI) && threadIdx.x < G.B) {
-    mk_argmax_pair* pairs = static_cast<mk_argmax_pair*>(p.bufs[d.reserved[3]]);
+    mk_argmax_pair* pairs = rec_ptr<mk_argmax_pair>(c, kPPairs);
     mk_argmax_pair pr;
     pr.value = red[96 + threadIdx.x];
     pr.index = reinterpret_cast<int*>(red)[104 + threadIdx.x];
@@ -898,13 +979,12 @@ __device__ void tc_gemv_task(Ctx& c, const mk_task_descriptor& d) {
   GemvGeom G;
   gemv_geom(d, G);
   TcGeom T;
-  tc_geom(p, d, T);
+  tc_geom(c.rec->tm_rows, d, T);
   float* red = gemv_red(c);
   float* acc = c.scratch;  // [seg * rows][8] results (the GEMV slot area is unused here)
   gemv_prologue(d, G, red);
-  const float* x = static_cast<const float*>(p.bufs[d.in_buf[0]]);
-  const uint16_t* gamma =
-      (d.flags & MK_F_RMS_NORM_INPUT) ? static_cast<const uint16_t*>(p.bufs[d.in_buf[2]]) : nullptr;
+  const float* x = rec_ptr<const float>(c, kPIn0);
+  const uint16_t* gamma = (d.flags & MK_F_RMS_NORM_INPUT) ? rec_ptr<const uint16_t>(c, kPIn2) : nullptr;
   const int kpt = 2 * T.nkb;  // columns of x per lane and K range
   const uint32_t xb0 = smem_addr(c.xbuf);
   if (tid == 0) {  // the mbarrier arrive publishes the mailbox (release)
@@ -1000,12 +1080,13 @@ __device__ void tc_gemv_task(Ctx& c, const mk_task_descriptor& d) {
     }
     cbar();
     if (tid == 0) mbar_arrive(&ctl->acc_empty);  // tensor memory is free for the next row group
-    gemv_epilogue(p, d, G, g0, rows_g, acc, red, nullptr, nullptr, nullptr, c.task);
+    gemv_epilogue(p, d, G, g0, rows_g, acc, red, nullptr, rec_ptr<float>(c, kPOut),
+                  (d.flags & MK_F_ADD_RESIDUAL) ? rec_ptr<const float>(c, kPIn2) : nullptr, nullptr, nullptr, c.task);
   }
   for (int g0 = 0; g0 < G.cn; g0 += T.RG)
     for (int i = 0; i < T.nkr * T.seg; ++i) c.rp.advance(c.nst);
   if ((d.flags & MK_F_ARGMAX_EPI) && threadIdx.x < G.B) {
-    mk_argmax_pair* pairs = static_cast<mk_argmax_pair*>(p.bufs[d.reserved[3]]);
+    mk_argmax_pair* pairs = rec_ptr<mk_argmax_pair>(c, kPPairs);
     mk_argmax_pair pr;
     pr.value = red[96 + threadIdx.x];
     pr.index = reinterpret_cast<int*>(red)[104 + threadIdx.x];
@@ -1107,15 +1188,14 @@ __device__ void append_task(Ctx& c, const mk_task_descriptor& d) {
   const KParams& p = *c.p;
   const int s = d.reserved[0], g = d.reserved[1], Hkv = d.reserved[2];
   const int D = d.n, Hq = d.k, cap = d.kv_len, half = D / 2;
-  int32_t* state = static_cast<int32_t*>(p.bufs[MK_BUF_STATE]);
-  const int pos = ld_relaxed(state + 2 * s + 1);
+  const int pos = ld_relaxed(c.state + 2 * s + 1);
   if (pos < 0 || pos >= cap) {
     if (threadIdx.x == 0) raise_error(p, MK_DEV_CAPACITY, c.task);
     return;
   }
-  const float* qkv = static_cast<const float*>(p.bufs[d.in_buf[0]]) + (size_t)s * (Hq + 2 * Hkv) * D;
-  __nv_bfloat16* Kc = static_cast<__nv_bfloat16*>(p.bufs[d.in_buf[1]]);
-  __nv_bfloat16* Vc = static_cast<__nv_bfloat16*>(p.bufs[d.in_buf[2]]);
+  const float* qkv = rec_ptr<const float>(c, kPIn0) + (size_t)s * (Hq + 2 * Hkv) * D;
+  __nv_bfloat16* Kc = rec_ptr<__nv_bfloat16>(c, kPIn1);
+  __nv_bfloat16* Vc = rec_ptr<__nv_bfloat16>(c, kPIn2);
   const size_t row = (((size_t)s * Hkv + g) * cap + pos) * D;
   const int t = threadIdx.x;
   if (t < half) {
@@ -1206,7 +1286,7 @@ __device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom
   const int G = q.G, half = D / 2;
   float* qs = c.scratch;                    // [G][D]
   float* mrg = c.scratch + MAXG * D;        // [8 warps][G][D + 2]
-  const float* qkv = static_cast<const float*>(p.bufs[d.in_buf[0]]) + (size_t)q.s * (q.Hq + 2 * q.Hkv) * D;
+  const float* qkv = rec_ptr<const float>(c, kPIn0) + (size_t)q.s * (q.Hq + 2 * q.Hkv) * D;
   const float scale = 1.4426950408889634f / sqrtf((float)D);
   // RoPE on the group's query heads at position pos
   for (int i = tid; i < G * half; i += kConsumerThreads) {
@@ -1299,7 +1379,7 @@ __device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom
     }
   }
   cbar();
-  float* scr = static_cast<float*>(p.bufs[d.out_buf]) + (size_t)q.slot * G * (D + 2);
+  float* scr = rec_ptr<float>(c, kPOut) + (size_t)q.slot * G * (D + 2);
   for (int i = tid; i < G * D; i += kConsumerThreads) {
     const int h = i / D, e = i % D;
     float M = -INFINITY;
@@ -1323,7 +1403,7 @@ __device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom
 
 __device__ void partial_task(Ctx& c, const mk_task_descriptor& d) {
   PartGeom q;
-  part_geom(*c.p, d, q);
+  part_geom(c.state, d, q);
   if (q.bad) {
     if (threadIdx.x == 0) raise_error(*c.p, MK_DEV_CAPACITY, c.task);
     return;
@@ -1354,9 +1434,9 @@ __device__ void combine_task(Ctx& c, const mk_task_descriptor& d) {
   const int P = d.reserved[3], base = d.reserved[4];
   const int D = d.n, Hq = d.k, G = Hq / Hkv;
   const int rec = G * (D + 2);
-  const float* scr = static_cast<const float*>(p.bufs[d.in_buf[0]]) + (size_t)base * rec;
-  float* out = static_cast<float*>(p.bufs[d.out_buf]);
-  uint64_t* om = p.mode == MK_MODE_MEGA ? p.mirrors[d.out_buf] : nullptr;
+  const float* scr = rec_ptr<const float>(c, kPIn0) + (size_t)base * rec;
+  float* out = rec_ptr<float>(c, kPOut);
+  uint64_t* om = rec_ptr<uint64_t>(c, kMirOut);
   // each thread produces two adjacent outputs (e, e + 1) of one head
   for (int i = threadIdx.x; i < G * D / 2; i += kConsumerThreads) {
     const int h = (2 * i) / D, e = (2 * i) % D;
@@ -1393,15 +1473,14 @@ __device__ void combine_task(Ctx& c, const mk_task_descriptor& d) {
 __device__ void embed_task(Ctx& c, const mk_task_descriptor& d) {
   const KParams& p = *c.p;
   const int s = d.reserved[0], V = d.reserved[1], H = d.n;
-  const int32_t* state = static_cast<const int32_t*>(p.bufs[MK_BUF_STATE]);
-  const int tok = ld_relaxed(state + 2 * s);
+  const int tok = ld_relaxed(c.state + 2 * s);
   if (tok < 0 || tok >= V) {
     if (threadIdx.x == 0) raise_error(p, MK_DEV_BAD_INDEX, c.task);
     return;
   }
-  const uint16_t* E = static_cast<const uint16_t*>(p.bufs[d.in_buf[0]]) + (size_t)tok * H;
-  float* out = static_cast<float*>(p.bufs[d.out_buf]) + (size_t)s * H;
-  uint64_t* om = p.mode == MK_MODE_MEGA ? p.mirrors[d.out_buf] : nullptr;
+  const uint16_t* E = rec_ptr<const uint16_t>(c, kPIn0) + (size_t)tok * H;
+  float* out = rec_ptr<float>(c, kPOut) + (size_t)s * H;
+  uint64_t* om = rec_ptr<uint64_t>(c, kMirOut);
   for (int i = threadIdx.x * 8; i < H; i += kConsumerThreads * 8) {
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(E + i));
     float4 a = make_float4(bf_lo(v.x), bf_hi(v.x), bf_lo(v.y), bf_hi(v.y));
@@ -1426,12 +1505,11 @@ __device__ void embed_task(Ctx& c, const mk_task_descriptor& d) {
 __device__ void rmsnorm_task(Ctx& c, const mk_task_descriptor& d) {
   const KParams& p = *c.p;
   const int s = (int)d.reserved[0], H = d.n, tid = threadIdx.x;
-  const float* x = static_cast<const float*>(p.bufs[d.in_buf[0]]) + (size_t)s * H;
-  const uint16_t* gamma = static_cast<const uint16_t*>(p.bufs[d.in_buf[1]]);
-  const float* res =
-      (d.flags & MK_F_ADD_RESIDUAL) ? static_cast<const float*>(p.bufs[d.in_buf[2]]) + (size_t)s * H : nullptr;
-  float* out = static_cast<float*>(p.bufs[d.out_buf]) + (size_t)s * H;
-  uint64_t* om = p.mode == MK_MODE_MEGA ? p.mirrors[d.out_buf] : nullptr;
+  const float* x = rec_ptr<const float>(c, kPIn0) + (size_t)s * H;
+  const uint16_t* gamma = rec_ptr<const uint16_t>(c, kPIn1);
+  const float* res = (d.flags & MK_F_ADD_RESIDUAL) ? rec_ptr<const float>(c, kPIn2) + (size_t)s * H : nullptr;
+  float* out = rec_ptr<float>(c, kPOut) + (size_t)s * H;
+  uint64_t* om = rec_ptr<uint64_t>(c, kMirOut);
   float* red = c.scratch;
   float ss = 0.f;
 #pragma unroll 1
@@ -1461,7 +1539,7 @@ __device__ void rmsnorm_task(Ctx& c, const mk_task_descriptor& d) {
 __device__ void sample_task(Ctx& c, const mk_task_descriptor& d) {
   const KParams& p = *c.p;
   const int s = d.reserved[0], B = d.m, T = d.k, cap = d.kv_len;
-  const mk_argmax_pair* pairs = static_cast<const mk_argmax_pair*>(p.bufs[d.in_buf[0]]);
+  const mk_argmax_pair* pairs = rec_ptr<const mk_argmax_pair>(c, kPIn0);
   float bv = -FLT_MAX;
   int bi = INT_MAX;
   for (int t = threadIdx.x; t < T; t += kConsumerThreads) {
@@ -1474,8 +1552,8 @@ __device__ void sample_task(Ctx& c, const mk_task_descriptor& d) {
   }
   block_argmax(bv, bi, c.scratch);
   if (threadIdx.x == 0) {
-    int32_t* state = static_cast<int32_t*>(p.bufs[MK_BUF_STATE]);
-    int32_t* hist = static_cast<int32_t*>(p.bufs[d.out_buf]);
+    int32_t* state = c.state;
+    int32_t* hist = rec_ptr<int32_t>(c, kPOut);
     const int pos = ld_relaxed(state + 2 * s + 1);
     if (pos < 0 || pos + 1 >= cap) {
       raise_error(p, MK_DEV_CAPACITY, c.task);
@@ -1490,17 +1568,19 @@ __device__ void sample_task(Ctx& c, const mk_task_descriptor& d) {
 // ------------------------------------------------------------------ consumer loop
 // Wait (consumer warp 0) until every counter the task's plan names reaches
 // epoch * count.  Lane i polls entry i with acquire loads; entries are
-// usually one (a whole-group counter or the task's own) or two.
-__device__ bool wait_deps(const KParams& p, int task) {
-  if (aborted(p)) return false;
+// usually none (tagged inputs), one (a whole-group counter or the task's
+// own) or two, taken from the task record.  An abort is noticed while
+// waiting; a task whose counters are already met just runs.
+__device__ bool wait_deps(const KParams& p, const TaskRec* r, int task) {
   const int lane = threadIdx.x & 31;
-  const uint32_t w0 = __ldg(p.wait_off + task), nw = __ldg(p.wait_off + task + 1) - w0;
+  const uint32_t w0 = r->w0, nw = r->nw;
   for (uint32_t base = 0; base < nw; base += 32) {
-    const bool mine = base + lane < nw;
+    const uint32_t i = base + lane;
+    const bool mine = i < nw;
     const uint32_t* ctr = p.counters;
     uint32_t target = 0;
     if (mine) {
-      const uint2 e = __ldg(p.wait + w0 + base + lane);
+      const uint2 e = i < 4 ? r->wi[i] : __ldg(p.wait + w0 + i);
       ctr = p.counters + e.x;
       target = p.epoch * e.y;
     }
@@ -1543,47 +1623,63 @@ __device__ bool level_barrier(const KParams& p, int k) {
 
 template <int BCLASS>
 __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64_t* empty, float* scratch,
-                         volatile int* sflag, uint8_t* xbuf, TcCtl* ctl, uint32_t taddr) {
-  Ctx c{&p, ring, full, empty, scratch, RingPos{}, p.nstages, -1, {0, 0, 0}, 0u, xbuf, ctl, taddr, 0u};
-  Seq sq;
-  seq_init(sq, p);
-  int task, lvl, cur_lvl = 0;
+                         volatile int* sflag, uint8_t* xbuf, TcCtl* ctl, uint32_t taddr, const TaskRec* recs,
+                         uint64_t* rfull, uint64_t* rempty) {
+  Ctx c{&p, ring, full, empty, scratch, RingPos{}, p.nstages, -1, {0, 0, 0}, 0u, xbuf, ctl, taddr, 0u,
+        nullptr, static_cast<int32_t*>(p.bufs[MK_BUF_STATE])};
+  int cur_lvl = 0;
   const int tid = threadIdx.x;
-  while (seq_next(sq, p, task, lvl)) {
-    c.task = task;
+  for (uint32_t k = 0;; ++k) {
+    const uint32_t e = k & (kRecs - 1);
+    const TaskRec* r = recs + e;
     c.mark[0] = c.mark[1] = c.mark[2] = 0;
     c.ring_waits = 0;
-    const mk_task_descriptor d = load_desc(p.tasks + task);
     uint64_t t_wait = 0, t_start = 0;
-    if (tid < 32) {  // warp 0 waits (MEGA: all lanes; other modes: thread 0)
-      bool ok = true;
-      if (p.trace) t_wait = globaltimer();
-      if (p.mode == MK_MODE_MEGA) {
-        ok = wait_deps(p, task);
-      } else if (tid == 0 && p.mode == MK_MODE_LEVELS) {
-        while (ok && cur_lvl < lvl) ok = level_barrier(p, ++cur_lvl);
-        ok = ok && !aborted(p);
-      } else if (p.mode == MK_MODE_PER_OP_PDL) {
-        // the previous op's kernel has completed and its writes are
-        // visible; only then may the next kernel launch (so its producer,
-        // which starts before its own wait, never runs ahead of two ops)
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-        if (tid == 0) {
-          asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (tid < 32) {  // warp 0 takes the record, then waits (MEGA: all lanes; other modes: thread 0)
+      int run = 1;   // 1: run the task, 0: stop (abort or timeout), 2: no more tasks
+      if (tid == 0 && !bar_wait(p, &rfull[e], (k / kRecs) & 1u, -1, true)) run = 0;
+      __syncwarp();  // orders lane 0's acquire of the record before the other lanes' reads
+      run = __shfl_sync(0xffffffffu, run, 0);
+      if (run && r->task < 0) run = 2;
+      if (run == 1) {
+        const int task = r->task;
+        bool ok = true;
+        if (p.trace) t_wait = globaltimer();
+        if (p.mode == MK_MODE_MEGA) {
+          ok = wait_deps(p, r, task);
+        } else if (tid == 0 && p.mode == MK_MODE_LEVELS) {
+          const int lvl = r->lvl;
+          while (ok && cur_lvl < lvl) ok = level_barrier(p, ++cur_lvl);
+          ok = ok && !aborted(p);
+        } else if (p.mode == MK_MODE_PER_OP_PDL) {
+          // the previous op's kernel has completed and its writes are
+          // visible; only then may the next kernel launch (so its producer,
+          // which starts before its own wait, never runs ahead of two ops)
+          asm volatile("griddepcontrol.wait;" ::: "memory");
+          if (tid == 0) {
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+            ok = !aborted(p);
+          }
+        } else if (tid == 0) {
           ok = !aborted(p);
         }
-      } else if (tid == 0) {
-        ok = !aborted(p);
+        if (p.trace) t_start = globaltimer();
+        if (!ok) run = 0;
       }
-      if (p.trace) t_start = globaltimer();
-      if (tid == 0) *sflag = ok ? 1 : 0;
+      if (tid == 0) *sflag = run;
     }
     cbar();
-    if (!*sflag) return;
+    const int run = *sflag;
+    if (run == 0) return;
+    if (run == 2) break;
+    const mk_task_descriptor d = r->d;
+    const int task = r->task;
+    c.task = task;
+    c.rec = r;
     switch (d.op_id) {
       case MK_OP_GEMV:
         if constexpr (BCLASS == 2) {
-          if (d.config_id == 1 && p.tm_rows[d.in_buf[1]] > 0) {
+          if (d.config_id == 1 && r->tm_rows > 0) {
             tc_gemv_task(c, d);
             break;
           }
@@ -1605,23 +1701,27 @@ __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
     if (p.trace && tid == 0) {
       // end stamp taken before the dependents are released, so a child's
       // start stamp is never earlier than its parents' end stamps
-      uint64_t* r = p.trace + (size_t)task * 8;
-      r[0] = ((uint64_t)blockIdx.x << 32) | smid();
-      r[1] = t_wait;
-      r[2] = t_start;
-      r[3] = globaltimer();
-      r[4] = c.mark[0];
-      r[5] = c.mark[1];
-      r[6] = c.mark[2];
-      r[7] = c.ring_waits;
+      uint64_t* tr = p.trace + (size_t)task * 8;
+      tr[0] = ((uint64_t)blockIdx.x << 32) | smid();
+      tr[1] = t_wait;
+      tr[2] = t_start;
+      tr[3] = globaltimer();
+      tr[4] = c.mark[0];
+      tr[5] = c.mark[1];
+      tr[6] = c.mark[2];
+      tr[7] = c.ring_waits;
     }
-    if (p.mode == MK_MODE_MEGA && tid < 32) {
-      // release: one gpu-scope fence per signalling lane (covering, through
-      // the barrier above, every consumer thread's output writes), then
-      // relaxed adds that the dependents' acquire loads synchronise with
-      const uint32_t s0 = __ldg(p.sig_off + task), ns = __ldg(p.sig_off + task + 1) - s0;
-      if ((uint32_t)tid < ns) fence_acq_rel_gpu();
-      for (uint32_t i = tid; i < ns; i += 32) red_relaxed_add(p.counters + __ldg(p.sig + s0 + i), 1u);
+    if (tid < 32) {
+      if (p.mode == MK_MODE_MEGA) {
+        // release: one gpu-scope fence per signalling lane (covering, through
+        // the barrier above, every consumer thread's output writes), then
+        // relaxed adds that the dependents' acquire loads synchronise with
+        const uint32_t s0 = r->s0, ns = r->ns;
+        if ((uint32_t)tid < ns) fence_acq_rel_gpu();
+        for (uint32_t i = tid; i < ns; i += 32) red_relaxed_add(p.counters + (i < 4 ? r->si[i] : __ldg(p.sig + s0 + i)), 1u);
+      }
+      __syncwarp();
+      if (tid == 0) mbar_arrive(&rempty[e]);  // the record may be reused
     }
   }
   // LEVELS: arrive at the barriers of the remaining levels so no CTA waits on us
@@ -1631,9 +1731,11 @@ __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
 }
 
 // Shared memory: [activation staging (B >= 8 kernel)] [ring] [full, empty
-// mbarriers] [control block] [scratch].
+// mbarriers] [control block] [task records] [record full, empty mbarriers]
+// [scratch].
 int smem_bytes_for(int nstages, int batch) {
-  return (batch > 4 ? kXbufBytes : 0) + nstages * kStageBytes + 2 * nstages * 8 + kCtlBytes + kScratchBytes;
+  return (batch > 4 ? kXbufBytes : 0) + nstages * kStageBytes + 2 * nstages * 8 + kCtlBytes +
+         kRecs * (kRecBytes + 16) + kScratchBytes;
 }
 
 template <int BCLASS>
@@ -1652,7 +1754,10 @@ __global__ void __launch_bounds__(kThreads, 1) mk_interpreter_kernel(const __gri
   uint64_t* empty = full + nst;
   TcCtl* ctl = reinterpret_cast<TcCtl*>(empty + nst);
   volatile int* sflag = &ctl->run;
-  float* scratch = reinterpret_cast<float*>(ring + (size_t)nst * kStageBytes + 2 * nst * 8 + kCtlBytes);
+  TaskRec* recs = reinterpret_cast<TaskRec*>(reinterpret_cast<uint8_t*>(ctl) + kCtlBytes);
+  uint64_t* rfull = reinterpret_cast<uint64_t*>(recs + kRecs);
+  uint64_t* rempty = rfull + kRecs;
+  float* scratch = reinterpret_cast<float*>(rempty + kRecs);
   // the swizzled operand layouts assume 1024-byte aligned tiles
   const bool aligned = (smem_addr(smem) & 1023u) == 0;
   if (threadIdx.x == 0) {
@@ -1667,6 +1772,10 @@ __global__ void __launch_bounds__(kThreads, 1) mk_interpreter_kernel(const __gri
     mbar_init(&ctl->acc_full, 1);
     mbar_init(&ctl->acc_empty, 1);
     mbar_init(&ctl->task_go, 1);
+    for (int i = 0; i < kRecs; ++i) {
+      mbar_init(&rfull[i], 1);
+      mbar_init(&rempty[i], 2);  // the producer and consumer thread 0
+    }
     fence_mbar_init();
     if (BCLASS == 2 && !aligned) raise_error(p, MK_DEV_BAD_OP, -1);
   }
@@ -1681,13 +1790,16 @@ __global__ void __launch_bounds__(kThreads, 1) mk_interpreter_kernel(const __gri
   if constexpr (BCLASS == 2) tc_fence_after();
   const uint32_t taddr = BCLASS == 2 ? ctl->tmem : 0u;
   if (threadIdx.x >= kConsumerThreads) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(BCLASS == 2 ? kProducerRegsTc : kProducerRegs));
-    if (threadIdx.x < kConsumerThreads + 32) producer(p, ring, full, empty);
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
+    if (threadIdx.x < kConsumerThreads + 32) producer(p, ring, full, empty, recs, rfull, rempty);
     else if (BCLASS == 2 && threadIdx.x < kConsumerThreads + 64)
       tc_mma_warp(p, ring, full, empty, ctl, smem_addr(xbuf), taddr);
+    else if (threadIdx.x >= kConsumerThreads + 64 && threadIdx.x < kConsumerThreads + 96)
+      record_warp(p, recs, rfull, rempty);
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(BCLASS == 2 ? kConsumerRegsTc : kConsumerRegs));
-    if (BCLASS != 2 || aligned) consumer<BCLASS>(p, ring, full, empty, scratch, sflag, xbuf, ctl, taddr);
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
+    if (BCLASS != 2 || aligned)
+      consumer<BCLASS>(p, ring, full, empty, scratch, sflag, xbuf, ctl, taddr, recs, rfull, rempty);
     if (BCLASS == 2) {
       // every tensor-core operation has completed (the consumers waited for
       // each row group's last commit): tell the MMA warp to stop, free the

@@ -103,6 +103,7 @@ KParams base_params(const mk_graph* g) {
   p.tm_rows = d->tm_rows;
   p.mirrors = d->mirrors;
   p.tag = d->tag;
+  p.num_bufs = (int32_t)g->bufs.size();
   p.queue_off = d->queue_off;
   p.queue = d->queue;
   p.level_off = d->level_off;
