@@ -540,7 +540,7 @@ __device__ __forceinline__ bool ll_ready(uint64_t v, uint32_t tag) { return (uin
 __device__ uint64_t ll_wait(const KParams& p, const uint64_t* m, int task) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1;; ++it) {
-    __nanosleep(32);
+    __nanosleep(64);
     const uint64_t v = ld_relaxed_u64(m);
     if (ll_ready(v, p.tag)) return v;
     if ((it & 15u) == 0) {
@@ -574,11 +574,14 @@ __device__ __forceinline__ uint32_t ll_piece(const uint64_t* m, uint32_t tag, fl
 }
 
 // x for this lane's pieces (b, v) of 8 columns from the mirror xm: all
-// pieces are loaded at once; while some hold stale pairs, wait for one
-// stale pair to turn, then reload the pieces still pending.
+// pieces are loaded at once; while some lane holds stale pairs, one lane
+// (the lowest with a stale pair) polls that pair until it turns and the
+// warp then reloads its pending pieces.  One poller per warp keeps the
+// polling traffic on the producers' lines low.  Warp-collective.
 template <int B, int NV>
 __device__ __forceinline__ void ll_load_x(const KParams& p, int task, float (&xr)[B][NV][8], const uint64_t* xm,
                                           int K, int col0, int Bact) {
+  const int lane = threadIdx.x & 31;
   uint32_t pend = 0;
   const uint64_t* probe = nullptr;
 #pragma unroll
@@ -598,8 +601,13 @@ __device__ __forceinline__ void ll_load_x(const KParams& p, int task, float (&xr
       }
     }
   }
-  while (pend) {
-    if (!ll_ready(ll_wait(p, probe, task), p.tag)) break;
+  for (;;) {
+    const uint32_t want = __ballot_sync(0xffffffffu, pend != 0);
+    if (!want) break;
+    const int leader = __ffs(want) - 1;
+    int ready = 1;
+    if (lane == leader) ready = ll_ready(ll_wait(p, probe, task), p.tag) ? 1 : 0;
+    if (!__shfl_sync(0xffffffffu, ready, leader)) break;  // abort or timeout: carry on with what is loaded
     probe = nullptr;
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
@@ -886,20 +894,33 @@ __device__ void gemv_task(Ctx& c, const mk_task_descriptor& d) {
   const float* res = (d.flags & MK_F_ADD_RESIDUAL) ? rec_ptr<const float>(c, kPIn2) : nullptr;
   const bool stage_res = (d.flags & MK_F_ADD_RESIDUAL) && G.cn <= kConsumerThreads && G.RG >= G.cn;
   float rv[8];
-  if (stage_res && threadIdx.x < G.cn) {
-    if (rm) {
-      uint64_t q[8];
+  if (stage_res && rm) {
+    // warp-collective: threads past the tile's columns load nothing
+    const bool mine = threadIdx.x < G.cn;
+    const uint64_t* rc = rm + G.c0 + threadIdx.x;
+    uint64_t q[8];
 #pragma unroll
-      for (int b = 0; b < 8; ++b) q[b] = b < G.B ? ld_relaxed_u64(rm + (size_t)b * G.n + G.c0 + threadIdx.x) : 0u;
+    for (int b = 0; b < 8; ++b) q[b] = mine && b < G.B ? ld_relaxed_u64(rc + (size_t)b * G.n) : ll_pack(0.f, p.tag);
+    for (;;) {
+      int first = -1;
 #pragma unroll
-      for (int b = 0; b < 8; ++b) {
-        if (b < G.B && !ll_ready(q[b], p.tag)) q[b] = ll_wait(p, rm + (size_t)b * G.n + G.c0 + threadIdx.x, c.task);
-        rv[b] = b < G.B ? __uint_as_float((uint32_t)q[b]) : 0.f;
-      }
-    } else {
+      for (int b = 7; b >= 0; --b)
+        if (!ll_ready(q[b], p.tag)) first = b;
+      const uint32_t want = __ballot_sync(0xffffffffu, first >= 0);
+      if (!want) break;
+      const int leader = __ffs(want) - 1;
+      int ready = 1;
+      if ((int)(threadIdx.x & 31) == leader) ready = ll_ready(ll_wait(p, rc + (size_t)first * G.n, c.task), p.tag);
+      if (!__shfl_sync(0xffffffffu, ready, leader)) break;
 #pragma unroll
-      for (int b = 0; b < 8; ++b) rv[b] = b < G.B ? __ldcg(res + (size_t)b * G.n + G.c0 + threadIdx.x) : 0.f;
+      for (int b = 0; b < 8; ++b)
+        if (!ll_ready(q[b], p.tag)) q[b] = ld_relaxed_u64(rc + (size_t)b * G.n);
     }
+#pragma unroll
+    for (int b = 0; b < 8; ++b) rv[b] = __uint_as_float((uint32_t)q[b]);
+  } else if (stage_res && threadIdx.x < G.cn) {
+#pragma unroll
+    for (int b = 0; b < 8; ++b) rv[b] = b < G.B ? __ldcg(res + (size_t)b * G.n + G.c0 + threadIdx.x) : 0.f;
   }
   for (int g0 = 0; g0 < G.cn; g0 += G.RG) {
     const int rows_g = min(G.RG, G.cn - g0);
@@ -1211,64 +1232,77 @@ __device__ void append_task(Ctx& c, const mk_task_descriptor& d) {
 
 // Sum 32 per-lane values across the warp, transposed: afterwards lane l
 // holds the warp-wide sum of value l (31 shuffles instead of 32 x 5).
-__device__ __forceinline__ float transpose_reduce32(float (&v)[32], int lane) {
+// Eight keys of the online softmax (base 2) for the query heads of a KV
+// group.  Lane = 8 * head + slice: the lane holds dims [slice * DS, slice *
+// DS + DS) of its head's query (qr) and output (o); m and l are its head's
+// running max and sum (equal in the head's 8 lanes).  Keys k0 .. k0 + 7
+// (nvalid of them real) are read from shared memory (rows of DS * 8 bf16
+// at kb and vb): each lane reads its slice of every key, so the four heads'
+// lanes share each address.  A score needs a sum over the head's 8 lanes
+// only: a transposed reduction leaves key `slice`'s score in that lane.
+template <int DS>
+__device__ __forceinline__ void partial_group8(const float (&qr)[DS], float (&o)[DS], float& m, float& l,
+                                               uint32_t kb, uint32_t vb, int k0, int nvalid, bool hlive,
+                                               int lane) {
+  constexpr int D = DS * 8;
+  const int sl = lane & 7;
+  float v[8];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const bool up = (lane & o) != 0;
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t a = kb + (uint32_t)((k0 + (j < nvalid ? j : 0)) * D + sl * DS) * 2;
+    float sc = 0.f;
 #pragma unroll
-    for (int i = 0; i < o; ++i) {
-      const float send = up ? v[i] : v[i + o];
-      const float keep = up ? v[i + o] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    for (int c4 = 0; c4 < DS / 8; ++c4) {
+      const uint4 w = lds128(a + c4 * 16);
+      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        sc = fmaf(qr[c4 * 8 + 2 * t], bf_lo(u[t]), sc);
+        sc = fmaf(qr[c4 * 8 + 2 * t + 1], bf_hi(u[t]), sc);
+      }
+    }
+    v[j] = sc;
+  }
+  // transposed sum over the 8 lanes of the head: afterwards lane sl holds key sl's score
+#pragma unroll
+  for (int t = 0; t < 3; ++t) {
+    const int o2 = 4 >> t, n = 8 >> t;
+    const bool up = (lane & o2) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = up ? v[i] : v[i + n / 2];
+      const float keep = up ? v[i + n / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o2);
     }
   }
-  return v[0];
-}
-
-// Eight keys of the online softmax for the (up to 4) query heads of a KV
-// group, base 2.  kf/vf: this lane's DPL dims of each key and value; nvalid
-// keys are real.  m/l/o are kept identical in every lane of the warp.
-template <int DPL>
-__device__ __forceinline__ void partial_group(const float (&qr)[4][DPL], float (&o)[4][DPL], float (&m)[4],
-                                              float (&l)[4], const float (&kf)[8][DPL], const float (&vf)[8][DPL],
-                                              int nvalid, int G, int lane) {
-  float v[32];
-#pragma unroll
-  for (int h = 0; h < 4; ++h)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      float sc = 0.f;
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) sc = fmaf(qr[h][e], kf[j][e], sc);
-      v[h * 8 + j] = sc;
-    }
-  const int hl = lane >> 3, jl = lane & 7;  // this lane's (head, key) after the reduce
-  float val = transpose_reduce32(v, lane);
-  const bool live = jl < nvalid && hl < G;
-  float gmax = live ? val : -INFINITY;
+  const bool live = hlive && sl < nvalid;
+  float gmax = live ? v[0] : -INFINITY;
 #pragma unroll
   for (int off = 1; off < 8; off <<= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, off));
-  const float mold = hl == 0 ? m[0] : hl == 1 ? m[1] : hl == 2 ? m[2] : m[3];
-  const float mnew = fmaxf(mold, gmax);
-  const float pr = live ? exp2f(val - mnew) : 0.f;
+  const float mnew = fmaxf(m, gmax);
+  const float pr = live ? exp2f(v[0] - mnew) : 0.f;
   float psum = pr;
 #pragma unroll
   for (int off = 1; off < 8; off <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
+  const float sa = exp2f(m - mnew);  // 0 while m is -inf and mnew finite; exp2(nan) never: mnew >= m
+  l = fmaf(l, mnew == -INFINITY ? 1.f : sa, psum);
+  const float sc = mnew == -INFINITY ? 1.f : sa;
 #pragma unroll
-  for (int h = 0; h < 4; ++h) {
-    if (h < G) {
-      const float mh = __shfl_sync(0xffffffffu, mnew, h * 8);
-      const float ph = __shfl_sync(0xffffffffu, psum, h * 8);
-      const float a = exp2f(m[h] - mh);
-      l[h] = fmaf(l[h], a, ph);
-      m[h] = mh;
+  for (int e = 0; e < DS; ++e) o[e] *= sc;
+  m = mnew;
+  const int hb = lane & ~7;
 #pragma unroll
-      for (int e = 0; e < DPL; ++e) o[h][e] *= a;
+  for (int j = 0; j < 8; ++j) {
+    const float pj = __shfl_sync(0xffffffffu, pr, hb | j);
+    const uint32_t a = vb + (uint32_t)((k0 + (j < nvalid ? j : 0)) * D + sl * DS) * 2;
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float pj = __shfl_sync(0xffffffffu, pr, h * 8 + j);
+    for (int c4 = 0; c4 < DS / 8; ++c4) {
+      const uint4 w = lds128(a + c4 * 16);
+      const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int e = 0; e < DPL; ++e) o[h][e] = fmaf(pj, vf[j][e], o[h][e]);
+      for (int t = 0; t < 4; ++t) {
+        o[c4 * 8 + 2 * t] = fmaf(pj, bf_lo(u[t]), o[c4 * 8 + 2 * t]);
+        o[c4 * 8 + 2 * t + 1] = fmaf(pj, bf_hi(u[t]), o[c4 * 8 + 2 * t + 1]);
       }
     }
   }
@@ -1277,38 +1311,52 @@ __device__ __forceinline__ void partial_group(const float (&qr)[4][DPL], float (
 // Online softmax of G query heads over one KV chunk (log2 domain: scores
 // are scaled by log2(e)/sqrt(D) and exponentials taken base 2).  Writes
 // (m, l, o[D]) per head to the chunk's scratch slot.
-template <int DPL>  // dims per lane: D / 32
+template <int DS>  // dims per lane: D / 8
 __device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom& q) {
-  constexpr int D = DPL * 32;
+  constexpr int D = DS * 8;
   constexpr int MAXG = 4;
   const KParams& p = *c.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = q.G, half = D / 2;
-  float* qs = c.scratch;                    // [G][D]
-  float* mrg = c.scratch + MAXG * D;        // [8 warps][G][D + 2]
+  const int h = lane >> 3, sl = lane & 7;
+  const bool hlive = h < G;
+  float* qs = c.scratch;                              // [G][D]
+  float* mrg = c.scratch + MAXG * D;                  // [8 warps][G][D + 2]
+  uint16_t* nkv = reinterpret_cast<uint16_t*>(mrg + kConsumerWarps * MAXG * (D + 2));  // new key, value rows
   const float* qkv = rec_ptr<const float>(c, kPIn0) + (size_t)q.s * (q.Hq + 2 * q.Hkv) * D;
   const float scale = 1.4426950408889634f / sqrtf((float)D);
   // RoPE on the group's query heads at position pos
   for (int i = tid; i < G * half; i += kConsumerThreads) {
-    const int h = i / half, j = i % half;
-    const float* qh = qkv + (size_t)(q.g * G + h) * D;
+    const int hh = i / half, j = i % half;
+    const float* qh = qkv + (size_t)(q.g * G + hh) * D;
     const float a = __ldcg(qh + j), b = __ldcg(qh + j + half);
     const float cs = p.rope_cos[(size_t)q.pos * p.rope_half + j];
     const float sn = p.rope_sin[(size_t)q.pos * p.rope_half + j];
-    qs[h * D + j] = (a * cs - b * sn) * scale;
-    qs[h * D + j + half] = (b * cs + a * sn) * scale;
+    qs[hh * D + j] = (a * cs - b * sn) * scale;
+    qs[hh * D + j + half] = (b * cs + a * sn) * scale;
+  }
+  if (q.has_new && warp == kConsumerWarps - 1) {
+    // the key/value of the token at pos come straight from qkv, rotated and
+    // rounded to bf16 exactly as ATTENTION_APPEND stores them, so this task
+    // does not wait for the append
+    const float* kq = qkv + (size_t)q.Hq * D + (size_t)q.g * D;
+    const float* vq = qkv + (size_t)(q.Hq + q.Hkv) * D + (size_t)q.g * D;
+    for (int dd = lane; dd < D; dd += 32) {
+      const int jj = dd < half ? dd : dd - half;
+      const float cs = p.rope_cos[(size_t)q.pos * p.rope_half + jj];
+      const float sn = p.rope_sin[(size_t)q.pos * p.rope_half + jj];
+      const float k1 = __ldcg(kq + jj), k2 = __ldcg(kq + jj + half);
+      const float kr = dd < half ? k1 * cs - k2 * sn : k2 * cs + k1 * sn;
+      nkv[dd] = __bfloat16_as_ushort(__float2bfloat16_rn(kr));
+      nkv[D + dd] = __bfloat16_as_ushort(__float2bfloat16_rn(__ldcg(vq + dd)));
+    }
   }
   cbar();
-  float qr[MAXG][DPL], o[MAXG][DPL], m[MAXG], l[MAXG];
+  float qr[DS], o[DS], m = -INFINITY, l = 0.f;
 #pragma unroll
-  for (int h = 0; h < MAXG; ++h) {
-    m[h] = -INFINITY;
-    l[h] = 0.f;
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) {
-      qr[h][e] = h < G ? qs[h * D + lane * DPL + e] : 0.f;
-      o[h][e] = 0.f;
-    }
+  for (int e = 0; e < DS; ++e) {
+    qr[e] = hlive ? qs[h * D + sl * DS + e] : 0.f;
+    o[e] = 0.f;
   }
   const int kpw = q.R / kConsumerWarps;  // keys per warp per slot (a multiple of 8)
   for (int i = 0; i < q.nstage; ++i) {
@@ -1317,86 +1365,44 @@ __device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom
     if (i == 0) trace_mark(c, 0);
     const uint32_t kb = smem_addr(c.ring + (size_t)slot * kStageBytes);
     const uint32_t vb = kb + kStageBytes / 2;
-    for (int k0 = warp * kpw; k0 < min(nr, (warp + 1) * kpw); k0 += 8) {
-      const int nvalid = min(8, nr - k0);
-      float kf[8][DPL], vf[8][DPL];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t off = (uint32_t)((k0 + (j < nvalid ? j : 0)) * D + lane * DPL) * 2;
-        if constexpr (DPL == 4) {
-          const uint2 kv = lds64(kb + off), vv = lds64(vb + off);
-          kf[j][0] = bf_lo(kv.x); kf[j][1] = bf_hi(kv.x); kf[j][2] = bf_lo(kv.y); kf[j][3] = bf_hi(kv.y);
-          vf[j][0] = bf_lo(vv.x); vf[j][1] = bf_hi(vv.x); vf[j][2] = bf_lo(vv.y); vf[j][3] = bf_hi(vv.y);
-        } else {
-          const uint32_t kv = lds32(kb + off), vv = lds32(vb + off);
-          kf[j][0] = bf_lo(kv); kf[j][1] = bf_hi(kv);
-          vf[j][0] = bf_lo(vv); vf[j][1] = bf_hi(vv);
-        }
-      }
-      partial_group<DPL>(qr, o, m, l, kf, vf, nvalid, G, lane);
-    }
+    for (int k0 = warp * kpw; k0 < min(nr, (warp + 1) * kpw); k0 += 8)
+      partial_group8<DS>(qr, o, m, l, kb, vb, k0, min(8, nr - k0), hlive, lane);
     consume_end(c, slot);
   }
   if (q.has_new && warp == kConsumerWarps - 1) {
-    // the key/value of the token at pos come straight from qkv, rotated and
-    // rounded to bf16 exactly as ATTENTION_APPEND stores them, so this task
-    // does not wait for the append
-    const float* kq = qkv + (size_t)q.Hq * D + (size_t)q.g * D;
-    const float* vq = qkv + (size_t)(q.Hq + q.Hkv) * D + (size_t)q.g * D;
-    float kf[8][DPL], vf[8][DPL];
-#pragma unroll
-    for (int e = 0; e < DPL; ++e) {
-      const int dd = lane * DPL + e;
-      const int jj = dd < half ? dd : dd - half;
-      const float cs = p.rope_cos[(size_t)q.pos * p.rope_half + jj];
-      const float sn = p.rope_sin[(size_t)q.pos * p.rope_half + jj];
-      const float k1 = __ldcg(kq + jj), k2 = __ldcg(kq + jj + half);
-      const float kr = dd < half ? k1 * cs - k2 * sn : k2 * cs + k1 * sn;
-      kf[0][e] = __bfloat162float(__float2bfloat16_rn(kr));
-      vf[0][e] = __bfloat162float(__float2bfloat16_rn(__ldcg(vq + dd)));
-    }
-#pragma unroll
-    for (int j = 1; j < 8; ++j)
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) {
-        kf[j][e] = kf[0][e];
-        vf[j][e] = vf[0][e];
-      }
-    partial_group<DPL>(qr, o, m, l, kf, vf, 1, G, lane);
+    const uint32_t nb = smem_addr(nkv);
+    partial_group8<DS>(qr, o, m, l, nb, nb + D * 2, 0, 1, hlive, lane);
   }
   trace_mark(c, 1);
   // merge the 8 warps' states
-#pragma unroll
-  for (int h = 0; h < MAXG; ++h) {
-    if (h < G) {
-      float* r = mrg + (warp * MAXG + h) * (D + 2);
-      if (lane == 0) {
-        r[0] = m[h];
-        r[1] = l[h];
-      }
-#pragma unroll
-      for (int e = 0; e < DPL; ++e) r[2 + lane * DPL + e] = o[h][e];
+  if (hlive) {
+    float* r = mrg + (warp * MAXG + h) * (D + 2);
+    if (sl == 0) {
+      r[0] = m;
+      r[1] = l;
     }
+#pragma unroll
+    for (int e = 0; e < DS; ++e) r[2 + sl * DS + e] = o[e];
   }
   cbar();
   float* scr = rec_ptr<float>(c, kPOut) + (size_t)q.slot * G * (D + 2);
   for (int i = tid; i < G * D; i += kConsumerThreads) {
-    const int h = i / D, e = i % D;
+    const int hh = i / D, e = i % D;
     float M = -INFINITY;
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mrg[(w * MAXG + h) * (D + 2)]);
+    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mrg[(w * MAXG + hh) * (D + 2)]);
     float Ls = 0.f, O = 0.f;
     if (M != -INFINITY) {
       for (int w = 0; w < kConsumerWarps; ++w) {
-        const float* r = mrg + (w * MAXG + h) * (D + 2);
+        const float* r = mrg + (w * MAXG + hh) * (D + 2);
         const float f = exp2f(r[0] - M);
         Ls = fmaf(r[1], f, Ls);
         O = fmaf(r[2 + e], f, O);
       }
     }
-    scr[h * (D + 2) + 2 + e] = O;
+    scr[hh * (D + 2) + 2 + e] = O;
     if (e == 0) {
-      scr[h * (D + 2)] = M;
-      scr[h * (D + 2) + 1] = Ls;
+      scr[hh * (D + 2)] = M;
+      scr[hh * (D + 2) + 1] = Ls;
     }
   }
 }
@@ -1408,8 +1414,8 @@ __device__ void partial_task(Ctx& c, const mk_task_descriptor& d) {
     if (threadIdx.x == 0) raise_error(*c.p, MK_DEV_CAPACITY, c.task);
     return;
   }
-  if (q.D == 128) partial_body<4>(c, d, q);
-  else partial_body<2>(c, d, q);
+  if (q.D == 128) partial_body<16>(c, d, q);
+  else partial_body<8>(c, d, q);
 }
 
 // Log-sum-exp merge of the P partials of one (sequence, kv head), as a
