@@ -704,15 +704,17 @@ extern "C" int mk_lower(mk_graph* g) {
 }
 
 // Tagged hand-offs.  At B <= 4 the activations a GEMV reads (its x, and
-// its residual) are also written by their producers as (value, step tag)
-// pairs into a library-owned mirror.  Such a GEMV polls its inputs' tags
-// instead of waiting on counters: the data and the news that it is ready
+// its residual) and the qkv rows a split-KV partial reads are also written
+// by their producers as (value, step tag) pairs into a library-owned
+// mirror.  Such a reader polls its inputs' tags instead of waiting on
+// counters: the data and the news that it is ready
 // arrive in one round trip, where a counter costs the producer's fence,
 // the counter's round trip and then the data's.  A buffer qualifies when
 // it is f32, written exactly once per step (once[b]) and only by GEMV,
 // COMBINE, embedding MEMCPY or RMSNORM tasks (the bodies that write the
 // pairs); a GEMV qualifies when its x and residual do and every one of its
-// parents writes one of them (weights and gamma have no writers).
+// parents writes one of them (weights and gamma have no writers), a split-KV
+// partial when its qkv does and every parent writes qkv.
 void mk::build_ll_plan(mk_graph* g, const std::vector<std::vector<int>>& parents,
                        const std::vector<uint8_t>& once) {
   const size_t NB = g->bufs.size(), N = g->tasks.size();
@@ -725,6 +727,7 @@ void mk::build_ll_plan(mk_graph* g, const std::vector<std::vector<int>>& parents
       read_as_input[d.in_buf[0]] = 1;
       if (d.flags & MK_F_ADD_RESIDUAL) read_as_input[d.in_buf[2]] = 1;
     }
+    if (d.op_id == MK_OP_ATTENTION_PARTIAL) read_as_input[d.in_buf[0]] = 1;
     if (d.out_buf >= NB) continue;
     const bool ok = d.op_id == MK_OP_GEMV || d.op_id == MK_OP_ATTENTION_COMBINE || d.op_id == MK_OP_MEMCPY ||
                     d.op_id == MK_OP_RMSNORM;
@@ -734,6 +737,14 @@ void mk::build_ll_plan(mk_graph* g, const std::vector<std::vector<int>>& parents
     g->ll_buf[b] = read_as_input[b] && once[b] && !bad_writer[b] && g->bufs[b].dtype == MK_F32;
   for (size_t t = 0; t < N; ++t) {
     const mk_task_descriptor& d = g->tasks[t];
+    if (d.op_id == MK_OP_ATTENTION_PARTIAL) {
+      // its query and (last chunk) new key and value come from qkv; the cache
+      // rows it reads have no writer this step
+      bool ok = g->ll_buf[d.in_buf[0]];
+      for (int q : parents[t]) ok = ok && g->tasks[q].out_buf == d.in_buf[0];
+      g->ll_task[t] = ok;
+      continue;
+    }
     if (d.op_id != MK_OP_GEMV) continue;
     const bool res = d.flags & MK_F_ADD_RESIDUAL;
     bool ok = g->ll_buf[d.in_buf[0]] && (!res || g->ll_buf[d.in_buf[2]]);

@@ -559,6 +559,40 @@ __device__ __forceinline__ float ll_load1(const KParams& p, const uint64_t* m, i
   return __uint_as_float((uint32_t)v);
 }
 
+// Warp-collective: lane loads the pairs at m[i] where use[i]; while some
+// lane holds a stale pair, the lowest such lane polls it and every lane
+// then reloads its stale pairs.
+template <int N>
+__device__ __forceinline__ void ll_gather(const KParams& p, int task, const uint64_t* const (&m)[N],
+                                          const bool (&use)[N], float (&out)[N]) {
+  uint64_t q[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) q[i] = use[i] ? ld_relaxed_u64(m[i]) : ll_pack(0.f, p.tag);
+  for (;;) {
+    int first = -1;
+#pragma unroll
+    for (int i = N - 1; i >= 0; --i)
+      if (!ll_ready(q[i], p.tag)) first = i;
+    const uint32_t want = __ballot_sync(0xffffffffu, first >= 0);
+    if (!want) break;
+    const int leader = __ffs(want) - 1;
+    int ready = 1;
+    if ((int)(threadIdx.x & 31) == leader) {
+      const uint64_t* pm = m[0];
+#pragma unroll
+      for (int i = 1; i < N; ++i)
+        if (first == i) pm = m[i];
+      ready = ll_ready(ll_wait(p, pm, task), p.tag) ? 1 : 0;
+    }
+    if (!__shfl_sync(0xffffffffu, ready, leader)) break;
+#pragma unroll
+    for (int i = 0; i < N; ++i)
+      if (!ll_ready(q[i], p.tag)) q[i] = ld_relaxed_u64(m[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < N; ++i) out[i] = __uint_as_float((uint32_t)q[i]);
+}
+
 // Eight consecutive pairs into o; returns the mask of those already tagged.
 __device__ __forceinline__ uint32_t ll_piece(const uint64_t* m, uint32_t tag, float (&o)[8]) {
   const ulonglong2 a = ld_relaxed_v2u64(m), b = ld_relaxed_v2u64(m + 2), e = ld_relaxed_v2u64(m + 4),
@@ -1323,32 +1357,62 @@ __device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom
   float* qs = c.scratch;                              // [G][D]
   float* mrg = c.scratch + MAXG * D;                  // [8 warps][G][D + 2]
   uint16_t* nkv = reinterpret_cast<uint16_t*>(mrg + kConsumerWarps * MAXG * (D + 2));  // new key, value rows
-  const float* qkv = rec_ptr<const float>(c, kPIn0) + (size_t)q.s * (q.Hq + 2 * q.Hkv) * D;
+  const size_t row = (size_t)q.s * (q.Hq + 2 * q.Hkv) * D;
+  const float* qkv = rec_ptr<const float>(c, kPIn0) + row;
+  const uint64_t* qm = rec_ptr<const uint64_t>(c, kMirX);  // tagged qkv (MEGA, B <= 4), else null
+  if (qm) qm += row;
   const float scale = 1.4426950408889634f / sqrtf((float)D);
-  // RoPE on the group's query heads at position pos
-  for (int i = tid; i < G * half; i += kConsumerThreads) {
-    const int hh = i / half, j = i % half;
-    const float* qh = qkv + (size_t)(q.g * G + hh) * D;
-    const float a = __ldcg(qh + j), b = __ldcg(qh + j + half);
-    const float cs = p.rope_cos[(size_t)q.pos * p.rope_half + j];
-    const float sn = p.rope_sin[(size_t)q.pos * p.rope_half + j];
-    qs[hh * D + j] = (a * cs - b * sn) * scale;
-    qs[hh * D + j + half] = (b * cs + a * sn) * scale;
+  // RoPE on the group's query heads at position pos (G * D / 2 <= 256
+  // items: one per thread)
+  {
+    const int hh = tid / half, j = tid % half;
+    const bool act = tid < G * half;
+    const size_t o = (size_t)(q.g * G + (act ? hh : 0)) * D + j;
+    float a, b;
+    if (qm) {
+      const uint64_t* const mm[2] = {qm + o, qm + o + half};
+      const bool use[2] = {act, act};
+      float v[2];
+      ll_gather<2>(p, c.task, mm, use, v);
+      a = v[0];
+      b = v[1];
+    } else {
+      a = act ? __ldcg(qkv + o) : 0.f;
+      b = act ? __ldcg(qkv + o + half) : 0.f;
+    }
+    if (act) {
+      const float cs = p.rope_cos[(size_t)q.pos * p.rope_half + j];
+      const float sn = p.rope_sin[(size_t)q.pos * p.rope_half + j];
+      qs[hh * D + j] = (a * cs - b * sn) * scale;
+      qs[hh * D + j + half] = (b * cs + a * sn) * scale;
+    }
   }
   if (q.has_new && warp == kConsumerWarps - 1) {
     // the key/value of the token at pos come straight from qkv, rotated and
     // rounded to bf16 exactly as ATTENTION_APPEND stores them, so this task
     // does not wait for the append
-    const float* kq = qkv + (size_t)q.Hq * D + (size_t)q.g * D;
-    const float* vq = qkv + (size_t)(q.Hq + q.Hkv) * D + (size_t)q.g * D;
+    const size_t ko = (size_t)q.Hq * D + (size_t)q.g * D, vo = (size_t)(q.Hq + q.Hkv) * D + (size_t)q.g * D;
     for (int dd = lane; dd < D; dd += 32) {
       const int jj = dd < half ? dd : dd - half;
       const float cs = p.rope_cos[(size_t)q.pos * p.rope_half + jj];
       const float sn = p.rope_sin[(size_t)q.pos * p.rope_half + jj];
-      const float k1 = __ldcg(kq + jj), k2 = __ldcg(kq + jj + half);
+      float k1, k2, vv;
+      if (qm) {
+        const uint64_t* const mm[3] = {qm + ko + jj, qm + ko + jj + half, qm + vo + dd};
+        const bool use[3] = {true, true, true};
+        float v[3];
+        ll_gather<3>(p, c.task, mm, use, v);
+        k1 = v[0];
+        k2 = v[1];
+        vv = v[2];
+      } else {
+        k1 = __ldcg(qkv + ko + jj);
+        k2 = __ldcg(qkv + ko + jj + half);
+        vv = __ldcg(qkv + vo + dd);
+      }
       const float kr = dd < half ? k1 * cs - k2 * sn : k2 * cs + k1 * sn;
       nkv[dd] = __bfloat16_as_ushort(__float2bfloat16_rn(kr));
-      nkv[D + dd] = __bfloat16_as_ushort(__float2bfloat16_rn(__ldcg(vq + dd)));
+      nkv[D + dd] = __bfloat16_as_ushort(__float2bfloat16_rn(vv));
     }
   }
   cbar();
@@ -1418,10 +1482,12 @@ __device__ void partial_task(Ctx& c, const mk_task_descriptor& d) {
   else partial_body<8>(c, d, q);
 }
 
-// Log-sum-exp merge of the P partials of one (sequence, kv head), as a
-// running merge with a running maximum; empty partials (m = -inf) add
-// nothing.  Up to 32 partials a thread issues every load it needs at once
-// (one L2 round trip); more partials go through a loop.
+// Log-sum-exp merge of the P partials of one (sequence, kv head):
+// out = sum_k 2^(m_k - M) o_k / sum_k 2^(m_k - M) l_k with M = max_k m_k;
+// empty partials (m = -inf) add nothing.  Up to 32 partials, 8 / G warps
+// serve each head: lane k reads partial k's (m, l) while every lane reads
+// its output dims of all P partials at once (one L2 round trip), then the
+// weights travel by shuffles.  More partials go through a running merge.
 __device__ __forceinline__ void lse_fold(float& M, float& Ls, float& O0, float& O1, float m, float l, float o0,
                                          float o1) {
   if (m != -INFINITY) {
@@ -1443,31 +1509,47 @@ __device__ void combine_task(Ctx& c, const mk_task_descriptor& d) {
   const float* scr = rec_ptr<const float>(c, kPIn0) + (size_t)base * rec;
   float* out = rec_ptr<float>(c, kPOut);
   uint64_t* om = rec_ptr<uint64_t>(c, kMirOut);
+  if (P <= 32) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wph = kConsumerWarps / G;  // warps per head (G divides 8)
+    const int h = warp / wph, dpw = D / wph;
+    const int e = (warp % wph) * dpw + lane * 2;
+    const bool mine = lane * 2 < dpw;
+    const float* r = scr + h * (D + 2);
+    const float mk = lane < P ? __ldcg(r + (size_t)lane * rec) : -INFINITY;
+    const float lk = lane < P ? __ldcg(r + (size_t)lane * rec + 1) : 0.f;
+    float2 ov[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      ov[k] = (k < P && mine) ? __ldcg(reinterpret_cast<const float2*>(r + (size_t)k * rec + 2 + e))
+                              : make_float2(0.f, 0.f);
+    const float M = warp_max(mk);
+    const float wk = mk == -INFINITY ? 0.f : exp2f(mk - M);
+    const float L = warp_sum(wk * lk);
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const float w = __shfl_sync(0xffffffffu, wk, k);
+      a0 = fmaf(w, ov[k].x, a0);
+      a1 = fmaf(w, ov[k].y, a1);
+    }
+    if (mine) {
+      const float inv = 1.f / L;
+      const size_t o = (size_t)s * Hq * D + (size_t)(g * G + h) * D + e;
+      *reinterpret_cast<float2*>(out + o) = make_float2(a0 * inv, a1 * inv);
+      if (om) st_relaxed_v2u64(om + o, ll_pack(a0 * inv, p.tag), ll_pack(a1 * inv, p.tag));
+    }
+    return;
+  }
   // each thread produces two adjacent outputs (e, e + 1) of one head
   for (int i = threadIdx.x; i < G * D / 2; i += kConsumerThreads) {
     const int h = (2 * i) / D, e = (2 * i) % D;
     const float* r = scr + h * (D + 2);
     float M = -INFINITY, Ls = 0.f, O0 = 0.f, O1 = 0.f;
-    if (P <= 32) {
-      float mv[32], lv[32], o0[32], o1[32];
-#pragma unroll
-      for (int k = 0; k < 32; ++k) {
-        const bool ok = k < P;
-        const float* rr = r + (size_t)k * rec;
-        mv[k] = ok ? __ldcg(rr) : -INFINITY;
-        lv[k] = ok ? __ldcg(rr + 1) : 0.f;
-        const float2 ov = ok ? __ldcg(reinterpret_cast<const float2*>(rr + 2 + e)) : make_float2(0.f, 0.f);
-        o0[k] = ov.x;
-        o1[k] = ov.y;
-      }
-#pragma unroll
-      for (int k = 0; k < 32; ++k) lse_fold(M, Ls, O0, O1, mv[k], lv[k], o0[k], o1[k]);
-    } else {
-      for (int k = 0; k < P; ++k) {
-        const float* rr = r + (size_t)k * rec;
-        const float2 ov = __ldcg(reinterpret_cast<const float2*>(rr + 2 + e));
-        lse_fold(M, Ls, O0, O1, __ldcg(rr), __ldcg(rr + 1), ov.x, ov.y);
-      }
+    for (int k = 0; k < P; ++k) {
+      const float* rr = r + (size_t)k * rec;
+      const float2 ov = __ldcg(reinterpret_cast<const float2*>(rr + 2 + e));
+      lse_fold(M, Ls, O0, O1, __ldcg(rr), __ldcg(rr + 1), ov.x, ov.y);
     }
     const float inv = 1.f / Ls;
     const size_t o = (size_t)s * Hq * D + (size_t)(g * G + h) * D + e;

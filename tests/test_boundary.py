@@ -236,8 +236,9 @@ def _check_sync_plan(tasks, edges, plan, ll=None):
         covered = set()
         entries = wait[wait_off[t]:wait_off[t + 1]]
         if task_ll[t]:
-            assert int(tasks["op_id"][t]) == ol.OP_GEMV and len(entries) == 0
-            res = int(tasks["flags"][t]) & ol.F_ADD_RESIDUAL
+            op = int(tasks["op_id"][t])
+            assert op in (ol.OP_GEMV, ol.OP_ATT_PARTIAL) and len(entries) == 0
+            res = op == ol.OP_GEMV and int(tasks["flags"][t]) & ol.F_ADD_RESIDUAL
             x, aux = int(tasks["in_buf"][t][0]), int(tasks["in_buf"][t][2])
             assert buf_ll[x] and (not res or buf_ll[aux])
             for p in parents[t]:
@@ -269,11 +270,11 @@ def test_sync_plan_is_equivalent_to_the_edges(L, name):
         plan = L.mk_get_sync_plan(g, len(tasks))
         ll = L.mk_get_ll_plan(g, len(tasks), len(spec["buffers"]))
         _check_sync_plan(tasks, L.mk_get_edges(g), plan, ll)
-        gemv = tasks["op_id"] == ol.OP_GEMV
+        polls = (tasks["op_id"] == ol.OP_GEMV) | (tasks["op_id"] == ol.OP_ATT_PARTIAL)
         if w.B <= 4:
-            # every GEMV reads tagged pairs (its inputs come from GEMV,
-            # COMBINE, embedding or norm tasks), and no other task does
-            assert np.all(ll[0][gemv] == 1) and np.all(ll[0][~gemv] == 0)
+            # every GEMV and split-KV partial reads tagged pairs (their inputs
+            # come from GEMV, COMBINE, embedding or norm tasks), no other task does
+            assert np.all(ll[0][polls] == 1) and np.all(ll[0][~polls] == 0)
         else:
             assert not ll[0].any() and not ll[1].any()
         # a B = 1 hand-off between GEMVs costs one atomic per tile, not one per edge
