@@ -704,7 +704,7 @@ extern "C" int mk_lower(mk_graph* g) {
 }
 
 // Tagged hand-offs.  At B <= 4 the activations a GEMV reads (its x, and
-// its residual) and the qkv rows a split-KV partial reads are also written
+// its residual) and the qkv rows attention tasks read are also written
 // by their producers as (value, step tag) pairs into a library-owned
 // mirror.  Such a reader polls its inputs' tags instead of waiting on
 // counters: the data and the news that it is ready
@@ -714,7 +714,7 @@ extern "C" int mk_lower(mk_graph* g) {
 // COMBINE, embedding MEMCPY or RMSNORM tasks (the bodies that write the
 // pairs); a GEMV qualifies when its x and residual do and every one of its
 // parents writes one of them (weights and gamma have no writers), a split-KV
-// partial when its qkv does and every parent writes qkv.
+// partial or a cache append when its qkv does and every parent writes qkv.
 void mk::build_ll_plan(mk_graph* g, const std::vector<std::vector<int>>& parents,
                        const std::vector<uint8_t>& once) {
   const size_t NB = g->bufs.size(), N = g->tasks.size();
@@ -727,7 +727,7 @@ void mk::build_ll_plan(mk_graph* g, const std::vector<std::vector<int>>& parents
       read_as_input[d.in_buf[0]] = 1;
       if (d.flags & MK_F_ADD_RESIDUAL) read_as_input[d.in_buf[2]] = 1;
     }
-    if (d.op_id == MK_OP_ATTENTION_PARTIAL) read_as_input[d.in_buf[0]] = 1;
+    if (d.op_id == MK_OP_ATTENTION_PARTIAL || d.op_id == MK_OP_ATTENTION_APPEND) read_as_input[d.in_buf[0]] = 1;
     if (d.out_buf >= NB) continue;
     const bool ok = d.op_id == MK_OP_GEMV || d.op_id == MK_OP_ATTENTION_COMBINE || d.op_id == MK_OP_MEMCPY ||
                     d.op_id == MK_OP_RMSNORM;
@@ -737,9 +737,9 @@ void mk::build_ll_plan(mk_graph* g, const std::vector<std::vector<int>>& parents
     g->ll_buf[b] = read_as_input[b] && once[b] && !bad_writer[b] && g->bufs[b].dtype == MK_F32;
   for (size_t t = 0; t < N; ++t) {
     const mk_task_descriptor& d = g->tasks[t];
-    if (d.op_id == MK_OP_ATTENTION_PARTIAL) {
-      // its query and (last chunk) new key and value come from qkv; the cache
-      // rows it reads have no writer this step
+    if (d.op_id == MK_OP_ATTENTION_PARTIAL || d.op_id == MK_OP_ATTENTION_APPEND) {
+      // the query and new key and value come from qkv; the cache rows a
+      // partial reads and the decode state have no writer before them
       bool ok = g->ll_buf[d.in_buf[0]];
       for (int q : parents[t]) ok = ok && g->tasks[q].out_buf == d.in_buf[0];
       g->ll_task[t] = ok;

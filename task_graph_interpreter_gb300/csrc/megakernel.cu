@@ -1248,24 +1248,40 @@ __device__ void append_task(Ctx& c, const mk_task_descriptor& d) {
     if (threadIdx.x == 0) raise_error(p, MK_DEV_CAPACITY, c.task);
     return;
   }
-  const float* qkv = rec_ptr<const float>(c, kPIn0) + (size_t)s * (Hq + 2 * Hkv) * D;
+  const size_t seq = (size_t)s * (Hq + 2 * Hkv) * D;
+  const float* qkv = rec_ptr<const float>(c, kPIn0) + seq;
+  const uint64_t* qm = rec_ptr<const uint64_t>(c, kMirX);  // tagged qkv (MEGA, B <= 4), else null
   __nv_bfloat16* Kc = rec_ptr<__nv_bfloat16>(c, kPIn1);
   __nv_bfloat16* Vc = rec_ptr<__nv_bfloat16>(c, kPIn2);
   const size_t row = (((size_t)s * Hkv + g) * cap + pos) * D;
   const int t = threadIdx.x;
+  const size_t ko = (size_t)Hq * D + (size_t)g * D + (t < half ? t : 0);
+  const size_t vo = (size_t)(Hq + Hkv) * D + (size_t)g * D + (t < D ? t : 0);
+  float k1 = 0.f, k2 = 0.f, vv = 0.f;
+  if (qm) {
+    const uint64_t* const mm[3] = {qm + seq + ko, qm + seq + ko + half, qm + seq + vo};
+    const bool use[3] = {t < half, t < half, t < D};
+    float v[3];
+    ll_gather<3>(p, c.task, mm, use, v);
+    k1 = v[0];
+    k2 = v[1];
+    vv = v[2];
+  } else {
+    if (t < half) {
+      k1 = __ldcg(qkv + ko);
+      k2 = __ldcg(qkv + ko + half);
+    }
+    if (t < D) vv = __ldcg(qkv + vo);
+  }
   if (t < half) {
-    const float k1 = __ldcg(qkv + Hq * D + g * D + t);
-    const float k2 = __ldcg(qkv + Hq * D + g * D + t + half);
     const float cs = p.rope_cos[(size_t)pos * p.rope_half + t];
     const float sn = p.rope_sin[(size_t)pos * p.rope_half + t];
     Kc[row + t] = __float2bfloat16_rn(k1 * cs - k2 * sn);
     Kc[row + t + half] = __float2bfloat16_rn(k2 * cs + k1 * sn);
   }
-  if (t < D) Vc[row + t] = __float2bfloat16_rn(__ldcg(qkv + (Hq + Hkv) * D + g * D + t));
+  if (t < D) Vc[row + t] = __float2bfloat16_rn(vv);
 }
 
-// Sum 32 per-lane values across the warp, transposed: afterwards lane l
-// holds the warp-wide sum of value l (31 shuffles instead of 32 x 5).
 // Eight keys of the online softmax (base 2) for the query heads of a KV
 // group.  Lane = 8 * head + slice: the lane holds dims [slice * DS, slice *
 // DS + DS) of its head's query (qr) and output (o); m and l are its head's

@@ -88,8 +88,38 @@ def test_cpp_lowering_is_byte_identical_to_oracle(L, name, num_ctas, col_align):
         for c in range(num_ctas):
             qq = q[off[c]:off[c + 1]]
             assert np.all(np.diff(qq) > 0), "each CTA queue must be in topological order"
+        _check_queues_deadlock_free(tasks, edges, off, q)
     finally:
         L.mk_destroy(g)
+
+
+def _check_queues_deadlock_free(tasks, edges, off, q):
+    """The dependency edges plus 'runs after' within each CTA queue form an
+    acyclic graph: some task is always at the head of its queue with every
+    parent done, so all co-resident CTAs finish."""
+    N = len(tasks)
+    succ = [[] for _ in range(N)]
+    indeg = np.zeros(N, np.int64)
+    for p in range(N):
+        o, n = int(tasks["dependents_offset"][p]), int(tasks["num_dependents"][p])
+        for c in edges[o:o + n]:
+            succ[p].append(int(c))
+            indeg[int(c)] += 1
+    for c in range(len(off) - 1):
+        qq = q[off[c]:off[c + 1]]
+        for a, b in zip(qq[:-1], qq[1:]):
+            succ[int(a)].append(int(b))
+            indeg[int(b)] += 1
+    ready = [t for t in range(N) if indeg[t] == 0]
+    seen = 0
+    while ready:
+        t = ready.pop()
+        seen += 1
+        for c in succ[t]:
+            indeg[c] -= 1
+            if indeg[c] == 0:
+                ready.append(c)
+    assert seen == N, "CTA queues and dependencies form a cycle"
 
 
 def test_cpp_lowering_validates(L):
@@ -237,7 +267,7 @@ def _check_sync_plan(tasks, edges, plan, ll=None):
         entries = wait[wait_off[t]:wait_off[t + 1]]
         if task_ll[t]:
             op = int(tasks["op_id"][t])
-            assert op in (ol.OP_GEMV, ol.OP_ATT_PARTIAL) and len(entries) == 0
+            assert op in (ol.OP_GEMV, ol.OP_ATT_PARTIAL, ol.OP_ATT_APPEND) and len(entries) == 0
             res = op == ol.OP_GEMV and int(tasks["flags"][t]) & ol.F_ADD_RESIDUAL
             x, aux = int(tasks["in_buf"][t][0]), int(tasks["in_buf"][t][2])
             assert buf_ll[x] and (not res or buf_ll[aux])
@@ -270,10 +300,11 @@ def test_sync_plan_is_equivalent_to_the_edges(L, name):
         plan = L.mk_get_sync_plan(g, len(tasks))
         ll = L.mk_get_ll_plan(g, len(tasks), len(spec["buffers"]))
         _check_sync_plan(tasks, L.mk_get_edges(g), plan, ll)
-        polls = (tasks["op_id"] == ol.OP_GEMV) | (tasks["op_id"] == ol.OP_ATT_PARTIAL)
+        polls = np.isin(tasks["op_id"], [ol.OP_GEMV, ol.OP_ATT_PARTIAL, ol.OP_ATT_APPEND])
         if w.B <= 4:
-            # every GEMV and split-KV partial reads tagged pairs (their inputs
-            # come from GEMV, COMBINE, embedding or norm tasks), no other task does
+            # every GEMV, split-KV partial and cache append reads tagged pairs
+            # (their inputs come from GEMV, COMBINE, embedding or norm tasks),
+            # no other task does
             assert np.all(ll[0][polls] == 1) and np.all(ll[0][~polls] == 0)
         else:
             assert not ll[0].any() and not ll[1].any()
