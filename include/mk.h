@@ -271,11 +271,14 @@ int mk_debug_patch_task(mk_graph* g, int task, const mk_task_descriptor* d);
 int mk_get_sync_plan(const mk_graph* g, const uint32_t** wait_off, const uint32_t** wait,
                      const uint32_t** sig_off, const uint32_t** sig, uint32_t* counter_words);
 
-/* Tagged hand-offs (B <= 4): task_ll[t] = 1 for the GEMV tasks that read
- * all their activation inputs as (value, step tag) pairs and so wait on no
- * counter; buf_ll[b] = 1 for the buffers whose producers also write those
- * pairs (into library-owned mirrors).  uint8 arrays of the task and buffer
- * counts, owned by the graph.  Errors: MK_ERR_STATE (not lowered). */
+/* Tagged hand-offs (B <= 4, megakernel mode): task_ll[t] = 1 for the GEMV,
+ * ATTENTION_PARTIAL and ATTENTION_APPEND tasks that read all their
+ * activation inputs as (step tag, value) pairs and so wait on no counter;
+ * buf_ll[b] = 1 for the buffers whose producers also write those pairs (into
+ * library-owned mirrors: f32 buffers written once per step by one op's
+ * GEMV, COMBINE, embedding or RMSNORM tasks).  uint8 arrays of the task and
+ * buffer counts, owned by the graph, fixed at lowering.  Errors: MK_ERR_ARG
+ * (null argument), MK_ERR_STATE (not lowered). */
 int mk_get_ll_plan(const mk_graph* g, const uint8_t** task_ll, const uint8_t** buf_ll);
 
 /* Per-CTA task queues: offsets int32[num_ctas + 1] into tasks int32[]. */
