@@ -12,8 +12,9 @@
  * copies descriptors, edges and the buffer pointer table to the device
  * (same page: the buffer-table and upload part).  mk_decode_step() runs one
  * persistent kernel, one CTA per SM, that walks a static per-CTA queue of
- * tasks; each task waits only for its own producers through per-task
- * counters in global memory, with no grid-wide barrier ("Megakernels",
+ * tasks; each task waits only for its own producers, through counters in
+ * global memory or, at B <= 4, by polling its inputs' (step tag, value)
+ * pairs, with no grid-wide barrier ("Megakernels",
  * runhoid.com: the "Hoid's approach to megakernels" section and its Fig. 5,
  * the on-GPU interpreter in which a block waits only for its producers).
  *
@@ -29,7 +30,8 @@
  *    allocates them, keeps them alive while the graph exists and frees them
  *    after mk_destroy.  The LIBRARY owns what it allocates in mk_upload:
  *    the device blob (descriptors, edges, buffer table, per-CTA queues,
- *    dependency counters, status word, RoPE tables, trace ring).
+ *    dependency counters, tagged mirrors, status word, RoPE tables, trace
+ *    ring).
  *  - Functions up to mk_get_queues need no GPU unless num_ctas is 0.
  *  - Sizes are elements unless stated; all device pointers must be 256-byte
  *    aligned (PyTorch allocations are).
@@ -90,7 +92,7 @@ extern "C" {
 #define MK_PAIR 4                  /* mk_argmax_pair, 8 bytes */
 
 /* ---- execution modes for mk_decode_step_ex ------------------------------ */
-#define MK_MODE_MEGA 0            /* persistent kernel, per-task counters */
+#define MK_MODE_MEGA 0            /* persistent kernel, counters and tagged hand-offs */
 #define MK_MODE_PER_OP 1          /* one kernel launch per op, one CTA per task */
 #define MK_MODE_PER_OP_GRAPH 2    /* MK_MODE_PER_OP captured once into a CUDA graph */
 #define MK_MODE_LEVELS 3          /* persistent kernel, barrier per topological level */
