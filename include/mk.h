@@ -228,6 +228,13 @@ int mk_attention_scratch_rows(const mk_graph* g, int B, int Hkv, const int32_t* 
 /* Number of column tiles an n-column GEMV fans out into. */
 int mk_gemv_tiles(const mk_graph* g, int n, int32_t* tiles);
 
+/* Bytes the registered buffer `buf` needs as the scratch of the attention
+ * ops or the argmax pairs of the matmul ops already added that name it (the
+ * largest if several do); lets a caller check an allocation made from
+ * mk_attention_scratch_rows / mk_gemv_tiles.  Errors: MK_ERR_ARG (null
+ * argument, or no added op uses buf that way). */
+int mk_scratch_size(const mk_graph* g, uint16_t buf, size_t* bytes);
+
 /* Lower every op to descriptors and edges and build the per-CTA queues;
  * freezes the graph.  Descriptor fields by op (unused in_buf = MK_NO_BUF,
  * unused fields 0):

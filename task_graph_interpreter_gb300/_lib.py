@@ -28,7 +28,7 @@ MK_NO_BUF = 0xFFFF
 EXPORTS = [
     "mk_graph_create", "mk_set_state", "mk_add_buffer", "mk_add_embed", "mk_add_rmsnorm", "mk_fuse_rmsnorm",
     "mk_add_matmul",
-    "mk_add_attention", "mk_add_sample", "mk_attention_scratch_rows", "mk_gemv_tiles",
+    "mk_add_attention", "mk_add_sample", "mk_attention_scratch_rows", "mk_gemv_tiles", "mk_scratch_size",
     "mk_lower", "mk_get_tasks", "mk_get_edges", "mk_get_sync_plan", "mk_get_ll_plan", "mk_get_queues",
     "mk_upload",
     "mk_decode_step", "mk_decode_step_ex", "mk_decode_step_host", "mk_status",
@@ -72,6 +72,7 @@ def lib():
         "mk_add_sample": (c_int, [G, c_uint16, c_uint16, c_int, c_int, c_int]),
         "mk_attention_scratch_rows": (c_int, [G, c_int, c_int, POINTER(c_int32), c_int, POINTER(c_int64)]),
         "mk_gemv_tiles": (c_int, [G, c_int, POINTER(c_int32)]),
+        "mk_scratch_size": (c_int, [G, c_uint16, POINTER(c_size_t)]),
         "mk_lower": (c_int, [G]),
         "mk_get_tasks": (c_int, [G, POINTER(c_void_p), POINTER(c_size_t)]),
         "mk_get_edges": (c_int, [G, POINTER(c_void_p), POINTER(c_size_t)]),
@@ -167,6 +168,12 @@ def mk_gemv_tiles(g, n) -> int:
     t = c_int32()
     check(lib().mk_gemv_tiles(g, n, ctypes.byref(t)), "mk_gemv_tiles")
     return t.value
+
+
+def mk_scratch_size(g, buf) -> int:
+    n = c_size_t()
+    check(lib().mk_scratch_size(g, buf, ctypes.byref(n)), "mk_scratch_size")
+    return n.value
 
 
 def mk_lower(g):

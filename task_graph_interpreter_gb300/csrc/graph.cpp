@@ -317,6 +317,29 @@ extern "C" int mk_gemv_tiles(const mk_graph* g, int n, int32_t* tiles) {
   return MK_OK;
 }
 
+extern "C" int mk_scratch_size(const mk_graph* g, uint16_t buf, size_t* bytes) {
+  if (!g || !bytes) return fail(MK_ERR_ARG, "mk_scratch_size: null argument");
+  size_t need = 0;
+  bool used = false;
+  for (const OpRec& op : g->ops) {
+    if (op.kind == K_ATTENTION && op.a[4] == buf) {
+      const auto P = partials_per_sequence(op.len0, op.Hkv, op.chunk, g->num_ctas);
+      size_t rows = 0;
+      for (int q : P) rows += (size_t)q * op.Hkv;
+      need = std::max(need, rows * (size_t)(op.Hq / op.Hkv) * (size_t)(op.D + 2) * 4);
+      used = true;
+    }
+    if (op.kind == K_MATMUL && op.a[4] == buf && buf != MK_NO_BUF) {
+      need = std::max(need, (size_t)tile_count(op.n, g->tiles_target, g->col_align) * (size_t)op.B * 8);
+      used = true;
+    }
+  }
+  if (!used) return fail(MK_ERR_ARG, "mk_scratch_size: buffer " + std::to_string(buf) +
+                                         " is no op's attention scratch or argmax pairs");
+  *bytes = need;
+  return MK_OK;
+}
+
 extern "C" int mk_add_attention(mk_graph* g, uint16_t qkv, uint16_t kcache, uint16_t vcache,
                                 uint16_t out, uint16_t scratch, int B, int Hq, int Hkv, int D,
                                 int capacity, const int32_t* len0, int chunk, double rope_theta) {

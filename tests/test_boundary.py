@@ -122,6 +122,26 @@ def _check_queues_deadlock_free(tasks, edges, off, q):
     assert seen == N, "CTA queues and dependencies form a cycle"
 
 
+@pytest.mark.parametrize("name", ["tiny", "8b_b8", "8b_long"])
+def test_scratch_size_matches_the_allocation(L, name):
+    # the attention scratch and argmax pairs the spec allocates are exactly
+    # the bytes the library asks for
+    w = synth.workload(name)
+    spec = llama_decode_spec(w.model, w.B, w.kv_len, w.capacity, w.chunk, 152, col_align=4)
+    g = _replay(L, spec, w.B)
+    try:
+        for op in spec["ops"]:
+            buf = op.get("scratch") if op["kind"] == "attention" else op.get("pairs") if op["kind"] == "matmul" else None
+            if buf is None or buf == ol.NO_BUF:
+                continue
+            dt, rows, cols = spec["buffers"][buf]
+            assert L.mk_scratch_size(g, buf) == rows * cols * (8 if dt == 4 else 4)   # MK_PAIR is 8 bytes
+        with pytest.raises(L.MkError):
+            L.mk_scratch_size(g, 3)   # the embedding table is neither
+    finally:
+        L.mk_destroy(g)
+
+
 def test_cpp_lowering_validates(L):
     w = synth.workload("1b")
     spec = llama_decode_spec(w.model, w.B, w.kv_len, w.capacity, w.chunk, 152)
