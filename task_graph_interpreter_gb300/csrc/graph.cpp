@@ -728,7 +728,7 @@ extern "C" int mk_lower(mk_graph* g) {
 
 // Tagged hand-offs.  At B <= 4 the activations a GEMV reads (its x, and
 // its residual) and the qkv rows attention tasks read are also written
-// by their producers as (value, step tag) pairs into a library-owned
+// by their producers as (step tag, value) pairs into a library-owned
 // mirror.  Such a reader polls its inputs' tags instead of waiting on
 // counters: the data and the news that it is ready
 // arrive in one round trip, where a counter costs the producer's fence,

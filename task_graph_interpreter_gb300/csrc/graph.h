@@ -64,8 +64,8 @@ struct mk_graph {
   std::vector<uint32_t> wait_off, wait, sig_off, sig;  // wait holds (counter, count) pairs
   uint32_t counter_words = 0;
   // tagged hand-offs (B <= 4): buffers whose values are also written as
-  // (value, step tag) pairs, and the GEMV tasks that read all their inputs
-  // from such pairs instead of waiting on counters
+  // (step tag, value) pairs, and the GEMV, partial and append tasks that
+  // read all their inputs from such pairs instead of waiting on counters
   std::vector<uint8_t> ll_buf, ll_task;
   // kernel geometry
   int max_m = 1;

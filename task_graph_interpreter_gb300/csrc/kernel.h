@@ -50,7 +50,7 @@ struct KParams {
   const int32_t* level_tasks; // LEVELS: task ids grouped by level
   uint32_t* level_bar;        // LEVELS: one arrival counter per level boundary
   int32_t* status;            // int32[4]
-  uint64_t* const* mirrors;   // MEGA, B <= 4: per buffer index, its (value, tag) pairs or null
+  uint64_t* const* mirrors;   // MEGA, B <= 4: per buffer index, its (step tag, value) pairs or null
   uint32_t tag;               // MEGA: this step's tag (monotone across steps, never 0)
   const uint8_t* tmaps;       // CUtensorMap per buffer index (tensor-core weights), kTmapBytes each
   const int32_t* tm_rows;     // per buffer index: rows of its tensor map's box, 0 = no map

@@ -523,11 +523,12 @@ __device__ void block_argmax(float& v, int& idx, float* red) {
 }
 
 // ------------------------------------------------------------------ tagged hand-offs
-// At B <= 4 the activations that GEMVs read also travel as (value, step
-// tag) pairs in mirrors of their buffers (MEGA mode only; every launch has
-// a new tag, so pairs of earlier steps never match).  A GEMV whose inputs
-// all have mirrors waits on no counter: it loads its pairs and polls those
-// whose tag is not yet this step's.
+// At B <= 4 the activations that GEMVs read, and the qkv rows that
+// appends and partials read, also travel as (step tag, value) pairs in
+// mirrors of their buffers: one 8-byte word, tag in the high half (MEGA mode
+// only; every launch has a new tag, so pairs of earlier steps never match).
+// A task whose inputs all have mirrors waits on no counter: it loads its
+// pairs and polls those whose tag is not yet this step's.
 __device__ __forceinline__ uint64_t ll_pack(float v, uint32_t tag) {
   return ((uint64_t)tag << 32) | __float_as_uint(v);
 }

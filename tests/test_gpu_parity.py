@@ -104,6 +104,27 @@ def test_modes_are_bitwise_identical_and_deterministic():
             assert torch.equal(a, b)
 
 
+def test_modes_interleaved_on_one_graph():
+    # megakernel steps write and poll tagged pairs, the other modes do not:
+    # pairs left by an earlier megakernel step (or by none) must never pass
+    # for the current one, so every step still matches the oracle
+    w = synth.custom(synth.TINY, 2, [40, 128], 6, name="tiny_mix")
+    dec = build_gpu(w)
+    W = NpWeights(w.model, 0)
+    st = oracle_state(w, 0)
+    try:
+        for mode in ("mega", "per_op", "mega", "levels", "per_op_pdl", "mega"):
+            dec.graph.step(MODES[mode])
+            code, task = dec.graph.status()
+            assert code == 0, f"{mode}: device status {code} at task {task}"
+            res = of.decode_step(w.model, W, st)
+            _, clear = compare_step(dec, res, st)
+            if not clear:
+                break
+    finally:
+        dec.graph.close()
+
+
 @pytest.mark.slow
 def test_1b_full_size_two_steps():
     w = synth.custom(synth.LLAMA_1B, 1, [1024], 2, name="1b2")
