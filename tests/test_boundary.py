@@ -335,6 +335,61 @@ def test_sync_plan_is_equivalent_to_the_edges(L, name):
         L.mk_destroy(g)
 
 
+def _tagged_plan(L, spec, B):
+    g = _replay(L, spec, B)
+    try:
+        tasks = np.frombuffer(L.mk_get_tasks(g), dtype=ol.TASK_DTYPE).copy()
+        plan = L.mk_get_sync_plan(g, len(tasks))
+        ll = L.mk_get_ll_plan(g, len(tasks), len(spec["buffers"]))
+        _check_sync_plan(tasks, L.mk_get_edges(g), plan, ll)
+        return tasks, ll
+    finally:
+        L.mk_destroy(g)
+
+
+def test_tagged_plan_takes_standalone_norm_outputs(L):
+    # RMSNORM bodies write pairs too: with standalone norms every GEMV and
+    # attention reader still polls, and the norm outputs carry pairs
+    w = synth.workload("1b")
+    spec = llama_decode_spec(w.model, w.B, w.kv_len, w.capacity, w.chunk, 152, col_align=4, norms="standalone")
+    tasks, (task_ll, buf_ll) = _tagged_plan(L, spec, w.B)
+    norms = tasks["op_id"] == ol.OP_RMSNORM
+    assert norms.any() and not task_ll[norms].any()
+    assert all(buf_ll[int(o)] for o in tasks["out_buf"][norms])
+    polls = np.isin(tasks["op_id"], [ol.OP_GEMV, ol.OP_ATT_PARTIAL, ol.OP_ATT_APPEND])
+    assert np.all(task_ll[polls] == 1)
+
+
+def test_tagged_plan_refuses_a_buffer_written_twice(L):
+    # two matmuls writing one buffer: its readers could not tell the two
+    # writes apart by the step tag, so the buffer carries no pairs and its
+    # reader waits on counters
+    g = L.mk_graph_create(num_ctas=16, tiles_target=16, col_align=4)
+    base = 1 << 40
+    try:
+        L.mk_set_state(g, base, 1)
+        H = 256
+        x = L.mk_add_buffer(g, base + 1 * (1 << 24), L.MK_F32, 1, H)
+        w1 = L.mk_add_buffer(g, base + 2 * (1 << 24), L.MK_BF16, H, H)
+        w2 = L.mk_add_buffer(g, base + 3 * (1 << 24), L.MK_BF16, H, H)
+        y = L.mk_add_buffer(g, base + 4 * (1 << 24), L.MK_F32, 1, H)
+        z = L.mk_add_buffer(g, base + 5 * (1 << 24), L.MK_F32, 1, H)
+        u = L.mk_add_buffer(g, base + 6 * (1 << 24), L.MK_F32, 1, H)
+        L.mk_add_matmul(g, x, w1, y, ol.NO_BUF, ol.NO_BUF, 0, 1, H, H, 0.0)
+        L.mk_add_matmul(g, y, w2, z, ol.NO_BUF, ol.NO_BUF, 0, 1, H, H, 0.0)   # reads y once written
+        L.mk_add_matmul(g, z, w1, y, ol.NO_BUF, ol.NO_BUF, 0, 1, H, H, 0.0)   # writes y again
+        L.mk_add_matmul(g, y, w2, u, ol.NO_BUF, ol.NO_BUF, 0, 1, H, H, 0.0)
+        L.mk_lower(g)
+        tasks = np.frombuffer(L.mk_get_tasks(g), dtype=ol.TASK_DTYPE)
+        task_ll, buf_ll = L.mk_get_ll_plan(g, len(tasks), u + 1)
+        assert buf_ll[z] == 1 and buf_ll[y] == 0
+        reads_y = tasks["in_buf"][:, 0] == y
+        reads_z = tasks["in_buf"][:, 0] == z
+        assert not task_ll[reads_y].any() and task_ll[reads_z].all()
+    finally:
+        L.mk_destroy(g)
+
+
 def test_sync_plan_follows_a_patched_dependency_count(L):
     w = synth.workload("tiny")
     spec = llama_decode_spec(w.model, w.B, w.kv_len, w.capacity, w.chunk, 16, col_align=4)
