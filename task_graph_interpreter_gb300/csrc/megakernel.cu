@@ -1258,6 +1258,8 @@ __device__ void append_task(Ctx& c, const mk_task_descriptor& d) {
   const int t = threadIdx.x;
   const size_t ko = (size_t)Hq * D + (size_t)g * D + (t < half ? t : 0);
   const size_t vo = (size_t)(Hq + Hkv) * D + (size_t)g * D + (t < D ? t : 0);
+  const float cs = t < half ? __ldg(p.rope_cos + (size_t)pos * p.rope_half + t) : 1.f;
+  const float sn = t < half ? __ldg(p.rope_sin + (size_t)pos * p.rope_half + t) : 0.f;
   float k1 = 0.f, k2 = 0.f, vv = 0.f;
   if (qm) {
     const uint64_t* const mm[3] = {qm + seq + ko, qm + seq + ko + half, qm + seq + vo};
@@ -1275,8 +1277,6 @@ __device__ void append_task(Ctx& c, const mk_task_descriptor& d) {
     if (t < D) vv = __ldcg(qkv + vo);
   }
   if (t < half) {
-    const float cs = p.rope_cos[(size_t)pos * p.rope_half + t];
-    const float sn = p.rope_sin[(size_t)pos * p.rope_half + t];
     Kc[row + t] = __float2bfloat16_rn(k1 * cs - k2 * sn);
     Kc[row + t + half] = __float2bfloat16_rn(k2 * cs + k1 * sn);
   }
@@ -1385,6 +1385,9 @@ __device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom
     const int hh = tid / half, j = tid % half;
     const bool act = tid < G * half;
     const size_t o = (size_t)(q.g * G + (act ? hh : 0)) * D + j;
+    // the table rows do not depend on qkv: their loads go out before the wait
+    const float cs = act ? __ldg(p.rope_cos + (size_t)q.pos * p.rope_half + j) : 1.f;
+    const float sn = act ? __ldg(p.rope_sin + (size_t)q.pos * p.rope_half + j) : 0.f;
     float a, b;
     if (qm) {
       const uint64_t* const mm[2] = {qm + o, qm + o + half};
@@ -1398,8 +1401,6 @@ __device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom
       b = act ? __ldcg(qkv + o + half) : 0.f;
     }
     if (act) {
-      const float cs = p.rope_cos[(size_t)q.pos * p.rope_half + j];
-      const float sn = p.rope_sin[(size_t)q.pos * p.rope_half + j];
       qs[hh * D + j] = (a * cs - b * sn) * scale;
       qs[hh * D + j + half] = (b * cs + a * sn) * scale;
     }
