@@ -675,6 +675,14 @@ template <int B, int NV>
 __device__ __forceinline__ void gemv_load_x(const KParams& p, int task, float (&xr)[B][NV][8], float (&ss)[B],
                                             const float* __restrict__ x, const uint64_t* xm,
                                             const uint16_t* __restrict__ gamma, int K, int col0, int Bact) {
+  // the gains do not depend on x: with few pieces (every normalised GEMV
+  // has NV <= 2) their loads go out before x's, and before any wait for it
+  uint4 gv[NV <= 2 ? NV : 1];
+  if constexpr (NV <= 2) {
+#pragma unroll
+    for (int v = 0; v < NV; ++v)
+      gv[v] = gamma ? __ldg(reinterpret_cast<const uint4*>(gamma + col0 + v * 256)) : make_uint4(0u, 0u, 0u, 0u);
+  }
   if (xm) {
     ll_load_x<B, NV>(p, task, xr, xm, K, col0, Bact);
   } else {
@@ -699,9 +707,11 @@ __device__ __forceinline__ void gemv_load_x(const KParams& p, int task, float (&
     const int col = col0 + v * 256;
     float gm[8];
     if (gamma) {
-      const uint4 gv = __ldg(reinterpret_cast<const uint4*>(gamma + col));
-      gm[0] = bf_lo(gv.x); gm[1] = bf_hi(gv.x); gm[2] = bf_lo(gv.y); gm[3] = bf_hi(gv.y);
-      gm[4] = bf_lo(gv.z); gm[5] = bf_hi(gv.z); gm[6] = bf_lo(gv.w); gm[7] = bf_hi(gv.w);
+      uint4 g4;
+      if constexpr (NV <= 2) g4 = gv[v];
+      else g4 = __ldg(reinterpret_cast<const uint4*>(gamma + col));
+      gm[0] = bf_lo(g4.x); gm[1] = bf_hi(g4.x); gm[2] = bf_lo(g4.y); gm[3] = bf_hi(g4.y);
+      gm[4] = bf_lo(g4.z); gm[5] = bf_hi(g4.z); gm[6] = bf_lo(g4.w); gm[7] = bf_hi(g4.w);
     } else {
 #pragma unroll
       for (int k = 0; k < 8; ++k) gm[k] = 1.f;
