@@ -54,6 +54,23 @@ def dist_env():
     return r, ws, lr
 
 
+def check_whole_step(task_bytes, w, L):
+    """The timed graph is the whole decode step: every layer's attention,
+    the lm_head tiles and one SAMPLE per sequence (a benchmark of one layer,
+    or without the lm_head, is a known way to overstate decode speed)."""
+    import numpy as np
+    dt = np.dtype({"names": ["op_id", "m", "n"], "formats": ["<u2", "<i4", "<i4"], "offsets": [0, 28, 32],
+                   "itemsize": 64})
+    t = np.frombuffer(task_bytes, dtype=dt)
+    m = w.model
+    combines = int(np.count_nonzero(t["op_id"] == L.MK_OP_ATTENTION_COMBINE))
+    samples = int(np.count_nonzero(t["op_id"] == L.MK_OP_SAMPLE))
+    lm_tiles = int(np.count_nonzero((t["op_id"] == L.MK_OP_GEMV) & (t["n"] == m.V)))
+    if combines != m.L * w.B * m.Hkv or samples != w.B or lm_tiles < 1:
+        raise RuntimeError(f"timed graph is not a whole step: {combines} combines, {samples} samples, "
+                           f"{lm_tiles} lm_head tiles for {m.L} layers, B={w.B}")
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -285,6 +302,7 @@ def main():
     g.upload()
     stream = torch.cuda.current_stream(dev)
     n_tasks = len(g.tasks_bytes()) // 64
+    check_whole_step(g.tasks_bytes(), w, L)
 
     def barrier():
         if ws > 1:
@@ -310,6 +328,9 @@ def main():
         code, task = g.status()
         if code != 0:
             raise RuntimeError(f"device status {code} at task {task} in mode {mode}")
+        # every timed step generated one token per sequence
+        if positions() != [p + K for p in pos0]:
+            raise RuntimeError(f"mode {mode}: positions {positions()} after {K} steps from {pos0}")
         nbytes = sum(algorithmic_bytes(w.model, w.B, [p + i for p in pos0]) for i in range(K))
         return ms, nbytes
 

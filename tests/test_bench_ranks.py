@@ -53,3 +53,27 @@ def test_single_rank_is_the_identity():
     import bench
     assert bench.reduce_max(1.25, 1) == 1.25
     assert bench.job_throughput(8, 64, 2.0, 1) == pytest.approx(256.0)
+
+
+def test_bench_checks_the_timed_graph_is_a_whole_step():
+    # the harness refuses a graph without every layer, the lm_head or SAMPLE
+    import importlib.util
+    import numpy as np
+    import pytest
+    import synth
+    from oracle import lowering as ol
+    from oracle.graph import llama_decode_spec
+    from task_graph_interpreter_gb300 import _lib as L
+    spec = importlib.util.spec_from_file_location("bench", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    w = synth.workload("1b")
+    tasks, _ = ol.lower(llama_decode_spec(w.model, w.B, w.kv_len, w.capacity, w.chunk, 152, col_align=4))
+    bench.check_whole_step(tasks.tobytes(), w, L)
+    no_sample = tasks[tasks["op_id"] != ol.OP_SAMPLE]
+    with pytest.raises(RuntimeError):
+        bench.check_whole_step(no_sample.tobytes(), w, L)
+    one_layer_less = tasks[np.nonzero(tasks["op_id"] == ol.OP_ATT_COMBINE)[0][w.B * w.model.Hkv]:]
+    with pytest.raises(RuntimeError):
+        bench.check_whole_step(one_layer_less.tobytes(), w, L)
+
