@@ -152,6 +152,11 @@ class Graph:
     def trace(self):
         return L.mk_get_trace(self.h)
 
+    def chrome_trace(self, path: str = None) -> dict:
+        """The last traced step as Chrome trace-event JSON (see trace.py)."""
+        from .trace import chrome_trace
+        return chrome_trace(self.trace(), self.tasks_bytes(), path)
+
     def tensor_core_tiles(self) -> int:
         """GEMV tiles that run on the tensor-core path (batch-8 ops)."""
         return L.mk_gemv_tensor_core_tiles(self.h)

@@ -475,3 +475,33 @@ def test_fusion_pass_leaves_norms_with_other_readers(L):
         assert (t["op_id"] == ol.OP_RMSNORM).sum() == 1
     finally:
         L.mk_destroy(g)
+
+
+def test_chrome_trace_export_from_records(L, tmp_path):
+    # synthetic records for the tiny graph: one task after another on two CTAs
+    import json
+    from task_graph_interpreter_gb300.trace import chrome_trace
+    w = synth.workload("tiny")
+    tasks, _ = ol.lower(llama_decode_spec(w.model, w.B, w.kv_len, w.capacity, w.chunk, 2, col_align=4))
+    N = len(tasks)
+    rec = np.zeros((N, 8), np.uint64)
+    t = 1_000_000
+    for i in range(N):
+        rec[i, 0] = ((i % 2) << 32) | (10 + i % 2)
+        rec[i, 1], rec[i, 2], rec[i, 3] = t, t + 500, t + 2500   # 0.5 us wait, 2 us body
+        if tasks["op_id"][i] == ol.OP_GEMV:
+            rec[i, 4] = t + 700
+        t += 3000
+    rec[N - 1, 3] = 0                                            # a task that did not run
+    out = chrome_trace(rec, tasks.tobytes(), str(tmp_path / "step.json"))
+    ev = json.load(open(tmp_path / "step.json"))["traceEvents"]
+    assert ev == out["traceEvents"]
+    bodies = [e for e in ev if e["cat"] == "task"]
+    waits = [e for e in ev if e["cat"] == "wait"]
+    assert len(bodies) == N - 1 and len(waits) == N - 1
+    assert bodies[0]["ts"] == 0.5 and bodies[0]["dur"] == 2.0 and waits[0]["ts"] == 0.0
+    assert {e["tid"] for e in bodies} == {0, 1}
+    assert any(e["name"].startswith("gemv n=") for e in bodies)
+    assert sum(e["cat"] == "mark" for e in ev) == int(np.count_nonzero(tasks["op_id"][:N - 1] == ol.OP_GEMV))
+    with pytest.raises(ValueError):
+        chrome_trace(rec[:-1], tasks.tobytes())

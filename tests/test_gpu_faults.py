@@ -134,4 +134,6 @@ def test_trace_respects_every_dependency():
         ll = ch[task_ll[ch] == 1]
         assert np.all(tr[ctr, 2] >= tr[p, 3]), f"a child of task {p} started before it ended"
         assert np.all(tr[ll, 3] >= tr[p, 2]), f"a tagged child of task {p} ended before it began"
+    ev = dec.graph.chrome_trace()["traceEvents"]
+    assert sum(e["cat"] == "task" for e in ev) == N
     dec.graph.close()
