@@ -212,6 +212,62 @@ def decode_step(model, weights, st: DecodeState, keep_hidden: bool = True) -> St
     return res
 
 
+def chunk_step(model, weights, st: DecodeState, tokens: np.ndarray) -> StepResult:
+    """Several tokens per sequence in one step (a prefill chunk, or a batch
+    of draft tokens to verify): ``tokens`` [B, T] are the inputs at
+    positions pos .. pos + T - 1, the first of them the pending token
+    ``st.token``.  Each layer runs on all B * T rows; token t appends its
+    key/value row at pos + t and attends, causally, to rows 0 .. pos + t
+    (the cache plus the chunk's earlier tokens).  Returns the logits of
+    every row ([B, T, V]) and hidden states [B, T, H]; the next token is the
+    argmax of each sequence's last row; history gets the given tokens and
+    the sampled one, pos advances by T.  This is T decode steps with the
+    inputs fixed in advance, written as the plain definition."""
+    W = weights if callable(weights) else weights.__getitem__
+    tokens = np.asarray(tokens, dtype=np.int64)
+    B, T = tokens.shape
+    assert np.array_equal(tokens[:, 0], st.token), "the chunk starts with the pending token"
+    H, Hq, Hkv, D, F = model.H, model.Hq, model.Hkv, model.D, model.F
+    G = Hq // Hkv
+    h = bf16_to_f64(W("embed")[tokens.reshape(-1)])               # [B*T, H], row s*T + t
+    res = StepResult(logits=None)
+    for l in range(model.L):
+        xn = rmsnorm(h, bf16_to_f64(W(f"layer{l}.attn_norm")), model.eps)
+        qkv = _gemv(W(f"layer{l}.wqkv"), xn)
+        att = np.zeros((B * T, Hq * D))
+        Kc, Vc = st.kcache[l], st.vcache[l]
+        for s in range(B):
+            for t in range(T):
+                r, p = s * T + t, int(st.pos[s]) + t
+                q = qkv[r, : Hq * D].reshape(Hq, D)
+                k = qkv[r, Hq * D: (Hq + Hkv) * D].reshape(Hkv, D)
+                v = qkv[r, (Hq + Hkv) * D:].reshape(Hkv, D)
+                Kc[s, :, p, :] = round_to_bf16_via_f32(rope(k, p, model.theta))
+                Vc[s, :, p, :] = round_to_bf16_via_f32(v)
+                qr = rope(q, p, model.theta)
+                for g in range(Hkv):
+                    o = attention_single(qr[g * G:(g + 1) * G], bf16_to_f64(Kc[s, g, : p + 1]),
+                                         bf16_to_f64(Vc[s, g, : p + 1]))
+                    att[r, g * G * D:(g + 1) * G * D] = o.reshape(-1)
+        h = h + _gemv(W(f"layer{l}.wo"), att)
+        xn = rmsnorm(h, bf16_to_f64(W(f"layer{l}.mlp_norm")), model.eps)
+        gu = _gemv(W(f"layer{l}.wgu"), xn)
+        h = h + _gemv(W(f"layer{l}.wd"), silu(gu[:, :F]) * gu[:, F:])
+        res.hidden.append(h.reshape(B, T, H).copy())
+    xn = rmsnorm(h, bf16_to_f64(W("final_norm")), model.eps)
+    logits = _gemv(W("embed") if model.tied else W("lm_head"), xn).reshape(B, T, -1)
+    res.logits = logits
+    res.tokens = np.array([argmax_first(logits[s, -1]) for s in range(B)], dtype=np.int64)
+    res.margin = np.array([top2_margin(logits[s, -1]) for s in range(B)])
+    for s in range(B):
+        p = int(st.pos[s])
+        st.history[s, p + 1: p + T] = tokens[s, 1:]
+        st.history[s, p + T] = res.tokens[s]
+        st.token[s] = res.tokens[s]
+        st.pos[s] = p + T
+    return res
+
+
 def initial_state(model, B: int, cap: int, kv_len, tokens, kv_provider) -> DecodeState:
     """State before the first step: ``kv_provider(layer, 'k'|'v')`` returns a
     [B, Hkv, cap, D] uint16 cache holding kv_len[s] valid rows."""

@@ -340,3 +340,53 @@ def test_auto_chunking_fits_one_wave_with_the_smallest_chunk():
             if E > floor:  # one key less per chunk would overflow the wave
                 assert Hkv * sum(max(1, ceil_div(l, E - 1)) for l in lens) > ctas
         assert all(p == max(1, ceil_div(l, E)) or ceil_div(l, p) <= E for l, p in zip(lens, P))
+
+
+def _chunk_inputs(T, seed=5):
+    import copy
+    w = synth.custom(synth.TINY, 2, [40, 120], T, name="tiny_chunk")
+    W = NpWeights(w.model)
+    st = oracle_state(w)
+    rng = np.random.default_rng(seed)
+    toks = np.concatenate([st.token[:, None], rng.integers(0, w.model.V, size=(w.B, T - 1))], axis=1)
+    return w, W, st, copy.deepcopy(st), toks
+
+
+def test_chunk_step_equals_steps_with_the_inputs_fixed():
+    # T tokens through one chunk step = T single-token steps fed the same
+    # inputs (each step's argmax replaced by the next given token)
+    T = 4
+    w, W, st_chunk, st_seq, toks = _chunk_inputs(T)
+    res = of.chunk_step(w.model, W, st_chunk, toks)
+    for i in range(T):
+        if i:
+            st_seq.token[:] = toks[:, i]
+        r = of.decode_step(w.model, W, st_seq)
+        np.testing.assert_allclose(res.logits[:, i], r.logits, rtol=1e-12, atol=1e-12)
+        for l in range(w.model.L):
+            np.testing.assert_allclose(res.hidden[l][:, i], r.hidden[l], rtol=1e-12, atol=1e-12)
+    for l in range(w.model.L):
+        assert np.array_equal(st_chunk.kcache[l], st_seq.kcache[l])
+        assert np.array_equal(st_chunk.vcache[l], st_seq.vcache[l])
+    assert np.array_equal(st_chunk.pos, st_seq.pos) and np.array_equal(st_chunk.token, st_seq.token)
+    for s in range(w.B):
+        p = int(st_chunk.pos[s])
+        assert np.array_equal(st_chunk.history[s, p - T + 1: p], toks[s, 1:])
+        assert st_chunk.history[s, p] == st_seq.history[s, p]
+
+
+def test_chunk_step_is_causal_and_one_token_is_a_decode_step():
+    # a later token of the chunk never changes an earlier row's logits, and a
+    # one-token chunk is exactly a decode step
+    T = 3
+    w, W, st_a, st_b, toks = _chunk_inputs(T)
+    other = toks.copy()
+    other[:, -1] = (other[:, -1] + 17) % w.model.V
+    ra = of.chunk_step(w.model, W, st_a, toks)
+    rb = of.chunk_step(w.model, W, st_b, other)
+    assert np.array_equal(ra.logits[:, :-1], rb.logits[:, :-1])
+    assert not np.allclose(ra.logits[:, -1], rb.logits[:, -1])
+    w, W, st_c, st_d, toks = _chunk_inputs(1)
+    rc = of.chunk_step(w.model, W, st_c, toks)
+    rd = of.decode_step(w.model, W, st_d)
+    assert np.array_equal(rc.logits[:, 0], rd.logits) and np.array_equal(rc.tokens, rd.tokens)
