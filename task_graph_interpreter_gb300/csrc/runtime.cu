@@ -355,7 +355,8 @@ extern "C" int mk_decode_step_ex(mk_graph* g, void* stream_, int mode, uint32_t 
     case MK_MODE_MEGA: {
       KParams p = base_params(g);
       p.epoch = d->epoch + 1;
-      p.tag = ++d->tag;
+      if (++d->tag == 0) d->tag = 1;  // 0 is the zeroed mirrors' tag: never a step's
+      p.tag = d->tag;
       p.trace = tr;
       CUDA_TRY(launch_interpreter(p, g->B, g->num_ctas, true, stream));
       d->epoch += 1;
