@@ -166,61 +166,107 @@ def algorithmic_bytes(model, B, pos_list):
     return w + kv + new + B * model.V * 4
 
 
-def oracle_sample(workload, repeats=1, seed=0):
-    """Time the CPU oracle on a bounded sample of the workload: one decode
-    step of the model truncated to one decoder layer (full width, full
-    vocabulary, same KV length).  Scaled to the full model by algorithmic
-    bytes, since the float64 oracle is bound by streaming its weights."""
+def blas_threads_env():
+    """Threads the BLAS may use in this process, as its environment sets them
+    (the oracle's widening and elementwise numpy work runs on one thread)."""
+    for k in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(k):
+            return int(os.environ[k])
+    return os.cpu_count() or 1
+
+
+def oracle_steps(workload, steps, warmup, budget_s=None, seed=0):
+    """Greedy decode steps of the float64 CPU oracle on the whole workload
+    (every layer, full width and vocabulary, the workload's KV lengths),
+    timed one by one on this host.  Inputs are generated first (untimed).
+    Runs ``warmup`` untimed steps, then up to ``steps`` timed ones, stopping
+    early once ``budget_s`` seconds of timed work are done.  Returns the
+    per-step seconds."""
     import dataclasses
-    import numpy as np
     import synth
     from oracle import forward as of
     m = workload.model
-    m1 = dataclasses.replace(m, L=1)
-    w1 = dataclasses.replace(workload, model=m1)
-    W = {n: synth.normal_bf16_np(n, shape, mu, sig, seed) for (n, shape, mu, sig) in synth.weight_names(m1)}
-    cap = w1.capacity + repeats + 1
+    w = dataclasses.replace(workload, steps=steps + warmup + 1)
+    W = {n: synth.normal_bf16_np(n, shape, mu, sig, seed) for (n, shape, mu, sig) in synth.weight_names(m)}
+    st = of.initial_state(m, w.B, w.capacity, w.kv_len, synth.prompt_tokens_np(w, seed),
+                          lambda l, k: synth.kv_cache_np(synth.kv_name(l, k), w.B, m.Hkv, w.capacity, m.D,
+                                                         w.kv_len, seed))
+    for _ in range(warmup):
+        of.decode_step(m, W, st, keep_hidden=False)
     times = []
-    for r in range(repeats):
-        st = of.initial_state(m1, w1.B, cap, w1.kv_len, synth.prompt_tokens_np(w1, seed),
-                              lambda l, k: synth.kv_cache_np(synth.kv_name(l, k), w1.B, m1.Hkv, cap, m1.D,
-                                                             w1.kv_len, seed))
+    for _ in range(steps):
         t0 = time.perf_counter()
-        of.decode_step(m1, W, st, keep_hidden=False)
+        of.decode_step(m, W, st, keep_hidden=False)
         times.append(time.perf_counter() - t0)
-    t1 = min(times)
-    full = algorithmic_bytes(m, workload.B, workload.kv_len)
-    part = algorithmic_bytes(m1, workload.B, workload.kv_len)
-    t_step = t1 * full / part
-    threads = os.environ.get("OPENBLAS_NUM_THREADS") or os.environ.get("OMP_NUM_THREADS") or str(os.cpu_count())
+        if budget_s is not None and sum(times) >= budget_s:
+            break
+    return times
+
+
+def oracle_child(config, layers, threads):
+    """Child process of ``cpu_baseline``: one warm-up and one timed full
+    oracle step with the BLAS limited to ``threads`` (set in the environment
+    before numpy loads); prints one JSON line."""
+    import dataclasses
+    import synth
+    w = synth.workload(config)
+    if layers:
+        w = dataclasses.replace(w, model=dataclasses.replace(w.model, L=layers))
+    t = oracle_steps(w, 1, 0)
+    print(json.dumps({"seconds": t[0], "blas_threads": blas_threads_env(), "cpus": os.cpu_count()}), flush=True)
+
+
+def cpu_baseline(args, workload):
+    """The CPU oracle timed on this host: one full greedy decode step of the
+    whole workload (inputs generated first, untimed), with the BLAS on every
+    core and on one core, each in a fresh process."""
+    runs = {}
+    for threads in (os.cpu_count() or 1, 1):
+        env = dict(os.environ, OPENBLAS_NUM_THREADS=str(threads), OMP_NUM_THREADS=str(threads),
+                   MKL_NUM_THREADS=str(threads))
+        cmd = [sys.executable, os.path.abspath(__file__), "--oracle-child", str(threads), "--config", args.config]
+        if args.layers:
+            cmd += ["--layers", str(args.layers)]
+        r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=1200)
+        if r.returncode != 0:
+            raise RuntimeError(f"oracle timing failed:\n{r.stderr[-2000:]}")
+        runs[threads] = json.loads(r.stdout.strip().splitlines()[-1])
+    allc = runs[os.cpu_count() or 1]
+    one = runs[1]
+    m = workload.model
     return {
-        "value": workload.B / t_step,
-        "unit": "tokens/s",
-        "cores": int(threads),
+        "value": workload.B / allc["seconds"], "unit": "tokens/s", "cores": allc["blas_threads"],
         "kind": "oracle",
-        "sample": (f"float64 numpy oracle, one decode step of the {m.name} model truncated to 1 of {m.L} "
-                   f"layers (full width and vocabulary, KV {max(workload.kv_len)}), {t1:.2f} s, scaled by "
-                   f"algorithmic bytes x{full / part:.2f} to the full step"),
-        "seconds_per_step": t_step,
+        "sample": (f"one full greedy decode step of the float64 numpy oracle on the whole {m.name} workload "
+                   f"({m.L} layers, B={workload.B}, KV {max(workload.kv_len)}), timed after generating its "
+                   f"inputs, {allc['seconds']:.2f} s with the BLAS on {allc['blas_threads']} threads of "
+                   f"{allc['cpus']} CPUs (the oracle's bf16 widening runs on one thread)"),
+        "seconds_per_step": allc["seconds"],
+        "one_core": {"value": workload.B / one["seconds"], "unit": "tokens/s", "cores": 1,
+                     "seconds_per_step": one["seconds"]},
     }
 
 
 def run_reference(args, workload):
+    """The reference arm: the CPU oracle, as it stands, on the same workload
+    and metric.  One warm-up step, then full greedy steps until K are timed
+    or about two minutes of timed work are done; the line reports the steps
+    it really timed."""
     rank, ws, _ = dist_env()
     if rank != 0:
         return
-    import numpy as np
-    samples = []
-    for _ in range(args.warmup):
-        oracle_sample(workload, 1)
-    for _ in range(args.steps):
-        samples.append(oracle_sample(workload, 1))
-    v = float(np.median([s["value"] for s in samples]))
-    cb = dict(samples[0])
-    cb["value"] = v
+    warm = min(args.warmup, 1)
+    times = oracle_steps(workload, args.steps, warm, budget_s=120.0)
+    t = sum(times) / len(times)
+    v = workload.B / t
+    m = workload.model
+    cb = {"value": v, "unit": "tokens/s", "cores": blas_threads_env(), "kind": "oracle",
+          "sample": (f"{len(times)} full greedy decode steps of the float64 numpy oracle on the whole {m.name} "
+                     f"workload ({m.L} layers, B={workload.B}, KV {max(workload.kv_len)}) after {warm} warm-up "
+                     f"step(s), BLAS on {blas_threads_env()} threads of {os.cpu_count()} CPUs")}
     line = {
         "impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000.0 * workload.B / v,
+        "steps": len(times), "warmup": warm, "ms_per_step": 1000.0 * t,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": config_dict(args, workload),
         "cpu_baseline": cb, "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -267,7 +313,11 @@ def main():
     ap.add_argument("--no-modes", action="store_true")
     ap.add_argument("--layers", type=int, default=0,
                     help="truncate the model to this many layers (small cases for profiling)")
+    ap.add_argument("--oracle-child", type=int, default=0, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_child:
+        oracle_child(args.config, args.layers, args.oracle_child)
+        return
 
     import dataclasses
     import synth
@@ -375,8 +425,7 @@ def main():
 
     cpu = None
     if not args.no_cpu_baseline and ws == 1:  # the oracle baseline is timed at N=1 only
-        cpu = oracle_sample(base, repeats=2)
-        cpu.pop("seconds_per_step", None)
+        cpu = cpu_baseline(args, base)
 
     traffic = profiled_traffic(args.config)
     line = {

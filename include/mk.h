@@ -139,9 +139,15 @@ typedef struct mk_config {
   uint32_t wait_timeout_us;  /* bound on every device wait; 0 = 2,000,000 */
 } mk_config;
 
-/* Create an empty graph.  Errors: MK_ERR_ABI on a version mismatch,
- * MK_ERR_ARG on negative sizes, MK_ERR_CUDA if num_ctas == 0 and no device
- * can be queried.  Buffer indices 1 and 2 are reserved for the RoPE tables. */
+/* Create an empty graph: the object a decode step is composed on ("mega
+ * kernel initial", 1y33.com, graph-building part: the decoder layer written
+ * as ops called on a Graph object; abi_version is the check the same page
+ * asks for when the descriptor layout on the two sides could drift: the
+ * version is bumped and a mismatch fails loudly).  Errors:
+ * MK_ERR_ABI on a version mismatch, MK_ERR_ARG on negative sizes,
+ * MK_ERR_CUDA if num_ctas == 0 and no device can be queried.  Buffer
+ * indices 1 and 2 are reserved for the RoPE tables; the caller frees the
+ * graph with mk_destroy. */
 int mk_graph_create(const mk_config* cfg, mk_graph** out);
 
 /* Register the decode state as buffer 0: int32 [B, 2], row s = (token the
@@ -236,8 +242,12 @@ int mk_gemv_tiles(const mk_graph* g, int n, int32_t* tiles);
 int mk_scratch_size(const mk_graph* g, uint16_t buf, size_t* bytes);
 
 /* Lower every op to descriptors and edges and build the per-CTA queues;
- * freezes the graph.  Descriptor fields by op (unused in_buf = MK_NO_BUF,
- * unused fields 0):
+ * freezes the graph ("mega kernel initial", 1y33.com, lowering part: each op
+ * becomes 64-byte TaskDescriptors, a matmul fans out into column tiles and
+ * attention into split-KV partials and a combine; and the edge part: every
+ * task's parents are found from the column ranges it reads, flipped into
+ * dependents lists and flattened into one edge array in topological order).
+ * Descriptor fields by op (unused in_buf = MK_NO_BUF, unused fields 0):
  *  RMSNORM  in={x,gamma,residual} out=out m=B n=H flags=FUSED_RESIDUAL (bit 1)
  *           with a residual; reserved={s, float bits of eps}
  *  GEMV     in={x,W,aux} out=y m=B n k; reserved={col_begin, col_count,
@@ -296,8 +306,12 @@ int mk_get_queues(const mk_graph* g, const int32_t** offsets, const int32_t** ta
 
 /* Copy descriptors, edges, queues and the buffer pointer table to the
  * current device, build the RoPE tables (float64 on the host, stored as
- * float), and zero the dependency counters.  Synchronises `stream`.
- * Errors: MK_ERR_STATE (not lowered), MK_ERR_CUDA, MK_ERR_NOMEM. */
+ * float), and zero the dependency counters ("mega kernel initial",
+ * 1y33.com, buffer-table and upload part: one contiguous blob of header,
+ * tasks and edges copied to the device at once, with the table of buffer
+ * pointers beside it).  The blob belongs to the library until mk_destroy.
+ * Synchronises `stream`.  Errors: MK_ERR_STATE (not lowered), MK_ERR_CUDA,
+ * MK_ERR_NOMEM. */
 int mk_upload(mk_graph* g, void* stream);
 
 /* Number of GEMV tiles of an uploaded graph that run on the tensor-core
@@ -310,7 +324,15 @@ int mk_upload(mk_graph* g, void* stream);
  * MK_ERR_ARG. */
 int mk_gemv_tensor_core_tiles(const mk_graph* g, int* tiles);
 
-/* One decode step with the persistent kernel (MK_MODE_MEGA). */
+/* One decode step with the persistent kernel (MK_MODE_MEGA): one CTA per
+ * SM walks its static queue, each task waits only for its own producers
+ * and releases its dependents when done, with no grid-wide barrier
+ * ("Megakernels", runhoid.com, "Hoid's approach to megakernels" and Fig. 5:
+ * the on-GPU interpreter whose blocks wait only for their producers).
+ * Enqueued on `stream`; the caller's registered tensors are read and
+ * written in place (the state advances by one position per sequence).
+ * Errors: MK_ERR_STATE (not uploaded), MK_ERR_CUDA (launch failed); device
+ * failures are read with mk_status. */
 int mk_decode_step(mk_graph* g, void* stream);
 
 /* One decode step in `mode` (MK_MODE_*).  trace != 0 records, per task, the
@@ -341,6 +363,15 @@ int mk_status(mk_graph* g, void* stream, int* dev_code, int32_t* task_id);
  * the consumers reached them. */
 int mk_get_trace(mk_graph* g, const uint64_t** records, size_t* count);
 
+/* Test hook for the wrap-around of the dependency counters: put an uploaded
+ * graph in the state it would have after `epoch` megakernel steps (every
+ * counter at epoch times the adds it receives per step, modulo 2^32) with
+ * `tag` as the last step tag; the next step is then step epoch + 1 with tag
+ * tag + 1 (0 skipped).  Lets a test run steps across the point where
+ * counters and their targets wrap.  Synchronises `stream`.  Errors:
+ * MK_ERR_STATE (not uploaded), MK_ERR_CUDA. */
+int mk_debug_set_epoch(mk_graph* g, void* stream, uint32_t epoch, uint32_t tag);
+
 /* Bytes of shared memory the kernel uses per CTA and its thread count. */
 int mk_kernel_info(const mk_graph* g, int* smem_bytes, int* threads, int* stages);
 
@@ -362,9 +393,12 @@ int mk_kernel_info(const mk_graph* g, int* smem_bytes, int* threads, int* stages
  * library holds until the process exits; a call needing more returns
  * MK_ERR_LIMIT.  No cudaMalloc, cudaFree or other allocation happens here.
  * The first call on a device looks up the array's device address (with that
- * device current); make that first call before any stream capture.  All
- * calls share the array: calls whose kernels overlap on the GPU race.
- * Enqueued on `stream`; errors: MK_ERR_ARG, MK_ERR_LIMIT, MK_ERR_CUDA. */
+ * device current) and keeps it for the life of the process; make that first
+ * call before any stream capture, and do not call cudaDeviceReset after it.
+ * All calls share the array: calls whose kernels overlap on the GPU race.
+ * Enqueued on `stream`; errors: MK_ERR_ARG, MK_ERR_LIMIT, MK_ERR_CUDA (also
+ * when an error from the caller's earlier work is pending: it is reported,
+ * not cleared, and nothing is launched). */
 #define MK_NOALLOC_SCRATCH_FLOATS (1 << 20)
 int mk_attention_decode_noalloc(void* stream, const float* qkv, void* kcache, void* vcache, float* out,
                                 int B, int Hq, int Hkv, int D, int capacity, const int32_t* pos,

@@ -18,7 +18,7 @@ def prompt_tokens_torch(w: Workload, seed: int = 0, device="cpu"):
     return uniform_ints_torch("prompt_token", w.B, 0, w.model.V, seed, device)
 
 
-from .device import kv_name, device_inputs  # noqa: E402
+from .device import kv_name, device_inputs, host_inputs, to_device  # noqa: E402
 
 
 __all__ = [n for n in dir() if not n.startswith("_")]

@@ -33,7 +33,7 @@ EXPORTS = [
     "mk_upload",
     "mk_decode_step", "mk_decode_step_ex", "mk_decode_step_host", "mk_status",
     "mk_get_trace", "mk_kernel_info", "mk_destroy", "mk_last_error", "mk_debug_patch_task",
-    "mk_attention_decode_noalloc", "mk_gemv_tensor_core_tiles",
+    "mk_attention_decode_noalloc", "mk_gemv_tensor_core_tiles", "mk_debug_set_epoch",
 ]
 
 
@@ -89,6 +89,7 @@ def lib():
         "mk_kernel_info": (c_int, [G, POINTER(c_int), POINTER(c_int), POINTER(c_int)]),
         "mk_destroy": (None, [G]),
         "mk_debug_patch_task": (c_int, [G, c_int, c_void_p]),
+        "mk_debug_set_epoch": (c_int, [G, c_void_p, c_uint32, c_uint32]),
         "mk_add_rmsnorm": (c_int, [G, c_uint16, c_uint16, c_uint16, c_uint16, c_int, c_int, c_float]),
         "mk_fuse_rmsnorm": (c_int, [G, POINTER(c_int)]),
         "mk_gemv_tensor_core_tiles": (c_int, [G, POINTER(c_int)]),
@@ -277,6 +278,11 @@ def mk_debug_patch_task(g, task: int, desc: bytes):
     assert len(desc) == 64
     buf = ctypes.create_string_buffer(desc, 64)
     check(lib().mk_debug_patch_task(g, task, buf), "mk_debug_patch_task")
+
+
+def mk_debug_set_epoch(g, stream: int, epoch: int, tag: int):
+    check(lib().mk_debug_set_epoch(g, c_void_p(stream), epoch & 0xFFFFFFFF, tag & 0xFFFFFFFF),
+          "mk_debug_set_epoch")
 
 
 def mk_attention_decode_noalloc(stream: int, qkv: int, kcache: int, vcache: int, out: int, B: int, Hq: int,

@@ -1687,6 +1687,14 @@ __device__ void sample_task(Ctx& c, const mk_task_descriptor& d) {
 // usually none (tagged inputs), one (a whole-group counter or the task's
 // own) or two, taken from the task record.  An abort is noticed while
 // waiting; a task whose counters are already met just runs.
+// Counters and targets are uint32 and wrap (a whole-group counter that
+// gains a few thousand per step wraps after about a million steps), so the
+// test is on the signed difference: at the start of step e a counter holds
+// (e - 1) * count, never more than count < 2^31 below its target.
+__device__ __forceinline__ bool counter_met(const uint32_t* ctr, uint32_t target) {
+  return (int32_t)(ld_acquire(ctr) - target) >= 0;
+}
+
 __device__ bool wait_deps(const KParams& p, const TaskRec* r, int task) {
   const int lane = threadIdx.x & 31;
   const uint32_t w0 = r->w0, nw = r->nw;
@@ -1700,11 +1708,11 @@ __device__ bool wait_deps(const KParams& p, const TaskRec* r, int task) {
       ctr = p.counters + e.x;
       target = p.epoch * e.y;
     }
-    bool done = !mine || ld_acquire(ctr) >= target;
+    bool done = !mine || counter_met(ctr, target);
     if (__all_sync(0xffffffffu, done)) continue;
     const uint64_t t0 = globaltimer();
     for (uint32_t it = 1;; ++it) {
-      if (!done) done = ld_acquire(ctr) >= target;
+      if (!done) done = counter_met(ctr, target);
       if (__all_sync(0xffffffffu, done)) break;
       if ((it & 63u) == 0) {
         if (aborted(p)) return false;

@@ -16,6 +16,10 @@
 // exits.  All calls share it, so calls whose kernels overlap on the GPU (on
 // different streams, or from different threads) race on it.  Every slot a
 // call reads is written by the same call first, so nothing needs clearing.
+// The array's device address is looked up once per device, on the first
+// call with that device current, and kept for the life of the process; a
+// cudaDeviceReset after that first call is not supported (the reloaded
+// module's array may sit elsewhere).
 #include <cuda_runtime.h>
 
 #include <cfloat>
@@ -288,8 +292,14 @@ extern "C" int mk_attention_decode_noalloc(void* stream_, const float* qkv, void
   p.theta = rope_theta;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   const size_t smem = (size_t)(G * D + 2 * D + 8 * 4 * (D + 2)) * sizeof(float);
+  // an error left by the caller's earlier work stays the caller's: report it
+  // without clearing it, and launch nothing
+  cudaError_t e = cudaPeekAtLastError();
+  if (e != cudaSuccess)
+    return fail(MK_ERR_CUDA, std::string("mk_attention_decode_noalloc: an earlier CUDA error is pending: ") +
+                                 cudaGetErrorString(e));
   noalloc_partial_kernel<<<(unsigned)slots, kThreadsNA, smem, stream>>>(p);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess)
     return fail(MK_ERR_CUDA, std::string("mk_attention_decode_noalloc: partial launch: ") + cudaGetErrorString(e));
   noalloc_combine_kernel<<<(unsigned)(B * Hkv), kThreadsNA, 0, stream>>>(p);

@@ -444,6 +444,25 @@ extern "C" int mk_status(mk_graph* g, void* stream_, int* dev_code, int32_t* tas
   return MK_OK;
 }
 
+extern "C" int mk_debug_set_epoch(mk_graph* g, void* stream_, uint32_t epoch, uint32_t tag) {
+  if (!g) return fail(MK_ERR_ARG, "mk_debug_set_epoch: null graph");
+  if (!g->uploaded) return fail(MK_ERR_STATE, "mk_debug_set_epoch: call mk_upload first");
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  DeviceState* d = g->dev;
+  // each counter gains, per step, one add per plan entry that names it
+  std::vector<uint32_t> ctr(d->counter_words, 0u);
+  for (uint32_t c : g->sig) {
+    if (c >= d->counter_words) return fail(MK_ERR_ARG, "mk_debug_set_epoch: plan names a counter out of range");
+    ctr[c] += 1u;
+  }
+  for (uint32_t& c : ctr) c *= epoch;  // modulo 2^32, as the device counters run
+  CUDA_TRY(cudaStreamSynchronize(stream));
+  CUDA_TRY(cudaMemcpy(d->counters, ctr.data(), ctr.size() * 4, cudaMemcpyHostToDevice));
+  d->epoch = epoch;
+  d->tag = tag;
+  return MK_OK;
+}
+
 extern "C" int mk_get_trace(mk_graph* g, const uint64_t** records, size_t* count) {
   if (!g || !records || !count) return fail(MK_ERR_ARG, "mk_get_trace: null argument");
   if (!g->uploaded) return fail(MK_ERR_STATE, "mk_get_trace: call mk_upload first");

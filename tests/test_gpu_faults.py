@@ -137,3 +137,41 @@ def test_trace_respects_every_dependency():
     ev = dec.graph.chrome_trace()["traceEvents"]
     assert sum(e["cat"] == "task" for e in ev) == N
     dec.graph.close()
+
+
+@pytest.mark.parametrize("B", [1, 8])
+def test_steps_across_the_counter_and_tag_wrap(B):
+    # Dependency counters and their targets (epoch x adds per step) are
+    # uint32 and wrap after 2^32 / adds steps, and so does the step tag of
+    # the tagged pairs.  Put the graph a step before the counter that gains
+    # the most per step wraps (and the tag just before 2^32), then run steps
+    # across both wraps: every step must still match the oracle (an unsigned
+    # comparison would let waits pass early once a target wraps).
+    from task_graph_interpreter_gb300 import _lib as L
+    lens = [128, 5, 64, 128, 100, 17, 128, 90][:B]
+    w = synth.custom(synth.TINY, B, lens, 5, name=f"tiny_wrap{B}")
+    dec = build_gpu_wrap(w)
+    n = len(dec.graph.tasks_bytes()) // 64
+    _, _, _, sig, _ = L.mk_get_sync_plan(dec.graph.h, n)
+    adds = int(np.bincount(sig.astype(np.int64)).max())
+    epoch = (2 ** 32 - 1) // adds - 1          # (epoch + 2) * adds passes 2^32
+    s = torch.cuda.current_stream().cuda_stream
+    L.mk_debug_set_epoch(dec.graph.h, s, epoch, 2 ** 32 - 3)
+    W = NpWeights(w.model, 0)
+    st = oracle_state(w, 0)
+    try:
+        for _ in range(4):
+            dec.graph.step()
+            code, task = dec.graph.status()
+            assert code == 0, f"device status {code} at task {task}"
+            res = of.decode_step(w.model, W, st)
+            _, clear = compare_step(dec, res, st)
+            if not clear:
+                break
+    finally:
+        dec.graph.close()
+
+
+def build_gpu_wrap(w):
+    from tests.gpu_common import build_gpu
+    return build_gpu(w, 0, wait_timeout_us=200000)
