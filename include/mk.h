@@ -164,16 +164,37 @@ int mk_set_state(mk_graph* g, void* state_dptr, int B);
 int mk_add_buffer(mk_graph* g, void* dptr, int dtype, int64_t rows, int64_t cols,
                   uint16_t* out_idx);
 
+/* Make every step of this graph a chunk step of T >= 2 tokens per sequence
+ * (a prefill chunk, or draft tokens to verify in speculative decoding):
+ * token t of sequence s sits at position pos[s] + t and attends causally to
+ * the cache and the chunk's earlier tokens.  Activations then have B * T
+ * rows (row s * T + t) and every matmul has m = B * T (at most 8).  Token 0
+ * is the pending token in the state; tokens 1..T-1 are read each step from
+ * `tokens`, a registered int32 [B, T] buffer the caller fills (column 0 is
+ * not read).  SAMPLE takes the argmax of each sequence's last row, writes
+ * tokens 1..T-1 and the sampled token to history[s, pos+1 .. pos+T] and
+ * advances the state by T.  Per-token tasks (the embedding gathers and the
+ * cache appends) carry t in the descriptor's `step` field ("mega kernel
+ * initial", 1y33.com, the TaskDescriptor listing: `step` is the tag of a
+ * speculative draft step); attention descriptors carry T - 1 in the high
+ * half of reserved[2].  Must follow mk_set_state and the registration of
+ * `tokens`, and precede every op.  Errors: MK_ERR_ARG (T < 2, B * T > 8,
+ * tokens not an int32 [B, T] buffer), MK_ERR_STATE (ops already added,
+ * already set, or lowered). */
+int mk_set_chunk(mk_graph* g, int T, uint16_t tokens);
+
 /* Embedding row gather (a MEMCPY task per sequence, our reading: the OpId
  * table lists MEMCPY as a utility and no embedding op):
  * out[s, :] = float(table[state[s].token, :]).  table bf16 [V, H],
- * out f32 [B, H]. */
+ * out f32 [B, H].  In a chunk step (mk_set_chunk) one task per (s, t):
+ * out[s * T + t, :] = float(table[token t of s, :]), out f32 [B * T, H]. */
 int mk_add_embed(mk_graph* g, uint16_t table, uint16_t out, int B, int H);
 
-/* Standalone RMS norm, one RMSNORM task per sequence ("mega kernel
+/* Standalone RMS norm, one RMSNORM task per activation row ("mega kernel
  * initial", OpId table: usually fused into a GEMV, rarely standalone):
- *   y = x (+ residual);  out[s, :] = y / sqrt(mean(y^2) + eps) * gamma.
- * x, residual, out f32 [B, H]; gamma bf16 [1, H]; residual = MK_NO_BUF for
+ *   y = x (+ residual);  out[r, :] = y / sqrt(mean(y^2) + eps) * gamma.
+ * B is the state's batch; x, residual, out f32 [B * T, H] (T = 1 unless
+ * mk_set_chunk); gamma bf16 [1, H]; residual = MK_NO_BUF for
  * none (with one, the task carries FUSED_RESIDUAL, flag bit 1; our reading:
  * only the normalised sum is written).  H a multiple of 8, at most 16384.
  * Errors: MK_ERR_ARG, MK_ERR_STATE. */
@@ -197,7 +218,8 @@ int mk_fuse_rmsnorm(mk_graph* g, int* fused);
  *  pairs MK_PAIR [T, m] (tile-major; T = mk_gemv_tiles(n)) with ARGMAX_EPI, else MK_NO_BUF.
  *  RMS_NORM_INPUT: x_hat = x / sqrt(mean(x^2) + eps) * gamma.
  *  SILU_MUL: out = silu(W_gate x) * (W_up x).  ADD_RESIDUAL: out += residual.
- * Limits: 1 <= m <= 8; k a multiple of 256 and at most 65536.
+ * Limits: m = B * T (the activation rows), 1 <= m <= 8; k a multiple of 256
+ * and at most 65536.
  * Errors: MK_ERR_ARG (shape/dtype mismatch, both RMS_NORM_INPUT and
  * ADD_RESIDUAL, missing pairs), MK_ERR_STATE. */
 int mk_add_matmul(mk_graph* g, uint16_t x, uint16_t w, uint16_t out, uint16_t aux,
@@ -211,6 +233,10 @@ int mk_add_matmul(mk_graph* g, uint16_t x, uint16_t w, uint16_t out, uint16_t au
  *  qkv  f32 [B, (Hq + 2 Hkv) D]: q heads, then k heads, then v heads.
  *  kcache / vcache bf16 [B * Hkv, capacity * D] (= [B, Hkv, capacity, D]).
  *  out  f32 [B, Hq D].     scratch f32 [mk_attention_scratch_rows, G (D + 2)].
+ *  In a chunk step (mk_set_chunk) qkv and out have B * T rows, there is one
+ *  APPEND per (sequence, KV head, token) storing token t's row at pos + t,
+ *  each PARTIAL serves all T tokens (token t sees keys 0 .. pos + t), and
+ *  the scratch has T G (D + 2) columns; (Hq / Hkv) T <= 16.
  *  len0[B]: cached keys per sequence when the graph is built (fixes the chunk
  *  count).  chunk: keys per chunk, 0 = automatic.  D in {64, 128}; Hq/Hkv <= 4;
  *  at most 2048 / (Hq/Hkv) chunks per sequence (MK_ERR_LIMIT beyond).
@@ -223,11 +249,15 @@ int mk_add_attention(mk_graph* g, uint16_t qkv, uint16_t kcache, uint16_t vcache
 
 /* SAMPLE per sequence: token = argmax over the lm_head tiles' pairs (first
  * index on ties); history[s, pos + 1] = token; state[s] = (token, pos + 1).
- * pairs MK_PAIR [T, B] (tile-major), history int32 [B, capacity]. */
+ * pairs MK_PAIR [T, B] (tile-major), history int32 [B, capacity].  In a
+ * chunk step of T tokens the pairs are [tiles, B * T] and the argmax is
+ * taken over row s * T + T - 1; history[s, pos + 1 .. pos + T - 1] gets the
+ * step's input tokens 1..T-1, history[s, pos + T] the sampled token, and
+ * the state becomes (token, pos + T). */
 int mk_add_sample(mk_graph* g, uint16_t pairs, uint16_t history, int B, int V, int capacity);
 
 /* Rows the scratch buffer of mk_add_attention needs (its columns are
- * G * (D + 2) floats). */
+ * T * G * (D + 2) floats, T = 1 unless mk_set_chunk). */
 int mk_attention_scratch_rows(const mk_graph* g, int B, int Hkv, const int32_t* len0,
                               int chunk, int64_t* rows);
 
@@ -259,7 +289,13 @@ int mk_scratch_size(const mk_graph* g, uint16_t buf, size_t* bytes);
  *  COMBINE  in={scratch,K,V} out=att, same m/n/k/kv_len, reserved={s,g,Hkv,P_s,first slot}
  *           (K and V order the append before the attention output)
  *  MEMCPY   in={table} out=h m=B n=H reserved={s, rows of the table}
- *  SAMPLE   in={pairs} out=history m=B n=V k=T kv_len=capacity reserved={s}
+ *  SAMPLE   in={pairs} out=history m=B n=V k=tiles kv_len=capacity reserved={s}
+ * A chunk step of T tokens (mk_set_chunk) changes only: attention tasks
+ * carry Hkv | (T-1) << 16 in reserved[2]; APPEND is one task per token t
+ * with step = t; MEMCPY is one task per (s, t) with step = t, in_buf[1] =
+ * tokens and reserved[2] = T-1; SAMPLE has in_buf[1] = tokens and
+ * reserved[1] = T-1; RMSNORM is one task per activation row, reserved[0] =
+ * the row.  With T = 1 every byte is as above.
  * Errors: MK_ERR_STATE (already lowered or no ops). */
 int mk_lower(mk_graph* g);
 

@@ -15,7 +15,9 @@ builder follows the same convention, so indices agree):
   weights in ``synth.weight_names`` order
   per layer: K cache, V cache ([B*Hkv, cap*D] bf16)
   history [B, cap] int32
+  (chunk steps, T > 1: tokens [B, T] int32, the step's input tokens)
   then activations and scratch as each op allocates its output.
+Activations have B*T rows (row s*T + t); T = 1 is the decode step.
 """
 from __future__ import annotations
 
@@ -26,7 +28,8 @@ BF16, F32, I32, PAIR = 1, 2, 3, 4
 
 
 def llama_decode_spec(model, B: int, len0, cap: int, chunk: int, num_ctas: int,
-                      tiles_target: int = 0, col_align: int = 16, norms: str = "fused") -> dict:
+                      tiles_target: int = 0, col_align: int = 16, norms: str = "fused",
+                      T: int = 1) -> dict:
     """norms: "fused" sets RMS_NORM_INPUT on the GEMVs that consume a norm;
     "standalone" emits each norm as its own op (a fresh output buffer) read
     by a plain GEMV."""
@@ -55,6 +58,8 @@ def llama_decode_spec(model, B: int, len0, cap: int, chunk: int, num_ctas: int,
         reg(f"layer{l}.k_cache", BF16, B * m.Hkv, cap * m.D)
         reg(f"layer{l}.v_cache", BF16, B * m.Hkv, cap * m.D)
     hist = reg("history", I32, B, cap)
+    tok = reg("tokens", I32, B, T) if T > 1 else NO_BUF
+    M = B * T
 
     ops = []
     act = [0]
@@ -64,28 +69,28 @@ def llama_decode_spec(model, B: int, len0, cap: int, chunk: int, num_ctas: int,
         return reg(f"act{act[0]}", dtype, rows, cols)
 
     def matmul(x, w, n, k, aux=NO_BUF, flags=0, eps=0.0, pairs=NO_BUF, out=None):
-        out = fresh(F32, B, n) if out is None else out
+        out = fresh(F32, M, n) if out is None else out
         ops.append(dict(kind="matmul", x=x, w=w, out=out, aux=aux, pairs=pairs,
-                        flags=flags, m=B, n=n, k=k, eps=eps))
+                        flags=flags, m=M, n=n, k=k, eps=eps))
         return out
 
     def normed(x, gamma, flags):
         """(input, aux, flags) of a GEMV that reads RMSNorm(x) * gamma."""
         if norms == "fused":
             return x, gamma, flags | F_RMS_NORM_INPUT
-        xn = fresh(F32, B, m.H)
+        xn = fresh(F32, M, m.H)
         ops.append(dict(kind="rmsnorm", x=x, gamma=gamma, residual=NO_BUF, out=xn, B=B, H=m.H, eps=m.eps))
         return xn, NO_BUF, flags
 
-    h = fresh(F32, B, m.H)
+    h = fresh(F32, M, m.H)
     ops.append(dict(kind="embed", table=idx["embed"], out=h, B=B, H=m.H))
     G = m.Hq // m.Hkv
     P = partials_per_sequence(len0, m.Hkv, chunk, num_ctas)
     for l in range(m.L):
         x, a, f = normed(h, idx[f"layer{l}.attn_norm"], 0)
         qkv = matmul(x, idx[f"layer{l}.wqkv"], m.n_qkv, m.H, aux=a, flags=f, eps=m.eps)
-        scr = fresh(F32, B * m.Hkv * 0 + sum(P) * m.Hkv, G * (m.D + 2))
-        att = fresh(F32, B, m.Hq * m.D)
+        scr = fresh(F32, sum(P) * m.Hkv, T * G * (m.D + 2))
+        att = fresh(F32, M, m.Hq * m.D)
         ops.append(dict(kind="attention", qkv=qkv, k=idx[f"layer{l}.k_cache"],
                         v=idx[f"layer{l}.v_cache"], out=att, scratch=scr, B=B, Hq=m.Hq,
                         Hkv=m.Hkv, D=m.D, capacity=cap, len0=list(len0), chunk=chunk))
@@ -94,13 +99,13 @@ def llama_decode_spec(model, B: int, len0, cap: int, chunk: int, num_ctas: int,
         gu = matmul(x, idx[f"layer{l}.wgu"], m.F, m.H, aux=a, flags=f, eps=m.eps)
         h = matmul(gu, idx[f"layer{l}.wd"], m.H, m.F, aux=h1, flags=F_ADD_RESIDUAL)
     x, a, f = normed(h, idx["final_norm"], F_ARGMAX_EPI)
-    T = len(tiles(m.V, tt, col_align))
-    logits = fresh(F32, B, m.V)
-    pairs = fresh(PAIR, T, B)
+    NT = len(tiles(m.V, tt, col_align))
+    logits = fresh(F32, M, m.V)
+    pairs = fresh(PAIR, NT, M)
     matmul(x, lm, m.V, m.H, aux=a, flags=f, eps=m.eps, pairs=pairs, out=logits)
     ops.append(dict(kind="sample", pairs=pairs, history=hist, B=B, V=m.V, capacity=cap))
     return dict(num_ctas=num_ctas, tiles_target=tiles_target, col_align=col_align,
-                buffers=bufs, ops=ops, names=idx)
+                buffers=bufs, ops=ops, names=idx, T=T, tokens=tok)
 
 
 def fuse_rmsnorm(spec: dict):

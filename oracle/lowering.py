@@ -38,6 +38,18 @@ wait for the append.  COMBINE takes the appended row as an input (its
 in_buf[1..2] are the caches), so the append is complete before the
 attention output is and every reader of the decode state stays an
 ancestor of SAMPLE, which advances it.
+
+Chunk steps (T tokens per sequence per step, a prefill chunk or a batch of
+speculative draft tokens; the TaskDescriptor listing names ``step`` as the
+draft-step tag).  Our reading, byte-identical to the above when T = 1:
+activations have B*T rows (row s*T + t); the embedding gather and the cache
+append become one task per token with ``step`` = t; token t's appended row
+stands as columns [cap*D + t*D, cap*D + (t+1)*D) of its cache block; each
+partial serves the T tokens of its sequence and its scratch slot holds
+T*G*(D+2) floats; attention tasks carry T-1 in the high half of
+reserved[2], the embedding gather in reserved[2], SAMPLE in reserved[1];
+tokens 1..T-1 come from an int32 [B, T] input buffer (in_buf[1] of the
+embedding gathers and of SAMPLE), which no task writes.
 """
 from __future__ import annotations
 
@@ -77,6 +89,33 @@ def tiles(n: int, tiles_target: int, col_align: int):
     """[(col_begin, col_count)] of the GEMV column tiles of an n-column op."""
     w = tile_width(n, tiles_target, col_align)
     return [(c, min(w, n - c)) for c in range(0, n, w)]
+
+
+KSPLIT_BUF = 0xFFFE           # pseudo buffer: the library's K-split scratch records
+KSPLIT_REC = 256 * 8 + 8      # floats per record
+
+
+def ksplit_plan(n: int, k: int, flags: int, m: int, tiles_target: int, col_align: int):
+    """(W, nb, S) of a GEMV op: rows per tile or block, blocks, K splits.
+
+    Our reading for batch >= 8 (tensor-core GEMV tiles, whose every MMA costs
+    the same for up to 256 weight rows): when the usual per-SM tiles are
+    narrow (seg * width < 128 rows; seg = 2 with SILU_MUL, gate and up rows
+    sharing the MMA), the op is cut into blocks of up to 256 / seg rows
+    (ceil(seg * n / 256) blocks, width rounded up to 8) and each block into
+    S = min(k / 64, tiles_target // blocks) consecutive K ranges of whole
+    64-column blocks; S < 2, an argmax epilogue, or m < 8 keep the tiling."""
+    W = tile_width(n, tiles_target, col_align)
+    seg = 2 if flags & F_SILU_MUL else 1
+    plain = (W, ceil_div(n, W), 1)
+    if m < 8 or flags & F_ARGMAX_EPI or seg * W >= 128 or k % 64:
+        return plain
+    nb = ceil_div(seg * n, 256)
+    Wb = ceil_div(ceil_div(n, nb), 8) * 8
+    S = max(1, min(k // 64, tiles_target // ceil_div(n, Wb)))
+    if S < 2:
+        return plain
+    return Wb, ceil_div(n, Wb), S
 
 
 def partials_per_sequence(len0, Hkv: int, chunk: int, num_ctas: int):
@@ -139,9 +178,12 @@ def lower(spec: dict):
     tt = spec.get("tiles_target", 0) or num_ctas
     align = spec.get("col_align", 16)
     bufs = spec["buffers"]
+    T = spec.get("T", 1)                 # tokens per sequence per step
+    tok = spec.get("tokens", NO_BUF)     # int32 [B, T] input tokens (T > 1)
     descs = []       # list of dict fields
     parents = []     # list of sets
     W = _Writes()
+    records = 0      # K-split scratch records assigned so far
 
     def emit(fields, reads, writes):
         t = len(descs)
@@ -158,16 +200,45 @@ def lower(spec: dict):
         if kind == "embed":
             B, H = op["B"], op["H"]
             for s in range(B):
-                emit(dict(op_id=OP_MEMCPY, in_buf=(op["table"], NO_BUF, NO_BUF),
-                          out_buf=op["out"], m=B, n=H,
-                          reserved=(s, bufs[op["table"]][1], 0, 0, 0)),
-                     reads=[(BUF_STATE, s, s + 1, 0, 2)],
-                     writes=[(op["out"], s, s + 1, 0, H)])
+                for t in range(T):
+                    # token 0: the pending token in the state; 1..: the input buffer
+                    src = (BUF_STATE, s, s + 1, 0, 2) if t == 0 else (tok, s, s + 1, t, t + 1)
+                    emit(dict(op_id=OP_MEMCPY, step=t,
+                              in_buf=(op["table"], tok if T > 1 else NO_BUF, NO_BUF),
+                              out_buf=op["out"], m=B, n=H,
+                              reserved=(s, bufs[op["table"]][1], T - 1, 0, 0)),
+                         reads=[src],
+                         writes=[(op["out"], s * T + t, s * T + t + 1, 0, H)])
         elif kind == "matmul":
             B, n, K, fl = op["m"], op["n"], op["k"], op["flags"]
             aux = op.get("aux", NO_BUF)
             pairs = op.get("pairs", NO_BUF)
             eps_bits = f32_bits(op["eps"]) if fl & F_RMS_NORM_INPUT else 0
+            Wb, nb, S = ksplit_plan(n, K, fl, B, tt, align)
+            if S > 1:
+                # split j of a row block multiplies K columns [k0, k1); the
+                # last split adds the others' partial sums (read from their
+                # scratch records, in order) and runs the epilogue
+                KB = K // 64
+                for c0 in range(0, n, Wb):
+                    cn = min(Wb, n - c0)
+                    for j in range(S):
+                        k0, k1 = (j * KB // S) * 64, ((j + 1) * KB // S) * 64
+                        reads = [(op["x"], 0, B, k0, k1)]
+                        if j + 1 < S:
+                            writes = [(KSPLIT_BUF, records + j, records + j + 1, 0, KSPLIT_REC)]
+                        else:
+                            reads.append((KSPLIT_BUF, records, records + j, 0, KSPLIT_REC))
+                            if fl & F_ADD_RESIDUAL:
+                                reads.append((aux, 0, B, c0, c0 + cn))
+                            writes = [(op["out"], 0, B, c0, c0 + cn)]
+                        emit(dict(op_id=OP_GEMV, config_id=1, flags=fl,
+                                  in_buf=(op["x"], op["w"], aux), out_buf=op["out"],
+                                  m=B, n=n, k=K, kv_len=j | (S << 16),
+                                  reserved=(c0, cn, eps_bits, k0 | ((k1 - k0) << 16), records + j)),
+                             reads, writes)
+                    records += S
+                continue
             for t, (c0, cn) in enumerate(tiles(n, tt, align)):
                 reads = [(op["x"], 0, B, 0, K)]
                 if fl & F_ADD_RESIDUAL:
@@ -194,50 +265,56 @@ def lower(spec: dict):
                 base.append([acc + g * P[s] for g in range(Hkv)])
                 acc += Hkv * P[s]
             common = dict(m=B, n=D, k=Hq, kv_len=cap)
+            hkv_t = Hkv | ((T - 1) << 16)
+            rec = T * G * (D + 2)            # floats of one scratch slot
+            new0, new1 = cap * D, cap * D + T * D   # the columns standing for this step's rows
             for s in range(B):
                 for g in range(Hkv):
                     kcol = Hq * D + g * D
                     vcol = (Hq + Hkv) * D + g * D
                     row = s * Hkv + g
-                    emit(dict(op_id=OP_ATT_APPEND, config_id=cfg, in_buf=(qkv, kc, vc),
-                              out_buf=kc, reserved=(s, g, Hkv, 0, 0), **common),
-                         reads=[(qkv, s, s + 1, kcol, kcol + D),
-                                (qkv, s, s + 1, vcol, vcol + D),
-                                (BUF_STATE, s, s + 1, 0, 2)],
-                         writes=[(kc, row, row + 1, cap * D, cap * D + D),
-                                 (vc, row, row + 1, cap * D, cap * D + D)])
+                    for t in range(T):
+                        r = s * T + t
+                        emit(dict(op_id=OP_ATT_APPEND, config_id=cfg, step=t, in_buf=(qkv, kc, vc),
+                                  out_buf=kc, reserved=(s, g, hkv_t, 0, 0), **common),
+                             reads=[(qkv, r, r + 1, kcol, kcol + D),
+                                    (qkv, r, r + 1, vcol, vcol + D),
+                                    (BUF_STATE, s, s + 1, 0, 2)],
+                             writes=[(kc, row, row + 1, new0 + t * D, new0 + (t + 1) * D),
+                                     (vc, row, row + 1, new0 + t * D, new0 + (t + 1) * D)])
             for s in range(B):
                 for g in range(Hkv):
                     row = s * Hkv + g
+                    r0, r1 = s * T, s * T + T
                     for c in range(P[s]):
                         slot = base[s][g] + c
                         emit(dict(op_id=OP_ATT_PARTIAL, config_id=cfg, in_buf=(qkv, kc, vc),
                                   out_buf=scr,
-                                  reserved=(s, g, Hkv, c | (P[s] << 16), base[s][g]),
+                                  reserved=(s, g, hkv_t, c | (P[s] << 16), base[s][g]),
                                   **common),
-                             reads=[(qkv, s, s + 1, g * G * D, (g + 1) * G * D),
-                                    (qkv, s, s + 1, Hq * D + g * D, Hq * D + (g + 1) * D),
-                                    (qkv, s, s + 1, (Hq + Hkv) * D + g * D, (Hq + Hkv) * D + (g + 1) * D),
+                             reads=[(qkv, r0, r1, g * G * D, (g + 1) * G * D),
+                                    (qkv, r0, r1, Hq * D + g * D, Hq * D + (g + 1) * D),
+                                    (qkv, r0, r1, (Hq + Hkv) * D + g * D, (Hq + Hkv) * D + (g + 1) * D),
                                     (kc, row, row + 1, 0, cap * D),
                                     (vc, row, row + 1, 0, cap * D),
                                     (BUF_STATE, s, s + 1, 0, 2)],
-                             writes=[(scr, slot, slot + 1, 0, G * (D + 2))])
+                             writes=[(scr, slot, slot + 1, 0, rec)])
             for s in range(B):
                 for g in range(Hkv):
                     row = s * Hkv + g
                     emit(dict(op_id=OP_ATT_COMBINE, config_id=cfg,
                               in_buf=(scr, kc, vc), out_buf=out,
-                              reserved=(s, g, Hkv, P[s], base[s][g]), **common),
-                         reads=[(scr, base[s][g], base[s][g] + P[s], 0, G * (D + 2)),
-                                (kc, row, row + 1, cap * D, cap * D + D),
-                                (vc, row, row + 1, cap * D, cap * D + D)],
-                         writes=[(out, s, s + 1, g * G * D, (g + 1) * G * D)])
+                              reserved=(s, g, hkv_t, P[s], base[s][g]), **common),
+                         reads=[(scr, base[s][g], base[s][g] + P[s], 0, rec),
+                                (kc, row, row + 1, new0, new1),
+                                (vc, row, row + 1, new0, new1)],
+                         writes=[(out, s * T, s * T + T, g * G * D, (g + 1) * G * D)])
         elif kind == "rmsnorm":
             # standalone RMS norm per sequence (OpId table: usually fused,
             # rarely standalone); a residual makes it FUSED_RESIDUAL (bit 1)
             B, H = op["B"], op["H"]
             res = op.get("residual", NO_BUF)
-            for s in range(B):
+            for s in range(B * T):          # one task per activation row
                 reads = [(op["x"], s, s + 1, 0, H)]
                 if res != NO_BUF:
                     reads.append((res, s, s + 1, 0, H))
@@ -247,12 +324,16 @@ def lower(spec: dict):
                      reads, writes=[(op["out"], s, s + 1, 0, H)])
         elif kind == "sample":
             B, V, cap = op["B"], op["V"], op["capacity"]
-            T = len(tiles(V, tt, align))
+            NT = len(tiles(V, tt, align))
             for s in range(B):
-                emit(dict(op_id=OP_SAMPLE, in_buf=(op["pairs"], NO_BUF, NO_BUF),
-                          out_buf=op["history"], m=B, n=V, k=T, kv_len=cap,
-                          reserved=(s, 0, 0, 0, 0)),
-                     reads=[(op["pairs"], 0, T, s, s + 1), (BUF_STATE, s, s + 1, 0, 2)],
+                last = s * T + T - 1        # the sequence's last row decides the next token
+                reads = [(op["pairs"], 0, NT, last, last + 1), (BUF_STATE, s, s + 1, 0, 2)]
+                if T > 1:
+                    reads.append((tok, s, s + 1, 0, T))
+                emit(dict(op_id=OP_SAMPLE, in_buf=(op["pairs"], tok if T > 1 else NO_BUF, NO_BUF),
+                          out_buf=op["history"], m=B, n=V, k=NT, kv_len=cap,
+                          reserved=(s, T - 1, 0, 0, 0)),
+                     reads=reads,
                      writes=[(op["history"], s, s + 1, 0, cap),
                              (BUF_STATE, s, s + 1, 0, 2)])
         else:
@@ -271,7 +352,7 @@ def lower(spec: dict):
         d = tasks[t]
         d["op_id"] = f["op_id"]
         d["config_id"] = f.get("config_id", 0)
-        d["step"] = 0
+        d["step"] = f.get("step", 0)
         d["flags"] = f.get("flags", 0)
         d["remaining_deps"] = len(parents[t])
         d["num_dependents"] = len(children[t])

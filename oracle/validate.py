@@ -19,7 +19,11 @@ lowered graph and that the interpreter's correctness rests on:
   later.
 
 Access rectangles are decoded from the descriptor fields alone, by code
-separate from the lowering that produced them.
+separate from the lowering that produced them.  A chunk step of T tokens per
+sequence is read from the fields that carry T - 1 (reserved[2] of the
+embedding gathers, the high half of reserved[2] of attention tasks,
+reserved[1] of SAMPLE); ``step`` must be the token index of the per-token
+tasks (embedding gathers and cache appends) and 0 everywhere else.
 """
 from __future__ import annotations
 
@@ -28,7 +32,8 @@ from collections import defaultdict
 import numpy as np
 
 from .lowering import (OP_MEMCPY, OP_GEMV, OP_RMSNORM, OP_SAMPLE, OP_ATT_APPEND, OP_ATT_PARTIAL,
-                       OP_ATT_COMBINE, F_ADD_RESIDUAL, F_ARGMAX_EPI, NO_BUF, BUF_STATE)
+                       OP_ATT_COMBINE, F_ADD_RESIDUAL, F_ARGMAX_EPI, NO_BUF, BUF_STATE, KSPLIT_BUF,
+                       KSPLIT_REC)
 
 
 class ValidationError(AssertionError):
@@ -43,16 +48,35 @@ def task_accesses(d) -> tuple:
     rs = [int(x) for x in d["reserved"]]
     m, n, k, kv = int(d["m"]), int(d["n"]), int(d["k"]), int(d["kv_len"])
     R, Wr = [], []
+    step = int(d["step"])
     if op == OP_MEMCPY:
-        s = rs[0]
-        R.append((BUF_STATE, s, s + 1, 0, 2))
-        Wr.append((ob, s, s + 1, 0, n))
+        s, T = rs[0], rs[2] + 1
+        if step >= T:
+            raise ValidationError(f"embedding gather with step {step} >= T {T}")
+        R.append((BUF_STATE, s, s + 1, 0, 2) if step == 0 else (ib[1], s, s + 1, step, step + 1))
+        Wr.append((ob, s * T + step, s * T + step + 1, 0, n))
     elif op == OP_RMSNORM:
         s = rs[0]
         R.append((ib[0], s, s + 1, 0, n))
         if int(d["flags"]) & F_ADD_RESIDUAL:
             R.append((ib[2], s, s + 1, 0, n))
         Wr.append((ob, s, s + 1, 0, n))
+    elif op == OP_GEMV and int(d["config_id"]) == 1 and (kv >> 16) >= 2:
+        # split j of a K-split row block: its K range of x; the last split
+        # reads the others' scratch records and writes the block's outputs
+        c0, cn = rs[0], rs[1]
+        S, j = kv >> 16, kv & 0xFFFF
+        k0, kn = rs[3] & 0xFFFF, rs[3] >> 16
+        if j >= S or kn <= 0 or k0 + kn > k:
+            raise ValidationError(f"bad K split {j}/{S} [{k0}, {k0 + kn}) of K {k}")
+        R.append((ib[0], 0, m, k0, k0 + kn))
+        if j + 1 < S:
+            Wr.append((KSPLIT_BUF, rs[4], rs[4] + 1, 0, KSPLIT_REC))
+        else:
+            R.append((KSPLIT_BUF, rs[4] - j, rs[4], 0, KSPLIT_REC))
+            if int(d["flags"]) & F_ADD_RESIDUAL:
+                R.append((ib[2], 0, m, c0, c0 + cn))
+            Wr.append((ob, 0, m, c0, c0 + cn))
     elif op == OP_GEMV:
         c0, cn = rs[0], rs[1]
         R.append((ib[0], 0, m, 0, k))
@@ -63,39 +87,50 @@ def task_accesses(d) -> tuple:
             # the tile writes its (max, index) pairs into column reserved[4]
             Wr.append((rs[3], rs[4], rs[4] + 1, 0, m))
     elif op in (OP_ATT_APPEND, OP_ATT_PARTIAL, OP_ATT_COMBINE):
-        s, g, Hkv = rs[0], rs[1], rs[2]
+        s, g, Hkv, T = rs[0], rs[1], rs[2] & 0xFFFF, (rs[2] >> 16) + 1
         D, Hq, cap = n, k, kv
         G = Hq // Hkv
         row = s * Hkv + g
+        q0, q1 = s * T, s * T + T           # the sequence's activation rows
         if op == OP_ATT_APPEND:
-            R += [(ib[0], s, s + 1, Hq * D + g * D, Hq * D + (g + 1) * D),
-                  (ib[0], s, s + 1, (Hq + Hkv) * D + g * D, (Hq + Hkv) * D + (g + 1) * D),
+            if step >= T:
+                raise ValidationError(f"append with step {step} >= T {T}")
+            r = s * T + step
+            R += [(ib[0], r, r + 1, Hq * D + g * D, Hq * D + (g + 1) * D),
+                  (ib[0], r, r + 1, (Hq + Hkv) * D + g * D, (Hq + Hkv) * D + (g + 1) * D),
                   (BUF_STATE, s, s + 1, 0, 2)]
-            # the appended row: columns [cap*D, cap*D + D) of the (s, g) block
-            Wr += [(ib[1], row, row + 1, cap * D, cap * D + D), (ib[2], row, row + 1, cap * D, cap * D + D)]
+            # token t's row: columns [cap*D + t*D, cap*D + (t+1)*D) of the (s, g) block
+            a0 = cap * D + step * D
+            Wr += [(ib[1], row, row + 1, a0, a0 + D), (ib[2], row, row + 1, a0, a0 + D)]
         elif op == OP_ATT_PARTIAL:
             c, P = rs[3] & 0xFFFF, rs[3] >> 16
             assert c < P
             slot = rs[4] + c
             # q, k and v of the group from qkv; the cache rows of earlier
             # steps (columns [0, cap*D)), carried in from the previous step
-            R += [(ib[0], s, s + 1, g * G * D, (g + 1) * G * D),
-                  (ib[0], s, s + 1, Hq * D + g * D, Hq * D + (g + 1) * D),
-                  (ib[0], s, s + 1, (Hq + Hkv) * D + g * D, (Hq + Hkv) * D + (g + 1) * D),
+            R += [(ib[0], q0, q1, g * G * D, (g + 1) * G * D),
+                  (ib[0], q0, q1, Hq * D + g * D, Hq * D + (g + 1) * D),
+                  (ib[0], q0, q1, (Hq + Hkv) * D + g * D, (Hq + Hkv) * D + (g + 1) * D),
                   (ib[1], row, row + 1, 0, cap * D, True), (ib[2], row, row + 1, 0, cap * D, True),
                   (BUF_STATE, s, s + 1, 0, 2)]
-            Wr.append((ob, slot, slot + 1, 0, G * (D + 2)))
+            Wr.append((ob, slot, slot + 1, 0, T * G * (D + 2)))
         else:
             P, base = rs[3], rs[4]
-            R.append((ib[0], base, base + P, 0, G * (D + 2)))
-            R += [(ib[1], row, row + 1, cap * D, cap * D + D), (ib[2], row, row + 1, cap * D, cap * D + D)]
-            Wr.append((ob, s, s + 1, g * G * D, (g + 1) * G * D))
+            R.append((ib[0], base, base + P, 0, T * G * (D + 2)))
+            R += [(ib[1], row, row + 1, cap * D, cap * D + T * D),
+                  (ib[2], row, row + 1, cap * D, cap * D + T * D)]
+            Wr.append((ob, q0, q1, g * G * D, (g + 1) * G * D))
     elif op == OP_SAMPLE:
-        s = rs[0]
-        R += [(ib[0], 0, k, s, s + 1), (BUF_STATE, s, s + 1, 0, 2)]
+        s, T = rs[0], rs[1] + 1
+        last = s * T + T - 1
+        R += [(ib[0], 0, k, last, last + 1), (BUF_STATE, s, s + 1, 0, 2)]
+        if T > 1:
+            R.append((ib[1], s, s + 1, 0, T))
         Wr += [(ob, s, s + 1, 0, kv), (BUF_STATE, s, s + 1, 0, 2)]
     else:
         raise ValidationError(f"unknown op_id {op}")
+    if op not in (OP_MEMCPY, OP_ATT_APPEND) and step != 0:
+        raise ValidationError(f"op {op} with step {step}: only per-token tasks carry a step")
     return R, Wr
 
 
@@ -133,8 +168,6 @@ def validate(tasks: np.ndarray, edges: np.ndarray, check_hazards: bool = True) -
     for t in range(N):
         if len(parents[t]) != deps[t]:
             raise ValidationError(f"task {t}: remaining_deps {deps[t]} != {len(parents[t])} parents")
-        if int(tasks["step"][t]) != 0:
-            raise ValidationError("step field must be 0")
     level = np.zeros(N, dtype=np.int64)
     for t in range(N):
         if parents[t]:

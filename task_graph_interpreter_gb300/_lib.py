@@ -33,7 +33,7 @@ EXPORTS = [
     "mk_upload",
     "mk_decode_step", "mk_decode_step_ex", "mk_decode_step_host", "mk_status",
     "mk_get_trace", "mk_kernel_info", "mk_destroy", "mk_last_error", "mk_debug_patch_task",
-    "mk_attention_decode_noalloc", "mk_gemv_tensor_core_tiles", "mk_debug_set_epoch",
+    "mk_attention_decode_noalloc", "mk_gemv_tensor_core_tiles", "mk_debug_set_epoch", "mk_set_chunk",
 ]
 
 
@@ -63,6 +63,7 @@ def lib():
     sig = {
         "mk_graph_create": (c_int, [POINTER(MkConfig), POINTER(c_void_p)]),
         "mk_set_state": (c_int, [G, c_void_p, c_int]),
+        "mk_set_chunk": (c_int, [G, c_int, c_uint16]),
         "mk_add_buffer": (c_int, [G, c_void_p, c_int, c_int64, c_int64, POINTER(c_uint16)]),
         "mk_add_embed": (c_int, [G, c_uint16, c_uint16, c_int, c_int]),
         "mk_add_matmul": (c_int, [G, c_uint16, c_uint16, c_uint16, c_uint16, c_uint16, c_uint32,
@@ -122,6 +123,10 @@ def mk_graph_create(num_ctas=0, tiles_target=0, col_align=16, wait_timeout_us=0,
 
 def mk_set_state(g, dptr: int, B: int):
     check(lib().mk_set_state(g, c_void_p(dptr), B), "mk_set_state")
+
+
+def mk_set_chunk(g, T: int, tokens: int):
+    check(lib().mk_set_chunk(g, T, tokens), "mk_set_chunk")
 
 
 def mk_add_buffer(g, dptr: int, dtype: int, rows: int, cols: int) -> int:

@@ -51,6 +51,30 @@ int tile_count(int n, int tiles_target, int col_align) {
   return (int)cdiv(n, tile_width(n, tiles_target, col_align));
 }
 
+// Batch >= 8 GEMVs run on tensor cores, where every MMA instruction costs
+// the same whatever its N (up to 256 weight rows): a tile must put as many
+// rows as it can into each MMA.  When the per-SM tiles are narrow (seg *
+// width < 128 rows, seg = 2 for SiLU*mul's stacked gate and up rows), the op
+// is cut instead into row blocks of up to 256 / seg rows, each split into S
+// consecutive K ranges (in 64-column blocks) so that blocks * S stays within
+// tiles_target.  Split j of a block multiplies its K range only; the last
+// split adds the others' partial sums, in order, and runs the epilogue.
+// Ops with an argmax epilogue are never split.
+KSplit ksplit_plan(int n, int k, uint32_t flags, int m, int tiles_target, int col_align) {
+  KSplit r{tile_width(n, tiles_target, col_align), 1, 1};
+  r.nb = (int)cdiv(n, r.W);
+  const int seg = (flags & MK_F_SILU_MUL) ? 2 : 1;
+  if (m < 8 || (flags & MK_F_ARGMAX_EPI) || seg * r.W >= 128 || k % 64) return r;
+  const int nb = (int)cdiv((int64_t)seg * n, 256);
+  const int W = (int)(cdiv(cdiv(n, nb), 8) * 8);
+  const int S = std::max(1, std::min(k / 64, tiles_target / (int)cdiv(n, W)));
+  if (S < 2) return r;
+  r.W = W;
+  r.nb = (int)cdiv(n, W);
+  r.S = S;
+  return r;
+}
+
 // Split-KV chunk count per sequence, fixed at lowering time.  chunk > 0:
 // ceil(len0 / chunk).  chunk == 0: chunks of about
 // E = max(128, ceil(Hkv * sum(len0) / num_ctas)) keys, so that the partials
@@ -146,6 +170,20 @@ extern "C" int mk_add_buffer(mk_graph* g, void* dptr, int dtype, int64_t rows, i
   return MK_OK;
 }
 
+extern "C" int mk_set_chunk(mk_graph* g, int T, uint16_t tokens) {
+  if (!g) return fail(MK_ERR_ARG, "mk_set_chunk: null graph");
+  if (g->lowered) return fail(MK_ERR_STATE, "mk_set_chunk: graph already lowered");
+  if (!g->state_set) return fail(MK_ERR_STATE, "mk_set_chunk: call mk_set_state first");
+  if (!g->ops.empty() || g->T != 1) return fail(MK_ERR_STATE, "mk_set_chunk: must precede every op, once");
+  if (T < 2 || g->B * T > 8) return fail(MK_ERR_ARG, "mk_set_chunk: need T >= 2 and B * T <= 8");
+  if (tokens >= g->bufs.size() || tokens < 3 || g->bufs[tokens].dtype != MK_I32 || g->bufs[tokens].rows != g->B ||
+      g->bufs[tokens].cols != T)
+    return fail(MK_ERR_ARG, "mk_set_chunk: tokens must be a registered int32 [B, T] buffer");
+  g->T = T;
+  g->tokens = tokens;
+  return MK_OK;
+}
+
 static int check_buf(const mk_graph* g, uint16_t idx, int dtype, int64_t rows, int64_t cols,
                      const char* what) {
   if (idx >= g->bufs.size() || idx < 3)
@@ -177,7 +215,7 @@ extern "C" int mk_add_embed(mk_graph* g, uint16_t table, uint16_t out, int B, in
   CHECK(add_common(g, "mk_add_embed"));
   if (B != g->B || H <= 0 || H % 8) return fail(MK_ERR_ARG, "mk_add_embed: B must equal the state's B, H a multiple of 8");
   CHECK(check_buf(g, table, MK_BF16, -1, H, "mk_add_embed table"));
-  CHECK(check_buf(g, out, MK_F32, B, H, "mk_add_embed out"));
+  CHECK(check_buf(g, out, MK_F32, g->rows(), H, "mk_add_embed out"));
   OpRec op{K_EMBED};
   op.a[0] = table;
   op.a[1] = out;
@@ -193,10 +231,11 @@ extern "C" int mk_add_rmsnorm(mk_graph* g, uint16_t x, uint16_t gamma, uint16_t 
   if (B != g->B || H <= 0 || H % 8 || H > 16384)
     return fail(MK_ERR_ARG, "mk_add_rmsnorm: B must equal the state's B, H a multiple of 8 up to 16384");
   if (!std::isfinite(eps) || eps < 0.f) return fail(MK_ERR_ARG, "mk_add_rmsnorm: eps must be finite and >= 0");
-  CHECK(check_buf(g, x, MK_F32, B, H, "mk_add_rmsnorm x"));
+  const int M = g->rows();
+  CHECK(check_buf(g, x, MK_F32, M, H, "mk_add_rmsnorm x"));
   CHECK(check_buf(g, gamma, MK_BF16, 1, H, "mk_add_rmsnorm gamma"));
-  CHECK(check_buf(g, out, MK_F32, B, H, "mk_add_rmsnorm out"));
-  if (residual != MK_NO_BUF) CHECK(check_buf(g, residual, MK_F32, B, H, "mk_add_rmsnorm residual"));
+  CHECK(check_buf(g, out, MK_F32, M, H, "mk_add_rmsnorm out"));
+  if (residual != MK_NO_BUF) CHECK(check_buf(g, residual, MK_F32, M, H, "mk_add_rmsnorm residual"));
   if (out == x || out == residual) return fail(MK_ERR_ARG, "mk_add_rmsnorm: out must not alias an input");
   OpRec op{K_RMSNORM};
   op.a[0] = x;
@@ -268,7 +307,8 @@ extern "C" int mk_add_matmul(mk_graph* g, uint16_t x, uint16_t w, uint16_t out, 
     return fail(MK_ERR_ARG, "mk_add_matmul: unknown flag bits");
   if ((flags & MK_F_RMS_NORM_INPUT) && (flags & MK_F_ADD_RESIDUAL))
     return fail(MK_ERR_ARG, "mk_add_matmul: RMS_NORM_INPUT and ADD_RESIDUAL share the aux slot");
-  if (m < 1 || m > 8 || m != g->B) return fail(MK_ERR_ARG, "mk_add_matmul: need 1 <= m <= 8 and m == B");
+  if (m < 1 || m > 8 || m != g->rows())
+    return fail(MK_ERR_ARG, "mk_add_matmul: need 1 <= m <= 8 and m == B * T (the activation rows)");
   if (n < 1) return fail(MK_ERR_ARG, "mk_add_matmul: n must be positive");
   if (k < 256 || k % 256 || k > 65536) return fail(MK_ERR_ARG, "mk_add_matmul: k must be a multiple of 256 in [256, 65536]");
   if (!std::isfinite(eps) || eps < 0.f) return fail(MK_ERR_ARG, "mk_add_matmul: eps must be finite and >= 0");
@@ -326,7 +366,7 @@ extern "C" int mk_scratch_size(const mk_graph* g, uint16_t buf, size_t* bytes) {
       const auto P = partials_per_sequence(op.len0, op.Hkv, op.chunk, g->num_ctas);
       size_t rows = 0;
       for (int q : P) rows += (size_t)q * op.Hkv;
-      need = std::max(need, rows * (size_t)(op.Hq / op.Hkv) * (size_t)(op.D + 2) * 4);
+      need = std::max(need, rows * (size_t)g->T * (size_t)(op.Hq / op.Hkv) * (size_t)(op.D + 2) * 4);
       used = true;
     }
     if (op.kind == K_MATMUL && op.a[4] == buf && buf != MK_NO_BUF) {
@@ -356,11 +396,12 @@ extern "C" int mk_add_attention(mk_graph* g, uint16_t qkv, uint16_t kcache, uint
     if (len0[s] < 0 || len0[s] >= capacity) return fail(MK_ERR_ARG, "mk_add_attention: len0 out of [0, capacity)");
   if (g->rope_D && (g->rope_D != D || g->rope_theta != rope_theta || g->rope_cap != capacity))
     return fail(MK_ERR_ARG, "mk_add_attention: every attention op must share D, rope_theta and capacity");
-  const int G = Hq / Hkv;
-  CHECK(check_buf(g, qkv, MK_F32, B, (int64_t)(Hq + 2 * Hkv) * D, "mk_add_attention qkv"));
+  const int G = Hq / Hkv, M = g->rows();
+  if (G * g->T > 16) return fail(MK_ERR_ARG, "mk_add_attention: need (Hq / Hkv) * T <= 16");
+  CHECK(check_buf(g, qkv, MK_F32, M, (int64_t)(Hq + 2 * Hkv) * D, "mk_add_attention qkv"));
   CHECK(check_buf(g, kcache, MK_BF16, (int64_t)B * Hkv, (int64_t)capacity * D, "mk_add_attention kcache"));
   CHECK(check_buf(g, vcache, MK_BF16, (int64_t)B * Hkv, (int64_t)capacity * D, "mk_add_attention vcache"));
-  CHECK(check_buf(g, out, MK_F32, B, (int64_t)Hq * D, "mk_add_attention out"));
+  CHECK(check_buf(g, out, MK_F32, M, (int64_t)Hq * D, "mk_add_attention out"));
   {
     // a combine task stages 3 floats per (partial, head) in its shared scratch
     std::vector<int32_t> l(len0, len0 + B);
@@ -370,7 +411,7 @@ extern "C" int mk_add_attention(mk_graph* g, uint16_t qkv, uint16_t kcache, uint
   }
   int64_t need = 0;
   CHECK(mk_attention_scratch_rows(g, B, Hkv, len0, chunk, &need));
-  CHECK(check_buf(g, scratch, MK_F32, -1, (int64_t)G * (D + 2), "mk_add_attention scratch"));
+  CHECK(check_buf(g, scratch, MK_F32, -1, (int64_t)g->T * G * (D + 2), "mk_add_attention scratch"));
   if (g->bufs[scratch].rows < need)
     return fail(MK_ERR_ARG, "mk_add_attention: scratch needs " + std::to_string(need) + " rows");
   if (kcache == vcache) return fail(MK_ERR_ARG, "mk_add_attention: kcache and vcache must differ");
@@ -388,7 +429,8 @@ extern "C" int mk_add_attention(mk_graph* g, uint16_t qkv, uint16_t kcache, uint
 extern "C" int mk_add_sample(mk_graph* g, uint16_t pairs, uint16_t history, int B, int V, int capacity) {
   CHECK(add_common(g, "mk_add_sample"));
   if (B != g->B || V < 1 || capacity < 2) return fail(MK_ERR_ARG, "mk_add_sample: bad B, V or capacity");
-  CHECK(check_buf(g, pairs, MK_PAIR, tile_count(V, g->tiles_target, g->col_align), B, "mk_add_sample pairs"));
+  CHECK(check_buf(g, pairs, MK_PAIR, tile_count(V, g->tiles_target, g->col_align), g->rows(),
+                  "mk_add_sample pairs"));
   CHECK(check_buf(g, history, MK_I32, B, capacity, "mk_add_sample history"));
   OpRec op{K_SAMPLE};
   op.a[0] = pairs; op.a[1] = history;
@@ -412,22 +454,24 @@ struct Writer {
 
 struct Lowerer {
   mk_graph* g;
-  std::vector<std::vector<Writer>> writes;  // per buffer
+  std::vector<std::vector<Writer>> writes;  // per buffer (and the K-split scratch, last)
   std::vector<std::vector<int>> parents;
   std::vector<double> cost;                  // bytes-equivalent estimate per task
 
-  explicit Lowerer(mk_graph* gr) : g(gr), writes(gr->bufs.size()) {}
+  explicit Lowerer(mk_graph* gr) : g(gr), writes(gr->bufs.size() + 1) {}
+
+  std::vector<Writer>& at(int buf) { return buf == (int)kKsplitBuf ? writes.back() : writes[buf]; }
 
   int emit(const mk_task_descriptor& d, const std::vector<Rect>& reads, const std::vector<Rect>& wr,
            double c) {
     int t = (int)g->tasks.size();
     std::vector<int> ps;
     for (const Rect& r : reads)
-      for (const Writer& w : writes[r.buf])
+      for (const Writer& w : at(r.buf))
         if (w.r0 < r.r1 && r.r0 < w.r1 && w.c0 < r.c1 && r.c0 < w.c1) ps.push_back(w.task);
     std::sort(ps.begin(), ps.end());
     ps.erase(std::unique(ps.begin(), ps.end()), ps.end());
-    for (const Rect& r : wr) writes[r.buf].push_back(Writer{t, r.r0, r.r1, r.c0, r.c1});
+    for (const Rect& r : wr) at(r.buf).push_back(Writer{t, r.r0, r.r1, r.c0, r.c1});
     g->tasks.push_back(d);
     parents.push_back(std::move(ps));
     cost.push_back(c);
@@ -460,28 +504,80 @@ extern "C" int mk_lower(mk_graph* g) {
   if (g->lowered) return fail(MK_ERR_STATE, "mk_lower: already lowered");
   if (g->ops.empty()) return fail(MK_ERR_STATE, "mk_lower: no ops");
   Lowerer L(g);
+  g->ksplit_records = 0;
   const int tt = g->tiles_target, al = g->col_align;
+  const int T = g->T;  // tokens per sequence per step; activation row s * T + t
   g->group_off.clear();
   for (const OpRec& op : g->ops) {
     switch (op.kind) {
       case K_EMBED: {
+        // one row gather per (sequence, token of the step): token 0 is the
+        // pending token in the state, tokens 1.. come from the tokens buffer
         g->group_off.push_back((int)g->tasks.size());
-        for (int s = 0; s < op.B; ++s) {
-          mk_task_descriptor d = blank(MK_OP_MEMCPY);
-          d.in_buf[0] = op.a[0];
-          d.out_buf = op.a[1];
-          d.m = op.B;
-          d.n = op.H;
-          d.reserved[0] = s;
-          d.reserved[1] = (uint32_t)g->bufs[op.a[0]].rows;
-          L.emit(d, {{(int)MK_BUF_STATE, s, s + 1, 0, 2}}, {{op.a[1], s, s + 1, 0, op.H}},
-                 kTaskOverhead);
-        }
+        for (int s = 0; s < op.B; ++s)
+          for (int t = 0; t < T; ++t) {
+            mk_task_descriptor d = blank(MK_OP_MEMCPY);
+            d.step = (uint16_t)t;
+            d.in_buf[0] = op.a[0];
+            if (T > 1) d.in_buf[1] = g->tokens;
+            d.out_buf = op.a[1];
+            d.m = op.B;
+            d.n = op.H;
+            d.reserved[0] = s;
+            d.reserved[1] = (uint32_t)g->bufs[op.a[0]].rows;
+            d.reserved[2] = (uint32_t)(T - 1);
+            const int r = s * T + t;
+            std::vector<Rect> rd;
+            if (t == 0) rd.push_back({(int)MK_BUF_STATE, s, s + 1, 0, 2});
+            else rd.push_back({(int)g->tokens, s, s + 1, t, t + 1});
+            L.emit(d, rd, {{op.a[1], r, r + 1, 0, op.H}}, kTaskOverhead);
+          }
         break;
       }
       case K_MATMUL: {
         g->group_off.push_back((int)g->tasks.size());
-        const int w = tile_width(op.n, tt, al);
+        const KSplit ks = ksplit_plan(op.n, op.k, op.flags, op.B, tt, al);
+        if (ks.S > 1) {
+          // split j of row block b: K columns [k0, k0 + kn); the last split
+          // reads the others' partial sums (scratch records) and writes y
+          const int KB = op.k / 64;
+          const double rows = (op.flags & MK_F_SILU_MUL) ? 2.0 : 1.0;
+          for (int c0 = 0; c0 < op.n; c0 += ks.W) {
+            const int cn = std::min(ks.W, op.n - c0);
+            const uint32_t rec0 = g->ksplit_records;
+            for (int j = 0; j < ks.S; ++j) {
+              const int k0 = (int)((int64_t)j * KB / ks.S) * 64, k1 = (int)((int64_t)(j + 1) * KB / ks.S) * 64;
+              mk_task_descriptor d = blank(MK_OP_GEMV);
+              d.config_id = 1;
+              d.flags = (uint16_t)op.flags;
+              d.in_buf[0] = op.a[0];
+              d.in_buf[1] = op.a[1];
+              d.in_buf[2] = op.a[3];
+              d.out_buf = op.a[2];
+              d.m = op.B;
+              d.n = op.n;
+              d.k = op.k;
+              d.kv_len = j | (ks.S << 16);
+              d.reserved[0] = c0;
+              d.reserved[1] = cn;
+              d.reserved[2] = (op.flags & MK_F_RMS_NORM_INPUT) ? f32_bits(op.eps) : 0u;
+              d.reserved[3] = (uint32_t)k0 | ((uint32_t)(k1 - k0) << 16);
+              d.reserved[4] = rec0 + (uint32_t)j;
+              std::vector<Rect> rd{{op.a[0], 0, op.B, k0, k1}}, wr;
+              if (j + 1 < ks.S) {
+                wr.push_back({(int)kKsplitBuf, rec0 + j, rec0 + j + 1, 0, kKsplitRecFloats});
+              } else {
+                rd.push_back({(int)kKsplitBuf, rec0, rec0 + j, 0, kKsplitRecFloats});
+                if (op.flags & MK_F_ADD_RESIDUAL) rd.push_back({op.a[3], 0, op.B, c0, c0 + cn});
+                wr.push_back({op.a[2], 0, op.B, c0, c0 + cn});
+              }
+              L.emit(d, rd, wr, rows * cn * (k1 - k0) * 2.0 + kTaskOverhead);
+            }
+            g->ksplit_records += (uint32_t)ks.S;
+          }
+          break;
+        }
+        const int w = ks.W;
         int t = 0;
         for (int c0 = 0; c0 < op.n; c0 += w, ++t) {
           const int cn = std::min(w, op.n - c0);
@@ -527,23 +623,30 @@ extern "C" int mk_lower(mk_graph* g) {
           d.k = Hq;
           d.kv_len = cap;
         };
+        // Hkv in the low half of reserved[2], T - 1 in the high half
+        const uint32_t hkvT = (uint32_t)Hkv | ((uint32_t)(T - 1) << 16);
         const int64_t cacheCols = (int64_t)cap * D;
+        const int64_t RW = (int64_t)T * G * (D + 2);  // scratch record of one slot
         g->group_off.push_back((int)g->tasks.size());
         for (int s = 0; s < B; ++s)
-          for (int gg = 0; gg < Hkv; ++gg) {
-            mk_task_descriptor d = blank(MK_OP_ATTENTION_APPEND);
-            common(d);
-            d.in_buf[0] = qkv; d.in_buf[1] = kc; d.in_buf[2] = vc;
-            d.out_buf = kc;
-            d.reserved[0] = s; d.reserved[1] = gg; d.reserved[2] = Hkv;
-            const int64_t kcol = (int64_t)Hq * D + gg * D, vcol = (int64_t)(Hq + Hkv) * D + gg * D;
-            const int64_t row = (int64_t)s * Hkv + gg;
-            L.emit(d,
-                   {{qkv, s, s + 1, kcol, kcol + D}, {qkv, s, s + 1, vcol, vcol + D},
-                    {(int)MK_BUF_STATE, s, s + 1, 0, 2}},
-                   {{kc, row, row + 1, cacheCols, cacheCols + D}, {vc, row, row + 1, cacheCols, cacheCols + D}},
-                   kTaskOverhead);
-          }
+          for (int gg = 0; gg < Hkv; ++gg)
+            for (int t = 0; t < T; ++t) {
+              // token t's row goes to position pos + t: columns
+              // [cap*D + t*D, cap*D + (t+1)*D) of the (s, g) block stand for it
+              mk_task_descriptor d = blank(MK_OP_ATTENTION_APPEND);
+              common(d);
+              d.step = (uint16_t)t;
+              d.in_buf[0] = qkv; d.in_buf[1] = kc; d.in_buf[2] = vc;
+              d.out_buf = kc;
+              d.reserved[0] = s; d.reserved[1] = gg; d.reserved[2] = hkvT;
+              const int64_t kcol = (int64_t)Hq * D + gg * D, vcol = (int64_t)(Hq + Hkv) * D + gg * D;
+              const int64_t row = (int64_t)s * Hkv + gg, r = (int64_t)s * T + t;
+              const int64_t a0 = cacheCols + (int64_t)t * D;
+              L.emit(d,
+                     {{qkv, r, r + 1, kcol, kcol + D}, {qkv, r, r + 1, vcol, vcol + D},
+                      {(int)MK_BUF_STATE, s, s + 1, 0, 2}},
+                     {{kc, row, row + 1, a0, a0 + D}, {vc, row, row + 1, a0, a0 + D}}, kTaskOverhead);
+            }
         g->group_off.push_back((int)g->tasks.size());
         for (int s = 0; s < B; ++s)
           for (int gg = 0; gg < Hkv; ++gg) {
@@ -554,17 +657,18 @@ extern "C" int mk_lower(mk_graph* g) {
               common(d);
               d.in_buf[0] = qkv; d.in_buf[1] = kc; d.in_buf[2] = vc;
               d.out_buf = scr;
-              d.reserved[0] = s; d.reserved[1] = gg; d.reserved[2] = Hkv;
+              d.reserved[0] = s; d.reserved[1] = gg; d.reserved[2] = hkvT;
               d.reserved[3] = (uint32_t)c | ((uint32_t)P[s] << 16);
               d.reserved[4] = base[s * Hkv + gg];
               const int64_t slot = base[s * Hkv + gg] + c;
+              const int64_t r0 = (int64_t)s * T, r1 = r0 + T;
               L.emit(d,
-                     {{qkv, s, s + 1, (int64_t)gg * G * D, (int64_t)(gg + 1) * G * D},
-                      {qkv, s, s + 1, (int64_t)Hq * D + gg * D, (int64_t)Hq * D + (gg + 1) * D},
-                      {qkv, s, s + 1, (int64_t)(Hq + Hkv) * D + gg * D, (int64_t)(Hq + Hkv) * D + (gg + 1) * D},
+                     {{qkv, r0, r1, (int64_t)gg * G * D, (int64_t)(gg + 1) * G * D},
+                      {qkv, r0, r1, (int64_t)Hq * D + gg * D, (int64_t)Hq * D + (gg + 1) * D},
+                      {qkv, r0, r1, (int64_t)(Hq + Hkv) * D + gg * D, (int64_t)(Hq + Hkv) * D + (gg + 1) * D},
                       {kc, row, row + 1, 0, cacheCols}, {vc, row, row + 1, 0, cacheCols},
                       {(int)MK_BUF_STATE, s, s + 1, 0, 2}},
-                     {{scr, slot, slot + 1, 0, (int64_t)G * (D + 2)}},
+                     {{scr, slot, slot + 1, 0, RW}},
                      keys * D * 4.0 + kTaskOverhead);
             }
           }
@@ -577,22 +681,23 @@ extern "C" int mk_lower(mk_graph* g) {
             d.in_buf[1] = kc;
             d.in_buf[2] = vc;
             d.out_buf = out;
-            d.reserved[0] = s; d.reserved[1] = gg; d.reserved[2] = Hkv;
+            d.reserved[0] = s; d.reserved[1] = gg; d.reserved[2] = hkvT;
             d.reserved[3] = P[s];
             d.reserved[4] = base[s * Hkv + gg];
             const int64_t b0 = base[s * Hkv + gg];
             const int64_t row = (int64_t)s * Hkv + gg;
+            const int64_t a1 = cacheCols + (int64_t)T * D;
             L.emit(d,
-                   {{scr, b0, b0 + P[s], 0, (int64_t)G * (D + 2)},
-                    {kc, row, row + 1, cacheCols, cacheCols + D},
-                    {vc, row, row + 1, cacheCols, cacheCols + D}},
-                   {{out, s, s + 1, (int64_t)gg * G * D, (int64_t)(gg + 1) * G * D}}, kTaskOverhead);
+                   {{scr, b0, b0 + P[s], 0, RW}, {kc, row, row + 1, cacheCols, a1},
+                    {vc, row, row + 1, cacheCols, a1}},
+                   {{out, (int64_t)s * T, (int64_t)s * T + T, (int64_t)gg * G * D, (int64_t)(gg + 1) * G * D}},
+                   kTaskOverhead);
           }
         break;
       }
       case K_RMSNORM: {
         g->group_off.push_back((int)g->tasks.size());
-        for (int s = 0; s < op.B; ++s) {
+        for (int s = 0; s < op.B * T; ++s) {  // one task per activation row
           mk_task_descriptor d = blank(MK_OP_RMSNORM);
           d.flags = (uint16_t)op.flags;
           d.in_buf[0] = op.a[0];
@@ -611,18 +716,26 @@ extern "C" int mk_lower(mk_graph* g) {
       }
       case K_SAMPLE: {
         g->group_off.push_back((int)g->tasks.size());
-        const int T = tile_count(op.V, tt, al);
+        const int NT = tile_count(op.V, tt, al);
         for (int s = 0; s < op.B; ++s) {
           mk_task_descriptor d = blank(MK_OP_SAMPLE);
           d.in_buf[0] = op.a[0];
           d.out_buf = op.a[1];
           d.m = op.B;
           d.n = op.V;
-          d.k = T;
+          d.k = NT;
           d.kv_len = op.cap;
           d.reserved[0] = s;
-          L.emit(d, {{op.a[0], 0, T, s, s + 1}, {(int)MK_BUF_STATE, s, s + 1, 0, 2}},
-                 {{op.a[1], s, s + 1, 0, op.cap}, {(int)MK_BUF_STATE, s, s + 1, 0, 2}}, kTaskOverhead);
+          d.reserved[1] = (uint32_t)(T - 1);
+          // the argmax of the sequence's last row; a chunk step also copies
+          // its input tokens 1.. into the history
+          const int lr = s * T + T - 1;
+          std::vector<Rect> rd{{op.a[0], 0, NT, lr, lr + 1}, {(int)MK_BUF_STATE, s, s + 1, 0, 2}};
+          if (T > 1) {
+            d.in_buf[1] = g->tokens;
+            rd.push_back({(int)g->tokens, s, s + 1, 0, T});
+          }
+          L.emit(d, rd, {{op.a[1], s, s + 1, 0, op.cap}, {(int)MK_BUF_STATE, s, s + 1, 0, 2}}, kTaskOverhead);
         }
         break;
       }
@@ -743,7 +856,7 @@ void mk::build_ll_plan(mk_graph* g, const std::vector<std::vector<int>>& parents
   const size_t NB = g->bufs.size(), N = g->tasks.size();
   g->ll_buf.assign(NB, 0);
   g->ll_task.assign(N, 0);
-  if (g->B > 4) return;
+  if (g->rows() > 4) return;
   std::vector<uint8_t> read_as_input(NB, 0), bad_writer(NB, 0);
   for (const mk_task_descriptor& d : g->tasks) {
     if (d.op_id == MK_OP_GEMV) {
@@ -818,6 +931,19 @@ int mk::build_sync_plan(mk_graph* g) {
       parents[c].push_back(p);
     }
   }
+  // The last split of a K-split row block waits for its sibling splits
+  // inside its body (after its own partial product), through the block's
+  // arrival counter in the K-split scratch: those parents leave the plan.
+  std::vector<int> deferred(N, 0);
+  for (int t = 0; t < N; ++t) {
+    const mk_task_descriptor& d = g->tasks[t];
+    const int S = (int)((uint32_t)d.kv_len >> 16), j = d.kv_len & 0xFFFF;
+    if (d.op_id != MK_OP_GEMV || d.config_id != 1 || S < 2 || j != S - 1) continue;
+    std::vector<int>& ps = parents[t];
+    const size_t before = ps.size();
+    ps.erase(std::remove_if(ps.begin(), ps.end(), [&](int q) { return q >= t - (S - 1) && q < t; }), ps.end());
+    deferred[t] = (int)(before - ps.size());
+  }
   const uint32_t npad = (uint32_t)((N + 31) / 32 * 32);
   auto group_size = [&](int k) { return g->group_off[k + 1] - g->group_off[k]; };
   auto group_counter = [&](int k) { return npad + 32u * (uint32_t)k; };
@@ -833,7 +959,7 @@ int mk::build_sync_plan(mk_graph* g) {
     if (have_ll && g->ll_task[t]) {
       // reads every parent's output as tagged pairs: no counter, except a
       // surplus in a patched descriptor (which then can never be met)
-      own[t] = std::max(g->tasks[t].remaining_deps - (int)parents[t].size(), 0);
+      own[t] = std::max(g->tasks[t].remaining_deps - deferred[t] - (int)parents[t].size(), 0);
       own_ctr[t] = t;
       continue;
     }
@@ -852,7 +978,7 @@ int mk::build_sync_plan(mk_graph* g) {
     for (int p : parents[t])
       if (cnt[group_of[p]] != -1) rest.push_back(p);
     for (int p : parents[t]) cnt[group_of[p]] = 0;
-    own[t] = std::max(g->tasks[t].remaining_deps - covered, 0);
+    own[t] = std::max(g->tasks[t].remaining_deps - deferred[t] - covered, 0);
     own_ctr[t] = t;
     if (!rest.empty()) {  // tasks with the same remaining parents share one counter
       auto it = set_ctr.emplace(rest, t).first;

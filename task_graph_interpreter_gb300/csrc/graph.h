@@ -44,8 +44,11 @@ struct mk_graph {
   mk_config cfg{};
   int num_ctas = 0, tiles_target = 0, col_align = 16;
   uint32_t timeout_us = 2000000;
-  int B = 0;                       // from mk_set_state
+  int B = 0;                       // sequences, from mk_set_state
+  int T = 1;                       // tokens per sequence per step (mk_set_chunk)
+  uint16_t tokens = MK_NO_BUF;     // int32 [B, T] input tokens of a chunk step (T > 1)
   bool state_set = false, lowered = false, uploaded = false;
+  int rows() const { return B * T; }  // activation rows: row s * T + t
   std::vector<mk::BufferRec> bufs;  // index 0 state, 1/2 rope tables
   std::vector<mk::OpRec> ops;
   // rope parameters (shared by every attention op)
@@ -63,6 +66,7 @@ struct mk_graph {
   // counter[sig[j]] for every j in [sig_off[t], sig_off[t+1]).
   std::vector<uint32_t> wait_off, wait, sig_off, sig;  // wait holds (counter, count) pairs
   uint32_t counter_words = 0;
+  uint32_t ksplit_records = 0;     // K-split scratch records the lowering assigned
   // tagged hand-offs (B <= 4): buffers whose values are also written as
   // (step tag, value) pairs, and the GEMV, partial and append tasks that
   // read all their inputs from such pairs instead of waiting on counters
@@ -74,6 +78,18 @@ struct mk_graph {
 };
 
 namespace mk {
+// Row blocks and K splits of a GEMV op (ksplit_plan, graph.cpp): W rows per
+// tile or block, nb blocks, S splits of K (1: not split).
+struct KSplit {
+  int W, nb, S;
+};
+KSplit ksplit_plan(int n, int k, uint32_t flags, int m, int tiles_target, int col_align);
+// The library-owned scratch of the K-split partial sums, as a pseudo buffer
+// index in dependency rectangles: one record of kKsplitRecFloats floats per
+// split tile ([256 rows][8 batch] partial sums, then 8 partial sums of
+// squares of x); the last split's record holds its block's arrival counter.
+constexpr uint16_t kKsplitBuf = 0xFFFE;
+constexpr int kKsplitRecFloats = 256 * 8 + 8;
 int query_sm_count(int* out);  // runtime.cu
 int tile_width(int n, int tiles_target, int col_align);
 int tile_count(int n, int tiles_target, int col_align);

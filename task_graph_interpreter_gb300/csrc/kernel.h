@@ -65,7 +65,11 @@ struct KParams {
   int32_t nstages;            // ring slots in use
   int32_t rope_half;          // D/2 of the tables
   int32_t num_bufs;           // entries of bufs / mirrors / tm_rows
+  float* ksplit;              // K-split partial sums: kKsplitRecFloats floats per record
+  uint32_t* karr;             // K-split arrival counters, one per record (the last split's is its block's)
+  uint32_t kmul;              // a block's arrivals this step reach kmul * (S - 1)
 };
+constexpr int kKsplitRec = 256 * 8 + 8;  // floats per K-split record: [256 rows][8 batch] sums, 8 sums of squares
 
 int smem_bytes_for(int nstages, int batch);
 

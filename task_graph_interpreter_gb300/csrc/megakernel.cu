@@ -147,26 +147,48 @@ __device__ __forceinline__ void gemv_geom(const mk_task_descriptor& d, GemvGeom&
   g.RG = min(rg, g.cn);
 }
 
-// Tensor-core tile plan (B = 8): row groups of RG rows (the TMA box), N =
-// RG rounded up to 16, nkb K blocks of 64 columns per ring slot.
+// Tensor-core tile plan (B >= 8): row groups of RG rows (the TMA box).  The
+// MMA's N holds the group's rows of every segment (gate and up rows stacked
+// for SILU_MUL): segment sg occupies rows [sg * Nr, sg * Nr + RG) of the
+// weight tile and accumulator columns [sg * Nr, ...), N = seg * Nr <= 256.
+// A K-split tile (kv_len = j | S << 16, S >= 2) covers K columns [k0, k0 +
+// kn) only; otherwise k0 = 0, kn = K.  nkb K blocks of 64 columns per ring
+// slot, nkr K ranges.
 struct TcGeom {
-  int RG, Nr, nkb, nkr, seg, K;
+  int RG, Nr, N, nkb, nkr, seg, K, k0, kn, S, j;
 };
 
 __device__ __forceinline__ void tc_geom(int rows, const mk_task_descriptor& d, TcGeom& t) {
   t.RG = rows;
-  t.Nr = (t.RG + 15) & ~15;
   t.seg = (d.flags & MK_F_SILU_MUL) ? 2 : 1;
+  t.Nr = t.seg == 2 ? (t.RG + 7) & ~7 : (t.RG + 15) & ~15;
+  t.N = t.seg * t.Nr;
   t.K = d.k;
-  const int nkbt = d.k / 64;
+  t.S = (int)((uint32_t)d.kv_len >> 16);
+  if (t.S >= 2) {
+    t.j = d.kv_len & 0xFFFF;
+    t.k0 = (int)(d.reserved[3] & 0xFFFFu);
+    t.kn = (int)(d.reserved[3] >> 16);
+  } else {
+    t.S = 1;
+    t.j = 0;
+    t.k0 = 0;
+    t.kn = d.k;
+  }
+  const int nkbt = t.kn / 64;
   t.nkb = 4;  // K blocks per slot: the staged activations of 4 blocks fill one 12 KB tile
-  while (t.nkb > 1 && (t.nkb * t.Nr * 128 > kStageBytes || nkbt % t.nkb)) t.nkb >>= 1;
+  while (t.nkb > 1 && (t.nkb * t.N * 128 > kStageBytes || nkbt % t.nkb)) t.nkb >>= 1;
   t.nkr = nkbt / t.nkb;
 }
 
 // ------------------------------------------------------------------ PARTIAL plan
+// A chunk step of T tokens per sequence (T = 1: a decode step): token t
+// sits at pos + t and sees keys 0 .. pos + t.  The chunks split the keys of
+// the last token, [0, pos + T); keys below pos are cached rows of earlier
+// steps (streamed through the ring), keys from pos on are this step's rows,
+// taken from qkv.
 struct PartGeom {
-  int s, g, Hkv, c, P, slot, D, Hq, G, cap, pos, j0, j1, jst, R, nstage;
+  int s, g, Hkv, T, c, P, slot, D, Hq, G, cap, pos, j0, j1, jst, nb0, nn, R, nstage;
   bool has_new;
   bool bad;
 };
@@ -174,7 +196,8 @@ struct PartGeom {
 __device__ __forceinline__ void part_geom(const int32_t* state, const mk_task_descriptor& d, PartGeom& q) {
   q.s = (int)d.reserved[0];
   q.g = (int)d.reserved[1];
-  q.Hkv = (int)d.reserved[2];
+  q.Hkv = (int)(d.reserved[2] & 0xFFFFu);
+  q.T = (int)(d.reserved[2] >> 16) + 1;
   q.c = (int)(d.reserved[3] & 0xFFFFu);
   q.P = (int)(d.reserved[3] >> 16);
   q.slot = (int)d.reserved[4] + q.c;
@@ -183,23 +206,25 @@ __device__ __forceinline__ void part_geom(const int32_t* state, const mk_task_de
   q.G = q.Hq / q.Hkv;
   q.cap = d.kv_len;
   q.pos = ld_relaxed(state + 2 * q.s + 1);
-  q.bad = q.pos < 0 || q.pos >= q.cap;
+  q.bad = q.pos < 0 || q.pos + q.T > q.cap;
   if (q.bad) {
-    q.j0 = q.j1 = q.jst = 0;
+    q.j0 = q.j1 = q.jst = q.nb0 = q.nn = 0;
     q.nstage = 0;
     q.R = 1;
     q.has_new = false;
     return;
   }
-  const int L = q.pos + 1;
+  const int L = q.pos + q.T;
   const int e = (L + q.P - 1) / q.P;
   q.j0 = min(q.c * e, L);
   q.j1 = min(q.j0 + e, L);
   q.jst = min(q.j1, q.pos);
+  q.nb0 = max(q.j0, q.pos);           // this step's keys in the chunk: [nb0, j1)
+  q.nn = max(0, q.j1 - q.nb0);
   q.R = (kStageBytes / 4) / q.D;  // rows of K and of V per slot
   const int nrows = max(0, q.jst - q.j0);
   q.nstage = (nrows + q.R - 1) / q.R;
-  q.has_new = (q.j1 == L) && (q.j0 < q.j1);
+  q.has_new = q.nn > 0;
 }
 
 // ------------------------------------------------------------------ control block
@@ -299,17 +324,18 @@ __device__ void producer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
       const uint8_t* tmap = p.tmaps + (size_t)d.in_buf[1] * kTmapBytes;
       const int c0 = (int)d.reserved[0], cn = (int)d.reserved[1];
       if (d.flags & MK_F_RMS_NORM_INPUT) prefetch_l2(reinterpret_cast<const void*>(r->ptr[kPIn2]), (uint32_t)d.k * 2u);
+      // one slot per K range: nkb K blocks of every segment's RG rows
       for (int g0 = 0; g0 < cn && !stop; g0 += T.RG)
-        for (int kr = 0; kr < T.nkr && !stop; ++kr)
-          for (int sg = 0; sg < T.seg; ++sg) {
-            uint64_t* fb;
-            uint8_t* dst =
-                produce_slot(p, ring, full, empty, rp, issued, task, (uint32_t)(T.nkb * T.RG * 128), &fb);
-            if (!dst) { stop = true; break; }
-            const int row = (sg ? d.n : 0) + c0 + g0;
-            for (int kb = 0; kb < T.nkb; ++kb)
-              tma_load_2d(dst + (size_t)kb * T.Nr * 128, tmap, (kr * T.nkb + kb) * 64, row, fb, pol);
-          }
+        for (int kr = 0; kr < T.nkr && !stop; ++kr) {
+          uint64_t* fb;
+          uint8_t* dst = produce_slot(p, ring, full, empty, rp, issued, task,
+                                      (uint32_t)(T.nkb * T.seg * T.RG * 128), &fb);
+          if (!dst) { stop = true; break; }
+          for (int kb = 0; kb < T.nkb; ++kb)
+            for (int sg = 0; sg < T.seg; ++sg)
+              tma_load_2d(dst + (size_t)(kb * T.N + sg * T.Nr) * 128, tmap, T.k0 + (kr * T.nkb + kb) * 64,
+                          (sg ? d.n : 0) + c0 + g0, fb, pol);
+        }
     } else if (d.op_id == MK_OP_GEMV) {
       GemvGeom G;
       gemv_geom(d, G);
@@ -1038,6 +1064,10 @@ __device__ __forceinline__ void tc_load_x(float (&xv)[8], const float* x, int K,
 // of two staging tiles, read the accumulators from tensor memory at the
 // end of each row group, run the usual epilogue.  No CTA-wide barrier per K
 // range: the staging tile of range kr waits only for the MMAs of kr - 2.
+// A K-split tile (one K range of a row block) stores its partial sums and
+// sums of squares in its scratch record and counts itself in; the block's
+// last split waits for the others, adds their records in split order to its
+// own sums and runs the epilogue.
 __device__ void tc_gemv_task(Ctx& c, const mk_task_descriptor& d) {
   const KParams& p = *c.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1064,8 +1094,8 @@ __device__ void tc_gemv_task(Ctx& c, const mk_task_descriptor& d) {
     const int rows_g = min(T.RG, G.cn - g0);
     // x of the next two K ranges is in flight while a range is staged
     float xa[8], xb[8];
-    tc_load_x(xa, x, T.K, warp, G.B, lane * kpt, kpt);
-    if (T.nkr > 1) tc_load_x(xb, x, T.K, warp, G.B, T.nkb * 64 + lane * kpt, kpt);
+    tc_load_x(xa, x, T.K, warp, G.B, T.k0 + lane * kpt, kpt);
+    if (T.nkr > 1) tc_load_x(xb, x, T.K, warp, G.B, T.k0 + T.nkb * 64 + lane * kpt, kpt);
     for (int kr = 0; kr < T.nkr; ++kr) {
       float xc[8];
 #pragma unroll
@@ -1073,7 +1103,7 @@ __device__ void tc_gemv_task(Ctx& c, const mk_task_descriptor& d) {
         xc[e] = xa[e];
         xa[e] = xb[e];
       }
-      const int k0 = kr * T.nkb * 64 + lane * kpt;  // this lane's first column
+      const int k0 = T.k0 + kr * T.nkb * 64 + lane * kpt;  // this lane's first column
       if (kr + 2 < T.nkr) tc_load_x(xb, x, T.K, warp, G.B, k0 + 2 * T.nkb * 64, kpt);
       const int j = kr & 1;
       if (kr >= 2) {  // the MMAs of kr - 2 have read this staging tile
@@ -1119,10 +1149,9 @@ __device__ void tc_gemv_task(Ctx& c, const mk_task_descriptor& d) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->x_full[j]);
     }
-    if (g0 == 0 && gamma) {  // 1/rms per batch row (warp b holds row b's columns)
-      const float t = warp_sum(ss);
-      if (lane == 0) red[64 + warp] = 1.0f / sqrtf(t / (float)T.K + __uint_as_float(d.reserved[2]));
-    }
+    const float ssw = g0 == 0 ? warp_sum(ss) : 0.f;  // batch row `warp`: this tile's columns of x
+    if (g0 == 0 && gamma && T.S == 1 && lane == 0)  // 1/rms per batch row (warp b holds row b's columns)
+      red[64 + warp] = 1.0f / sqrtf(ssw / (float)T.K + __uint_as_float(d.reserved[2]));
     // the row group's MMAs are done (acc_full follows every earlier commit)
     if (lane == 0) bar_wait(p, &ctl->acc_full, (c.tc_ph >> 2) & 1u, c.task, false);
     __syncwarp();
@@ -1146,11 +1175,75 @@ __device__ void tc_gemv_task(Ctx& c, const mk_task_descriptor& d) {
     }
     cbar();
     if (tid == 0) mbar_arrive(&ctl->acc_empty);  // tensor memory is free for the next row group
+    if (T.S > 1) {
+      // K split (one row group): partial sums through the scratch records
+      const int rec0 = (int)d.reserved[4] - T.j, n8 = T.seg * rows_g * 8;
+      uint32_t* arr = p.karr + rec0 + T.S - 1;  // the block's arrival counter
+      if (T.j + 1 < T.S) {
+        float* rec = p.ksplit + (size_t)d.reserved[4] * kKsplitRec;
+        for (int i = tid * 4; i < n8; i += kConsumerThreads * 4)  // n8 is a multiple of 8
+          *reinterpret_cast<float4*>(rec + i) = *reinterpret_cast<const float4*>(acc + i);
+        if (lane == 0) rec[256 * 8 + warp] = ssw;
+        cbar();
+        if (tid == 0) {  // release: the record before the arrival
+          fence_acq_rel_gpu();
+          red_relaxed_add(arr, 1u);
+        }
+        break;  // the block's last split writes the outputs
+      }
+      if (lane == 0) red[warp] = ssw;  // this split's own sums of squares, per batch row
+      if (tid == 0) {  // wait for the other splits (bounded; abort on failure)
+        const uint32_t target = p.kmul * (uint32_t)(T.S - 1);
+        const uint64_t t0 = globaltimer();
+        for (uint32_t it = 0; (int32_t)(ld_acquire(arr) - target) < 0; ++it) {
+          if ((it & 63u) == 63u) {
+            if (aborted(p)) break;
+            if (globaltimer() - t0 > p.timeout_ns) {
+              raise_error(p, MK_DEV_DEP_TIMEOUT, c.task);
+              break;
+            }
+          }
+        }
+      }
+      cbar();
+      // the other splits' sums, added in split order; up to eight records'
+      // float4 loads are in flight at once (a dependent chain of L2 reads
+      // per element cost several microseconds)
+      for (int i = tid * 4; i < n8; i += kConsumerThreads * 4) {
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q0 = 0; q0 < T.S - 1; q0 += 8) {
+          float4 r[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            r[u] = q0 + u < T.S - 1
+                       ? __ldcg(reinterpret_cast<const float4*>(p.ksplit + (size_t)(rec0 + q0 + u) * kKsplitRec + i))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            if (q0 + u < T.S - 1) {
+              v.x += r[u].x;
+              v.y += r[u].y;
+              v.z += r[u].z;
+              v.w += r[u].w;
+            }
+          }
+        }
+        const float4 o = *reinterpret_cast<const float4*>(acc + i);
+        *reinterpret_cast<float4*>(acc + i) = make_float4(v.x + o.x, v.y + o.y, v.z + o.z, v.w + o.w);
+      }
+      if (gamma && tid < G.B) {
+        float t = 0.f;
+        for (int q = 0; q < T.S - 1; ++q) t += __ldcg(p.ksplit + (size_t)(rec0 + q) * kKsplitRec + 256 * 8 + tid);
+        t += red[tid];  // this split's own, last
+        red[64 + tid] = 1.0f / sqrtf(t / (float)T.K + __uint_as_float(d.reserved[2]));
+      }
+      cbar();
+    }
     gemv_epilogue(p, d, G, g0, rows_g, acc, red, nullptr, rec_ptr<float>(c, kPOut),
                   (d.flags & MK_F_ADD_RESIDUAL) ? rec_ptr<const float>(c, kPIn2) : nullptr, nullptr, nullptr, c.task);
   }
   for (int g0 = 0; g0 < G.cn; g0 += T.RG)
-    for (int i = 0; i < T.nkr * T.seg; ++i) c.rp.advance(c.nst);
+    for (int i = 0; i < T.nkr; ++i) c.rp.advance(c.nst);
   if ((d.flags & MK_F_ARGMAX_EPI) && threadIdx.x < G.B) {
     mk_argmax_pair* pairs = rec_ptr<mk_argmax_pair>(c, kPPairs);
     mk_argmax_pair pr;
@@ -1189,14 +1282,17 @@ __device__ void tc_mma_warp(const KParams& p, uint8_t* ring, uint64_t* full, uin
     rp.phase = rel.phase = ctl->mb_phase;
     // only the fields the schedule needs (this warp runs on few registers)
     const mk_task_descriptor* td = p.tasks + task;
-    const int K = __ldg(&td->k), cn = (int)__ldg(&td->reserved[1]);
+    const int cn = (int)__ldg(&td->reserved[1]);
     const int seg = (__ldg(&td->flags) & MK_F_SILU_MUL) ? 2 : 1;
-    const int RG = p.tm_rows[__ldg(&td->in_buf[1])], Nr = (RG + 15) & ~15;
+    const int RG = p.tm_rows[__ldg(&td->in_buf[1])];
+    const int N = seg * (seg == 2 ? (RG + 7) & ~7 : (RG + 15) & ~15);
+    const int S = (int)((uint32_t)__ldg(&td->kv_len) >> 16);
+    const int kn = S >= 2 ? (int)(__ldg(&td->reserved[3]) >> 16) : __ldg(&td->k);
     int nkb = 4;
-    while (nkb > 1 && (nkb * Nr * 128 > kStageBytes || (K / 64) % nkb)) nkb >>= 1;
-    const int nkr = K / 64 / nkb;
-    const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)Nr);
-    const uint32_t bstep = (uint32_t)(Nr * 128) >> 4;  // one K block of the weight tile, in 16 bytes
+    while (nkb > 1 && (nkb * N * 128 > kStageBytes || (kn / 64) % nkb)) nkb >>= 1;
+    const int nkr = kn / 64 / nkb;
+    const uint32_t idesc = idesc_bf16_f32(128, (uint32_t)N);
+    const uint32_t bstep = (uint32_t)(N * 128) >> 4;  // one K block of the weight tile, in 16 bytes
     for (int g0 = 0; g0 < cn; g0 += RG) {
       if (!first) {  // the consumers have read the previous accumulators
         if (!bar_wait(p, &ctl->acc_empty, (ph >> 5) & 1u, task, false)) ok = false;
@@ -1207,32 +1303,28 @@ __device__ void tc_mma_warp(const KParams& p, uint8_t* ring, uint64_t* full, uin
         const int j = kr & 1;
         if (!bar_wait(p, &ctl->x_full[j], (ph >> (1 + j)) & 1u, task, false)) ok = false;
         ph ^= 1u << (1 + j);
-        if (kr >= 2) {  // range kr - 2 is done: its slots go back to the producer
+        if (kr >= 2) {  // range kr - 2 is done: its slot goes back to the producer
           if (!bar_wait(p, &ctl->mma_bar[j], (ph >> (3 + j)) & 1u, task, false)) ok = false;
           ph ^= 1u << (3 + j);
-          for (int sg = 0; sg < seg; ++sg) {
-            mbar_arrive_cnt(&empty[rel.slot], kConsumerWarps);
-            rel.advance(nst);
-          }
+          mbar_arrive_cnt(&empty[rel.slot], kConsumerWarps);
+          rel.advance(nst);
         }
         tc_fence_after();
         const uint64_t ad0 = smem_desc_sw128(xb0 + (uint32_t)j * (kXbufBytes / 2), 1024u);
-        for (int sg = 0; sg < seg; ++sg) {
-          if (ok && !bar_wait(p, &full[rp.slot], rp.phase, task, true)) ok = false;
-          if (ok) {
-            // descriptors of the first K step; later steps add their byte
-            // offset / 16 to the start-address field (no carry: < 256 KB)
-            const uint64_t bd0 = smem_desc_sw128(smem_addr(ring + (size_t)rp.slot * kStageBytes), 1024u);
-            const uint32_t dcol = taddr + (uint32_t)(sg * Nr);
+        if (ok && !bar_wait(p, &full[rp.slot], rp.phase, task, true)) ok = false;
+        if (ok) {
+          // descriptors of the first K step; later steps add their byte
+          // offset / 16 to the start-address field (no carry: < 256 KB).
+          // One MMA covers every segment's rows (N = seg * Nr).
+          const uint64_t bd0 = smem_desc_sw128(smem_addr(ring + (size_t)rp.slot * kStageBytes), 1024u);
 #pragma unroll 1
-            for (int q = 0; q < nkb * 4; ++q) {  // K block q / 4, K step q % 4
-              const uint32_t kb = (uint32_t)q >> 2, ks = (uint32_t)q & 3u;
-              tc_mma_bf16(dcol, ad0 + (uint64_t)(kb * (3072u >> 4) + ks * 2u), bd0 + (uint64_t)(kb * bstep + ks * 2u),
-                          idesc, (kr | q) != 0 ? 1u : 0u);
-            }
+          for (int q = 0; q < nkb * 4; ++q) {  // K block q / 4, K step q % 4
+            const uint32_t kb = (uint32_t)q >> 2, ks = (uint32_t)q & 3u;
+            tc_mma_bf16(taddr, ad0 + (uint64_t)(kb * (3072u >> 4) + ks * 2u), bd0 + (uint64_t)(kb * bstep + ks * 2u),
+                        idesc, (kr | q) != 0 ? 1u : 0u);
           }
-          rp.advance(nst);
         }
+        rp.advance(nst);
         tc_commit(&ctl->mma_bar[j]);
       }
       tc_commit(&ctl->acc_full);
@@ -1240,26 +1332,27 @@ __device__ void tc_mma_warp(const KParams& p, uint8_t* ring, uint64_t* full, uin
         const int j = kr & 1;
         if (!bar_wait(p, &ctl->mma_bar[j], (ph >> (3 + j)) & 1u, task, false)) ok = false;
         ph ^= 1u << (3 + j);
-        for (int sg = 0; sg < seg; ++sg) {
-          mbar_arrive_cnt(&empty[rel.slot], kConsumerWarps);
-          rel.advance(nst);
-        }
+        mbar_arrive_cnt(&empty[rel.slot], kConsumerWarps);
+        rel.advance(nst);
       }
     }
   }
 }
 
 // ------------------------------------------------------------------ attention bodies
+// Token t (= the descriptor's step) of sequence s: its rotated key and its
+// value go to row pos + t of the (s, g) cache block.
 __device__ void append_task(Ctx& c, const mk_task_descriptor& d) {
   const KParams& p = *c.p;
-  const int s = d.reserved[0], g = d.reserved[1], Hkv = d.reserved[2];
+  const int s = d.reserved[0], g = d.reserved[1], Hkv = d.reserved[2] & 0xFFFFu;
+  const int T = (int)(d.reserved[2] >> 16) + 1, t_ = d.step;
   const int D = d.n, Hq = d.k, cap = d.kv_len, half = D / 2;
-  const int pos = ld_relaxed(c.state + 2 * s + 1);
-  if (pos < 0 || pos >= cap) {
+  const int pos = ld_relaxed(c.state + 2 * s + 1) + t_;
+  if (pos < 0 || pos >= cap || t_ >= T) {
     if (threadIdx.x == 0) raise_error(p, MK_DEV_CAPACITY, c.task);
     return;
   }
-  const size_t seq = (size_t)s * (Hq + 2 * Hkv) * D;
+  const size_t seq = (size_t)(s * T + t_) * (Hq + 2 * Hkv) * D;
   const float* qkv = rec_ptr<const float>(c, kPIn0) + seq;
   const uint64_t* qm = rec_ptr<const uint64_t>(c, kMirX);  // tagged qkv (MEGA, B <= 4), else null
   __nv_bfloat16* Kc = rec_ptr<__nv_bfloat16>(c, kPIn1);
@@ -1293,18 +1386,20 @@ __device__ void append_task(Ctx& c, const mk_task_descriptor& d) {
   if (t < D) Vc[row + t] = __float2bfloat16_rn(vv);
 }
 
-// Eight keys of the online softmax (base 2) for the query heads of a KV
-// group.  Lane = 8 * head + slice: the lane holds dims [slice * DS, slice *
-// DS + DS) of its head's query (qr) and output (o); m and l are its head's
-// running max and sum (equal in the head's 8 lanes).  Keys k0 .. k0 + 7
-// (nvalid of them real) are read from shared memory (rows of DS * 8 bf16
-// at kb and vb): each lane reads its slice of every key, so the four heads'
-// lanes share each address.  A score needs a sum over the head's 8 lanes
-// only: a transposed reduction leaves key `slice`'s score in that lane.
+// Eight keys of the online softmax (base 2) for four query rows (a KV
+// group's heads, or (token, head) rows of a chunk step).  Lane = 8 * row +
+// slice: the lane holds dims [slice * DS, slice * DS + DS) of its row's
+// query (qr) and output (o); m and l are its row's running max and sum
+// (equal in the row's 8 lanes).  Keys k0 .. k0 + 7 (nvalid of them real)
+// are read from shared memory (rows of DS * 8 bf16 at kb and vb): each lane
+// reads its slice of every key, so the four rows' lanes share each
+// address.  A score needs a sum over the row's 8 lanes only: a transposed
+// reduction leaves key `slice`'s score in that lane.  The row sees only its
+// first nlive of the keys (causal masking in a chunk step; nvalid else).
 template <int DS>
 __device__ __forceinline__ void partial_group8(const float (&qr)[DS], float (&o)[DS], float& m, float& l,
-                                               uint32_t kb, uint32_t vb, int k0, int nvalid, bool hlive,
-                                               int lane) {
+                                               uint32_t kb, uint32_t vb, int k0, int nvalid, int nlive,
+                                               bool hlive, int lane) {
   constexpr int D = DS * 8;
   const int sl = lane & 7;
   float v[8];
@@ -1336,7 +1431,7 @@ __device__ __forceinline__ void partial_group8(const float (&qr)[DS], float (&o)
       v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o2);
     }
   }
-  const bool live = hlive && sl < nvalid;
+  const bool live = hlive && sl < nlive;
   float gmax = live ? v[0] : -INFINITY;
 #pragma unroll
   for (int off = 1; off < 8; off <<= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, off));
@@ -1369,35 +1464,52 @@ __device__ __forceinline__ void partial_group8(const float (&qr)[DS], float (&o)
   }
 }
 
-// Online softmax of G query heads over one KV chunk (log2 domain: scores
-// are scaled by log2(e)/sqrt(D) and exponentials taken base 2).  Writes
-// (m, l, o[D]) per head to the chunk's scratch slot.
+// Online softmax over one KV chunk for the G query heads of a KV group and
+// the T tokens of a chunk step (T = 1: a decode step), NR = T * G query rows
+// (token t, head h) = row t * G + h (log2 domain: scores are scaled by
+// log2(e)/sqrt(D) and exponentials taken base 2).  Rows go in groups of four
+// to WPG = 8 / ceil(NR / 4) warps, which split each ring slot's keys; row
+// (t, h) sees keys up to pos + t.  This step's keys (positions pos ..) come
+// from qkv, rotated and rounded to bf16 exactly as ATTENTION_APPEND stores
+// them, so the partial does not wait for the appends.  Writes (m, l, o[D])
+// per row to the chunk's scratch slot.
 template <int DS>  // dims per lane: D / 8
 __device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom& q) {
   constexpr int D = DS * 8;
-  constexpr int MAXG = 4;
   const KParams& p = *c.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int G = q.G, half = D / 2;
-  const int h = lane >> 3, sl = lane & 7;
-  const bool hlive = h < G;
-  float* qs = c.scratch;                              // [G][D]
-  float* mrg = c.scratch + MAXG * D;                  // [8 warps][G][D + 2]
-  uint16_t* nkv = reinterpret_cast<uint16_t*>(mrg + kConsumerWarps * MAXG * (D + 2));  // new key, value rows
-  const size_t row = (size_t)q.s * (q.Hq + 2 * q.Hkv) * D;
-  const float* qkv = rec_ptr<const float>(c, kPIn0) + row;
+  const int G = q.G, T = q.T, NR = G * T, half = D / 2;
+  const int NGR = (NR + 3) >> 2;         // groups of four rows
+  const int WPG = kConsumerWarps / NGR;  // warps per group
+  const int grp = warp / WPG, sub = warp - grp * WPG;
+  const bool wlive = grp < NGR;
+  const int rr = grp * 4 + (lane >> 3), sl = lane & 7;
+  const bool hlive = wlive && rr < NR;
+  const int tq = hlive ? rr / G : 0;     // the row's token
+  // shared scratch: qs [NR][D] rotated, scaled queries; nkv this step's keys
+  // [T][D] then values [T][D] (bf16); mrg [8 warps][4][D + 2] after them,
+  // or over them (after a barrier) when the three do not fit side by side
+  float* qs = c.scratch;
+  uint16_t* nkv = reinterpret_cast<uint16_t*>(c.scratch + NR * D);
+  const bool mrg_apart = (NR * D * 4 + 2 * T * D * 2 + kConsumerWarps * 4 * (D + 2) * 4) <= kScratchBytes;
+  float* mrg = mrg_apart ? c.scratch + NR * D + T * D : c.scratch;  // nkv takes T * D floats
+  const size_t rowlen = (size_t)(q.Hq + 2 * q.Hkv) * D;
+  const size_t row0 = (size_t)q.s * q.T * rowlen;  // the sequence's first activation row
+  const float* qkv = rec_ptr<const float>(c, kPIn0) + row0;
   const uint64_t* qm = rec_ptr<const uint64_t>(c, kMirX);  // tagged qkv (MEGA, B <= 4), else null
-  if (qm) qm += row;
+  if (qm) qm += row0;
   const float scale = 1.4426950408889634f / sqrtf((float)D);
-  // RoPE on the group's query heads at position pos (G * D / 2 <= 256
-  // items: one per thread)
-  {
-    const int hh = tid / half, j = tid % half;
-    const bool act = tid < G * half;
-    const size_t o = (size_t)(q.g * G + (act ? hh : 0)) * D + j;
+  // RoPE on the rows' queries: item (row, j) rotates the pair (j, j + D/2)
+  for (int base = 0; base < NR * half; base += kConsumerThreads) {
+    const int i = base + tid;
+    const bool act = i < NR * half;
+    const int r = act ? i / half : 0, j = i - r * half;
+    const int t = r / G, h = r - t * G;
+    const size_t o = (size_t)t * rowlen + (size_t)(q.g * G + h) * D + j;
     // the table rows do not depend on qkv: their loads go out before the wait
-    const float cs = act ? __ldg(p.rope_cos + (size_t)q.pos * p.rope_half + j) : 1.f;
-    const float sn = act ? __ldg(p.rope_sin + (size_t)q.pos * p.rope_half + j) : 0.f;
+    const size_t tr = (size_t)(q.pos + t) * p.rope_half + j;
+    const float cs = act ? __ldg(p.rope_cos + tr) : 1.f;
+    const float sn = act ? __ldg(p.rope_sin + tr) : 0.f;
     float a, b;
     if (qm) {
       const uint64_t* const mm[2] = {qm + o, qm + o + half};
@@ -1411,64 +1523,71 @@ __device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom
       b = act ? __ldcg(qkv + o + half) : 0.f;
     }
     if (act) {
-      qs[hh * D + j] = (a * cs - b * sn) * scale;
-      qs[hh * D + j + half] = (b * cs + a * sn) * scale;
+      qs[r * D + j] = (a * cs - b * sn) * scale;
+      qs[r * D + j + half] = (b * cs + a * sn) * scale;
     }
   }
-  if (q.has_new && warp == kConsumerWarps - 1) {
-    // the key/value of the token at pos come straight from qkv, rotated and
-    // rounded to bf16 exactly as ATTENTION_APPEND stores them, so this task
-    // does not wait for the append
-    const size_t ko = (size_t)q.Hq * D + (size_t)q.g * D, vo = (size_t)(q.Hq + q.Hkv) * D + (size_t)q.g * D;
-    for (int dd = lane; dd < D; dd += 32) {
-      const int jj = dd < half ? dd : dd - half;
-      const float cs = p.rope_cos[(size_t)q.pos * p.rope_half + jj];
-      const float sn = p.rope_sin[(size_t)q.pos * p.rope_half + jj];
-      float k1, k2, vv;
-      if (qm) {
-        const uint64_t* const mm[3] = {qm + ko + jj, qm + ko + jj + half, qm + vo + dd};
-        const bool use[3] = {true, true, true};
-        float v[3];
-        ll_gather<3>(p, c.task, mm, use, v);
-        k1 = v[0];
-        k2 = v[1];
-        vv = v[2];
-      } else {
-        k1 = __ldcg(qkv + ko + jj);
-        k2 = __ldcg(qkv + ko + jj + half);
-        vv = __ldcg(qkv + vo + dd);
-      }
+  // this step's keys in the chunk, positions nb0 .. nb0 + nn - 1: key kk
+  // is token nb0 + kk - pos's row of qkv
+  for (int base = 0; base < q.nn * D; base += kConsumerThreads) {
+    const int i = base + tid;
+    const bool act = i < q.nn * D;
+    const int kk = act ? i / D : 0, dd = i - kk * D;
+    const int pk = q.nb0 + kk, jj = dd < half ? dd : dd - half;
+    const size_t rb = (size_t)(pk - q.pos) * rowlen;
+    const size_t ko = rb + (size_t)q.Hq * D + (size_t)q.g * D, vo = rb + (size_t)(q.Hq + q.Hkv) * D + (size_t)q.g * D;
+    const float cs = act ? p.rope_cos[(size_t)pk * p.rope_half + jj] : 1.f;
+    const float sn = act ? p.rope_sin[(size_t)pk * p.rope_half + jj] : 0.f;
+    float k1 = 0.f, k2 = 0.f, vv = 0.f;
+    if (qm) {
+      const uint64_t* const mm[3] = {qm + ko + jj, qm + ko + jj + half, qm + vo + dd};
+      const bool use[3] = {act, act, act};
+      float v[3];
+      ll_gather<3>(p, c.task, mm, use, v);
+      k1 = v[0];
+      k2 = v[1];
+      vv = v[2];
+    } else if (act) {
+      k1 = __ldcg(qkv + ko + jj);
+      k2 = __ldcg(qkv + ko + jj + half);
+      vv = __ldcg(qkv + vo + dd);
+    }
+    if (act) {
       const float kr = dd < half ? k1 * cs - k2 * sn : k2 * cs + k1 * sn;
-      nkv[dd] = __bfloat16_as_ushort(__float2bfloat16_rn(kr));
-      nkv[D + dd] = __bfloat16_as_ushort(__float2bfloat16_rn(vv));
+      nkv[kk * D + dd] = __bfloat16_as_ushort(__float2bfloat16_rn(kr));
+      nkv[(T + kk) * D + dd] = __bfloat16_as_ushort(__float2bfloat16_rn(vv));
     }
   }
   cbar();
   float qr[DS], o[DS], m = -INFINITY, l = 0.f;
 #pragma unroll
   for (int e = 0; e < DS; ++e) {
-    qr[e] = hlive ? qs[h * D + sl * DS + e] : 0.f;
+    qr[e] = hlive ? qs[rr * D + sl * DS + e] : 0.f;
     o[e] = 0.f;
   }
-  const int kpw = q.R / kConsumerWarps;  // keys per warp per slot (a multiple of 8)
+  const int kpw = q.R / WPG;  // keys per warp per slot (a multiple of 8)
   for (int i = 0; i < q.nstage; ++i) {
     const int nr = min(q.R, q.jst - (q.j0 + i * q.R));
     const uint32_t slot = consume_begin(c);
     if (i == 0) trace_mark(c, 0);
     const uint32_t kb = smem_addr(c.ring + (size_t)slot * kStageBytes);
     const uint32_t vb = kb + kStageBytes / 2;
-    for (int k0 = warp * kpw; k0 < min(nr, (warp + 1) * kpw); k0 += 8)
-      partial_group8<DS>(qr, o, m, l, kb, vb, k0, min(8, nr - k0), hlive, lane);
+    if (wlive)  // cached keys precede every row's own position
+      for (int k0 = sub * kpw; k0 < min(nr, (sub + 1) * kpw); k0 += 8)
+        partial_group8<DS>(qr, o, m, l, kb, vb, k0, min(8, nr - k0), min(8, nr - k0), hlive, lane);
     consume_end(c, slot);
   }
-  if (q.has_new && warp == kConsumerWarps - 1) {
+  if (q.has_new && wlive && sub == WPG - 1) {
+    // this step's keys last: row (t, h) sees those at positions <= pos + t
     const uint32_t nb = smem_addr(nkv);
-    partial_group8<DS>(qr, o, m, l, nb, nb + D * 2, 0, 1, hlive, lane);
+    const int nlive = max(0, min(q.nn, q.pos + tq + 1 - q.nb0));
+    partial_group8<DS>(qr, o, m, l, nb, nb + T * D * 2, 0, q.nn, nlive, hlive, lane);
   }
   trace_mark(c, 1);
-  // merge the 8 warps' states
+  if (!mrg_apart) cbar();  // every warp is done with qs and nkv, which the merge area overlays
+  // merge the warps of each row group
   if (hlive) {
-    float* r = mrg + (warp * MAXG + h) * (D + 2);
+    float* r = mrg + (warp * 4 + (lane >> 3)) * (D + 2);
     if (sl == 0) {
       r[0] = m;
       r[1] = l;
@@ -1477,24 +1596,25 @@ __device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom
     for (int e = 0; e < DS; ++e) r[2 + sl * DS + e] = o[e];
   }
   cbar();
-  float* scr = rec_ptr<float>(c, kPOut) + (size_t)q.slot * G * (D + 2);
-  for (int i = tid; i < G * D; i += kConsumerThreads) {
-    const int hh = i / D, e = i % D;
+  float* scr = rec_ptr<float>(c, kPOut) + (size_t)q.slot * NR * (D + 2);
+  for (int i = tid; i < NR * D; i += kConsumerThreads) {
+    const int r = i / D, e = i - r * D;
+    const int w0 = (r >> 2) * WPG, rs = r & 3;
     float M = -INFINITY;
-    for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, mrg[(w * MAXG + hh) * (D + 2)]);
+    for (int w = w0; w < w0 + WPG; ++w) M = fmaxf(M, mrg[(w * 4 + rs) * (D + 2)]);
     float Ls = 0.f, O = 0.f;
     if (M != -INFINITY) {
-      for (int w = 0; w < kConsumerWarps; ++w) {
-        const float* r = mrg + (w * MAXG + hh) * (D + 2);
-        const float f = exp2f(r[0] - M);
-        Ls = fmaf(r[1], f, Ls);
-        O = fmaf(r[2 + e], f, O);
+      for (int w = w0; w < w0 + WPG; ++w) {
+        const float* rp = mrg + (w * 4 + rs) * (D + 2);
+        const float f = exp2f(rp[0] - M);
+        Ls = fmaf(rp[1], f, Ls);
+        O = fmaf(rp[2 + e], f, O);
       }
     }
-    scr[hh * (D + 2) + 2 + e] = O;
+    scr[r * (D + 2) + 2 + e] = O;
     if (e == 0) {
-      scr[hh * (D + 2)] = M;
-      scr[hh * (D + 2) + 1] = Ls;
+      scr[r * (D + 2)] = M;
+      scr[r * (D + 2) + 1] = Ls;
     }
   }
 }
@@ -1530,72 +1650,96 @@ __device__ __forceinline__ void lse_fold(float& M, float& Ls, float& O0, float& 
 
 __device__ void combine_task(Ctx& c, const mk_task_descriptor& d) {
   const KParams& p = *c.p;
-  const int s = d.reserved[0], g = d.reserved[1], Hkv = d.reserved[2];
+  const int s = d.reserved[0], g = d.reserved[1], Hkv = d.reserved[2] & 0xFFFFu;
+  const int T = (int)(d.reserved[2] >> 16) + 1;
   const int P = d.reserved[3], base = d.reserved[4];
-  const int D = d.n, Hq = d.k, G = Hq / Hkv;
-  const int rec = G * (D + 2);
+  const int D = d.n, Hq = d.k, G = Hq / Hkv, NR = T * G;  // query rows (token t, head h) = t * G + h
+  const int rec = NR * (D + 2);
   const float* scr = rec_ptr<const float>(c, kPIn0) + (size_t)base * rec;
   float* out = rec_ptr<float>(c, kPOut);
   uint64_t* om = rec_ptr<uint64_t>(c, kMirOut);
   if (P <= 32) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int wph = kConsumerWarps / G;  // warps per head (G divides 8)
-    const int h = warp / wph, dpw = D / wph;
-    const int e = (warp % wph) * dpw + lane * 2;
-    const bool mine = lane * 2 < dpw;
-    const float* r = scr + h * (D + 2);
-    const float mk = lane < P ? __ldcg(r + (size_t)lane * rec) : -INFINITY;
-    const float lk = lane < P ? __ldcg(r + (size_t)lane * rec + 1) : 0.f;
-    float2 ov[32];
+    // wpr warps share a row (its dims split between them) when the rows
+    // divide the 8 warps, else each warp takes whole rows in turn
+    const int wpr = (NR <= kConsumerWarps && kConsumerWarps % NR == 0) ? kConsumerWarps / NR : 1;
+    const int dpw = D / wpr;
+    for (int u = warp; u < NR * wpr; u += kConsumerWarps) {
+      const int r = u / wpr, part = u - r * wpr;
+      const int t = r / G, h = r - t * G;
+      const float* rp = scr + r * (D + 2);
+      // lane k reads partial k's (m, l) while every lane reads its first two
+      // output dims of all P partials: one L2 round trip
+      const float mk = lane < P ? __ldcg(rp + (size_t)lane * rec) : -INFINITY;
+      const float lk = lane < P ? __ldcg(rp + (size_t)lane * rec + 1) : 0.f;
+      const int e1 = (part + 1) * dpw;  // this warp's dims: [part * dpw, e1), two per lane
+      float2 ov[32];
 #pragma unroll
-    for (int k = 0; k < 32; ++k)
-      ov[k] = (k < P && mine) ? __ldcg(reinterpret_cast<const float2*>(r + (size_t)k * rec + 2 + e))
-                              : make_float2(0.f, 0.f);
-    const float M = warp_max(mk);
-    const float wk = mk == -INFINITY ? 0.f : exp2f(mk - M);
-    const float L = warp_sum(wk * lk);
-    float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-    for (int k = 0; k < 32; ++k) {
-      const float w = __shfl_sync(0xffffffffu, wk, k);
-      a0 = fmaf(w, ov[k].x, a0);
-      a1 = fmaf(w, ov[k].y, a1);
-    }
-    if (mine) {
+      for (int k = 0; k < 32; ++k)
+        ov[k] = (k < P && part * dpw + lane * 2 < e1)
+                    ? __ldcg(reinterpret_cast<const float2*>(rp + (size_t)k * rec + 2 + part * dpw + lane * 2))
+                    : make_float2(0.f, 0.f);
+      const float M = warp_max(mk);
+      const float wk = mk == -INFINITY ? 0.f : exp2f(mk - M);
+      const float L = warp_sum(wk * lk);
       const float inv = 1.f / L;
-      const size_t o = (size_t)s * Hq * D + (size_t)(g * G + h) * D + e;
-      *reinterpret_cast<float2*>(out + o) = make_float2(a0 * inv, a1 * inv);
-      if (om) st_relaxed_v2u64(om + o, ll_pack(a0 * inv, p.tag), ll_pack(a1 * inv, p.tag));
+      const size_t ob = (size_t)(s * T + t) * Hq * D + (size_t)(g * G + h) * D;
+      for (int e0 = part * dpw; e0 < e1; e0 += 64) {
+        const int e = e0 + lane * 2;
+        const bool mine = e < e1;
+        if (e0 != part * dpw) {  // a whole row of D = 128 per warp: the second 64 dims
+#pragma unroll
+          for (int k = 0; k < 32; ++k)
+            ov[k] = (k < P && mine) ? __ldcg(reinterpret_cast<const float2*>(rp + (size_t)k * rec + 2 + e))
+                                    : make_float2(0.f, 0.f);
+        }
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const float w = __shfl_sync(0xffffffffu, wk, k);
+          a0 = fmaf(w, ov[k].x, a0);
+          a1 = fmaf(w, ov[k].y, a1);
+        }
+        if (mine) {
+          *reinterpret_cast<float2*>(out + ob + e) = make_float2(a0 * inv, a1 * inv);
+          if (om) st_relaxed_v2u64(om + ob + e, ll_pack(a0 * inv, p.tag), ll_pack(a1 * inv, p.tag));
+        }
+      }
     }
     return;
   }
-  // each thread produces two adjacent outputs (e, e + 1) of one head
-  for (int i = threadIdx.x; i < G * D / 2; i += kConsumerThreads) {
-    const int h = (2 * i) / D, e = (2 * i) % D;
-    const float* r = scr + h * (D + 2);
+  // each thread produces two adjacent outputs (e, e + 1) of one row
+  for (int i = threadIdx.x; i < NR * D / 2; i += kConsumerThreads) {
+    const int r = (2 * i) / D, e = (2 * i) % D;
+    const int t = r / G, h = r - t * G;
+    const float* rp = scr + r * (D + 2);
     float M = -INFINITY, Ls = 0.f, O0 = 0.f, O1 = 0.f;
     for (int k = 0; k < P; ++k) {
-      const float* rr = r + (size_t)k * rec;
+      const float* rr = rp + (size_t)k * rec;
       const float2 ov = __ldcg(reinterpret_cast<const float2*>(rr + 2 + e));
       lse_fold(M, Ls, O0, O1, __ldcg(rr), __ldcg(rr + 1), ov.x, ov.y);
     }
     const float inv = 1.f / Ls;
-    const size_t o = (size_t)s * Hq * D + (size_t)(g * G + h) * D + e;
+    const size_t o = (size_t)(s * T + t) * Hq * D + (size_t)(g * G + h) * D + e;
     *reinterpret_cast<float2*>(out + o) = make_float2(O0 * inv, O1 * inv);
     if (om) st_relaxed_v2u64(om + o, ll_pack(O0 * inv, p.tag), ll_pack(O1 * inv, p.tag));
   }
 }
 
+// Embedding gather of token t (the descriptor's step) of sequence s: token 0
+// is the pending token in the state, later tokens of a chunk step come from
+// the step's tokens buffer.
 __device__ void embed_task(Ctx& c, const mk_task_descriptor& d) {
   const KParams& p = *c.p;
   const int s = d.reserved[0], V = d.reserved[1], H = d.n;
-  const int tok = ld_relaxed(c.state + 2 * s);
-  if (tok < 0 || tok >= V) {
+  const int T = (int)d.reserved[2] + 1, t = d.step, row = s * T + t;
+  const int tok = t == 0 ? ld_relaxed(c.state + 2 * s) : rec_ptr<const int32_t>(c, kPIn1)[(size_t)s * T + t];
+  if (tok < 0 || tok >= V || t >= T) {
     if (threadIdx.x == 0) raise_error(p, MK_DEV_BAD_INDEX, c.task);
     return;
   }
   const uint16_t* E = rec_ptr<const uint16_t>(c, kPIn0) + (size_t)tok * H;
-  float* out = rec_ptr<float>(c, kPOut) + (size_t)s * H;
+  float* out = rec_ptr<float>(c, kPOut) + (size_t)row * H;
   uint64_t* om = rec_ptr<uint64_t>(c, kMirOut);
   for (int i = threadIdx.x * 8; i < H; i += kConsumerThreads * 8) {
     const uint4 v = __ldg(reinterpret_cast<const uint4*>(E + i));
@@ -1604,7 +1748,7 @@ __device__ void embed_task(Ctx& c, const mk_task_descriptor& d) {
     *reinterpret_cast<float4*>(out + i) = a;
     *reinterpret_cast<float4*>(out + i + 4) = b;
     if (om) {
-      uint64_t* m = om + (size_t)s * H + i;
+      uint64_t* m = om + (size_t)row * H + i;
       const uint32_t t = p.tag;
       st_relaxed_v2u64(m, ll_pack(a.x, t), ll_pack(a.y, t));
       st_relaxed_v2u64(m + 2, ll_pack(a.z, t), ll_pack(a.w, t));
@@ -1652,14 +1796,18 @@ __device__ void rmsnorm_task(Ctx& c, const mk_task_descriptor& d) {
   }
 }
 
+// The argmax of the sequence's last activation row over the lm_head tiles'
+// (max, index) pairs; a chunk step of TQ tokens also records its input
+// tokens 1 .. TQ-1 in the history, and the state advances by TQ.
 __device__ void sample_task(Ctx& c, const mk_task_descriptor& d) {
   const KParams& p = *c.p;
-  const int s = d.reserved[0], B = d.m, T = d.k, cap = d.kv_len;
+  const int s = d.reserved[0], TQ = (int)d.reserved[1] + 1, M = d.m * TQ, T = d.k, cap = d.kv_len;
+  const int col = s * TQ + TQ - 1;
   const mk_argmax_pair* pairs = rec_ptr<const mk_argmax_pair>(c, kPIn0);
   float bv = -FLT_MAX;
   int bi = INT_MAX;
   for (int t = threadIdx.x; t < T; t += kConsumerThreads) {
-    const float2 pr = __ldcg(reinterpret_cast<const float2*>(pairs + (size_t)t * B + s));
+    const float2 pr = __ldcg(reinterpret_cast<const float2*>(pairs + (size_t)t * M + col));
     const int idx = __float_as_int(pr.y);
     if (pr.x > bv || (pr.x == bv && idx < bi)) {
       bv = pr.x;
@@ -1671,13 +1819,15 @@ __device__ void sample_task(Ctx& c, const mk_task_descriptor& d) {
     int32_t* state = c.state;
     int32_t* hist = rec_ptr<int32_t>(c, kPOut);
     const int pos = ld_relaxed(state + 2 * s + 1);
-    if (pos < 0 || pos + 1 >= cap) {
+    if (pos < 0 || pos + TQ >= cap) {
       raise_error(p, MK_DEV_CAPACITY, c.task);
       return;
     }
-    hist[(size_t)s * cap + pos + 1] = bi;
+    const int32_t* toks = rec_ptr<const int32_t>(c, kPIn1);
+    for (int t = 1; t < TQ; ++t) hist[(size_t)s * cap + pos + t] = toks[(size_t)s * TQ + t];
+    hist[(size_t)s * cap + pos + TQ] = bi;
     state[2 * s] = bi;
-    state[2 * s + 1] = pos + 1;
+    state[2 * s + 1] = pos + TQ;
   }
 }
 

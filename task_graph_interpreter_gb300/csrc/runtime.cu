@@ -51,6 +51,10 @@ struct DeviceState {
   float* rope_cos = nullptr;
   float* rope_sin = nullptr;
   uint64_t* trace = nullptr;
+  float* ksplit = nullptr;        // K-split partial-sum records
+  uint32_t* karr_mega = nullptr;  // K-split arrivals in megakernel steps (monotone, like the counters)
+  uint32_t* karr_step = nullptr;  // K-split arrivals in the other modes (cleared before each step)
+  size_t krecords = 0;
   uint32_t epoch = 0;
   int nstages = kMaxStages;
   cudaGraphExec_t per_op_exec = nullptr;
@@ -120,7 +124,17 @@ KParams base_params(const mk_graph* g) {
   p.num_levels = (int)g->level_off.size() - 1;
   p.nstages = d->nstages;
   p.rope_half = g->rope_D / 2;
+  p.ksplit = d->ksplit;
+  p.karr = d->karr_step;
+  p.kmul = 1;
   return p;
+}
+
+// Clear the K-split arrival counters that a non-megakernel step counts in
+// (their target is then S - 1 per block), on the step's stream.
+cudaError_t clear_step_arrivals(const DeviceState* d, cudaStream_t stream) {
+  if (!d->krecords) return cudaSuccess;
+  return cudaMemsetAsync(d->karr_step, 0, d->krecords * 4, stream);
 }
 
 // Tensor maps of the weights that B >= 8 GEMV tiles stream through the
@@ -141,7 +155,8 @@ int build_tensor_maps(const mk_graph* g, std::vector<uint8_t>& maps, std::vector
   for (const OpRec& op : g->ops) {
     if (op.kind != K_MATMUL || op.B < 8 || op.k % 64 != 0) continue;
     const int seg = (op.flags & MK_F_SILU_MUL) ? 2 : 1;
-    const int cw = tile_width(op.n, g->tiles_target, g->col_align);
+    // the tile (or, K-split, the row block) width
+    const int cw = ksplit_plan(op.n, op.k, op.flags, op.B, g->tiles_target, g->col_align).W;
     const int rgmax = seg == 2 ? 128 : 256;
     const int ng = (cw + rgmax - 1) / rgmax;
     const int rg = (cw + ng - 1) / ng;
@@ -183,11 +198,12 @@ int launch_per_op(mk_graph* g, cudaStream_t stream, uint64_t* trace, int mode = 
   KParams p = base_params(g);
   p.mode = mode;
   p.trace = trace;
+  CUDA_TRY(clear_step_arrivals(g->dev, stream));
   for (size_t i = 0; i + 1 < g->group_off.size(); ++i) {
     p.first_task = g->group_off[i];
     const int n = g->group_off[i + 1] - g->group_off[i];
     if (n <= 0) continue;
-    CUDA_TRY(launch_interpreter(p, g->B, n, false, stream));
+    CUDA_TRY(launch_interpreter(p, g->rows(), n, false, stream));
   }
   return MK_OK;
 }
@@ -208,9 +224,9 @@ extern "C" int mk_upload(mk_graph* g, void* stream_) {
     int optin = 0;
     cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, d->device);
     d->nstages = kMaxStages;
-    while (d->nstages > 2 && smem_bytes_for(d->nstages, g->B) > optin) --d->nstages;
+    while (d->nstages > 2 && smem_bytes_for(d->nstages, g->rows()) > optin) --d->nstages;
     int regs = 0;
-    if (configure_interpreter(g->B, d->nstages, &regs) != cudaSuccess) {
+    if (configure_interpreter(g->rows(), d->nstages, &regs) != cudaSuccess) {
       rc = fail(MK_ERR_CUDA, "mk_upload: cannot configure the interpreter kernel");
       break;
     }
@@ -221,7 +237,7 @@ extern "C" int mk_upload(mk_graph* g, void* stream_) {
       break;
     }
     int per_sm = 0, sms = 0;
-    if (max_coresident_ctas(g->B, d->nstages, &per_sm) != cudaSuccess || per_sm < 1) {
+    if (max_coresident_ctas(g->rows(), d->nstages, &per_sm) != cudaSuccess || per_sm < 1) {
       rc = fail(MK_ERR_CUDA, "mk_upload: the interpreter kernel cannot be resident");
       break;
     }
@@ -256,7 +272,9 @@ extern "C" int mk_upload(mk_graph* g, void* stream_) {
     for (size_t b = 0; b < NB; ++b)
       if (b < g->ll_buf.size() && g->ll_buf[b]) o_mir[b] = take((size_t)g->bufs[b].rows * g->bufs[b].cols * 8);
     const size_t o_ctr = take((size_t)g->counter_words * 4), o_status = take(16), o_lbar = take(g->level_off.size() * 4),
-                 o_trace = take(N * 64);
+                 o_trace = take(N * 64), o_kam = take((size_t)g->ksplit_records * 4),
+                 o_kas = take((size_t)g->ksplit_records * 4),
+                 o_ksp = take((size_t)g->ksplit_records * kKsplitRecFloats * 4);
     d->blob_bytes = off;
     if (cudaMalloc(&d->blob, d->blob_bytes) != cudaSuccess) {
       rc = fail(MK_ERR_NOMEM, "mk_upload: cudaMalloc of " + std::to_string(d->blob_bytes) + " bytes failed");
@@ -327,10 +345,14 @@ extern "C" int mk_upload(mk_graph* g, void* stream_) {
     d->tm_rows = reinterpret_cast<int32_t*>(base + o_tmr);
     d->mirrors = reinterpret_cast<uint64_t**>(base + o_mtab);
     for (const mk_task_descriptor& t : g->tasks)
-      if (t.op_id == MK_OP_GEMV && t.config_id == 1 && g->B > 4 && tm_rows[t.in_buf[1]] > 0) ++d->tc_tiles;
+      if (t.op_id == MK_OP_GEMV && t.config_id == 1 && g->rows() > 4 && tm_rows[t.in_buf[1]] > 0) ++d->tc_tiles;
     d->status = reinterpret_cast<int32_t*>(base + o_status);
     d->level_bar = reinterpret_cast<uint32_t*>(base + o_lbar);
     d->trace = reinterpret_cast<uint64_t*>(base + o_trace);
+    d->krecords = g->ksplit_records;
+    d->karr_mega = reinterpret_cast<uint32_t*>(base + o_kam);
+    d->karr_step = reinterpret_cast<uint32_t*>(base + o_kas);
+    d->ksplit = reinterpret_cast<float*>(base + o_ksp);
     if (cudaStreamSynchronize(stream) != cudaSuccess) {
       rc = fail(MK_ERR_CUDA, "mk_upload: stream synchronisation failed");
       break;
@@ -358,7 +380,9 @@ extern "C" int mk_decode_step_ex(mk_graph* g, void* stream_, int mode, uint32_t 
       if (++d->tag == 0) d->tag = 1;  // 0 is the zeroed mirrors' tag: never a step's
       p.tag = d->tag;
       p.trace = tr;
-      CUDA_TRY(launch_interpreter(p, g->B, g->num_ctas, true, stream));
+      p.karr = d->karr_mega;
+      p.kmul = p.epoch;
+      CUDA_TRY(launch_interpreter(p, g->rows(), g->num_ctas, true, stream));
       d->epoch += 1;
       return MK_OK;
     }
@@ -367,7 +391,8 @@ extern "C" int mk_decode_step_ex(mk_graph* g, void* stream_, int mode, uint32_t 
       p.mode = MK_MODE_LEVELS;
       p.trace = tr;
       CUDA_TRY(cudaMemsetAsync(d->level_bar, 0, g->level_off.size() * 4, stream));
-      CUDA_TRY(launch_interpreter(p, g->B, g->num_ctas, true, stream));
+      CUDA_TRY(clear_step_arrivals(d, stream));
+      CUDA_TRY(launch_interpreter(p, g->rows(), g->num_ctas, true, stream));
       return MK_OK;
     }
     case MK_MODE_PER_OP:
@@ -437,6 +462,7 @@ extern "C" int mk_status(mk_graph* g, void* stream_, int* dev_code, int32_t* tas
   if (st[kStatusCode] || st[kStatusAbort]) {
     // A failed step leaves counters part-way; start the epochs afresh.
     CUDA_TRY(cudaMemsetAsync(d->counters, 0, d->counter_words * 4, stream));
+    if (d->krecords) CUDA_TRY(cudaMemsetAsync(d->karr_mega, 0, d->krecords * 4, stream));
     CUDA_TRY(cudaMemsetAsync(d->status, 0, 16, stream));
     CUDA_TRY(cudaStreamSynchronize(stream));
     d->epoch = 0;
@@ -456,8 +482,16 @@ extern "C" int mk_debug_set_epoch(mk_graph* g, void* stream_, uint32_t epoch, ui
     ctr[c] += 1u;
   }
   for (uint32_t& c : ctr) c *= epoch;  // modulo 2^32, as the device counters run
+  // a K-split block's arrival counter gains S - 1 per megakernel step
+  std::vector<uint32_t> karr(d->krecords, 0u);
+  for (const mk_task_descriptor& t : g->tasks) {
+    const uint32_t S = (uint32_t)t.kv_len >> 16, j = (uint32_t)t.kv_len & 0xFFFFu;
+    if (t.op_id == MK_OP_GEMV && t.config_id == 1 && S >= 2 && j == S - 1 && t.reserved[4] < d->krecords)
+      karr[t.reserved[4]] = epoch * (S - 1);
+  }
   CUDA_TRY(cudaStreamSynchronize(stream));
   CUDA_TRY(cudaMemcpy(d->counters, ctr.data(), ctr.size() * 4, cudaMemcpyHostToDevice));
+  if (d->krecords) CUDA_TRY(cudaMemcpy(d->karr_mega, karr.data(), karr.size() * 4, cudaMemcpyHostToDevice));
   d->epoch = epoch;
   d->tag = tag;
   return MK_OK;
@@ -477,7 +511,7 @@ extern "C" int mk_get_trace(mk_graph* g, const uint64_t** records, size_t* count
 extern "C" int mk_kernel_info(const mk_graph* g, int* smem_bytes, int* threads, int* stages) {
   if (!g || !smem_bytes || !threads || !stages) return fail(MK_ERR_ARG, "mk_kernel_info: null argument");
   const int nst = g->dev ? g->dev->nstages : kMaxStages;
-  *smem_bytes = smem_bytes_for(nst, g->B);
+  *smem_bytes = smem_bytes_for(nst, g->rows());
   *threads = kThreads;
   *stages = nst;
   return MK_OK;

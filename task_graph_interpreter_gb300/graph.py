@@ -35,6 +35,8 @@ class Graph:
         self.h = L.mk_graph_create(num_ctas, tiles_target, col_align, wait_timeout_us)
         self.state = torch.zeros(B, 2, dtype=torch.int32, device=self.device)
         L.mk_set_state(self.h, self.state.data_ptr(), B)
+        self.T = 1             # tokens per sequence per step (set_chunk)
+        self.tokens = None     # int32 [B, T] input tokens of a chunk step
         self.bufs = []
         self.ops = []        # op records (kind, fields) in call order, for inspection
         self.uploaded = False
@@ -53,20 +55,35 @@ class Graph:
     def _fresh(self, rows, cols, dtype=torch.float32) -> Buf:
         return self.register(torch.empty(rows, cols, dtype=dtype, device=self.device))
 
+    @property
+    def rows(self) -> int:
+        """Activation rows: B * T (row s * T + t)."""
+        return self.B * self.T
+
+    def set_chunk(self, T: int) -> Buf:
+        """Make every step a chunk step of T tokens per sequence (a prefill
+        chunk or draft tokens to verify).  Returns the int32 [B, T] tokens
+        buffer the caller fills before each step with tokens 1..T-1 of each
+        sequence (column 0 is the pending token in the state)."""
+        self.tokens = self.register(torch.zeros(self.B, T, dtype=torch.int32, device=self.device))
+        L.mk_set_chunk(self.h, T, self.tokens.idx)
+        self.T = T
+        return self.tokens
+
     # ------------------------------------------------------------ ops
     def embed(self, table: Buf) -> Buf:
         H = table.tensor.shape[-1]
-        out = self._fresh(self.B, H)
+        out = self._fresh(self.rows, H)
         L.mk_add_embed(self.h, table.idx, out.idx, self.B, H)
         self.ops.append(("embed", table.idx, out.idx))
         return out
 
     def rmsnorm(self, x: Buf, gamma: Buf, residual: Buf = None, eps: float = 1e-5) -> Buf:
         """Standalone RMS norm (one task per sequence): RMSNorm(x [+ residual]) * gamma."""
-        B, H = x.tensor.shape
-        out = self._fresh(B, H)
+        M, H = x.tensor.shape
+        out = self._fresh(M, H)
         L.mk_add_rmsnorm(self.h, x.idx, gamma.idx, residual.idx if residual is not None else L.MK_NO_BUF,
-                         out.idx, B, H, eps)
+                         out.idx, self.B, H, eps)
         self.ops.append(("rmsnorm", x.idx, gamma.idx, out.idx))
         return out
 
@@ -107,8 +124,8 @@ class Graph:
                   len0, chunk: int = 0, rope_theta: float = 5e5) -> Buf:
         G = Hq // Hkv
         rows = L.mk_attention_scratch_rows(self.h, self.B, Hkv, len0, chunk)
-        scratch = self._fresh(rows, G * (D + 2))
-        out = self._fresh(self.B, Hq * D)
+        scratch = self._fresh(rows, self.T * G * (D + 2))
+        out = self._fresh(self.rows, Hq * D)
         L.mk_add_attention(self.h, qkv.idx, kcache.idx, vcache.idx, out.idx, scratch.idx, self.B, Hq, Hkv, D,
                            capacity, len0, chunk, rope_theta)
         self.ops.append(("attention", qkv.idx, kcache.idx, vcache.idx, out.idx, scratch.idx))

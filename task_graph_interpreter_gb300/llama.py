@@ -29,16 +29,20 @@ class LlamaDecode:
     kcache: list = field(default_factory=list)
     vcache: list = field(default_factory=list)
     fused_norms: int = 0                        # norms folded by the fusion pass
+    tokens: Buf = None                          # chunk steps: int32 [B, T] input tokens
 
 
 def build_llama_decode(model, B: int, len0, capacity: int, weights: dict, kcache: list, vcache: list,
                        history: torch.Tensor, chunk: int = 0, device="cuda", num_ctas: int = 0,
                        tiles_target: int = 0, col_align: int = 4, wait_timeout_us: int = 0,
-                       norms: str = "fused") -> LlamaDecode:
+                       norms: str = "fused", T: int = 1) -> LlamaDecode:
     """weights: name -> bf16 tensor (names of synth.weight_names);
     kcache/vcache: per layer bf16 [B, Hkv, capacity, D]; history int32 [B, capacity].
     norms: "fused" (RMS_NORM_INPUT on the consuming GEMVs), "standalone"
-    (RMSNORM tasks), or "fuse_pass" (standalone norms folded by the fusion pass)."""
+    (RMSNORM tasks), or "fuse_pass" (standalone norms folded by the fusion pass).
+    T > 1: every step is a chunk step of T tokens per sequence (their
+    activations are rows s * T + t); the caller writes tokens 1..T-1 into
+    ``tokens`` before each step."""
     assert norms in ("fused", "standalone", "fuse_pass")
     m = model
     g = Graph(B, device=device, num_ctas=num_ctas, tiles_target=tiles_target, col_align=col_align,
@@ -62,6 +66,8 @@ def build_llama_decode(model, B: int, len0, capacity: int, weights: dict, kcache
         out.kcache.append(reg(f"layer{l}.k_cache", kcache[l], B * m.Hkv, capacity * m.D))
         out.vcache.append(reg(f"layer{l}.v_cache", vcache[l], B * m.Hkv, capacity * m.D))
     out.history = reg("history", history)
+    if T > 1:
+        out.tokens = g.set_chunk(T)
 
     def normed(x, gamma):
         """(input, gamma kwarg) of a GEMV that reads RMSNorm(x) * gamma."""

@@ -47,6 +47,8 @@ def _replay(L, spec, B, fuse=False, g_fused=[0]):
     for i, (dt, rows, cols) in enumerate(spec["buffers"][3:], start=3):
         idx = L.mk_add_buffer(g, base + i * (1 << 24), dt, rows, cols)
         assert idx == i
+    if spec.get("T", 1) > 1:
+        L.mk_set_chunk(g, spec["T"], spec["tokens"])
     for op in spec["ops"]:
         k = op["kind"]
         if k == "embed":
@@ -295,6 +297,17 @@ def _check_sync_plan(tasks, edges, plan, ll=None):
                 assert int(tasks["out_buf"][p]) in ((x, aux) if res else (x,)), f"task {t}: parent {p}"
             assert int(tasks["remaining_deps"][t]) == len(parents[t])
             continue
+        # the last split of a K-split row block waits for its sibling splits
+        # inside its body (the block's arrival counter), not through the plan
+        S, j = int(tasks["kv_len"][t]) >> 16, int(tasks["kv_len"][t]) & 0xFFFF
+        deferred = set()
+        if int(tasks["op_id"][t]) == ol.OP_GEMV and int(tasks["config_id"][t]) == 1 and S >= 2 and j == S - 1:
+            deferred = set(range(t - (S - 1), t))
+            assert deferred <= parents[t], f"task {t}: sibling splits are not its parents"
+            for q in deferred:
+                assert int(tasks["kv_len"][q]) == (q - (t - (S - 1))) | (S << 16)
+                assert tuple(tasks["reserved"][q][:2]) == tuple(tasks["reserved"][t][:2])
+            covered = set(deferred)
         assert len({int(c) for c, _ in entries}) == len(entries)
         for c, n in entries:
             c, n = int(c), int(n)
@@ -307,7 +320,7 @@ def _check_sync_plan(tasks, edges, plan, ll=None):
             assert not (who & covered)
             covered |= who
         assert covered == parents[t], f"task {t}: waits cover {len(covered)} of {len(parents[t])} parents"
-        assert sum(int(n) for _, n in entries) == int(tasks["remaining_deps"][t])
+        assert sum(int(n) for _, n in entries) + len(deferred) == int(tasks["remaining_deps"][t])
 
 
 @pytest.mark.parametrize("name", synth.WORKLOADS)
@@ -505,3 +518,113 @@ def test_chrome_trace_export_from_records(L, tmp_path):
     assert sum(e["cat"] == "mark" for e in ev) == int(np.count_nonzero(tasks["op_id"][:N - 1] == ol.OP_GEMV))
     with pytest.raises(ValueError):
         chrome_trace(rec[:-1], tasks.tobytes())
+
+
+@pytest.mark.parametrize("name,B,T", [("tiny", 1, 4), ("tiny", 2, 4), ("tiny", 3, 2), ("1b", 2, 4), ("tiny", 8, 1),
+                                      ("8b", 2, 4), ("8b_long", 2, 2)])
+@pytest.mark.parametrize("norms", ["fused", "standalone"])
+def test_chunk_step_lowering_is_byte_identical_and_valid(L, name, B, T, norms):
+    # chunk steps (T tokens per sequence): the C++ lowering and the oracle's
+    # independent lowering agree byte for byte, and the DAG validates
+    w = synth.workload(name)
+    lens = list(w.kv_len[:B]) + [w.kv_len[0]] * max(0, B - len(w.kv_len))
+    cap = max(lens) + 2 * T + 1
+    spec = llama_decode_spec(w.model, B, lens, cap, w.chunk, 152, col_align=4, norms=norms, T=T)
+    tasks, edges = ol.lower(spec)
+    g = _replay(L, spec, B)
+    try:
+        assert L.mk_get_tasks(g) == tasks.tobytes()
+        assert np.array_equal(L.mk_get_edges(g), edges)
+    finally:
+        L.mk_destroy(g)
+    if name == "tiny":
+        validate(tasks, edges)
+    else:
+        validate(tasks, edges, check_hazards=False)
+    # per-token tasks carry their token index; T - 1 rides in the fields the spec names
+    emb = tasks[tasks["op_id"] == ol.OP_MEMCPY]
+    app = tasks[tasks["op_id"] == ol.OP_ATT_APPEND]
+    assert sorted(emb["step"].tolist()) == sorted(list(range(T)) * B)
+    assert set(app["step"].tolist()) == set(range(T))
+    assert np.all(app["reserved"][:, 2] >> 16 == T - 1)
+    assert np.all(tasks[tasks["op_id"] == ol.OP_SAMPLE]["reserved"][:, 1] == T - 1)
+
+
+def test_chunk_step_validator_catches_a_missing_causal_edge(L):
+    # the combine of a chunk step must wait for every token's append: drop
+    # one append -> combine edge and the validator reports the race
+    w = synth.workload("tiny")
+    spec = llama_decode_spec(w.model, 1, [128], 140, 0, 16, col_align=4, T=4)
+    tasks, edges = ol.lower(spec)
+    validate(tasks, edges)
+    app = [int(i) for i in np.nonzero(tasks["op_id"] == ol.OP_ATT_APPEND)[0] if tasks["step"][i] == 3]
+    t = app[0]
+    off, cnt = int(tasks["dependents_offset"][t]), int(tasks["num_dependents"][t])
+    kids = [int(c) for c in edges[off:off + cnt]]
+    comb = [c for c in kids if tasks["op_id"][c] == ol.OP_ATT_COMBINE][0]
+    bad_t = tasks.copy()
+    keep = [c for c in kids if c != comb]
+    new_edges = np.concatenate([edges[:off], np.array(keep, dtype=np.uint32), edges[off + cnt:]])
+    bad_t["num_dependents"][t] = cnt - 1
+    bad_t["dependents_offset"][t + 1:] -= 1
+    bad_t["remaining_deps"][comb] -= 1
+    with pytest.raises(AssertionError):
+        validate(bad_t, new_edges)
+
+
+def test_chunk_step_errors(L):
+    g = L.mk_graph_create(num_ctas=8)
+    try:
+        base = 1 << 40
+        L.mk_set_state(g, base, 2)
+        tok = L.mk_add_buffer(g, base + (1 << 24), L.MK_I32, 2, 4)
+        bad = L.mk_add_buffer(g, base + (2 << 24), L.MK_I32, 2, 5)
+        with pytest.raises(L.MkError):
+            L.mk_set_chunk(g, 4, bad)          # not [B, T]
+        with pytest.raises(L.MkError):
+            L.mk_set_chunk(g, 1, tok)          # T < 2
+        bigtok = L.mk_add_buffer(g, base + (3 << 24), L.MK_I32, 2, 8)
+        with pytest.raises(L.MkError):
+            L.mk_set_chunk(g, 8, bigtok)       # B * T > 8
+        L.mk_set_chunk(g, 4, tok)
+        with pytest.raises(L.MkError) as e:
+            L.mk_set_chunk(g, 4, tok)          # once
+        assert e.value.code == L.MK_ERR_STATE
+    finally:
+        L.mk_destroy(g)
+
+
+@pytest.mark.parametrize("name,num_ctas", [("tiny", 152), ("tiny", 16), ("8b_b8", 152)])
+def test_ksplit_lowering_validates(L, name, num_ctas):
+    # batch-8 GEMVs with narrow per-SM tiles become K-split row blocks: the
+    # DAG (splits -> the block's last split -> readers) validates, each
+    # block's splits cover K exactly once in order, and its last split is
+    # the only writer of the block's outputs
+    w = synth.workload(name) if name != "tiny" else synth.custom(synth.TINY, 8, [128] * 8, 2, name="tiny8")
+    spec = llama_decode_spec(w.model, w.B, w.kv_len, w.capacity, w.chunk, num_ctas, col_align=4)
+    tasks, edges = ol.lower(spec)
+    validate(tasks, edges, check_hazards=(name == "tiny"))
+    g = _replay(L, spec, w.B)
+    try:
+        assert L.mk_get_tasks(g) == tasks.tobytes()
+    finally:
+        L.mk_destroy(g)
+    gemv = tasks[tasks["op_id"] == ol.OP_GEMV]
+    split = gemv[(gemv["kv_len"] >> 16) >= 2]
+    assert len(split) > 0
+    K = {}
+    for d in split:
+        key = (int(d["in_buf"][1]), int(d["reserved"][0]), int(d["in_buf"][0]))
+        K.setdefault(key, []).append((int(d["kv_len"]) & 0xFFFF, int(d["reserved"][3]) & 0xFFFF,
+                                      int(d["reserved"][3]) >> 16, int(d["k"]), int(d["kv_len"]) >> 16))
+    for key, parts in K.items():
+        parts.sort()
+        S = parts[0][4]
+        assert [p[0] for p in parts] == list(range(S))
+        col = 0
+        for (_, k0, kn, k, _) in parts:
+            assert k0 == col and kn % 64 == 0 and kn > 0
+            col += kn
+        assert col == parts[0][3]
+    # every split tile of an op fits the tile target; rows per block <= 256 / seg
+    assert np.all(split["reserved"][:, 1] * np.where(split["flags"] & ol.F_SILU_MUL, 2, 1) <= 256)

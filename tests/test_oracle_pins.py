@@ -239,8 +239,13 @@ def test_lowered_graph_validates(name):
     # every layer's tasks, the lm_head tiles and SAMPLE are present (a timed
     # step that skips layers or the lm_head would not contain them)
     n_gemv = int((tasks["op_id"] == ol.OP_GEMV).sum())
-    T = lambda n: len(ol.tiles(n, 152, 16))
-    assert n_gemv == m.L * (T(m.n_qkv) + T(m.H) + T(m.F) + T(m.H)) + T(m.V)
+
+    def T(n, k, flags):  # GEMV tasks of an op: tiles, or row blocks x K splits
+        _, nb, S = ol.ksplit_plan(n, k, flags, w.B, 152, 16)
+        return nb * S
+    per_layer = (T(m.n_qkv, m.H, ol.F_RMS_NORM_INPUT) + T(m.H, m.Hq * m.D, ol.F_ADD_RESIDUAL)
+                 + T(m.F, m.H, ol.F_RMS_NORM_INPUT | ol.F_SILU_MUL) + T(m.H, m.F, ol.F_ADD_RESIDUAL))
+    assert n_gemv == m.L * per_layer + T(m.V, m.H, ol.F_RMS_NORM_INPUT | ol.F_ARGMAX_EPI)
     assert int((tasks["op_id"] == ol.OP_SAMPLE).sum()) == w.B
     assert int((tasks["op_id"] == ol.OP_ATT_APPEND).sum()) == m.L * w.B * m.Hkv
     assert st["levels"] > 0
