@@ -1388,14 +1388,17 @@ __device__ void append_task(Ctx& c, const mk_task_descriptor& d) {
 
 // Eight keys of the online softmax (base 2) for four query rows (a KV
 // group's heads, or (token, head) rows of a chunk step).  Lane = 8 * row +
-// slice: the lane holds dims [slice * DS, slice * DS + DS) of its row's
-// query (qr) and output (o); m and l are its row's running max and sum
-// (equal in the row's 8 lanes).  Keys k0 .. k0 + 7 (nvalid of them real)
-// are read from shared memory (rows of DS * 8 bf16 at kb and vb): each lane
-// reads its slice of every key, so the four rows' lanes share each
-// address.  A score needs a sum over the row's 8 lanes only: a transposed
-// reduction leaves key `slice`'s score in that lane.  The row sees only its
-// first nlive of the keys (causal masking in a chunk step; nvalid else).
+// slice: the lane holds dims {c * 64 + slice * 8 + [0, 8) : c < DS / 8} of
+// its row's query (qr) and output (o), element c * 8 + e at dim c * 64 +
+// slice * 8 + e, so that the 8 slices of a 16-byte load cover 128
+// consecutive bytes (every bank once); m and l are its row's running max and
+// sum (equal in the row's 8 lanes).  Keys k0 .. k0 + 7 (nvalid of them
+// real) are read from shared memory (rows of DS * 8 bf16 at kb and vb):
+// each lane reads its slices of every key, so the four rows' lanes share
+// each address.  A score needs a sum over the row's 8 lanes only: a
+// transposed reduction leaves key `slice`'s score in that lane.  The row
+// sees only its first nlive of the keys (causal masking in a chunk step;
+// nvalid else).
 template <int DS>
 __device__ __forceinline__ void partial_group8(const float (&qr)[DS], float (&o)[DS], float& m, float& l,
                                                uint32_t kb, uint32_t vb, int k0, int nvalid, int nlive,
@@ -1405,11 +1408,11 @@ __device__ __forceinline__ void partial_group8(const float (&qr)[DS], float (&o)
   float v[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const uint32_t a = kb + (uint32_t)((k0 + (j < nvalid ? j : 0)) * D + sl * DS) * 2;
+    const uint32_t a = kb + (uint32_t)((k0 + (j < nvalid ? j : 0)) * D) * 2 + (uint32_t)sl * 16;
     float sc = 0.f;
 #pragma unroll
     for (int c4 = 0; c4 < DS / 8; ++c4) {
-      const uint4 w = lds128(a + c4 * 16);
+      const uint4 w = lds128(a + c4 * 128);
       const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -1450,10 +1453,10 @@ __device__ __forceinline__ void partial_group8(const float (&qr)[DS], float (&o)
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const float pj = __shfl_sync(0xffffffffu, pr, hb | j);
-    const uint32_t a = vb + (uint32_t)((k0 + (j < nvalid ? j : 0)) * D + sl * DS) * 2;
+    const uint32_t a = vb + (uint32_t)((k0 + (j < nvalid ? j : 0)) * D) * 2 + (uint32_t)sl * 16;
 #pragma unroll
     for (int c4 = 0; c4 < DS / 8; ++c4) {
-      const uint4 w = lds128(a + c4 * 16);
+      const uint4 w = lds128(a + c4 * 128);
       const uint32_t u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
@@ -1473,19 +1476,21 @@ __device__ __forceinline__ void partial_group8(const float (&qr)[DS], float (&o)
 // from qkv, rotated and rounded to bf16 exactly as ATTENTION_APPEND stores
 // them, so the partial does not wait for the appends.  Writes (m, l, o[D])
 // per row to the chunk's scratch slot.
-template <int DS>  // dims per lane: D / 8
+// CH: a chunk step (T >= 1 tokens, loops over rows and keys); else a decode
+// step, T = 1, specialised at compile time.
+template <int DS, bool CH>  // dims per lane: D / 8
 __device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom& q) {
   constexpr int D = DS * 8;
   const KParams& p = *c.p;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int G = q.G, T = q.T, NR = G * T, half = D / 2;
-  const int NGR = (NR + 3) >> 2;         // groups of four rows
-  const int WPG = kConsumerWarps / NGR;  // warps per group
-  const int grp = warp / WPG, sub = warp - grp * WPG;
+  const int G = q.G, T = CH ? q.T : 1, NR = CH ? G * T : G, half = D / 2;
+  const int NGR = CH ? (NR + 3) >> 2 : 1;                  // groups of four rows
+  const int WPG = CH ? kConsumerWarps / NGR : kConsumerWarps;  // warps per group
+  const int grp = CH ? warp / WPG : 0, sub = warp - grp * WPG;
   const bool wlive = grp < NGR;
   const int rr = grp * 4 + (lane >> 3), sl = lane & 7;
   const bool hlive = wlive && rr < NR;
-  const int tq = hlive ? rr / G : 0;     // the row's token
+  const int tq = CH && hlive ? rr / G : 0;  // the row's token
   // shared scratch: qs [NR][D] rotated, scaled queries; nkv this step's keys
   // [T][D] then values [T][D] (bf16); mrg [8 warps][4][D + 2] after them,
   // or over them (after a barrier) when the three do not fit side by side
@@ -1499,6 +1504,45 @@ __device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom
   const uint64_t* qm = rec_ptr<const uint64_t>(c, kMirX);  // tagged qkv (MEGA, B <= 4), else null
   if (qm) qm += row0;
   const float scale = 1.4426950408889634f / sqrtf((float)D);
+  if constexpr (!CH) {
+    // one pass, every load in flight at once: thread tid rotates query pair
+    // (tid / half, tid % half) of the group's heads and, in the chunk that
+    // holds the new token, stages dim tid of its key and value
+    const bool act = tid < G * half, nact = q.has_new && tid < D;
+    const int h = act ? tid / half : 0, j = tid - h * half;
+    const int dd = tid, jj = dd < half ? dd : dd - half;
+    const size_t o = (size_t)(q.g * G + h) * D + j;
+    const size_t ko = (size_t)q.Hq * D + (size_t)q.g * D, vo = (size_t)(q.Hq + q.Hkv) * D + (size_t)q.g * D;
+    // the table rows do not depend on qkv: their loads go out before the wait
+    const size_t tr = (size_t)q.pos * p.rope_half;
+    const float cs = act ? __ldg(p.rope_cos + tr + j) : 1.f, sn = act ? __ldg(p.rope_sin + tr + j) : 0.f;
+    const float ncs = nact ? __ldg(p.rope_cos + tr + jj) : 1.f, nsn = nact ? __ldg(p.rope_sin + tr + jj) : 0.f;
+    float v[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+    if (qm) {
+      const uint64_t* const mm[5] = {qm + o, qm + o + half, qm + ko + jj, qm + ko + jj + half, qm + vo + dd};
+      const bool use[5] = {act, act, nact, nact, nact};
+      ll_gather<5>(p, c.task, mm, use, v);
+    } else {
+      if (act) {
+        v[0] = __ldcg(qkv + o);
+        v[1] = __ldcg(qkv + o + half);
+      }
+      if (nact) {
+        v[2] = __ldcg(qkv + ko + jj);
+        v[3] = __ldcg(qkv + ko + jj + half);
+        v[4] = __ldcg(qkv + vo + dd);
+      }
+    }
+    if (act) {
+      qs[h * D + j] = (v[0] * cs - v[1] * sn) * scale;
+      qs[h * D + j + half] = (v[1] * cs + v[0] * sn) * scale;
+    }
+    if (nact) {
+      const float kr = dd < half ? v[2] * ncs - v[3] * nsn : v[3] * ncs + v[2] * nsn;
+      nkv[dd] = __bfloat16_as_ushort(__float2bfloat16_rn(kr));
+      nkv[D + dd] = __bfloat16_as_ushort(__float2bfloat16_rn(v[4]));
+    }
+  } else {
   // RoPE on the rows' queries: item (row, j) rotates the pair (j, j + D/2)
   for (int base = 0; base < NR * half; base += kConsumerThreads) {
     const int i = base + tid;
@@ -1558,11 +1602,12 @@ __device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom
       nkv[(T + kk) * D + dd] = __bfloat16_as_ushort(__float2bfloat16_rn(vv));
     }
   }
+  }
   cbar();
   float qr[DS], o[DS], m = -INFINITY, l = 0.f;
 #pragma unroll
-  for (int e = 0; e < DS; ++e) {
-    qr[e] = hlive ? qs[rr * D + sl * DS + e] : 0.f;
+  for (int e = 0; e < DS; ++e) {  // element e: dim (e / 8) * 64 + sl * 8 + e % 8
+    qr[e] = hlive ? qs[rr * D + (e >> 3) * 64 + sl * 8 + (e & 7)] : 0.f;
     o[e] = 0.f;
   }
   const int kpw = q.R / WPG;  // keys per warp per slot (a multiple of 8)
@@ -1593,7 +1638,7 @@ __device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom
       r[1] = l;
     }
 #pragma unroll
-    for (int e = 0; e < DS; ++e) r[2 + sl * DS + e] = o[e];
+    for (int e = 0; e < DS; ++e) r[2 + (e >> 3) * 64 + sl * 8 + (e & 7)] = o[e];
   }
   cbar();
   float* scr = rec_ptr<float>(c, kPOut) + (size_t)q.slot * NR * (D + 2);
@@ -1626,8 +1671,13 @@ __device__ void partial_task(Ctx& c, const mk_task_descriptor& d) {
     if (threadIdx.x == 0) raise_error(*c.p, MK_DEV_CAPACITY, c.task);
     return;
   }
-  if (q.D == 128) partial_body<16>(c, d, q);
-  else partial_body<8>(c, d, q);
+  if (q.T == 1) {
+    if (q.D == 128) partial_body<16, false>(c, d, q);
+    else partial_body<8, false>(c, d, q);
+  } else {
+    if (q.D == 128) partial_body<16, true>(c, d, q);
+    else partial_body<8, true>(c, d, q);
+  }
 }
 
 // Log-sum-exp merge of the P partials of one (sequence, kv head):
@@ -1658,6 +1708,41 @@ __device__ void combine_task(Ctx& c, const mk_task_descriptor& d) {
   const float* scr = rec_ptr<const float>(c, kPIn0) + (size_t)base * rec;
   float* out = rec_ptr<float>(c, kPOut);
   uint64_t* om = rec_ptr<uint64_t>(c, kMirOut);
+  if (P <= 32 && T == 1 && kConsumerWarps % G == 0) {
+    // decode step: 8 / G warps per head, two output dims per lane; lane k
+    // reads partial k's (m, l) while every lane reads its dims of all P
+    // partials at once (one L2 round trip)
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wph = kConsumerWarps / G;
+    const int h = warp / wph, dpw = D / wph;
+    const int e = (warp % wph) * dpw + lane * 2;
+    const bool mine = lane * 2 < dpw;
+    const float* r = scr + h * (D + 2);
+    const float mk = lane < P ? __ldcg(r + (size_t)lane * rec) : -INFINITY;
+    const float lk = lane < P ? __ldcg(r + (size_t)lane * rec + 1) : 0.f;
+    float2 ov[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k)
+      ov[k] = (k < P && mine) ? __ldcg(reinterpret_cast<const float2*>(r + (size_t)k * rec + 2 + e))
+                              : make_float2(0.f, 0.f);
+    const float M = warp_max(mk);
+    const float wk = mk == -INFINITY ? 0.f : exp2f(mk - M);
+    const float L = warp_sum(wk * lk);
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+      const float w = __shfl_sync(0xffffffffu, wk, k);
+      a0 = fmaf(w, ov[k].x, a0);
+      a1 = fmaf(w, ov[k].y, a1);
+    }
+    if (mine) {
+      const float inv = 1.f / L;
+      const size_t o = (size_t)s * Hq * D + (size_t)(g * G + h) * D + e;
+      *reinterpret_cast<float2*>(out + o) = make_float2(a0 * inv, a1 * inv);
+      if (om) st_relaxed_v2u64(om + o, ll_pack(a0 * inv, p.tag), ll_pack(a1 * inv, p.tag));
+    }
+    return;
+  }
   if (P <= 32) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // wpr warps share a row (its dims split between them) when the rows
