@@ -25,8 +25,14 @@ constexpr int kStageElems = kStageBytes / 2;     // bf16 elements per slot
 constexpr int kMaxStages = 6;
 constexpr int kScratchBytes = 24576;             // per-task shared scratch
 constexpr int kXbufBytes = 24576;                // B >= 8 kernel: two 12 KB activation staging tiles
-constexpr int kTmemCols = 256;                   // B >= 8 kernel: tensor-memory accumulator columns
+constexpr int kTmemCols = 256;                   // B >= 8 kernel: GEMV accumulator columns
+// Tensor memory per batch class: the B >= 8 kernel holds the GEMV
+// accumulators (256 columns) and, after them, the split-KV partials' two
+// 16-column score buffers; the others only the score buffers.
+__host__ __device__ constexpr uint32_t tmem_cols(int bclass) { return bclass == 2 ? 512u : 32u; }
+__host__ __device__ constexpr uint32_t tmem_part_col(int bclass) { return bclass == 2 ? 256u : 0u; }
 constexpr int kTmapBytes = 128;                  // one CUtensorMap
+constexpr int kKeyBlockRows = 128;               // keys per K box of the tensor-core split-KV partials
 constexpr int kRecs = 8;                         // task-record FIFO entries (a power of two)
 constexpr int kRecBytes = 256;                   // one task record
 constexpr int kSlotFloats = 4096;                // GEMV per-warp partial slots

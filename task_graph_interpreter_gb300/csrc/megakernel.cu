@@ -188,10 +188,23 @@ __device__ __forceinline__ void tc_geom(int rows, const mk_task_descriptor& d, T
 // steps (streamed through the ring), keys from pos on are this step's rows,
 // taken from qkv.
 struct PartGeom {
-  int s, g, Hkv, T, c, P, slot, D, Hq, G, cap, pos, j0, j1, jst, nb0, nn, R, nstage;
+  int s, g, Hkv, T, c, P, slot, D, Hq, G, cap, pos, j0, j1, jst, nb0, nn, R, nstage, nblk;
   bool has_new;
   bool bad;
 };
+
+// Tensor-core partials: the chunk's cached keys in blocks of kKeyBlock, each
+// block's K rows brought by 2-D TMA in the 128-byte swizzle (boxes of 64
+// dims x kKeyBlock rows) and its V rows by a bulk copy; used when the K
+// cache has a tensor map, the query rows (T tokens x G heads) number at most
+// four and the chunk holds at least two blocks of cached keys (for a single
+// block the tensor-core round trips cost more than the CUDA-core partial).
+constexpr int kKeyBlock = kKeyBlockRows;
+
+__device__ __forceinline__ bool tc_partial(const mk_task_descriptor& d, int tm_rows, int nblk) {
+  const int Hkv = (int)(d.reserved[2] & 0xFFFFu), T = (int)(d.reserved[2] >> 16) + 1;
+  return tm_rows == kKeyBlock && (d.k / Hkv) * T <= 4 && nblk >= 2;
+}
 
 __device__ __forceinline__ void part_geom(const int32_t* state, const mk_task_descriptor& d, PartGeom& q) {
   q.s = (int)d.reserved[0];
@@ -210,6 +223,7 @@ __device__ __forceinline__ void part_geom(const int32_t* state, const mk_task_de
   if (q.bad) {
     q.j0 = q.j1 = q.jst = q.nb0 = q.nn = 0;
     q.nstage = 0;
+    q.nblk = 0;
     q.R = 1;
     q.has_new = false;
     return;
@@ -224,6 +238,7 @@ __device__ __forceinline__ void part_geom(const int32_t* state, const mk_task_de
   q.R = (kStageBytes / 4) / q.D;  // rows of K and of V per slot
   const int nrows = max(0, q.jst - q.j0);
   q.nstage = (nrows + q.R - 1) / q.R;
+  q.nblk = (nrows + kKeyBlock - 1) / kKeyBlock;
   q.has_new = q.nn > 0;
 }
 
@@ -231,19 +246,27 @@ __device__ __forceinline__ void part_geom(const int32_t* state, const mk_task_de
 // Shared-memory words and mbarriers after the ring's full/empty barriers.
 struct TcCtl {
   volatile int32_t run;            // consumers: 1 while the current task may run
-  uint32_t tmem;                   // B >= 8 kernel: tensor-memory base address
+  uint32_t tmem;                   // tensor-memory base address
   volatile int32_t mb_task;        // mailbox to the MMA warp: task index, -1 = no more tasks
-  volatile uint32_t mb_slot;       //   ring slot and phase parity of its first weight slot
+  volatile uint32_t mb_slot;       //   ring slot and phase parity of its first weight / key slot
   volatile uint32_t mb_phase;
-  uint32_t pad[3];
-  uint64_t mma_bar[2];             // commit of each K range (alternating)
-  uint64_t x_full[2];              // a K range's activations are staged (one arrival per consumer warp)
-  uint64_t acc_full;               // commit after a row group's last MMA
-  uint64_t acc_empty;              // the consumers have read the accumulators
+  volatile uint32_t mb_nblk;       //   split-KV partial: blocks of 128 cached keys
+  volatile uint32_t mb_qt;         //   split-KV partial: shared address of the query tile
+  uint32_t pad;
+  uint64_t mma_bar[2];             // GEMV: commit of each K range (alternating)
+  uint64_t x_full[2];              // GEMV: a K range's activations are staged (one arrival per consumer warp)
+  uint64_t acc_full;               // GEMV: commit after a row group's last MMA
+  uint64_t acc_empty;              // GEMV: the consumers have read the accumulators
   uint64_t task_go;                // the mailbox holds a task
+  uint64_t s_full[2];              // partial: commit of a key block's scores (alternating buffers)
+  uint64_t s_empty[2];             // partial: the softmax warps have read a score buffer
+  uint64_t q_full;                 // partial: the query tile is staged (one arrival per consumer warp)
+  uint64_t p_full[2];              // partial: a block's probabilities are written (softmax warps)
+  uint64_t p_empty[2];             // partial: the P V warps have read them
+  uint64_t pad2;
 };
-static_assert(sizeof(TcCtl) == 88, "control block layout");
-constexpr int kCtlBytes = 96;
+static_assert(sizeof(TcCtl) == 168, "control block layout");
+constexpr int kCtlBytes = 192;
 
 // ------------------------------------------------------------------ task records
 // A warp of the producer group walks the CTA's task order ahead of the
@@ -372,6 +395,32 @@ __device__ void producer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
         prefetch_l2(p.rope_cos + (size_t)q.pos * p.rope_half, (uint32_t)p.rope_half * 4u);
         prefetch_l2(p.rope_sin + (size_t)q.pos * p.rope_half, (uint32_t)p.rope_half * 4u);
       }
+      if (tc_partial(d, tmr, q.nblk)) {
+        // per block of kKeyBlock cached keys: the K rows through the tensor
+        // map (D / 64 boxes), then the V rows (D = 128: a slot each; D = 64:
+        // K in the first half of one slot, V in the second)
+        const uint8_t* kmap = p.tmaps + (size_t)d.in_buf[1] * kTmapBytes;
+        const uint32_t kbytes = (uint32_t)(q.D / 64) * kKeyBlock * 128u;
+        for (int b = 0; b < q.nblk && !stop; ++b) {
+          const int j = q.j0 + b * kKeyBlock;
+          const int nr = min(kKeyBlock, q.jst - j);
+          const uint32_t vbytes = (uint32_t)nr * q.D * 2u;
+          uint64_t* fb;
+          uint8_t* dst = produce_slot(p, ring, full, empty, rp, issued, task, q.D == 128 ? kbytes : kbytes + vbytes, &fb);
+          if (!dst) { stop = true; break; }
+          for (int kb = 0; kb < q.D / 64; ++kb)
+            tma_load_2d(dst + (size_t)kb * kKeyBlock * 128, kmap, kb * 64, (int32_t)(rowbase + j), fb, pol);
+          if (q.D == 128) {
+            dst = produce_slot(p, ring, full, empty, rp, issued, task, vbytes, &fb);
+            if (!dst) { stop = true; break; }
+            bulk_g2s(dst, Vc + (rowbase + j) * q.D, vbytes, fb, pol);
+          } else {
+            bulk_g2s(dst + kbytes, Vc + (rowbase + j) * q.D, vbytes, fb, pol);
+          }
+        }
+        mbar_arrive(&rempty[e]);
+        continue;
+      }
       for (int i = 0; i < q.nstage && !stop; ++i) {
         const int j = q.j0 + i * q.R;
         const int nr = min(q.R, q.jst - j);
@@ -437,7 +486,10 @@ __device__ void record_warp(const KParams& p, TaskRec* recs, uint64_t* rfull, ui
       (&r->w0)[lane - 8] = ov;  // w0, nw, s0, ns hold the four offsets for now
     } else if (lane == 12) {
       const uint32_t in1 = d.in_buf[1];
-      r->tm_rows = (d.op_id == MK_OP_GEMV && d.config_id == 1 && in1 < (uint32_t)p.num_bufs) ? p.tm_rows[in1] : 0;
+      r->tm_rows = ((d.op_id == MK_OP_GEMV && d.config_id == 1) || d.op_id == MK_OP_ATTENTION_PARTIAL) &&
+                           in1 < (uint32_t)p.num_bufs
+                       ? p.tm_rows[in1]
+                       : 0;
     }
     __syncwarp();
     const uint32_t wb = r->w0, we = r->nw, sb = r->s0, se = r->ns;
@@ -473,6 +525,7 @@ struct Ctx {
   uint32_t tc_ph;       // completed phases seen: mma_bar[0] (bit 0), mma_bar[1] (bit 1), acc_full (bit 2)
   const TaskRec* rec;   // the current task's record
   int32_t* state;       // the decode state (token, position) per sequence
+  uint32_t pcol;        // tensor-memory column of the partials' score buffers
 };
 
 template <class T>
@@ -1260,11 +1313,19 @@ __device__ void tc_gemv_task(Ctx& c, const mk_task_descriptor& d) {
 // range's ring slots back to the producer.  Every wait is bounded; after a
 // failed wait no more MMAs are issued but every commit still is, so the
 // consumers' waits end.
+// Split-KV partials (any batch class) come through the same mailbox: per
+// block of kKeyBlock cached keys the warp waits for the block's K slot,
+// issues S^T[keys x 16] = K [keys x D] * Q^T (the query tile: three bf16
+// parts of each query row, K-major, 128-byte swizzle) into score buffer b % 2
+// at column pcol, and commits to s_full[b % 2]; before reusing a buffer it
+// waits until the softmax warps have read it (s_empty).
 __device__ void tc_mma_warp(const KParams& p, uint8_t* ring, uint64_t* full, uint64_t* empty, TcCtl* ctl,
-                            uint32_t xb0, uint32_t taddr) {
+                            uint32_t xb0, uint32_t taddr, uint32_t pcol) {
   if ((threadIdx.x & 31) != 0) return;
   const int nst = p.nstages;
-  uint32_t ph = 0;  // completed phases seen: task_go 0, x_full 1-2, mma_bar 3-4, acc_empty 5
+  // completed phases seen: task_go 0, x_full 1-2, mma_bar 3-4, acc_empty 5,
+  // s_empty 6-7, q_full 8
+  uint32_t ph = 0;
   bool first = true, ok = true;
   const uint64_t t0 = globaltimer();
   for (;;) {
@@ -1280,6 +1341,36 @@ __device__ void tc_mma_warp(const KParams& p, uint8_t* ring, uint64_t* full, uin
     RingPos rp, rel;
     rp.slot = rel.slot = ctl->mb_slot;
     rp.phase = rel.phase = ctl->mb_phase;
+    if (__ldg(&p.tasks[task].op_id) == MK_OP_ATTENTION_PARTIAL) {
+      const int D = __ldg(&p.tasks[task].n), nblk = (int)ctl->mb_nblk;
+      const uint32_t qt = ctl->mb_qt;
+      constexpr uint32_t NQ = 16;  // query tile rows: 3 parts x up to 4 query rows, padded
+      const uint32_t idesc = idesc_bf16_f32(kKeyBlock, NQ);
+      if (!bar_wait(p, &ctl->q_full, (ph >> 8) & 1u, task, false)) ok = false;
+      ph ^= 1u << 8;
+      for (int b = 0; b < nblk; ++b) {
+        const int j = b & 1;
+        if (b >= 2) {  // the softmax warps have read buffer j (block b - 2)
+          if (!bar_wait(p, &ctl->s_empty[j], (ph >> (6 + j)) & 1u, task, false)) ok = false;
+          ph ^= 1u << (6 + j);
+        }
+        if (ok && !bar_wait(p, &full[rp.slot], rp.phase, task, true)) ok = false;
+        tc_fence_after();
+        if (ok) {
+          const uint32_t ka = smem_addr(ring + (size_t)rp.slot * kStageBytes);
+#pragma unroll 1
+          for (int q = 0; q < D / 16; ++q) {  // 64-dim box q / 4, K step q % 4
+            const uint32_t kb = (uint32_t)q >> 2, ks = (uint32_t)q & 3u;
+            tc_mma_bf16(taddr + pcol + (uint32_t)j * NQ, smem_desc_sw128(ka + kb * (kKeyBlock * 128u), 1024u) + ks * 2u,
+                        smem_desc_sw128(qt + kb * (NQ * 128u), 1024u) + ks * 2u, idesc, q != 0 ? 1u : 0u);
+          }
+        }
+        tc_commit(&ctl->s_full[j]);  // also when a wait failed, so the consumers' waits end
+        rp.advance(nst);
+        if (D == 128) rp.advance(nst);  // the block's V slot
+      }
+      continue;
+    }
     // only the fields the schedule needs (this warp runs on few registers)
     const mk_task_descriptor* td = p.tasks + task;
     const int cn = (int)__ldg(&td->reserved[1]);
@@ -1476,28 +1567,18 @@ __device__ __forceinline__ void partial_group8(const float (&qr)[DS], float (&o)
 // from qkv, rotated and rounded to bf16 exactly as ATTENTION_APPEND stores
 // them, so the partial does not wait for the appends.  Writes (m, l, o[D])
 // per row to the chunk's scratch slot.
-// CH: a chunk step (T >= 1 tokens, loops over rows and keys); else a decode
-// step, T = 1, specialised at compile time.
-template <int DS, bool CH>  // dims per lane: D / 8
-__device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom& q) {
+// The partial's inputs from qkv: qs [NR][D] the rotated query rows, scaled
+// by log2(e) / sqrt(D) (row t * G + h: token t, head h of the KV group), and
+// nkv this step's keys in the chunk [nn][D] then their values (from row T
+// on), rotated and rounded to bf16 exactly as ATTENTION_APPEND stores them.
+// CH: a chunk step (T >= 1 tokens); else a decode step, T = 1, specialised
+// at compile time.  Ends before the barrier that publishes qs and nkv.
+template <int DS, bool CH>
+__device__ __forceinline__ void partial_stage(Ctx& c, const PartGeom& q, float* qs, uint16_t* nkv) {
   constexpr int D = DS * 8;
   const KParams& p = *c.p;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int tid = threadIdx.x;
   const int G = q.G, T = CH ? q.T : 1, NR = CH ? G * T : G, half = D / 2;
-  const int NGR = CH ? (NR + 3) >> 2 : 1;                  // groups of four rows
-  const int WPG = CH ? kConsumerWarps / NGR : kConsumerWarps;  // warps per group
-  const int grp = CH ? warp / WPG : 0, sub = warp - grp * WPG;
-  const bool wlive = grp < NGR;
-  const int rr = grp * 4 + (lane >> 3), sl = lane & 7;
-  const bool hlive = wlive && rr < NR;
-  const int tq = CH && hlive ? rr / G : 0;  // the row's token
-  // shared scratch: qs [NR][D] rotated, scaled queries; nkv this step's keys
-  // [T][D] then values [T][D] (bf16); mrg [8 warps][4][D + 2] after them,
-  // or over them (after a barrier) when the three do not fit side by side
-  float* qs = c.scratch;
-  uint16_t* nkv = reinterpret_cast<uint16_t*>(c.scratch + NR * D);
-  const bool mrg_apart = (NR * D * 4 + 2 * T * D * 2 + kConsumerWarps * 4 * (D + 2) * 4) <= kScratchBytes;
-  float* mrg = mrg_apart ? c.scratch + NR * D + T * D : c.scratch;  // nkv takes T * D floats
   const size_t rowlen = (size_t)(q.Hq + 2 * q.Hkv) * D;
   const size_t row0 = (size_t)q.s * q.T * rowlen;  // the sequence's first activation row
   const float* qkv = rec_ptr<const float>(c, kPIn0) + row0;
@@ -1603,6 +1684,30 @@ __device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom
     }
   }
   }
+}
+
+// CH: a chunk step (T >= 1 tokens, loops over rows and keys); else a decode
+// step, T = 1, specialised at compile time.
+template <int DS, bool CH>  // dims per lane: D / 8
+__device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom& q) {
+  constexpr int D = DS * 8;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = q.G, T = CH ? q.T : 1, NR = CH ? G * T : G;
+  const int NGR = CH ? (NR + 3) >> 2 : 1;                  // groups of four rows
+  const int WPG = CH ? kConsumerWarps / NGR : kConsumerWarps;  // warps per group
+  const int grp = CH ? warp / WPG : 0, sub = warp - grp * WPG;
+  const bool wlive = grp < NGR;
+  const int rr = grp * 4 + (lane >> 3), sl = lane & 7;
+  const bool hlive = wlive && rr < NR;
+  const int tq = CH && hlive ? rr / G : 0;  // the row's token
+  // shared scratch: qs [NR][D] rotated, scaled queries; nkv this step's keys
+  // [T][D] then values [T][D] (bf16); mrg [8 warps][4][D + 2] after them,
+  // or over them (after a barrier) when the three do not fit side by side
+  float* qs = c.scratch;
+  uint16_t* nkv = reinterpret_cast<uint16_t*>(c.scratch + NR * D);
+  const bool mrg_apart = (NR * D * 4 + 2 * T * D * 2 + kConsumerWarps * 4 * (D + 2) * 4) <= kScratchBytes;
+  float* mrg = mrg_apart ? c.scratch + NR * D + T * D : c.scratch;  // nkv takes T * D floats
+  partial_stage<DS, CH>(c, q, qs, nkv);
   cbar();
   float qr[DS], o[DS], m = -INFINITY, l = 0.f;
 #pragma unroll
@@ -1664,6 +1769,258 @@ __device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom
   }
 }
 
+// Split-KV partial on tensor cores, for at most four query rows (token t,
+// head h = row t * G + h).  The query tile (the three bf16 parts of each
+// rotated, scaled query row: tile row 3 r + part) is staged once; per block
+// of kKeyBlock cached keys the MMA warp computes S^T = K Q^T into a score
+// buffer.  Warps 0-3 (softmax warps; one key per thread: tensor-memory lane
+// = key) add the parts, take the block's row maxima, the new running maxima
+// and the probabilities p = 2^(s - m) (a block-wise online softmax: the
+// output sums of a block share one scale per row) and hand them, with the
+// rescale factors, to warps 4-7 (P V warps), which accumulate P V on CUDA
+// cores (warp w: keys w - 4, w, ...; lane: D / 32 dims) from the block's V
+// rows while the softmax warps go on to the next block.  This step's keys
+// (from qkv) are block 0 of that hand-off when the chunk holds some.  At
+// the end the four P V warps' sums are added in warp order.
+template <int DS, bool CH>
+__device__ void tc_partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom& q) {
+  constexpr int D = DS * 8;
+  constexpr int DQ = D / 32;     // dims per lane in P V
+  constexpr uint32_t NQ = 16;    // query tile rows
+  const KParams& p = *c.p;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  TcCtl* ctl = c.ctl;
+  const int G = q.G, NR = CH ? G * q.T : G;  // at most 4
+  // shared scratch from its first 1024-byte boundary: the query tile
+  // [D / 64][NQ][128 B] (4 KB), probabilities [2][kKeyBlock][4] (4 KB), qs
+  // [4][D] (2 KB), nkv [2 T][D] bf16 (2 KB), block maxima and sums, rescale
+  // factors, this step's key scores; at the end the P V warps' output sums
+  // [4][4][D] (8 KB) over the tile
+  const uint32_t s0 = smem_addr(c.scratch), sb = (s0 + 1023u) & ~1023u;
+  uint8_t* base = reinterpret_cast<uint8_t*>(c.scratch) + (sb - s0);
+  const uint32_t qt = sb;
+  float* pb = reinterpret_cast<float*>(base + 4096);
+  float* qs = reinterpret_cast<float*>(base + 8192);
+  uint16_t* nkv = reinterpret_cast<uint16_t*>(base + 10240);
+  float* red = reinterpret_cast<float*>(base + 12288);  // [2][32] maxima and sums, [2][4] factors, [32] new-key scores, [8] m, l
+  float* osum = reinterpret_cast<float*>(base);
+  if (tid == 0) {  // the MMA warp takes the task and waits for the query tile
+    ctl->mb_task = c.task;
+    ctl->mb_slot = c.rp.slot;
+    ctl->mb_phase = c.rp.phase;
+    ctl->mb_nblk = (uint32_t)q.nblk;
+    ctl->mb_qt = qt;
+    mbar_arrive(&ctl->task_go);
+  }
+  partial_stage<DS, CH>(c, q, qs, nkv);
+  cbar();
+  // query tile: dims (d2, d2 + 1) of row r, split into three bf16 parts
+  // (each the rounding of what the previous leave), at tile rows 3 r + part
+  for (int i = tid; i < NR * (D / 2); i += kConsumerThreads) {
+    const int r = i / (D / 2), d2 = (i - r * (D / 2)) * 2;
+    float v0 = qs[r * D + d2], v1 = qs[r * D + d2 + 1];
+    const uint32_t kb = (uint32_t)d2 >> 6, kk = (uint32_t)d2 & 63u;
+    const uint32_t ch = kk >> 3, cb = (kk & 7u) * 2u;
+#pragma unroll
+    for (int pt = 0; pt < 3; ++pt) {
+      const __nv_bfloat162 a = __float22bfloat162_rn(make_float2(v0, v1));
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(&a);
+      v0 -= bf_lo(w);
+      v1 -= bf_hi(w);
+      const uint32_t ra = qt + kb * (NQ * 128u) + (uint32_t)(3 * r + pt) * 128u;
+      sts32(ra + ((ch ^ ((ra >> 7) & 7u)) << 4) + cb, w);
+    }
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&ctl->q_full);
+  // hand-off blocks: this step's keys first (if any), then the cached blocks
+  const int nb0 = q.has_new ? 1 : 0, nvb = nb0 + q.nblk;
+  float o[4][DQ];  // P V warps: the output sums of rows 0-3 over this lane's dims
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int e = 0; e < DQ; ++e) o[r][e] = 0.f;
+  if (warp < 4) {
+    // ---- softmax warps
+    float* ns = red + 72;  // [8 keys][4 rows] scores of this step's keys
+    float m[4], l[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      m[r] = -INFINITY;
+      l[r] = 0.f;
+    }
+    if (q.has_new) {  // score (kk, r) by softmax warp (kk * NR + r) % 4
+      for (int it = warp; it < q.nn * NR; it += 4) {
+        const int kk = it / NR, r = it - kk * NR;
+        float sc = 0.f;
+#pragma unroll
+        for (int e = 0; e < DQ; ++e)
+          sc = fmaf(qs[r * D + lane * DQ + e], __uint_as_float((uint32_t)nkv[kk * D + lane * DQ + e] << 16), sc);
+        sc = warp_sum(sc);
+        const int tq = CH ? r / G : 0;  // row r sees this step's keys up to its own token
+        if (lane == 0) ns[kk * 4 + r] = (q.nb0 + kk <= q.pos + tq) ? sc : -INFINITY;
+      }
+      named_bar_sync(2, 128);
+    }
+    for (int v = 0; v < nvb; ++v) {
+      const int j = v & 1, b = v - nb0;
+      float* P = pb + j * kKeyBlock * 4;
+      float* rb = red + j * 32;  // [4 warps][4] maxima, [4 warps][4] sums
+      const int key = warp * 32 + lane;
+      float sc[4];
+      if (b < 0) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r) sc[r] = (key < q.nn && r < NR) ? ns[key * 4 + r] : -INFINITY;
+      } else {
+        const int nv = min(kKeyBlock, q.jst - (q.j0 + b * kKeyBlock));  // real keys in the block
+        const int jb = b & 1;
+        if (lane == 0) bar_wait(p, &ctl->s_full[jb], (c.tc_ph >> (3 + jb)) & 1u, c.task, false);
+        __syncwarp();
+        c.tc_ph ^= 1u << (3 + jb);
+        if (b == 0) trace_mark(c, 0);
+        tc_fence_after();
+        float s16[16];
+        tmem_ld16(c.taddr + ((uint32_t)(warp * 32) << 16) + c.pcol + (uint32_t)jb * NQ, s16);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          if (b + 2 < q.nblk) mbar_arrive(&ctl->s_empty[jb]);  // the MMA warp may refill the buffer
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+          sc[r] = (key < nv && r < NR) ? s16[3 * r] + s16[3 * r + 1] + s16[3 * r + 2] : -INFINITY;
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float mx = warp_max(sc[r]);
+        if (lane == 0) rb[warp * 4 + r] = mx;
+      }
+      named_bar_sync(2, 128);
+      float mn[4], pr[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float bm = fmaxf(fmaxf(rb[r], rb[4 + r]), fmaxf(rb[8 + r], rb[12 + r]));
+        mn[r] = fmaxf(m[r], bm);
+        pr[r] = sc[r] == -INFINITY ? 0.f : exp2f(sc[r] - mn[r]);
+      }
+      if (v >= 2) {  // the P V warps are done with buffer j (hand-off v - 2)
+        if (lane == 0) bar_wait(p, &ctl->p_empty[j], (c.tc_ph >> (5 + j)) & 1u, c.task, false);
+        __syncwarp();
+        c.tc_ph ^= 1u << (5 + j);
+      }
+      *reinterpret_cast<float4*>(P + key * 4) = make_float4(pr[0], pr[1], pr[2], pr[3]);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float sm = warp_sum(pr[r]);
+        if (lane == 0) rb[16 + warp * 4 + r] = sm;
+      }
+      named_bar_sync(2, 128);
+      float* fac = red + 64 + j * 4;  // the rescale factors of hand-off v
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float al = mn[r] == -INFINITY ? 1.f : exp2f(m[r] - mn[r]);  // 0 while m is -inf and mn finite
+        l[r] = fmaf(l[r], al, (rb[16 + r] + rb[20 + r]) + (rb[24 + r] + rb[28 + r]));
+        m[r] = mn[r];
+        if (tid == r) fac[r] = al;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ctl->p_full[j]);  // release: the probabilities and factors
+      if (b >= 0) {
+        if (D == 128) {  // the K slot: its scores were read, so the MMAs are done with it
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&c.empty[c.rp.slot]);
+          c.rp.advance(c.nst);
+        }
+        // the V slot (or the block's slot at D = 64): the P V warps read it;
+        // these warps count themselves in once it has been filled
+        const uint32_t vslot = consume_begin(c);
+        consume_end(c, vslot);
+      }
+    }
+    trace_mark(c, 1);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {  // m and l of the rows, for the record
+      if (tid == r) {
+        red[104 + r] = m[r];
+        red[108 + r] = l[r];
+      }
+    }
+  } else {
+    // ---- P V warps
+    const int w4 = warp - 4;
+    for (int v = 0; v < nvb; ++v) {
+      const int j = v & 1, b = v - nb0;
+      if (lane == 0) bar_wait(p, &ctl->p_full[j], (c.tc_ph >> (7 + j)) & 1u, c.task, false);
+      __syncwarp();
+      c.tc_ph ^= 1u << (7 + j);
+      const float* fac = red + 64 + j * 4;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float al = fac[r];
+#pragma unroll
+        for (int e = 0; e < DQ; ++e) o[r][e] *= al;
+      }
+      int nv;
+      uint32_t vb, vslot = 0;
+      if (b < 0) {
+        nv = q.nn;
+        vb = smem_addr(nkv + q.T * D);  // this step's values
+      } else {
+        nv = min(kKeyBlock, q.jst - (q.j0 + b * kKeyBlock));
+        if (D == 128) {  // the K slot: the softmax warps saw its scores, the MMAs are done with it
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&c.empty[c.rp.slot]);
+          c.rp.advance(c.nst);
+        }
+        vslot = consume_begin(c);
+        vb = smem_addr(c.ring + (size_t)vslot * kStageBytes) + (D == 128 ? 0u : kKeyBlock * 128u);
+      }
+      const uint32_t pa = smem_addr(pb + j * kKeyBlock * 4);
+      for (int k = w4; k < nv; k += 4) {
+        const uint4 pw = lds128(pa + (uint32_t)k * 16u);
+        const float pk[4] = {__uint_as_float(pw.x), __uint_as_float(pw.y), __uint_as_float(pw.z),
+                             __uint_as_float(pw.w)};
+        float vv[DQ];
+        if constexpr (DQ == 4) {
+          const uint2 w = lds64(vb + (uint32_t)(k * D + lane * 4) * 2u);
+          vv[0] = bf_lo(w.x); vv[1] = bf_hi(w.x); vv[2] = bf_lo(w.y); vv[3] = bf_hi(w.y);
+        } else {
+          const uint32_t w = lds32(vb + (uint32_t)(k * D + lane * 2) * 2u);
+          vv[0] = bf_lo(w); vv[1] = bf_hi(w);
+        }
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int e = 0; e < DQ; ++e) o[r][e] = fmaf(pk[r], vv[e], o[r][e]);
+      }
+      __syncwarp();
+      if (lane == 0 && v + 2 < nvb) mbar_arrive(&ctl->p_empty[j]);  // the softmax warps may rewrite buffer j
+      if (b >= 0) consume_end(c, vslot);
+    }
+  }
+  cbar();  // every warp is done with the tile, the probabilities, qs and nkv; m and l are parked
+  if (warp >= 4) {  // the P V warps' sums overlay the tile
+#pragma unroll
+    for (int r = 0; r < 4; ++r)
+#pragma unroll
+      for (int e = 0; e < DQ; ++e) osum[((warp - 4) * 4 + r) * D + lane * DQ + e] = o[r][e];
+  }
+  cbar();
+  float* scr = rec_ptr<float>(c, kPOut) + (size_t)q.slot * NR * (D + 2);
+  for (int i = tid; i < NR * D; i += kConsumerThreads) {
+    const int r = i / D, e = i - r * D;
+    float O = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) O += osum[(w * 4 + r) * D + e];
+    scr[r * (D + 2) + 2 + e] = O;
+    if (e == 0) {
+      scr[r * (D + 2)] = red[104 + r];
+      scr[r * (D + 2) + 1] = red[108 + r];
+    }
+  }
+}
+
 __device__ void partial_task(Ctx& c, const mk_task_descriptor& d) {
   PartGeom q;
   part_geom(c.state, d, q);
@@ -1671,7 +2028,15 @@ __device__ void partial_task(Ctx& c, const mk_task_descriptor& d) {
     if (threadIdx.x == 0) raise_error(*c.p, MK_DEV_CAPACITY, c.task);
     return;
   }
-  if (q.T == 1) {
+  if (tc_partial(d, c.rec->tm_rows, q.nblk)) {
+    if (q.T == 1) {
+      if (q.D == 128) tc_partial_body<16, false>(c, d, q);
+      else tc_partial_body<8, false>(c, d, q);
+    } else {
+      if (q.D == 128) tc_partial_body<16, true>(c, d, q);
+      else tc_partial_body<8, true>(c, d, q);
+    }
+  } else if (q.T == 1) {
     if (q.D == 128) partial_body<16, false>(c, d, q);
     else partial_body<8, false>(c, d, q);
   } else {
@@ -1985,7 +2350,7 @@ __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
                          volatile int* sflag, uint8_t* xbuf, TcCtl* ctl, uint32_t taddr, const TaskRec* recs,
                          uint64_t* rfull, uint64_t* rempty) {
   Ctx c{&p, ring, full, empty, scratch, RingPos{}, p.nstages, -1, {0, 0, 0}, 0u, xbuf, ctl, taddr, 0u,
-        nullptr, static_cast<int32_t*>(p.bufs[MK_BUF_STATE])};
+        nullptr, static_cast<int32_t*>(p.bufs[MK_BUF_STATE]), tmem_part_col(BCLASS)};
   int cur_lvl = 0;
   const int tid = threadIdx.x;
   for (uint32_t k = 0;; ++k) {
@@ -2131,47 +2496,52 @@ __global__ void __launch_bounds__(kThreads, 1) mk_interpreter_kernel(const __gri
     mbar_init(&ctl->acc_full, 1);
     mbar_init(&ctl->acc_empty, 1);
     mbar_init(&ctl->task_go, 1);
+    mbar_init(&ctl->s_full[0], 1);
+    mbar_init(&ctl->s_full[1], 1);
+    mbar_init(&ctl->s_empty[0], 4);  // the four softmax warps
+    mbar_init(&ctl->s_empty[1], 4);
+    mbar_init(&ctl->q_full, kConsumerWarps);
+    mbar_init(&ctl->p_full[0], 4);   // the four softmax warps
+    mbar_init(&ctl->p_full[1], 4);
+    mbar_init(&ctl->p_empty[0], 4);  // the four P V warps
+    mbar_init(&ctl->p_empty[1], 4);
     for (int i = 0; i < kRecs; ++i) {
       mbar_init(&rfull[i], 1);
       mbar_init(&rempty[i], 2);  // the producer and consumer thread 0
     }
     fence_mbar_init();
-    if (BCLASS == 2 && !aligned) raise_error(p, MK_DEV_BAD_OP, -1);
+    if (!aligned) raise_error(p, MK_DEV_BAD_OP, -1);
   }
-  if constexpr (BCLASS == 2) {
-    if (threadIdx.x < 32) {  // one warp allocates the accumulator columns
-      tmem_alloc(&ctl->tmem, kTmemCols);
-      tmem_relinquish();
-    }
-    tc_fence_before();
+  constexpr uint32_t tcols = tmem_cols(BCLASS);
+  if (threadIdx.x < 32) {  // one warp allocates the accumulator columns
+    tmem_alloc(&ctl->tmem, tcols);
+    tmem_relinquish();
   }
+  tc_fence_before();
   __syncthreads();
-  if constexpr (BCLASS == 2) tc_fence_after();
-  const uint32_t taddr = BCLASS == 2 ? ctl->tmem : 0u;
+  tc_fence_after();
+  const uint32_t taddr = ctl->tmem;
   if (threadIdx.x >= kConsumerThreads) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
     if (threadIdx.x < kConsumerThreads + 32) producer(p, ring, full, empty, recs, rfull, rempty);
-    else if (BCLASS == 2 && threadIdx.x < kConsumerThreads + 64)
-      tc_mma_warp(p, ring, full, empty, ctl, smem_addr(xbuf), taddr);
-    else if (threadIdx.x >= kConsumerThreads + 64 && threadIdx.x < kConsumerThreads + 96)
+    else if (threadIdx.x < kConsumerThreads + 64)
+      tc_mma_warp(p, ring, full, empty, ctl, smem_addr(xbuf), taddr, tmem_part_col(BCLASS));
+    else if (threadIdx.x < kConsumerThreads + 96)
       record_warp(p, recs, rfull, rempty);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
-    if (BCLASS != 2 || aligned)
-      consumer<BCLASS>(p, ring, full, empty, scratch, sflag, xbuf, ctl, taddr, recs, rfull, rempty);
-    if (BCLASS == 2) {
-      // every tensor-core operation has completed (the consumers waited for
-      // each row group's last commit): tell the MMA warp to stop, free the
-      // columns
-      named_bar_sync(1, kConsumerThreads);
-      if (threadIdx.x == 0) {
-        ctl->mb_task = -1;
-        mbar_arrive(&ctl->task_go);
-      }
-      if (threadIdx.x < 32) {
-        tc_fence_after();
-        tmem_dealloc(taddr, kTmemCols);
-      }
+    if (aligned) consumer<BCLASS>(p, ring, full, empty, scratch, sflag, xbuf, ctl, taddr, recs, rfull, rempty);
+    // every tensor-core operation has completed (the consumers waited for
+    // each row group's last commit and each key block's scores): tell the
+    // MMA warp to stop, free the columns
+    named_bar_sync(1, kConsumerThreads);
+    if (threadIdx.x == 0) {
+      ctl->mb_task = -1;
+      mbar_arrive(&ctl->task_go);
+    }
+    if (threadIdx.x < 32) {
+      tc_fence_after();
+      tmem_dealloc(taddr, tcols);
     }
   }
 }

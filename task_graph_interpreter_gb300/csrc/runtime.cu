@@ -191,6 +191,37 @@ int build_tensor_maps(const mk_graph* g, std::vector<uint8_t>& maps, std::vector
     std::memcpy(maps.data() + (size_t)w * kTmapBytes, &m, kTmapBytes);
     rows[w] = rg;
   }
+  // K caches: a 2-D view [B * Hkv * capacity rows, D] with boxes of 64 dims
+  // x kKeyBlockRows keys in the 128-byte swizzle, for the tensor-core
+  // split-KV partials (their score MMAs read the key rows in that layout)
+  for (const OpRec& op : g->ops) {
+    if (op.kind != K_ATTENTION || (op.D != 64 && op.D != 128)) continue;
+    const int w = op.a[1];
+    if (rows[w] != 0) continue;
+    if (!enc) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return fail(MK_ERR_CUDA, "mk_upload: cuTensorMapEncodeTiled is not available");
+      enc = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    const BufferRec& b = g->bufs[w];
+    CUtensorMap m;
+    const cuuint64_t gdim[2] = {(cuuint64_t)op.D, (cuuint64_t)b.rows * (cuuint64_t)op.cap};
+    const cuuint64_t gstride[1] = {(cuuint64_t)op.D * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)kKeyBlockRows};
+    const cuuint32_t estride[2] = {1u, 1u};
+    const CUresult r = enc(&m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, b.ptr, gdim, gstride, box, estride,
+                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+      return fail(MK_ERR_CUDA, "mk_upload: tensor map of K cache " + std::to_string(w) + " failed (" +
+                                   std::to_string((int)r) + ")");
+    std::memcpy(maps.data() + (size_t)w * kTmapBytes, &m, kTmapBytes);
+    rows[w] = kKeyBlockRows;
+  }
   return MK_OK;
 }
 

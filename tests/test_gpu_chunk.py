@@ -106,3 +106,11 @@ def test_chunk_step_with_one_key_chunks():
     # only keys a row may not see yet (empty for those rows)
     w = synth.custom(synth.TINY, 1, [5], 3 * 4 + 1, chunk=1, name="tiny_chunk_c1")
     assert _run_chunks(w, 4, 3) >= 2
+
+
+def test_chunk_step_with_tensor_core_partials():
+    # T = 2 tokens x 2 heads = 4 query rows and chunks of 300 keys: the
+    # partials run on tensor cores, this step's keys through the same
+    # hand-off as the cached blocks
+    w = synth.custom(synth.TINY, 2, [600, 333], 3 * 2 + 1, chunk=300, name="tiny_chunk_tc")
+    assert _run_chunks(w, 2, 3) >= 2

@@ -137,3 +137,11 @@ def test_standalone_and_pass_fused_rmsnorm(norms):
     # after the fusion pass both match the oracle
     w = synth.custom(synth.TINY, 2, [40, 128], 3, name="tiny_norms")
     assert _run_and_compare(w, 3, norms=norms) >= 2
+
+
+def test_tiny_long_chunks_take_tensor_core_partials():
+    # chunks of 512 keys (four blocks of 128): the split-KV partials run on
+    # tensor cores (score MMAs on K blocks brought by TMA, P V on CUDA
+    # cores), at head dim 64; a short sequence keeps single-block chunks
+    w = synth.custom(synth.TINY, 3, [1000, 700, 90], 3, chunk=512, name="tiny_long_chunks")
+    assert _run_and_compare(w, 3) >= 2
