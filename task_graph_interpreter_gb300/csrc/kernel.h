@@ -28,8 +28,9 @@ constexpr int kXbufBytes = 24576;                // B >= 8 kernel: two 12 KB act
 constexpr int kTmemCols = 256;                   // B >= 8 kernel: GEMV accumulator columns
 // Tensor memory per batch class: the B >= 8 kernel holds the GEMV
 // accumulators (256 columns) and, after them, the split-KV partials' two
-// 16-column score buffers; the others only the score buffers.
-__host__ __device__ constexpr uint32_t tmem_cols(int bclass) { return bclass == 2 ? 512u : 32u; }
+// 16-column score buffers; the B <= 4 kernel only the score buffers; the
+// B <= 2 kernel none (it runs no tensor-core work).
+__host__ __device__ constexpr uint32_t tmem_cols(int bclass) { return bclass == 2 ? 512u : bclass == 1 ? 32u : 0u; }
 __host__ __device__ constexpr uint32_t tmem_part_col(int bclass) { return bclass == 2 ? 256u : 0u; }
 constexpr int kTmapBytes = 128;                  // one CUtensorMap
 constexpr int kKeyBlockRows = 128;               // keys per K box of the tensor-core split-KV partials

@@ -197,13 +197,15 @@ struct PartGeom {
 // block's K rows brought by 2-D TMA in the 128-byte swizzle (boxes of 64
 // dims x kKeyBlock rows) and its V rows by a bulk copy; used when the K
 // cache has a tensor map, the query rows (T tokens x G heads) number at most
-// four and the chunk holds at least two blocks of cached keys (for a single
-// block the tensor-core round trips cost more than the CUDA-core partial).
+// four and the chunk holds at least kMinTcBlocks blocks of cached keys (for
+// short chunks the tensor-core round trips cost more than the CUDA-core
+// partial saves: measured on 129- and 216-key chunks).
 constexpr int kKeyBlock = kKeyBlockRows;
+constexpr int kMinTcBlocks = 4;
 
 __device__ __forceinline__ bool tc_partial(const mk_task_descriptor& d, int tm_rows, int nblk) {
   const int Hkv = (int)(d.reserved[2] & 0xFFFFu), T = (int)(d.reserved[2] >> 16) + 1;
-  return tm_rows == kKeyBlock && (d.k / Hkv) * T <= 4 && nblk >= 2;
+  return tm_rows == kKeyBlock && (d.k / Hkv) * T <= 4 && nblk >= kMinTcBlocks;
 }
 
 __device__ __forceinline__ void part_geom(const int32_t* state, const mk_task_descriptor& d, PartGeom& q) {
@@ -2021,6 +2023,10 @@ __device__ void tc_partial_body(Ctx& c, const mk_task_descriptor& d, const PartG
   }
 }
 
+// The B <= 2 kernel has no tensor-core partials (its graphs carry no K-cache
+// tensor maps): its decode chunks are short, and the code it would add to
+// the consumer costs the hot GEMV loops more than it could save.
+template <int BCLASS>
 __device__ void partial_task(Ctx& c, const mk_task_descriptor& d) {
   PartGeom q;
   part_geom(c.state, d, q);
@@ -2028,13 +2034,15 @@ __device__ void partial_task(Ctx& c, const mk_task_descriptor& d) {
     if (threadIdx.x == 0) raise_error(*c.p, MK_DEV_CAPACITY, c.task);
     return;
   }
-  if (tc_partial(d, c.rec->tm_rows, q.nblk)) {
-    if (q.T == 1) {
-      if (q.D == 128) tc_partial_body<16, false>(c, d, q);
-      else tc_partial_body<8, false>(c, d, q);
-    } else {
-      if (q.D == 128) tc_partial_body<16, true>(c, d, q);
-      else tc_partial_body<8, true>(c, d, q);
+  if (BCLASS > 0 && tc_partial(d, c.rec->tm_rows, q.nblk)) {
+    if constexpr (BCLASS > 0) {
+      if (q.T == 1) {
+        if (q.D == 128) tc_partial_body<16, false>(c, d, q);
+        else tc_partial_body<8, false>(c, d, q);
+      } else {
+        if (q.D == 128) tc_partial_body<16, true>(c, d, q);
+        else tc_partial_body<8, true>(c, d, q);
+      }
     }
   } else if (q.T == 1) {
     if (q.D == 128) partial_body<16, false>(c, d, q);
@@ -2411,7 +2419,7 @@ __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
         gemv_task<BCLASS>(c, d);
         break;
       case MK_OP_ATTENTION_APPEND: append_task(c, d); break;
-      case MK_OP_ATTENTION_PARTIAL: partial_task(c, d); break;
+      case MK_OP_ATTENTION_PARTIAL: partial_task<BCLASS>(c, d); break;
       case MK_OP_ATTENTION_COMBINE: combine_task(c, d); break;
       case MK_OP_MEMCPY: embed_task(c, d); break;
       case MK_OP_RMSNORM: rmsnorm_task(c, d); break;
@@ -2510,38 +2518,44 @@ __global__ void __launch_bounds__(kThreads, 1) mk_interpreter_kernel(const __gri
       mbar_init(&rempty[i], 2);  // the producer and consumer thread 0
     }
     fence_mbar_init();
-    if (!aligned) raise_error(p, MK_DEV_BAD_OP, -1);
+    if (BCLASS > 0 && !aligned) raise_error(p, MK_DEV_BAD_OP, -1);  // the tensor-core operand tiles
   }
   constexpr uint32_t tcols = tmem_cols(BCLASS);
-  if (threadIdx.x < 32) {  // one warp allocates the accumulator columns
-    tmem_alloc(&ctl->tmem, tcols);
-    tmem_relinquish();
+  if constexpr (tcols > 0) {
+    if (threadIdx.x < 32) {  // one warp allocates the accumulator columns
+      tmem_alloc(&ctl->tmem, tcols);
+      tmem_relinquish();
+    }
+    tc_fence_before();
   }
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t taddr = ctl->tmem;
+  if constexpr (tcols > 0) tc_fence_after();
+  const uint32_t taddr = tcols > 0 ? ctl->tmem : 0u;
   if (threadIdx.x >= kConsumerThreads) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
     if (threadIdx.x < kConsumerThreads + 32) producer(p, ring, full, empty, recs, rfull, rempty);
-    else if (threadIdx.x < kConsumerThreads + 64)
-      tc_mma_warp(p, ring, full, empty, ctl, smem_addr(xbuf), taddr, tmem_part_col(BCLASS));
+    else if (threadIdx.x < kConsumerThreads + 64) {
+      if constexpr (tcols > 0) tc_mma_warp(p, ring, full, empty, ctl, smem_addr(xbuf), taddr, tmem_part_col(BCLASS));
+    }
     else if (threadIdx.x < kConsumerThreads + 96)
       record_warp(p, recs, rfull, rempty);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
-    if (aligned) consumer<BCLASS>(p, ring, full, empty, scratch, sflag, xbuf, ctl, taddr, recs, rfull, rempty);
-    // every tensor-core operation has completed (the consumers waited for
-    // each row group's last commit and each key block's scores): tell the
-    // MMA warp to stop, free the columns
-    named_bar_sync(1, kConsumerThreads);
-    if (threadIdx.x == 0) {
-      ctl->mb_task = -1;
-      mbar_arrive(&ctl->task_go);
-    }
-    if (threadIdx.x < 32) {
-      tc_fence_after();
-      tmem_dealloc(taddr, tcols);
+    if (BCLASS == 0 || aligned)
+      consumer<BCLASS>(p, ring, full, empty, scratch, sflag, xbuf, ctl, taddr, recs, rfull, rempty);
+    if constexpr (tcols > 0) {
+      // every tensor-core operation has completed (the consumers waited for
+      // each row group's last commit and each key block's scores): tell the
+      // MMA warp to stop, free the columns
+      named_bar_sync(1, kConsumerThreads);
+      if (threadIdx.x == 0) {
+        ctl->mb_task = -1;
+        mbar_arrive(&ctl->task_go);
+      }
+      if (threadIdx.x < 32) {
+        tc_fence_after();
+        tmem_dealloc(taddr, tcols);
+      }
     }
   }
 }

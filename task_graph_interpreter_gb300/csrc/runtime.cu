@@ -195,7 +195,8 @@ int build_tensor_maps(const mk_graph* g, std::vector<uint8_t>& maps, std::vector
   // x kKeyBlockRows keys in the 128-byte swizzle, for the tensor-core
   // split-KV partials (their score MMAs read the key rows in that layout)
   for (const OpRec& op : g->ops) {
-    if (op.kind != K_ATTENTION || (op.D != 64 && op.D != 128)) continue;
+    // (the B <= 2 kernel runs its partials on CUDA cores)
+    if (op.kind != K_ATTENTION || (op.D != 64 && op.D != 128) || g->rows() <= 2) continue;
     const int w = op.a[1];
     if (rows[w] != 0) continue;
     if (!enc) {

@@ -109,8 +109,8 @@ def test_chunk_step_with_one_key_chunks():
 
 
 def test_chunk_step_with_tensor_core_partials():
-    # T = 2 tokens x 2 heads = 4 query rows and chunks of 300 keys: the
-    # partials run on tensor cores, this step's keys through the same
-    # hand-off as the cached blocks
-    w = synth.custom(synth.TINY, 2, [600, 333], 3 * 2 + 1, chunk=300, name="tiny_chunk_tc")
+    # T = 2 tokens x 2 heads = 4 query rows and chunks of 600 keys (five
+    # blocks of 128): the partials run on tensor cores, this step's keys
+    # through the same hand-off as the cached blocks
+    w = synth.custom(synth.TINY, 2, [1200, 700], 3 * 2 + 1, chunk=600, name="tiny_chunk_tc")
     assert _run_chunks(w, 2, 3) >= 2

@@ -140,8 +140,8 @@ def test_standalone_and_pass_fused_rmsnorm(norms):
 
 
 def test_tiny_long_chunks_take_tensor_core_partials():
-    # chunks of 512 keys (four blocks of 128): the split-KV partials run on
+    # chunks of 1024 keys (eight blocks of 128): the split-KV partials run on
     # tensor cores (score MMAs on K blocks brought by TMA, P V on CUDA
     # cores), at head dim 64; a short sequence keeps single-block chunks
-    w = synth.custom(synth.TINY, 3, [1000, 700, 90], 3, chunk=512, name="tiny_long_chunks")
+    w = synth.custom(synth.TINY, 3, [2000, 1100, 90], 3, chunk=1024, name="tiny_long_chunks")
     assert _run_and_compare(w, 3) >= 2
