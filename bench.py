@@ -93,22 +93,29 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(config):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken
-    on the current kernel sources; else None."""
-    p = os.path.join(ROOT, "profiles", f"interpreter_kernel_{config}.md")
+def profiled_traffic(config, algo_bytes):
+    """DRAM bytes per launch from the committed ncu summary of a small case
+    of the same kernel (a few layers at full width, full LM head), scaled to
+    this launch by algorithmic bytes (every layer streams the same weights,
+    so traffic grows in proportion); None unless the capture was taken on
+    the current kernel sources.  Returns (bytes, note)."""
+    p = os.path.join(ROOT, "profiles", f"dram_traffic_{config}.md")
     if not os.path.exists(p):
-        return None
-    txt = open(p).read()
-    src = traffic = None
-    for line in txt.splitlines():
-        if line.startswith("kernel_source_hash:"):
-            src = line.split(":", 1)[1].strip()
-        if line.startswith("dram_bytes_per_launch:"):
-            traffic = float(line.split(":", 1)[1].strip())
-    if src != kernel_source_hash():
-        return None
-    return traffic
+        return None, None
+    fields = {}
+    for line in open(p).read().splitlines():
+        if ":" in line and not line.startswith(("#", "|", " ")):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    try:
+        if fields.get("kernel_source_hash") != kernel_source_hash():
+            return None, None
+        dram = float(fields["dram_bytes_per_launch"])
+        captured = float(fields["captured_algorithmic_bytes"])
+    except (KeyError, ValueError):
+        return None, None
+    return dram * algo_bytes / captured, (f"ncu dram__bytes_read.sum + dram__bytes_write.sum of {fields.get('captured_case')}"
+                                          f" ({dram:.4g} B), scaled by algorithmic bytes x{algo_bytes / captured:.3f}")
 
 
 class ClockSampler:
@@ -427,7 +434,7 @@ def main():
     if not args.no_cpu_baseline and ws == 1:  # the oracle baseline is timed at N=1 only
         cpu = cpu_baseline(args, base)
 
-    traffic = profiled_traffic(args.config)
+    traffic, traffic_note = profiled_traffic(args.config, nbytes / args.steps)
     line = {
         "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "us_per_step": 1000.0 * ms_step,
@@ -437,7 +444,8 @@ def main():
         "achieved_hbm_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_source": peak_kind,
-                     "traffic": traffic, "algorithmic_bytes_per_launch": nbytes / args.steps},
+                     "traffic": traffic, "traffic_source": traffic_note,
+                     "algorithmic_bytes_per_launch": nbytes / args.steps},
         "e2e": e2e, "gpu_launches": args.steps, "tasks_per_step": n_tasks,
         "modes": modes, "clocks": clocks, "cpu_baseline": cpu,
     }
