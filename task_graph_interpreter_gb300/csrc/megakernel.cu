@@ -141,7 +141,9 @@ __device__ __forceinline__ void gemv_geom(const mk_task_descriptor& d, GemvGeom&
     break;
   }
   g.lgW = g.WROW == 8 ? 3 : g.WROW == 4 ? 2 : g.WROW == 2 ? 1 : 0;
-  g.rs = kStageElems / g.KS;
+  // whole rows per slot, no more than the warps cover ((8 / NV) rows of
+  // every warp row: at NV = 7 and one warp column, 8 of the 9 that fit)
+  g.rs = min(kStageElems / g.KS, (8 / g.NV) * g.WROW);
   int rg = kSlotFloats / (g.seg * g.BT * g.WCOL);
   rg = min(rg, kAccFloats / (g.seg * g.BT));
   g.RG = min(rg, g.cn);
@@ -539,17 +541,15 @@ __device__ __forceinline__ void trace_mark(Ctx& c, int i) {
   if (c.p->trace && threadIdx.x == 0) c.mark[i] = globaltimer();
 }
 
-// Lane 0 waits for the slot, the warp then reads it.
+// Every lane waits for the slot (acquiring the bytes the copies wrote);
+// no divergent single-lane wait and warp barrier before the loads.
 // Slots are waited for and handed back in order; a consumer may wait for
 // the next slot before handing back the current one.
 __device__ __forceinline__ uint32_t consume_begin(Ctx& c) {
   const uint32_t slot = c.rp.slot, ph = c.rp.phase;
   c.rp.advance(c.nst);
-  if ((threadIdx.x & 31) == 0) {
-    if (c.p->trace && threadIdx.x == 0 && !mbar_try_wait(&c.full[slot], ph)) ++c.ring_waits;
-    bar_wait(*c.p, &c.full[slot], ph, c.task, true);
-  }
-  __syncwarp();
+  if (c.p->trace && threadIdx.x == 0 && !mbar_try_wait(&c.full[slot], ph)) ++c.ring_waits;
+  bar_wait(*c.p, &c.full[slot], ph, c.task, true);
   return slot;
 }
 
@@ -848,6 +848,9 @@ __device__ __forceinline__ float transpose_reduce(float (&v)[N], int lane) {
 // wrow, wrow + WROW, ... of each slot over its column block, with x in
 // registers: all shared loads of a slot first, independent FMA chains per
 // row, then one transposed reduction of the slot's (row, batch) sums.
+// Below batch 8 the loads are unconditional: rows past the slot's last
+// valid row read stale bytes of the same slot, and their sums are never
+// stored.
 // Results go to slots[(row, b, warp column)].
 template <int B, int NV>
 __device__ __forceinline__ void gemv_stages(Ctx& c, const mk_task_descriptor& d, const GemvGeom& G, int rows_g,
@@ -887,7 +890,10 @@ __device__ __forceinline__ void gemv_stages(Ctx& c, const mk_task_descriptor& d,
       for (int r = 0; r < RWM; ++r) {
         const uint32_t ra = base + (uint32_t)(wrow + r * G.WROW) * G.KS * 2;
 #pragma unroll
-        for (int v = 0; v < NV; ++v) w[r][v] = r < rw ? lds128(ra + v * 512) : make_uint4(0u, 0u, 0u, 0u);
+        for (int v = 0; v < NV; ++v) {
+          if constexpr (B >= 8) w[r][v] = r < rw ? lds128(ra + v * 512) : make_uint4(0u, 0u, 0u, 0u);  // no spills
+          else w[r][v] = lds128(ra + v * 512);
+        }
       }
       float acc[VPS];
 #pragma unroll

@@ -145,3 +145,16 @@ def test_tiny_long_chunks_take_tensor_core_partials():
     # cores), at head dim 64; a short sequence keeps single-block chunks
     w = synth.custom(synth.TINY, 3, [2000, 1100, 90], 3, chunk=1024, name="tiny_long_chunks")
     assert _run_and_compare(w, 3) >= 2
+
+
+@pytest.mark.parametrize("F,B", [(1792, 1), (1792, 2), (768, 1), (5376, 1)])
+def test_ffn_widths_of_every_gemv_slot_geometry(F, B):
+    # the down projection's K = F picks the GEMV's k-segment and warp layout:
+    # 1792 = 7 x 256 (seven 16-byte pieces per lane, one warp column: 8 rows
+    # per slot are covered, not the 9 that would fit), 768 (three 256-column
+    # k-segments), 5376 (three 1792-column k-segments); B = 2 takes the
+    # single-piece layout
+    import dataclasses
+    m = dataclasses.replace(synth.TINY, F=F, name=f"tiny_f{F}")
+    w = synth.custom(m, B, [100, 37][:B], 3, name=f"tiny_f{F}_b{B}")
+    assert _run_and_compare(w, 2) >= 1
