@@ -320,9 +320,12 @@ int mk_debug_patch_task(mk_graph* g, int task, const mk_task_descriptor* d);
  * ...) are waited for through that group's one shared counter; the other
  * parents through one counter shared by every task with the same remaining
  * parents (its index is the first such task's); counter_words is the size
- * of the counter array.  Arrays: wait_off and sig_off uint32[N + 1],
- * wait uint32[2 * wait_off[N]], sig uint32[sig_off[N]]; they belong to the
- * graph.  Errors: MK_ERR_STATE (not lowered), MK_ERR_ARG. */
+ * of the counter array.  Parents a task waits for in its body instead
+ * (the sibling splits of a K-split block's last split; the partials whose
+ * tagged records a decode COMBINE polls) leave its waits.  Arrays: wait_off
+ * and sig_off uint32[N + 1], wait uint32[2 * wait_off[N]], sig
+ * uint32[sig_off[N]]; they belong to the graph.  Errors: MK_ERR_STATE (not
+ * lowered), MK_ERR_ARG. */
 int mk_get_sync_plan(const mk_graph* g, const uint32_t** wait_off, const uint32_t** wait,
                      const uint32_t** sig_off, const uint32_t** sig, uint32_t* counter_words);
 
@@ -331,7 +334,10 @@ int mk_get_sync_plan(const mk_graph* g, const uint32_t** wait_off, const uint32_
  * activation inputs as (step tag, value) pairs and so wait on no counter;
  * buf_ll[b] = 1 for the buffers whose producers also write those pairs (into
  * library-owned mirrors: f32 buffers written once per step by one op's
- * GEMV, COMBINE, embedding or RMSNORM tasks).  uint8 arrays of the task and
+ * GEMV, COMBINE, embedding or RMSNORM tasks, and the attention scratch
+ * whose ATTENTION_PARTIAL records every reading COMBINE polls on its decode
+ * path: T = 1, at most 32 partials, G dividing 8; such a combine waits
+ * through counters for its appends only).  uint8 arrays of the task and
  * buffer counts, owned by the graph, fixed at lowering.  Errors: MK_ERR_ARG
  * (null argument), MK_ERR_STATE (not lowered). */
 int mk_get_ll_plan(const mk_graph* g, const uint8_t** task_ll, const uint8_t** buf_ll);

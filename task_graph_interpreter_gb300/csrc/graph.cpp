@@ -851,6 +851,12 @@ extern "C" int mk_lower(mk_graph* g) {
 // pairs); a GEMV qualifies when its x and residual do and every one of its
 // parents writes one of them (weights and gamma have no writers), a split-KV
 // partial or a cache append when its qkv does and every parent writes qkv.
+bool mk::combine_polls(const mk_task_descriptor& d) {
+  const uint32_t Hkv = d.reserved[2] & 0xFFFFu, T = (d.reserved[2] >> 16) + 1u;
+  return d.op_id == MK_OP_ATTENTION_COMBINE && T == 1u && d.reserved[3] <= 32u && Hkv > 0u && d.k % (int)Hkv == 0 &&
+         8 % (d.k / (int)Hkv) == 0;
+}
+
 void mk::build_ll_plan(mk_graph* g, const std::vector<std::vector<int>>& parents,
                        const std::vector<uint8_t>& once) {
   const size_t NB = g->bufs.size(), N = g->tasks.size();
@@ -864,9 +870,14 @@ void mk::build_ll_plan(mk_graph* g, const std::vector<std::vector<int>>& parents
       if (d.flags & MK_F_ADD_RESIDUAL) read_as_input[d.in_buf[2]] = 1;
     }
     if (d.op_id == MK_OP_ATTENTION_PARTIAL || d.op_id == MK_OP_ATTENTION_APPEND) read_as_input[d.in_buf[0]] = 1;
+    if (d.op_id == MK_OP_ATTENTION_COMBINE && d.in_buf[0] < NB) {
+      // a combine polls its partials' records only on its decode path
+      if (combine_polls(d)) read_as_input[d.in_buf[0]] = 1;
+      else bad_writer[d.in_buf[0]] = 1;
+    }
     if (d.out_buf >= NB) continue;
     const bool ok = d.op_id == MK_OP_GEMV || d.op_id == MK_OP_ATTENTION_COMBINE || d.op_id == MK_OP_MEMCPY ||
-                    d.op_id == MK_OP_RMSNORM;
+                    d.op_id == MK_OP_RMSNORM || d.op_id == MK_OP_ATTENTION_PARTIAL;
     if (!ok) bad_writer[d.out_buf] = 1;
   }
   for (size_t b = MK_BUF_ROPE_SIN + 1; b < NB; ++b)
@@ -934,9 +945,20 @@ int mk::build_sync_plan(mk_graph* g) {
   // The last split of a K-split row block waits for its sibling splits
   // inside its body (after its own partial product), through the block's
   // arrival counter in the K-split scratch: those parents leave the plan.
+  // So do a combine's partials when their records carry tagged pairs: the
+  // combine polls them (its cache appends stay in the plan).
   std::vector<int> deferred(N, 0);
+  const bool ll_ready_plan = g->ll_buf.size() == g->bufs.size();
   for (int t = 0; t < N; ++t) {
     const mk_task_descriptor& d = g->tasks[t];
+    if (ll_ready_plan && d.op_id == MK_OP_ATTENTION_COMBINE && d.in_buf[0] < g->bufs.size() && g->ll_buf[d.in_buf[0]]) {
+      std::vector<int>& ps = parents[t];
+      const size_t before = ps.size();
+      ps.erase(std::remove_if(ps.begin(), ps.end(), [&](int q) { return g->tasks[q].out_buf == d.in_buf[0]; }),
+               ps.end());
+      deferred[t] = (int)(before - ps.size());
+      continue;
+    }
     const int S = (int)((uint32_t)d.kv_len >> 16), j = d.kv_len & 0xFFFF;
     if (d.op_id != MK_OP_GEMV || d.config_id != 1 || S < 2 || j != S - 1) continue;
     std::vector<int>& ps = parents[t];

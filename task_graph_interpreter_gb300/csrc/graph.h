@@ -96,6 +96,9 @@ int tile_count(int n, int tiles_target, int col_align);
 int build_sync_plan(mk_graph* g);  // graph.cpp; from the descriptors and edges
 void build_ll_plan(mk_graph* g, const std::vector<std::vector<int>>& parents,
                    const std::vector<uint8_t>& once);  // graph.cpp; before build_sync_plan
+// A COMBINE that polls its partials' tagged records when they have them:
+// a decode step (T = 1) with at most 32 partials and G dividing 8 (graph.cpp)
+bool combine_polls(const mk_task_descriptor& d);
 std::vector<int> partials_per_sequence(const std::vector<int32_t>& len0, int Hkv, int chunk,
                                        int num_ctas);
 }  // namespace mk

@@ -1755,6 +1755,8 @@ __device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom
   }
   cbar();
   float* scr = rec_ptr<float>(c, kPOut) + (size_t)q.slot * NR * (D + 2);
+  uint64_t* sm = rec_ptr<uint64_t>(c, kMirOut);  // the record's tagged pairs (read by a tagged combine), or null
+  if (sm) sm += (size_t)q.slot * NR * (D + 2);
   for (int i = tid; i < NR * D; i += kConsumerThreads) {
     const int r = i / D, e = i - r * D;
     const int w0 = (r >> 2) * WPG, rs = r & 3;
@@ -1770,9 +1772,11 @@ __device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom
       }
     }
     scr[r * (D + 2) + 2 + e] = O;
+    if (sm) st_relaxed_u64(sm + r * (D + 2) + 2 + e, ll_pack(O, c.p->tag));
     if (e == 0) {
       scr[r * (D + 2)] = M;
       scr[r * (D + 2) + 1] = Ls;
+      if (sm) st_relaxed_v2u64(sm + r * (D + 2), ll_pack(M, c.p->tag), ll_pack(Ls, c.p->tag));
     }
   }
 }
@@ -2016,15 +2020,19 @@ __device__ void tc_partial_body(Ctx& c, const mk_task_descriptor& d, const PartG
   }
   cbar();
   float* scr = rec_ptr<float>(c, kPOut) + (size_t)q.slot * NR * (D + 2);
+  uint64_t* sm = rec_ptr<uint64_t>(c, kMirOut);  // the record's tagged pairs (read by a tagged combine), or null
+  if (sm) sm += (size_t)q.slot * NR * (D + 2);
   for (int i = tid; i < NR * D; i += kConsumerThreads) {
     const int r = i / D, e = i - r * D;
     float O = 0.f;
 #pragma unroll
     for (int w = 0; w < 4; ++w) O += osum[(w * 4 + r) * D + e];
     scr[r * (D + 2) + 2 + e] = O;
+    if (sm) st_relaxed_u64(sm + r * (D + 2) + 2 + e, ll_pack(O, c.p->tag));
     if (e == 0) {
       scr[r * (D + 2)] = red[104 + r];
       scr[r * (D + 2) + 1] = red[108 + r];
+      if (sm) st_relaxed_v2u64(sm + r * (D + 2), ll_pack(red[104 + r], c.p->tag), ll_pack(red[108 + r], c.p->tag));
     }
   }
 }
@@ -2077,6 +2085,10 @@ __device__ __forceinline__ void lse_fold(float& M, float& Ls, float& O0, float& 
   }
 }
 
+// Partials whose tagged records a decode combine loads at once (the 32
+// partials of a full warp would take 128 registers of pairs).
+constexpr int kCombGroup = 16;
+
 __device__ void combine_task(Ctx& c, const mk_task_descriptor& d) {
   const KParams& p = *c.p;
   const int s = d.reserved[0], g = d.reserved[1], Hkv = d.reserved[2] & 0xFFFFu;
@@ -2087,15 +2099,72 @@ __device__ void combine_task(Ctx& c, const mk_task_descriptor& d) {
   const float* scr = rec_ptr<const float>(c, kPIn0) + (size_t)base * rec;
   float* out = rec_ptr<float>(c, kPOut);
   uint64_t* om = rec_ptr<uint64_t>(c, kMirOut);
+  const uint64_t* sm = rec_ptr<const uint64_t>(c, kMirX);  // the partials' tagged records (MEGA), or null
   if (P <= 32 && T == 1 && kConsumerWarps % G == 0) {
     // decode step: 8 / G warps per head, two output dims per lane; lane k
     // reads partial k's (m, l) while every lane reads its dims of all P
-    // partials at once (one L2 round trip)
+    // partials at once (one L2 round trip).  With tagged records this task
+    // waited for no partial: while some lane holds a stale pair, the lowest
+    // such lane polls it and the warp reloads what is stale.
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int wph = kConsumerWarps / G;
     const int h = warp / wph, dpw = D / wph;
     const int e = (warp % wph) * dpw + lane * 2;
     const bool mine = lane * 2 < dpw;
+    if (sm) {
+      // tagged records: (m, l) of partial `lane`, then the dims of the
+      // partials in groups of kCombGroup (4 registers of pairs each in flight)
+      const uint64_t* r = sm + (size_t)base * rec + h * (D + 2);
+      ulonglong2 ml = lane < P ? ld_relaxed_v2u64(r + (size_t)lane * rec)
+                               : make_ulonglong2(ll_pack(-INFINITY, p.tag), ll_pack(0.f, p.tag));
+      float M = 0.f, L = 1.f, wk = 0.f, a0 = 0.f, a1 = 0.f;
+      for (int k0 = 0; k0 < P; k0 += kCombGroup) {
+        ulonglong2 qv[kCombGroup];
+#pragma unroll
+        for (int k = 0; k < kCombGroup; ++k)
+          qv[k] = (k0 + k < P && mine) ? ld_relaxed_v2u64(r + (size_t)(k0 + k) * rec + 2 + e)
+                                       : make_ulonglong2(ll_pack(0.f, p.tag), ll_pack(0.f, p.tag));
+        for (;;) {  // while a lane holds stale pairs, the lowest such lane polls one
+          uint32_t stale = (k0 == 0 && !(ll_ready(ml.x, p.tag) && ll_ready(ml.y, p.tag))) ? 1u << kCombGroup : 0u;
+#pragma unroll
+          for (int k = 0; k < kCombGroup; ++k)
+            stale |= (ll_ready(qv[k].x, p.tag) && ll_ready(qv[k].y, p.tag)) ? 0u : 1u << k;
+          const uint32_t want = __ballot_sync(0xffffffffu, stale != 0);
+          if (!want) break;
+          const int leader = __ffs(want) - 1;
+          int ready = 1;
+          if (lane == leader) {
+            const int k = __ffs(stale) - 1;
+            const uint64_t* pr = k == kCombGroup ? r + (size_t)lane * rec : r + (size_t)(k0 + k) * rec + 2 + e;
+            ready = ll_ready(ll_wait(p, pr, c.task), p.tag) && ll_ready(ll_wait(p, pr + 1, c.task), p.tag);
+          }
+          if (!__shfl_sync(0xffffffffu, ready, leader)) break;  // abort or timeout: carry on with what is loaded
+          if (stale >> kCombGroup) ml = ld_relaxed_v2u64(r + (size_t)lane * rec);
+#pragma unroll
+          for (int k = 0; k < kCombGroup; ++k)
+            if (stale & (1u << k)) qv[k] = ld_relaxed_v2u64(r + (size_t)(k0 + k) * rec + 2 + e);
+        }
+        if (k0 == 0) {
+          const float mk = __uint_as_float((uint32_t)ml.x), lk = __uint_as_float((uint32_t)ml.y);
+          M = warp_max(mk);
+          wk = mk == -INFINITY ? 0.f : exp2f(mk - M);
+          L = warp_sum(wk * lk);
+        }
+#pragma unroll
+        for (int k = 0; k < kCombGroup; ++k) {
+          const float w = __shfl_sync(0xffffffffu, wk, (k0 + k) & 31);
+          a0 = fmaf(w, __uint_as_float((uint32_t)qv[k].x), a0);
+          a1 = fmaf(w, __uint_as_float((uint32_t)qv[k].y), a1);
+        }
+      }
+      if (mine) {
+        const float inv = 1.f / L;
+        const size_t o = (size_t)s * Hq * D + (size_t)(g * G + h) * D + e;
+        *reinterpret_cast<float2*>(out + o) = make_float2(a0 * inv, a1 * inv);
+        if (om) st_relaxed_v2u64(om + o, ll_pack(a0 * inv, p.tag), ll_pack(a1 * inv, p.tag));
+      }
+      return;
+    }
     const float* r = scr + h * (D + 2);
     const float mk = lane < P ? __ldcg(r + (size_t)lane * rec) : -INFINITY;
     const float lk = lane < P ? __ldcg(r + (size_t)lane * rec + 1) : 0.f;

@@ -298,10 +298,18 @@ def _check_sync_plan(tasks, edges, plan, ll=None):
             assert int(tasks["remaining_deps"][t]) == len(parents[t])
             continue
         # the last split of a K-split row block waits for its sibling splits
-        # inside its body (the block's arrival counter), not through the plan
+        # inside its body (the block's arrival counter), not through the plan;
+        # a combine whose partials' records carry pairs polls those partials
         S, j = int(tasks["kv_len"][t]) >> 16, int(tasks["kv_len"][t]) & 0xFFFF
         deferred = set()
-        if int(tasks["op_id"][t]) == ol.OP_GEMV and int(tasks["config_id"][t]) == 1 and S >= 2 and j == S - 1:
+        scr = int(tasks["in_buf"][t][0])
+        if int(tasks["op_id"][t]) == ol.OP_ATT_COMBINE and buf_ll is not None and buf_ll[scr]:
+            deferred = {p for p in parents[t] if int(tasks["out_buf"][p]) == scr}
+            assert all(int(tasks["op_id"][p]) == ol.OP_ATT_PARTIAL for p in deferred)
+            assert len(deferred) == int(tasks["reserved"][t][3]), f"combine {t}: polls {len(deferred)} partials"
+            assert int(tasks["reserved"][t][2]) >> 16 == 0 and int(tasks["reserved"][t][3]) <= 32
+            covered = set(deferred)
+        elif int(tasks["op_id"][t]) == ol.OP_GEMV and int(tasks["config_id"][t]) == 1 and S >= 2 and j == S - 1:
             deferred = set(range(t - (S - 1), t))
             assert deferred <= parents[t], f"task {t}: sibling splits are not its parents"
             for q in deferred:
@@ -337,8 +345,11 @@ def test_sync_plan_is_equivalent_to_the_edges(L, name):
         if w.B <= 4:
             # every GEMV, split-KV partial and cache append reads tagged pairs
             # (their inputs come from GEMV, COMBINE, embedding or norm tasks),
-            # no other task does
+            # no other task does; every attention scratch carries pairs too
+            # (decode combines poll their partials' records)
             assert np.all(ll[0][polls] == 1) and np.all(ll[0][~polls] == 0)
+            comb = tasks[tasks["op_id"] == ol.OP_ATT_COMBINE]
+            assert all(ll[1][int(b)] for b in comb["in_buf"][:, 0])
         else:
             assert not ll[0].any() and not ll[1].any()
         # a B = 1 hand-off between GEMVs costs one atomic per tile, not one per edge

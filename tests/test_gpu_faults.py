@@ -123,15 +123,20 @@ def test_trace_respects_every_dependency():
     for c in range(len(off) - 1):
         assert np.all(cta[q[off[c]:off[c + 1]]] == c)
     from task_graph_interpreter_gb300 import _lib as L
-    task_ll, _ = L.mk_get_ll_plan(dec.graph.h, N, len(dec.graph.bufs) + 3)
+    task_ll, buf_ll = L.mk_get_ll_plan(dec.graph.h, N, len(dec.graph.bufs) + 3)
     assert task_ll.any()
+    # a decode combine polls its partials' tagged records
+    polled = np.zeros(N, dtype=bool)
+    polled[(t["op_id"] == ol.OP_ATT_COMBINE) & (buf_ll[t["in_buf"][:, 0]] == 1)] = True
+    assert polled.any()
     for p in range(N):
         ch = edges[t["dependents_offset"][p]: t["dependents_offset"][p] + t["num_dependents"][p]]
         # a child waiting on counters starts after its parents end; one that
         # polls tagged pairs starts at once and ends only after its parents
         # began (their output is written before their end stamp)
-        ctr = ch[task_ll[ch] == 0]
-        ll = ch[task_ll[ch] == 1]
+        tagged = (task_ll[ch] == 1) | (polled[ch] & (t["op_id"][p] == ol.OP_ATT_PARTIAL))
+        ctr = ch[~tagged]
+        ll = ch[tagged]
         assert np.all(tr[ctr, 2] >= tr[p, 3]), f"a child of task {p} started before it ended"
         assert np.all(tr[ll, 3] >= tr[p, 2]), f"a tagged child of task {p} ended before it began"
     ev = dec.graph.chrome_trace()["traceEvents"]
