@@ -1332,7 +1332,7 @@ __device__ void tc_mma_warp(const KParams& p, uint8_t* ring, uint64_t* full, uin
   if ((threadIdx.x & 31) != 0) return;
   const int nst = p.nstages;
   // completed phases seen: task_go 0, x_full 1-2, mma_bar 3-4, acc_empty 5,
-  // s_empty 6-7, q_full 8
+  // s_empty 6-7, q_full 8, s_full 9-10
   uint32_t ph = 0;
   bool first = true, ok = true;
   const uint64_t t0 = globaltimer();
@@ -1374,6 +1374,14 @@ __device__ void tc_mma_warp(const KParams& p, uint8_t* ring, uint64_t* full, uin
           }
         }
         tc_commit(&ctl->s_full[j]);  // also when a wait failed, so the consumers' waits end
+        if (D == 128) {
+          // the K slot is free once the block's score MMAs are done: hand it
+          // back now (for all eight consumer warps), so the copies of the
+          // blocks ahead need not wait for the block's softmax and P V
+          if (!bar_wait(p, &ctl->s_full[j], (ph >> (9 + j)) & 1u, task, false)) ok = false;
+          mbar_arrive_cnt(&empty[rp.slot], kConsumerWarps);
+        }
+        ph ^= 1u << (9 + j);  // one phase per commit, waited for or not
         rp.advance(nst);
         if (D == 128) rp.advance(nst);  // the block's V slot
       }
@@ -1939,11 +1947,7 @@ __device__ void tc_partial_body(Ctx& c, const mk_task_descriptor& d, const PartG
       __syncwarp();
       if (lane == 0) mbar_arrive(&ctl->p_full[j]);  // release: the probabilities and factors
       if (b >= 0) {
-        if (D == 128) {  // the K slot: its scores were read, so the MMAs are done with it
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&c.empty[c.rp.slot]);
-          c.rp.advance(c.nst);
-        }
+        if (D == 128) c.rp.advance(c.nst);  // the K slot: the MMA warp hands it back
         // the V slot (or the block's slot at D = 64): the P V warps read it;
         // these warps count themselves in once it has been filled
         const uint32_t vslot = consume_begin(c);
@@ -1980,11 +1984,7 @@ __device__ void tc_partial_body(Ctx& c, const mk_task_descriptor& d, const PartG
         vb = smem_addr(nkv + q.T * D);  // this step's values
       } else {
         nv = min(kKeyBlock, q.jst - (q.j0 + b * kKeyBlock));
-        if (D == 128) {  // the K slot: the softmax warps saw its scores, the MMAs are done with it
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&c.empty[c.rp.slot]);
-          c.rp.advance(c.nst);
-        }
+        if (D == 128) c.rp.advance(c.nst);  // the K slot: the MMA warp hands it back
         vslot = consume_begin(c);
         vb = smem_addr(c.ring + (size_t)vslot * kStageBytes) + (D == 128 ? 0u : kKeyBlock * 128u);
       }
