@@ -1109,14 +1109,17 @@ __device__ void gemv_task(Ctx& c, const mk_task_descriptor& d) {
 // which releases that range's ring slots and staging tile.
 // This thread's share of one K range of x: batch row = warp, kpt = 2 * nkb
 // consecutive columns from k0 (rows past the batch read as zero).
-__device__ __forceinline__ void tc_load_x(float (&xv)[8], const float* x, int K, int b, int Bact, int k0,
-                                          int kpt) {
+// This lane's kpt columns of x from k0 (row b; zero past the batch) and,
+// for a normalised input, the gains of those columns (bf16 pairs).
+__device__ __forceinline__ void tc_load_x(float (&xv)[8], uint32_t (&gv)[4], const float* x, const uint16_t* gamma,
+                                          int K, int b, int Bact, int k0, int kpt) {
 #pragma unroll
   for (int e = 0; e < 8; e += 2) {
     float2 v = make_float2(0.f, 0.f);
     if (e < kpt && b < Bact) v = __ldcg(reinterpret_cast<const float2*>(x + (size_t)b * K + k0 + e));
     xv[e] = v.x;
     xv[e + 1] = v.y;
+    gv[e >> 1] = (gamma && e < kpt) ? __ldg(reinterpret_cast<const uint32_t*>(gamma + k0 + e)) : 0u;
   }
 }
 
@@ -1153,23 +1156,30 @@ __device__ void tc_gemv_task(Ctx& c, const mk_task_descriptor& d) {
   float ss = 0.f;  // sum of squares of this lane's raw x (first row group)
   for (int g0 = 0; g0 < G.cn; g0 += T.RG) {
     const int rows_g = min(T.RG, G.cn - g0);
-    // x of the next two K ranges is in flight while a range is staged
+    // x (and the gains) of the next two K ranges are in flight while a
+    // range is staged
     float xa[8], xb[8];
-    tc_load_x(xa, x, T.K, warp, G.B, T.k0 + lane * kpt, kpt);
-    if (T.nkr > 1) tc_load_x(xb, x, T.K, warp, G.B, T.k0 + T.nkb * 64 + lane * kpt, kpt);
+    uint32_t ga[4], gb[4];
+    tc_load_x(xa, ga, x, gamma, T.K, warp, G.B, T.k0 + lane * kpt, kpt);
+    if (T.nkr > 1) tc_load_x(xb, gb, x, gamma, T.K, warp, G.B, T.k0 + T.nkb * 64 + lane * kpt, kpt);
     for (int kr = 0; kr < T.nkr; ++kr) {
       float xc[8];
+      uint32_t gc[4];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
         xc[e] = xa[e];
         xa[e] = xb[e];
       }
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        gc[e] = ga[e];
+        ga[e] = gb[e];
+      }
       const int k0 = T.k0 + kr * T.nkb * 64 + lane * kpt;  // this lane's first column
-      if (kr + 2 < T.nkr) tc_load_x(xb, x, T.K, warp, G.B, k0 + 2 * T.nkb * 64, kpt);
+      if (kr + 2 < T.nkr) tc_load_x(xb, gb, x, gamma, T.K, warp, G.B, k0 + 2 * T.nkb * 64, kpt);
       const int j = kr & 1;
       if (kr >= 2) {  // the MMAs of kr - 2 have read this staging tile
-        if (lane == 0) bar_wait(p, &ctl->mma_bar[j], (c.tc_ph >> j) & 1u, c.task, false);
-        __syncwarp();
+        bar_wait(p, &ctl->mma_bar[j], (c.tc_ph >> j) & 1u, c.task, false);  // every lane waits
         c.tc_ph ^= 1u << j;
       }
       const uint32_t xt = xb0 + (uint32_t)j * (kXbufBytes / 2);  // K block b at xt + b * 3072
@@ -1181,9 +1191,8 @@ __device__ void tc_gemv_task(Ctx& c, const mk_task_descriptor& d) {
           float v0 = xc[e], v1 = xc[e + 1];
           if (g0 == 0) ss += v0 * v0 + v1 * v1;
           if (gamma) {
-            const uint32_t gw = __ldg(reinterpret_cast<const uint32_t*>(gamma + k0 + e));
-            v0 *= bf_lo(gw);
-            v1 *= bf_hi(gw);
+            v0 *= bf_lo(gc[e >> 1]);
+            v1 *= bf_hi(gc[e >> 1]);
           }
           // exact three-part split: each part is the bf16 rounding of what
           // the previous parts leave (f32 subtractions of nearby values)
@@ -1214,8 +1223,7 @@ __device__ void tc_gemv_task(Ctx& c, const mk_task_descriptor& d) {
     if (g0 == 0 && gamma && T.S == 1 && lane == 0)  // 1/rms per batch row (warp b holds row b's columns)
       red[64 + warp] = 1.0f / sqrtf(ssw / (float)T.K + __uint_as_float(d.reserved[2]));
     // the row group's MMAs are done (acc_full follows every earlier commit)
-    if (lane == 0) bar_wait(p, &ctl->acc_full, (c.tc_ph >> 2) & 1u, c.task, false);
-    __syncwarp();
+    bar_wait(p, &ctl->acc_full, (c.tc_ph >> 2) & 1u, c.task, false);  // every lane waits
     c.tc_ph ^= 4u;
     for (int kr = max(T.nkr - 2, 0); kr < T.nkr; ++kr)
       c.tc_ph ^= 1u << (kr & 1);  // the last two ranges' commits (only the MMA warp waited on them)
@@ -1895,8 +1903,7 @@ __device__ void tc_partial_body(Ctx& c, const mk_task_descriptor& d, const PartG
       } else {
         const int nv = min(kKeyBlock, q.jst - (q.j0 + b * kKeyBlock));  // real keys in the block
         const int jb = b & 1;
-        if (lane == 0) bar_wait(p, &ctl->s_full[jb], (c.tc_ph >> (3 + jb)) & 1u, c.task, false);
-        __syncwarp();
+        bar_wait(p, &ctl->s_full[jb], (c.tc_ph >> (3 + jb)) & 1u, c.task, false);  // every lane waits
         c.tc_ph ^= 1u << (3 + jb);
         if (b == 0) trace_mark(c, 0);
         tc_fence_after();
@@ -1925,8 +1932,7 @@ __device__ void tc_partial_body(Ctx& c, const mk_task_descriptor& d, const PartG
         pr[r] = sc[r] == -INFINITY ? 0.f : exp2f(sc[r] - mn[r]);
       }
       if (v >= 2) {  // the P V warps are done with buffer j (hand-off v - 2)
-        if (lane == 0) bar_wait(p, &ctl->p_empty[j], (c.tc_ph >> (5 + j)) & 1u, c.task, false);
-        __syncwarp();
+        bar_wait(p, &ctl->p_empty[j], (c.tc_ph >> (5 + j)) & 1u, c.task, false);  // every lane waits
         c.tc_ph ^= 1u << (5 + j);
       }
       *reinterpret_cast<float4*>(P + key * 4) = make_float4(pr[0], pr[1], pr[2], pr[3]);
@@ -1967,8 +1973,7 @@ __device__ void tc_partial_body(Ctx& c, const mk_task_descriptor& d, const PartG
     const int w4 = warp - 4;
     for (int v = 0; v < nvb; ++v) {
       const int j = v & 1, b = v - nb0;
-      if (lane == 0) bar_wait(p, &ctl->p_full[j], (c.tc_ph >> (7 + j)) & 1u, c.task, false);
-      __syncwarp();
+      bar_wait(p, &ctl->p_full[j], (c.tc_ph >> (7 + j)) & 1u, c.task, false);  // every lane waits
       c.tc_ph ^= 1u << (7 + j);
       const float* fac = red + 64 + j * 4;
 #pragma unroll
