@@ -460,8 +460,7 @@ __device__ void record_warp(const KParams& p, TaskRec* recs, uint64_t* rfull, ui
     const uint32_t e = k & (kRecs - 1);
     TaskRec* r = recs + e;
     if (k >= (uint32_t)kRecs) {  // the consumers are done with this entry's previous task
-      int ok = 1;
-      if (lane == 0) ok = bar_wait(p, &rempty[e], ((k / kRecs) - 1) & 1u, -1, true) ? 1 : 0;
+      const int ok = bar_wait(p, &rempty[e], ((k / kRecs) - 1) & 1u, -1, true) ? 1 : 0;  // every lane waits
       if (!__shfl_sync(all, ok, 0)) return;
     }
     if (!seq_next(sq, p, task, lvl)) {
@@ -2449,8 +2448,8 @@ __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
     uint64_t t_wait = 0, t_start = 0;
     if (tid < 32) {  // warp 0 takes the record, then waits (MEGA: all lanes; other modes: thread 0)
       int run = 1;   // 1: run the task, 0: stop (abort or timeout), 2: no more tasks
-      if (tid == 0 && !bar_wait(p, &rfull[e], (k / kRecs) & 1u, -1, true)) run = 0;
-      __syncwarp();  // orders lane 0's acquire of the record before the other lanes' reads
+      // every lane acquires the record (no single-lane wait and warp barrier)
+      if (!bar_wait(p, &rfull[e], (k / kRecs) & 1u, -1, true)) run = 0;
       run = __shfl_sync(0xffffffffu, run, 0);
       if (run && r->task < 0) run = 2;
       if (run == 1) {
