@@ -634,6 +634,15 @@ __device__ uint64_t ll_wait(const KParams& p, const uint64_t* m, int task) {
   }
 }
 
+// Warp-uniform poll: every lane polls the pair the leader names (one
+// request per poll for the warp, no divergent single-lane loop); lane 0's
+// answer decides for the warp.
+__device__ __forceinline__ bool ll_poll_warp(const KParams& p, const uint64_t* pm, int leader, int task) {
+  pm = reinterpret_cast<const uint64_t*>(__shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(pm), leader));
+  const int ready = ll_ready(ll_wait(p, pm, task), p.tag) ? 1 : 0;
+  return __shfl_sync(0xffffffffu, ready, 0) != 0;
+}
+
 __device__ __forceinline__ float ll_load1(const KParams& p, const uint64_t* m, int task) {
   uint64_t v = ld_relaxed_u64(m);
   if (!ll_ready(v, p.tag)) v = ll_wait(p, m, task);
@@ -657,15 +666,11 @@ __device__ __forceinline__ void ll_gather(const KParams& p, int task, const uint
     const uint32_t want = __ballot_sync(0xffffffffu, first >= 0);
     if (!want) break;
     const int leader = __ffs(want) - 1;
-    int ready = 1;
-    if ((int)(threadIdx.x & 31) == leader) {
-      const uint64_t* pm = m[0];
+    const uint64_t* pm = m[0];
 #pragma unroll
-      for (int i = 1; i < N; ++i)
-        if (first == i) pm = m[i];
-      ready = ll_ready(ll_wait(p, pm, task), p.tag) ? 1 : 0;
-    }
-    if (!__shfl_sync(0xffffffffu, ready, leader)) break;
+    for (int i = 1; i < N; ++i)
+      if (first == i) pm = m[i];
+    if (!ll_poll_warp(p, pm, leader, task)) break;
 #pragma unroll
     for (int i = 0; i < N; ++i)
       if (!ll_ready(q[i], p.tag)) q[i] = ld_relaxed_u64(m[i]);
@@ -720,9 +725,7 @@ __device__ __forceinline__ void ll_load_x(const KParams& p, int task, float (&xr
     const uint32_t want = __ballot_sync(0xffffffffu, pend != 0);
     if (!want) break;
     const int leader = __ffs(want) - 1;
-    int ready = 1;
-    if (lane == leader) ready = ll_ready(ll_wait(p, probe, task), p.tag) ? 1 : 0;
-    if (!__shfl_sync(0xffffffffu, ready, leader)) break;  // abort or timeout: carry on with what is loaded
+    if (!ll_poll_warp(p, probe, leader, task)) break;  // abort or timeout: carry on with what is loaded
     probe = nullptr;
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
@@ -1040,9 +1043,7 @@ __device__ void gemv_task(Ctx& c, const mk_task_descriptor& d) {
       const uint32_t want = __ballot_sync(0xffffffffu, first >= 0);
       if (!want) break;
       const int leader = __ffs(want) - 1;
-      int ready = 1;
-      if ((int)(threadIdx.x & 31) == leader) ready = ll_ready(ll_wait(p, rc + (size_t)first * G.n, c.task), p.tag);
-      if (!__shfl_sync(0xffffffffu, ready, leader)) break;
+      if (!ll_poll_warp(p, rc + (size_t)(first < 0 ? 0 : first) * G.n, leader, c.task)) break;
 #pragma unroll
       for (int b = 0; b < 8; ++b)
         if (!ll_ready(q[b], p.tag)) q[b] = ld_relaxed_u64(rc + (size_t)b * G.n);
@@ -2136,13 +2137,14 @@ __device__ void combine_task(Ctx& c, const mk_task_descriptor& d) {
           const uint32_t want = __ballot_sync(0xffffffffu, stale != 0);
           if (!want) break;
           const int leader = __ffs(want) - 1;
-          int ready = 1;
-          if (lane == leader) {
-            const int k = __ffs(stale) - 1;
-            const uint64_t* pr = k == kCombGroup ? r + (size_t)lane * rec : r + (size_t)(k0 + k) * rec + 2 + e;
-            ready = ll_ready(ll_wait(p, pr, c.task), p.tag) && ll_ready(ll_wait(p, pr + 1, c.task), p.tag);
-          }
-          if (!__shfl_sync(0xffffffffu, ready, leader)) break;  // abort or timeout: carry on with what is loaded
+          const int k = stale ? __ffs(stale) - 1 : 0;
+          const uint64_t* pr = k == kCombGroup ? r + (size_t)lane * rec : r + (size_t)(k0 + k) * rec + 2 + e;
+          // the stale half of the leader's pair of pairs
+          bool second = ll_ready(ml.x, p.tag);
+#pragma unroll
+          for (int kk = 0; kk < kCombGroup; ++kk)  // no dynamic register indexing
+            if (kk == k) second = ll_ready(qv[kk].x, p.tag);
+          if (!ll_poll_warp(p, pr + (second ? 1 : 0), leader, c.task)) break;  // abort or timeout: carry on
           if (stale >> kCombGroup) ml = ld_relaxed_v2u64(r + (size_t)lane * rec);
 #pragma unroll
           for (int k = 0; k < kCombGroup; ++k)
