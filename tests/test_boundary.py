@@ -639,3 +639,21 @@ def test_ksplit_lowering_validates(L, name, num_ctas):
         assert col == parts[0][3]
     # every split tile of an op fits the tile target; rows per block <= 256 / seg
     assert np.all(split["reserved"][:, 1] * np.where(split["flags"] & ol.F_SILU_MUL, 2, 1) <= 256)
+
+
+def test_tagged_scratch_only_for_polling_combines(L):
+    # a decode combine polls its partials' tagged records only up to 32
+    # partials: 128 keys in chunks of 4 (32 partials) tag the scratch, in
+    # chunks of 3 (43) they do not, and neither does a chunk step
+    w = synth.workload("tiny")
+    for chunk, T, tagged in ((4, 1, True), (3, 1, False), (4, 2, False)):
+        spec = llama_decode_spec(w.model, 1, [128], 140, chunk, 16, col_align=4, T=T)
+        g = _replay(L, spec, 1)
+        try:
+            tasks = np.frombuffer(L.mk_get_tasks(g), dtype=ol.TASK_DTYPE)
+            task_ll, buf_ll = L.mk_get_ll_plan(g, len(tasks), len(spec["buffers"]))
+            comb = tasks[tasks["op_id"] == ol.OP_ATT_COMBINE]
+            assert all(bool(buf_ll[int(b)]) == tagged for b in comb["in_buf"][:, 0]), (chunk, T)
+            _check_sync_plan(tasks, L.mk_get_edges(g), L.mk_get_sync_plan(g, len(tasks)), (task_ll, buf_ll))
+        finally:
+            L.mk_destroy(g)

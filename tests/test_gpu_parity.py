@@ -158,3 +158,13 @@ def test_ffn_widths_of_every_gemv_slot_geometry(F, B):
     m = dataclasses.replace(synth.TINY, F=F, name=f"tiny_f{F}")
     w = synth.custom(m, B, [100, 37][:B], 3, name=f"tiny_f{F}_b{B}")
     assert _run_and_compare(w, 2) >= 1
+
+
+@pytest.mark.parametrize("chunk", [5, 4, 3])
+def test_combines_polling_one_and_two_groups_of_partials(chunk):
+    # 128 cached keys in chunks of 5, 4 and 3: 26, 32 and 43 partials per
+    # (sequence, KV head).  Up to 32 the decode combine polls its partials'
+    # tagged records (two load groups past 16); past 32 the scratch carries
+    # no pairs and the combine waits for its partials through counters
+    w = synth.custom(synth.TINY, 1, [128], 3, chunk=chunk, name=f"tiny_c{chunk}")
+    assert _run_and_compare(w, 2) >= 1
