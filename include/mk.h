@@ -13,7 +13,7 @@
  * (same page: the buffer-table and upload part).  mk_decode_step() runs one
  * persistent kernel, one CTA per SM, that walks a static per-CTA queue of
  * tasks; each task waits only for its own producers, through counters in
- * global memory or, at B <= 4, by polling its inputs' (step tag, value)
+ * global memory or, at one or two activation rows, by polling its inputs' (step tag, value)
  * pairs, with no grid-wide barrier ("Megakernels",
  * runhoid.com: the "Hoid's approach to megakernels" section and its Fig. 5,
  * the on-GPU interpreter in which a block waits only for its producers).
@@ -109,7 +109,7 @@ extern "C" {
  * copyable, remaining_deps 4-byte aligned for atomics. */
 typedef struct mk_task_descriptor {
   uint16_t op_id;              /*  0 */
-  uint16_t config_id;          /*  2  GEMV: 0 if m < 8 else 1; attention: 0 if D=64, 1 if D=128 */
+  uint16_t config_id;          /*  2  GEMV: 0 if m < 3 else 1; attention: 0 if D=64, 1 if D=128 */
   uint16_t step;               /*  4  speculative draft step tag; always 0 */
   uint16_t flags;              /*  6  MK_F_* */
   int32_t remaining_deps;      /*  8  number of distinct parents */
@@ -282,7 +282,11 @@ int mk_scratch_size(const mk_graph* g, uint16_t buf, size_t* bytes);
  *           with a residual; reserved={s, float bits of eps}
  *  GEMV     in={x,W,aux} out=y m=B n k; reserved={col_begin, col_count,
  *           float bits of eps (RMS_NORM_INPUT) or 0, pairs idx or 0,
- *           tile index (ARGMAX_EPI) or 0}
+ *           tile index (ARGMAX_EPI) or 0}.  config_id 1 (tensor cores, from
+ *           three activation rows) with a K split: kv_len = j | S << 16
+ *           (split j of S), reserved[3] = k_begin | k_count << 16,
+ *           reserved[4] = the split's scratch record (the last split's
+ *           record ends the block's S records)
  *  APPEND   in={qkv,K,V} out=K m=B n=D k=Hq kv_len=capacity reserved={s,g,Hkv,0,0}
  *  PARTIAL  in={qkv,K,V} out=scratch, same m/n/k/kv_len,
  *           reserved={s,g,Hkv, c | (P_s << 16), first slot of (s,g)}
@@ -329,7 +333,7 @@ int mk_debug_patch_task(mk_graph* g, int task, const mk_task_descriptor* d);
 int mk_get_sync_plan(const mk_graph* g, const uint32_t** wait_off, const uint32_t** wait,
                      const uint32_t** sig_off, const uint32_t** sig, uint32_t* counter_words);
 
-/* Tagged hand-offs (B <= 4, megakernel mode): task_ll[t] = 1 for the GEMV,
+/* Tagged hand-offs (one or two activation rows, megakernel mode): task_ll[t] = 1 for the GEMV,
  * ATTENTION_PARTIAL and ATTENTION_APPEND tasks that read all their
  * activation inputs as (step tag, value) pairs and so wait on no counter;
  * buf_ll[b] = 1 for the buffers whose producers also write those pairs (into
@@ -357,7 +361,8 @@ int mk_get_queues(const mk_graph* g, const int32_t** offsets, const int32_t** ta
 int mk_upload(mk_graph* g, void* stream);
 
 /* Number of GEMV tiles of an uploaded graph that run on the tensor-core
- * path: tiles of batch-8 ops (config_id 1) whose K is a multiple of 64.
+ * path: tiles of ops with three to eight activation rows (config_id 1;
+ * rows past B enter as zeros) whose K is a multiple of 64.
  * Their weights stream through TMA tensor copies (a tensor map per weight
  * buffer, built by mk_upload) and multiply on tcgen05 tensor cores with
  * f32 accumulators in tensor memory; the activations enter as three

@@ -64,6 +64,8 @@ OP_ATT_APPEND, OP_ATT_PARTIAL, OP_ATT_COMBINE = 7, 8, 9
 
 F_SILU_MUL, F_ADD_RESIDUAL, F_RMS_NORM_INPUT, F_ARGMAX_EPI = 1, 2, 4, 8
 
+TC_MIN_ROWS = 3   # activation rows from which GEMV tiles are config 1 (tensor cores)
+
 NO_BUF = 0xFFFF
 BUF_STATE, BUF_ROPE_COS, BUF_ROPE_SIN = 0, 1, 2
 
@@ -104,11 +106,11 @@ def ksplit_plan(n: int, k: int, flags: int, m: int, tiles_target: int, col_align
     sharing the MMA), the op is cut into blocks of up to 256 / seg rows
     (ceil(seg * n / 256) blocks, width rounded up to 8) and each block into
     S = min(k / 64, tiles_target // blocks) consecutive K ranges of whole
-    64-column blocks; S < 2, an argmax epilogue, or m < 8 keep the tiling."""
+    64-column blocks; S < 2, an argmax epilogue, or m < TC_MIN_ROWS keep the tiling."""
     W = tile_width(n, tiles_target, col_align)
     seg = 2 if flags & F_SILU_MUL else 1
     plain = (W, ceil_div(n, W), 1)
-    if m < 8 or flags & F_ARGMAX_EPI or seg * W >= 128 or k % 64:
+    if m < TC_MIN_ROWS or flags & F_ARGMAX_EPI or seg * W >= 128 or k % 64:
         return plain
     nb = ceil_div(seg * n, 256)
     Wb = ceil_div(ceil_div(n, nb), 8) * 8
@@ -246,7 +248,7 @@ def lower(spec: dict):
                 writes = [(op["out"], 0, B, c0, c0 + cn)]
                 if fl & F_ARGMAX_EPI:
                     writes.append((pairs, t, t + 1, 0, B))
-                emit(dict(op_id=OP_GEMV, config_id=0 if B < 8 else 1, flags=fl,
+                emit(dict(op_id=OP_GEMV, config_id=0 if B < TC_MIN_ROWS else 1, flags=fl,
                           in_buf=(op["x"], op["w"], aux), out_buf=op["out"],
                           m=B, n=n, k=K,
                           reserved=(c0, cn, eps_bits,

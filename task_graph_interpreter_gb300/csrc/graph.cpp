@@ -64,7 +64,7 @@ KSplit ksplit_plan(int n, int k, uint32_t flags, int m, int tiles_target, int co
   KSplit r{tile_width(n, tiles_target, col_align), 1, 1};
   r.nb = (int)cdiv(n, r.W);
   const int seg = (flags & MK_F_SILU_MUL) ? 2 : 1;
-  if (m < 8 || (flags & MK_F_ARGMAX_EPI) || seg * r.W >= 128 || k % 64) return r;
+  if (m < kTcMinRows || (flags & MK_F_ARGMAX_EPI) || seg * r.W >= 128 || k % 64) return r;
   const int nb = (int)cdiv((int64_t)seg * n, 256);
   const int W = (int)(cdiv(cdiv(n, nb), 8) * 8);
   const int S = std::max(1, std::min(k / 64, tiles_target / (int)cdiv(n, W)));
@@ -582,7 +582,7 @@ extern "C" int mk_lower(mk_graph* g) {
         for (int c0 = 0; c0 < op.n; c0 += w, ++t) {
           const int cn = std::min(w, op.n - c0);
           mk_task_descriptor d = blank(MK_OP_GEMV);
-          d.config_id = op.B < 8 ? 0 : 1;
+          d.config_id = op.B < kTcMinRows ? 0 : 1;
           d.flags = (uint16_t)op.flags;
           d.in_buf[0] = op.a[0];
           d.in_buf[1] = op.a[1];
@@ -839,7 +839,7 @@ extern "C" int mk_lower(mk_graph* g) {
   return MK_OK;
 }
 
-// Tagged hand-offs.  At B <= 4 the activations a GEMV reads (its x, and
+// Tagged hand-offs.  At one or two activation rows the activations a GEMV reads (its x, and
 // its residual) and the qkv rows attention tasks read are also written
 // by their producers as (step tag, value) pairs into a library-owned
 // mirror.  Such a reader polls its inputs' tags instead of waiting on
@@ -862,7 +862,7 @@ void mk::build_ll_plan(mk_graph* g, const std::vector<std::vector<int>>& parents
   const size_t NB = g->bufs.size(), N = g->tasks.size();
   g->ll_buf.assign(NB, 0);
   g->ll_task.assign(N, 0);
-  if (g->rows() > 4) return;
+  if (g->rows() >= kTcMinRows) return;
   std::vector<uint8_t> read_as_input(NB, 0), bad_writer(NB, 0);
   for (const mk_task_descriptor& d : g->tasks) {
     if (d.op_id == MK_OP_GEMV) {

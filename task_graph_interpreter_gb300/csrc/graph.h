@@ -67,7 +67,7 @@ struct mk_graph {
   std::vector<uint32_t> wait_off, wait, sig_off, sig;  // wait holds (counter, count) pairs
   uint32_t counter_words = 0;
   uint32_t ksplit_records = 0;     // K-split scratch records the lowering assigned
-  // tagged hand-offs (B <= 4): buffers whose values are also written as
+  // tagged hand-offs (one or two rows): buffers whose values are also written as
   // (step tag, value) pairs, and the GEMV, partial and append tasks that
   // read all their inputs from such pairs instead of waiting on counters
   std::vector<uint8_t> ll_buf, ll_task;
@@ -88,6 +88,9 @@ KSplit ksplit_plan(int n, int k, uint32_t flags, int m, int tiles_target, int co
 // index in dependency rectangles: one record of kKsplitRecFloats floats per
 // split tile ([256 rows][8 batch] partial sums, then 8 partial sums of
 // squares of x); the last split's record holds its block's arrival counter.
+// Activation rows (B * T) from which GEMVs are dense contractions on the
+// tensor cores (config_id 1, the batch-8 kernel; rows past B zero-padded)
+constexpr int kTcMinRows = 3;
 constexpr uint16_t kKsplitBuf = 0xFFFE;
 constexpr int kKsplitRecFloats = 256 * 8 + 8;
 int query_sm_count(int* out);  // runtime.cu

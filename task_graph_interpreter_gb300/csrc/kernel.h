@@ -15,7 +15,7 @@ constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 128;  // + one producer warpgroup
 constexpr int kLaunchRegs = 168;    // registers per thread at launch (384 threads, 1 CTA/SM)
 // The producer warpgroup runs the copy thread, the task-record warp and (in
-// the B >= 8 kernel) the MMA warp.
+// the class-2 kernel) the MMA warp.
 constexpr int kProducerRegs = 56;   // after setmaxnreg.dec in the producer warpgroup
 constexpr int kConsumerRegs = 224;  // after setmaxnreg.inc in the consumer warpgroups
 static_assert(128 * kProducerRegs + 2 * 128 * kConsumerRegs <= kThreads * kLaunchRegs,
@@ -24,13 +24,13 @@ constexpr int kStageBytes = 32768;               // one ring slot
 constexpr int kStageElems = kStageBytes / 2;     // bf16 elements per slot
 constexpr int kMaxStages = 6;
 constexpr int kScratchBytes = 24576;             // per-task shared scratch
-constexpr int kXbufBytes = 24576;                // B >= 8 kernel: two 12 KB activation staging tiles
-constexpr int kTmemCols = 256;                   // B >= 8 kernel: GEMV accumulator columns
-// Tensor memory per batch class: the B >= 8 kernel holds the GEMV
-// accumulators (256 columns) and, after them, the split-KV partials' two
-// 16-column score buffers; the B <= 4 kernel only the score buffers; the
-// B <= 2 kernel none (it runs no tensor-core work).
-__host__ __device__ constexpr uint32_t tmem_cols(int bclass) { return bclass == 2 ? 512u : bclass == 1 ? 32u : 0u; }
+constexpr int kXbufBytes = 24576;                // class-2 kernel: two 12 KB activation staging tiles
+constexpr int kTmemCols = 256;                   // class-2 kernel: GEMV accumulator columns
+// Tensor memory per batch class: the class-2 kernel (three to eight
+// activation rows) holds the GEMV accumulators (256 columns) and, after
+// them, the split-KV partials' two 16-column score buffers; the class-0
+// kernel (one or two rows) none: it runs no tensor-core work.
+__host__ __device__ constexpr uint32_t tmem_cols(int bclass) { return bclass == 2 ? 512u : 0u; }
 __host__ __device__ constexpr uint32_t tmem_part_col(int bclass) { return bclass == 2 ? 256u : 0u; }
 constexpr int kTmapBytes = 128;                  // one CUtensorMap
 constexpr int kKeyBlockRows = 128;               // keys per K box of the tensor-core split-KV partials
@@ -57,7 +57,7 @@ struct KParams {
   const int32_t* level_tasks; // LEVELS: task ids grouped by level
   uint32_t* level_bar;        // LEVELS: one arrival counter per level boundary
   int32_t* status;            // int32[4]
-  uint64_t* const* mirrors;   // MEGA, B <= 4: per buffer index, its (step tag, value) pairs or null
+  uint64_t* const* mirrors;   // MEGA, one or two rows: per buffer index, its (step tag, value) pairs or null
   uint32_t tag;               // MEGA: this step's tag (monotone across steps, never 0)
   const uint8_t* tmaps;       // CUtensorMap per buffer index (tensor-core weights), kTmapBytes each
   const int32_t* tm_rows;     // per buffer index: rows of its tensor map's box, 0 = no map

@@ -15,7 +15,9 @@
 //
 // Warp roles: warps 0-7 consume (compute), warp 8 produces (bulk copies).
 // Task bodies:
-//   GEMV (B < 8 and B = 8 on CUDA cores): one output-column tile; epilogues
+//   GEMV: one output-column tile (or one K split of a row block), on CUDA
+//     cores for one or two activation rows, on the tensor cores from three
+//     (up to eight, rows past B zero); epilogues
 //     RMS_NORM_INPUT, SILU_MUL, ADD_RESIDUAL, ARGMAX_EPI ("mega kernel
 //     initial", lowering part: the fusions are epilogue flags of one GEMV
 //     pass, and the final norm is fused into the lm_head GEMV).
@@ -121,7 +123,7 @@ struct GemvGeom {
 
 __device__ __forceinline__ void gemv_geom(const mk_task_descriptor& d, GemvGeom& g) {
   g.B = d.m;
-  g.BT = g.B == 1 ? 1 : g.B == 2 ? 2 : g.B <= 4 ? 4 : 8;  // instantiated batch width
+  g.BT = g.B == 1 ? 1 : g.B == 2 ? 2 : 8;  // instantiated batch width
   g.K = d.k;
   g.n = d.n;
   g.c0 = (int)d.reserved[0];
@@ -149,7 +151,7 @@ __device__ __forceinline__ void gemv_geom(const mk_task_descriptor& d, GemvGeom&
   g.RG = min(rg, g.cn);
 }
 
-// Tensor-core tile plan (B >= 8): row groups of RG rows (the TMA box).  The
+// Tensor-core tile plan (three or more rows): row groups of RG rows (the TMA box).  The
 // MMA's N holds the group's rows of every segment (gate and up rows stacked
 // for SILU_MUL): segment sg occupies rows [sg * Nr, sg * Nr + RG) of the
 // weight tile and accumulator columns [sg * Nr, ...), N = seg * Nr <= 256.
@@ -522,7 +524,7 @@ struct Ctx {
   int task;
   uint64_t mark[3];  // optional trace marks inside a task body (thread 0)
   uint32_t ring_waits;  // traced: ring slots thread 0 found not yet landed
-  uint8_t* xbuf;        // B >= 8 kernel: activation staging tiles (tensor-core A operand)
+  uint8_t* xbuf;        // class-2 kernel: activation staging tiles (tensor-core A operand)
   TcCtl* ctl;
   uint32_t taddr;       // tensor-memory accumulator base
   uint32_t tc_ph;       // completed phases seen: mma_bar[0] (bit 0), mma_bar[1] (bit 1), acc_full (bit 2)
@@ -603,7 +605,7 @@ __device__ void block_argmax(float& v, int& idx, float* red) {
 }
 
 // ------------------------------------------------------------------ tagged hand-offs
-// At B <= 4 the activations that GEMVs read, and the qkv rows that
+// At one or two rows the activations that GEMVs read, and the qkv rows that
 // appends and partials read, also travel as (step tag, value) pairs in
 // mirrors of their buffers: one 8-byte word, tag in the high half (MEGA mode
 // only; every launch has a new tag, so pairs of earlier steps never match).
@@ -1000,8 +1002,10 @@ __device__ __forceinline__ void gemv_epilogue(const KParams& p, const mk_task_de
   cbar();
 }
 
-// Batch class 0 serves B <= 2, class 1 serves B <= 4, class 2 serves B <= 8;
-// each class is its own kernel so register allocations are not shared.
+// Batch class 0 serves one or two activation rows (CUDA-core GEMVs), class
+// 2 three to eight (tensor-core GEMVs; CUDA cores at batch width 8 only for
+// a weight without a tensor map); each class is its own kernel so register
+// allocations are not shared.
 template <int BCLASS>
 __device__ void gemv_task(Ctx& c, const mk_task_descriptor& d) {
   GemvGeom G;
@@ -1010,7 +1014,7 @@ __device__ void gemv_task(Ctx& c, const mk_task_descriptor& d) {
   gemv_prologue(d, G, red);
   // A residual read by the epilogue is loaded now, so its latency hides
   // behind the slots; it is parked in the (then free) slot area afterwards.
-  // tagged pairs (B <= 4 only): the output's mirror, and the inputs' when
+  // tagged pairs (one or two rows only): the output's mirror, and the inputs' when
   // both x and the residual have one (the task then waited on no counter)
   const KParams& p = *c.p;
   const uint64_t *xm = nullptr, *rm = nullptr;
@@ -1065,8 +1069,6 @@ __device__ void gemv_task(Ctx& c, const mk_task_descriptor& d) {
           case 16 + 7: gemv_stages<1, 7>(c, d, G, rows_g, ks, g0 == 0, xm); break;
           default: gemv_stages<2, 1>(c, d, G, rows_g, ks, g0 == 0, xm); break;
         }
-      } else if constexpr (BCLASS == 1) {
-        gemv_stages<4, 1>(c, d, G, rows_g, ks, g0 == 0, xm);
       } else {
         gemv_stages<8, 1>(c, d, G, rows_g, ks, g0 == 0, xm);
       }
@@ -1095,7 +1097,7 @@ __device__ void gemv_task(Ctx& c, const mk_task_descriptor& d) {
 }
 
 // ------------------------------------------------------------------ GEMV on tensor cores (B = 8)
-// At batch 8 a tile is a real dense contraction (8 columns of x against the
+// From three rows a tile is a dense contraction (up to 8 columns of x against the
 // tile's weight rows), so it runs on the 5th-generation tensor cores:
 // D[128 x N] (+)= A[128 x K] * B[K x N] with
 //   B = the tile's weight rows (N = rows rounded up to 16), K-major, brought
@@ -1138,6 +1140,7 @@ __device__ void tc_gemv_task(Ctx& c, const mk_task_descriptor& d) {
   TcCtl* ctl = c.ctl;
   GemvGeom G;
   gemv_geom(d, G);
+  G.BT = 8;  // the accumulators hold 8 batch rows whatever B (rows past B are zero)
   TcGeom T;
   tc_geom(c.rec->tm_rows, d, T);
   float* red = gemv_red(c);
@@ -1322,7 +1325,7 @@ __device__ void tc_gemv_task(Ctx& c, const mk_task_descriptor& d) {
   }
 }
 
-// MMA warp of the B >= 8 kernel (lane 0 of the producer warpgroup's second
+// MMA warp of the class-2 kernel (lane 0 of the producer warpgroup's second
 // warp): takes tensor-core tiles from the mailbox in the consumers' order;
 // per K range it waits for the staged activations and the landed weight
 // slots, issues the MMAs and commits; the commit of range kr - 2 hands that
@@ -1469,7 +1472,7 @@ __device__ void append_task(Ctx& c, const mk_task_descriptor& d) {
   }
   const size_t seq = (size_t)(s * T + t_) * (Hq + 2 * Hkv) * D;
   const float* qkv = rec_ptr<const float>(c, kPIn0) + seq;
-  const uint64_t* qm = rec_ptr<const uint64_t>(c, kMirX);  // tagged qkv (MEGA, B <= 4), else null
+  const uint64_t* qm = rec_ptr<const uint64_t>(c, kMirX);  // tagged qkv (MEGA, one or two rows), else null
   __nv_bfloat16* Kc = rec_ptr<__nv_bfloat16>(c, kPIn1);
   __nv_bfloat16* Vc = rec_ptr<__nv_bfloat16>(c, kPIn2);
   const size_t row = (((size_t)s * Hkv + g) * cap + pos) * D;
@@ -1606,7 +1609,7 @@ __device__ __forceinline__ void partial_stage(Ctx& c, const PartGeom& q, float* 
   const size_t rowlen = (size_t)(q.Hq + 2 * q.Hkv) * D;
   const size_t row0 = (size_t)q.s * q.T * rowlen;  // the sequence's first activation row
   const float* qkv = rec_ptr<const float>(c, kPIn0) + row0;
-  const uint64_t* qm = rec_ptr<const uint64_t>(c, kMirX);  // tagged qkv (MEGA, B <= 4), else null
+  const uint64_t* qm = rec_ptr<const uint64_t>(c, kMirX);  // tagged qkv (MEGA, one or two rows), else null
   if (qm) qm += row0;
   const float scale = 1.4426950408889634f / sqrtf((float)D);
   if constexpr (!CH) {
@@ -2543,11 +2546,11 @@ __device__ void consumer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
   }
 }
 
-// Shared memory: [activation staging (B >= 8 kernel)] [ring] [full, empty
+// Shared memory: [activation staging (class-2 kernel)] [ring] [full, empty
 // mbarriers] [control block] [task records] [record full, empty mbarriers]
 // [scratch].
 int smem_bytes_for(int nstages, int batch) {
-  return (batch > 4 ? kXbufBytes : 0) + nstages * kStageBytes + 2 * nstages * 8 + kCtlBytes +
+  return (batch > 2 ? kXbufBytes : 0) + nstages * kStageBytes + 2 * nstages * 8 + kCtlBytes +
          kRecs * (kRecBytes + 16) + kScratchBytes;
 }
 
@@ -2647,8 +2650,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_interpreter_kernel(const __gri
 namespace mk {
 
 static const void* kernel_for(int batch) {
-  return batch <= 2 ? (const void*)mk_interpreter_kernel<0>
-                    : batch <= 4 ? (const void*)mk_interpreter_kernel<1> : (const void*)mk_interpreter_kernel<2>;
+  return batch <= 2 ? (const void*)mk_interpreter_kernel<0> : (const void*)mk_interpreter_kernel<2>;
 }
 
 cudaError_t configure_interpreter(int batch, int nstages, int* num_regs) {

@@ -137,7 +137,7 @@ cudaError_t clear_step_arrivals(const DeviceState* d, cudaStream_t stream) {
   return cudaMemsetAsync(d->karr_step, 0, d->krecords * 4, stream);
 }
 
-// Tensor maps of the weights that B >= 8 GEMV tiles stream through the
+// Tensor maps of the weights that tensor-core GEMV tiles stream through the
 // tensor-core path: a 2-D bf16 view [rows, K] with a box of 64 columns x RG
 // rows in the 128-byte swizzle.  RG splits the op's tile width into row
 // groups of at most 256 rows (128 per segment for SILU_MUL: gate and up
@@ -153,7 +153,7 @@ int build_tensor_maps(const mk_graph* g, std::vector<uint8_t>& maps, std::vector
   rows.assign(NB, 0);
   EncodeTiledFn enc = nullptr;
   for (const OpRec& op : g->ops) {
-    if (op.kind != K_MATMUL || op.B < 8 || op.k % 64 != 0) continue;
+    if (op.kind != K_MATMUL || op.B < kTcMinRows || op.k % 64 != 0) continue;
     const int seg = (op.flags & MK_F_SILU_MUL) ? 2 : 1;
     // the tile (or, K-split, the row block) width
     const int cw = ksplit_plan(op.n, op.k, op.flags, op.B, g->tiles_target, g->col_align).W;
@@ -163,7 +163,7 @@ int build_tensor_maps(const mk_graph* g, std::vector<uint8_t>& maps, std::vector
     const int w = op.a[1];
     if (rows[w] != 0) {
       if (rows[w] != rg) return fail(MK_ERR_ARG, "mk_upload: weight buffer " + std::to_string(w) +
-                                                   " used by B >= 8 GEMVs with different tile widths");
+                                                   " used by tensor-core GEMVs with different tile widths");
       continue;
     }
     if (!enc) {
@@ -377,7 +377,7 @@ extern "C" int mk_upload(mk_graph* g, void* stream_) {
     d->tm_rows = reinterpret_cast<int32_t*>(base + o_tmr);
     d->mirrors = reinterpret_cast<uint64_t**>(base + o_mtab);
     for (const mk_task_descriptor& t : g->tasks)
-      if (t.op_id == MK_OP_GEMV && t.config_id == 1 && g->rows() > 4 && tm_rows[t.in_buf[1]] > 0) ++d->tc_tiles;
+      if (t.op_id == MK_OP_GEMV && t.config_id == 1 && g->rows() >= kTcMinRows && tm_rows[t.in_buf[1]] > 0) ++d->tc_tiles;
     d->status = reinterpret_cast<int32_t*>(base + o_status);
     d->level_bar = reinterpret_cast<uint32_t*>(base + o_lbar);
     d->trace = reinterpret_cast<uint64_t*>(base + o_trace);

@@ -9,9 +9,8 @@ rows appended to every layer's caches.
   - the Llama-3.2-1B-shaped model at all 16 layers for 32 greedy steps
     (error build-up over depth and over a long greedy run);
   - the Llama-3-8B-shaped model at all 32 layers for 2 steps;
-  - batches of 5 and 7 (the kernel class that runs B = 5..8 on CUDA cores
-    at batch width 8, with rows past the batch zero) on the tiny model and
-    at 1B width;
+  - batches of 5 and 7 (tensor-core tiles with rows past the batch zero)
+    on the tiny model and at 1B width;
   - the ragged batch of 8 (tensor-core GEMV tiles) at 8B width, 2 layers,
     over 4 steps.
 """

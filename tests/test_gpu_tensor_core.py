@@ -1,4 +1,5 @@
-"""Batch-8 decode: GEMV tiles on the tcgen05 tensor-core path (TMA-loaded,
+"""Decode with three to eight activation rows: GEMV tiles on the tcgen05
+tensor-core path (rows past the batch enter as zeros; TMA-loaded,
 128-byte-swizzled weight tiles, activations as three bf16 parts, f32 accumulators
 in tensor memory) against the float64 oracle, through the C ABI.
 
@@ -53,3 +54,18 @@ def test_tiny_batch8_tensor_core_tiles_match_oracle():
 def test_1b_batch8_tensor_core_tiles_match_oracle():
     w = synth.custom(synth.LLAMA_1B, 8, [700, 64, 1024, 9, 300, 512, 1000, 128], 1, name="1b_b8")
     assert _run(w, 1) == 1
+
+
+@pytest.mark.parametrize("B", [3, 4])
+def test_tiny_batch3_and_4_tensor_core_tiles_match_oracle(B):
+    # the smallest batches on the tensor cores: 3 or 4 of the 8 activation
+    # rows live, the accumulators read back at batch width 8
+    w = synth.custom(synth.TINY, B, [128, 5, 77, 40][:B], 4, name=f"tiny_tc_b{B}")
+    assert _run(w, 4) >= 2
+
+
+def test_1b_width_batch4_tensor_core_tiles_match_oracle():
+    import dataclasses
+    m = dataclasses.replace(synth.LLAMA_1B, L=2)
+    w = synth.custom(m, 4, [1024, 300, 777, 64], 2, name="1b_b4_l2")
+    assert _run(w, 2) >= 1
