@@ -326,8 +326,44 @@ __device__ __forceinline__ uint8_t* produce_slot(const KParams& p, uint8_t* ring
   return ring + (size_t)slot * kStageBytes;
 }
 
+// During the attention phase of one or two rows HBM idles while the
+// partials and the combine run: after a partial's slots, the copy thread
+// warms the L2 with the weight tiles of the next GEMV tasks whose records
+// are already made: the next two (the output projection and the gate and
+// up projection), up to kL2AheadBytes beyond what the ring will hold.
+constexpr uint32_t kL2AheadBytes = 512u * 1024u;
+
+__device__ __forceinline__ void l2_ahead(const TaskRec* recs, uint64_t* rfull, uint32_t k) {
+  uint32_t budget = kL2AheadBytes + (uint32_t)kMaxStages * kStageBytes;
+  int gemvs = 0;  // the output projection and the next (gate and up) GEMV only
+  for (uint32_t a = 1; a < (uint32_t)kRecs && budget > 0 && gemvs < 2; ++a) {
+    const uint32_t kk = k + a, e = kk & (kRecs - 1);
+    if (!mbar_test_wait(&rfull[e], (kk / kRecs) & 1u)) break;  // not made yet
+    const TaskRec* r = recs + e;
+    if (r->task < 0) break;
+    const mk_task_descriptor& d = r->d;
+    if (d.op_id != MK_OP_GEMV || d.config_id != 0) continue;
+    ++gemvs;
+    const int seg = (d.flags & MK_F_SILU_MUL) ? 2 : 1;
+    const char* W = reinterpret_cast<const char*>(r->ptr[kPIn1]);
+    const uint64_t rowb = (uint64_t)d.k * 2u;
+    for (int sg = 0; sg < seg && budget > 0; ++sg) {
+      const char* src = W + ((uint64_t)(sg ? d.n : 0) + d.reserved[0]) * rowb;
+      uint64_t left = (uint64_t)d.reserved[1] * rowb;
+      while (left > 0 && budget > 0) {
+        const uint32_t c = (uint32_t)min(min(left, (uint64_t)kStageBytes), (uint64_t)budget);
+        prefetch_l2(src, c);
+        src += c;
+        left -= c;
+        budget -= c;
+      }
+    }
+  }
+}
+
 // Producer (one thread): walks the task records and streams every task's
 // operand tiles into the ring, at most nstages slots ahead of the consumers.
+template <int BCLASS>
 __device__ void producer(const KParams& p, uint8_t* ring, uint64_t* full, uint64_t* empty, const TaskRec* recs,
                          uint64_t* rfull, uint64_t* rempty) {
   if ((threadIdx.x & 31) != 0) return;
@@ -437,6 +473,7 @@ __device__ void producer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
         bulk_g2s(dst, Kc + (rowbase + j) * q.D, bytes, fb, pol);
         bulk_g2s(dst + kStageBytes / 2, Vc + (rowbase + j) * q.D, bytes, fb, pol);
       }
+      if (BCLASS == 0 && !stop) l2_ahead(recs, rfull, k);
     }
     mbar_arrive(&rempty[e]);  // done with the record (the consumers arrive too)
   }
@@ -2617,7 +2654,7 @@ __global__ void __launch_bounds__(kThreads, 1) mk_interpreter_kernel(const __gri
   const uint32_t taddr = tcols > 0 ? ctl->tmem : 0u;
   if (threadIdx.x >= kConsumerThreads) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
-    if (threadIdx.x < kConsumerThreads + 32) producer(p, ring, full, empty, recs, rfull, rempty);
+    if (threadIdx.x < kConsumerThreads + 32) producer<BCLASS>(p, ring, full, empty, recs, rfull, rempty);
     else if (threadIdx.x < kConsumerThreads + 64) {
       if constexpr (tcols > 0) tc_mma_warp(p, ring, full, empty, ctl, smem_addr(xbuf), taddr, tmem_part_col(BCLASS));
     }
