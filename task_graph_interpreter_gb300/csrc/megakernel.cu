@@ -1546,8 +1546,10 @@ __device__ void append_task(Ctx& c, const mk_task_descriptor& d) {
 // slice: the lane holds dims {c * 64 + slice * 8 + [0, 8) : c < DS / 8} of
 // its row's query (qr) and output (o), element c * 8 + e at dim c * 64 +
 // slice * 8 + e, so that the 8 slices of a 16-byte load cover 128
-// consecutive bytes (every bank once); m and l are its row's running max and
-// sum (equal in the row's 8 lanes).  Keys k0 .. k0 + 7 (nvalid of them
+// consecutive bytes (every bank once); m is its row's running max (equal in
+// the row's 8 lanes) and l the running sum of the probabilities of the keys
+// the lane scored (key `slice` of each group; the row's sum is the sum of
+// its 8 lanes' l, taken once at the end).  Keys k0 .. k0 + 7 (nvalid of them
 // real) are read from shared memory (rows of DS * 8 bf16 at kb and vb):
 // each lane reads its slices of every key, so the four rows' lanes share
 // each address.  A score needs a sum over the row's 8 lanes only: a
@@ -1595,12 +1597,9 @@ __device__ __forceinline__ void partial_group8(const float (&qr)[DS], float (&o)
   for (int off = 1; off < 8; off <<= 1) gmax = fmaxf(gmax, __shfl_xor_sync(0xffffffffu, gmax, off));
   const float mnew = fmaxf(m, gmax);
   const float pr = live ? exp2f(v[0] - mnew) : 0.f;
-  float psum = pr;
-#pragma unroll
-  for (int off = 1; off < 8; off <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, off);
   const float sa = exp2f(m - mnew);  // 0 while m is -inf and mnew finite; exp2(nan) never: mnew >= m
-  l = fmaf(l, mnew == -INFINITY ? 1.f : sa, psum);
   const float sc = mnew == -INFINITY ? 1.f : sa;
+  l = fmaf(l, sc, pr);  // this lane's key only: the row's eight lanes are added once, at the end
 #pragma unroll
   for (int e = 0; e < DS; ++e) o[e] *= sc;
   m = mnew;
@@ -1798,6 +1797,9 @@ __device__ void partial_body(Ctx& c, const mk_task_descriptor& d, const PartGeom
     partial_group8<DS>(qr, o, m, l, nb, nb + T * D * 2, 0, q.nn, nlive, hlive, lane);
   }
   trace_mark(c, 1);
+  // each of a row's eight lanes summed the probabilities of its own keys
+#pragma unroll
+  for (int off = 1; off < 8; off <<= 1) l += __shfl_xor_sync(0xffffffffu, l, off);
   if (!mrg_apart) cbar();  // every warp is done with qs and nkv, which the merge area overlays
   // merge the warps of each row group
   if (hlive) {
