@@ -718,11 +718,15 @@ __device__ __forceinline__ void ll_gather(const KParams& p, int task, const uint
   for (int i = 0; i < N; ++i) out[i] = __uint_as_float((uint32_t)q[i]);
 }
 
-// Eight consecutive pairs into o; returns the mask of those already tagged.
+// Eight consecutive pairs (m 64-byte aligned) into o; returns the mask of
+// those already tagged.  Two 32-byte loads: every L2 sector is requested
+// once (16-byte loads asked for each sector twice, and every SM reads the
+// same vector, so the L2's sector rate bounded the load).
 __device__ __forceinline__ uint32_t ll_piece(const uint64_t* m, uint32_t tag, float (&o)[8]) {
-  const ulonglong2 a = ld_relaxed_v2u64(m), b = ld_relaxed_v2u64(m + 2), e = ld_relaxed_v2u64(m + 4),
-                   f = ld_relaxed_v2u64(m + 6);
-  const uint64_t q[8] = {a.x, a.y, b.x, b.y, e.x, e.y, f.x, f.y};
+  uint64_t lo[4], hi[4];
+  ld_relaxed_v4u64(m, lo);
+  ld_relaxed_v4u64(m + 4, hi);
+  const uint64_t q[8] = {lo[0], lo[1], lo[2], lo[3], hi[0], hi[1], hi[2], hi[3]};
   uint32_t ok = 0;
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
@@ -812,13 +816,12 @@ __device__ __forceinline__ void gemv_load_x(const KParams& p, int task, float (&
     for (int v = 0; v < NV; ++v) {
 #pragma unroll
       for (int b = 0; b < B; ++b) {
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f), e = a;
         if (b < Bact) {
-          a = __ldcg(reinterpret_cast<const float4*>(x + (size_t)b * K + col0 + v * 256));
-          e = __ldcg(reinterpret_cast<const float4*>(x + (size_t)b * K + col0 + v * 256 + 4));
+          ldcg_v8f(x + (size_t)b * K + col0 + v * 256, xr[b][v]);  // one request per sector
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) xr[b][v][k] = 0.f;
         }
-        xr[b][v][0] = a.x; xr[b][v][1] = a.y; xr[b][v][2] = a.z; xr[b][v][3] = a.w;
-        xr[b][v][4] = e.x; xr[b][v][5] = e.y; xr[b][v][6] = e.z; xr[b][v][7] = e.w;
       }
     }
   }
@@ -1152,13 +1155,35 @@ __device__ void gemv_task(Ctx& c, const mk_task_descriptor& d) {
 // for a normalised input, the gains of those columns (bf16 pairs).
 __device__ __forceinline__ void tc_load_x(float (&xv)[8], uint32_t (&gv)[4], const float* x, const uint16_t* gamma,
                                           int K, int b, int Bact, int k0, int kpt) {
+  // the widest load that covers the lane's kpt (2, 4 or 8) columns: every
+  // L2 sector is requested once
 #pragma unroll
-  for (int e = 0; e < 8; e += 2) {
-    float2 v = make_float2(0.f, 0.f);
-    if (e < kpt && b < Bact) v = __ldcg(reinterpret_cast<const float2*>(x + (size_t)b * K + k0 + e));
-    xv[e] = v.x;
-    xv[e + 1] = v.y;
-    gv[e >> 1] = (gamma && e < kpt) ? __ldg(reinterpret_cast<const uint32_t*>(gamma + k0 + e)) : 0u;
+  for (int e = 0; e < 8; ++e) xv[e] = 0.f;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) gv[e] = 0u;
+  const float* px = x + (size_t)b * K + k0;
+  const bool live = b < Bact;
+  if (kpt == 8) {
+    if (live) ldcg_v8f(px, xv);
+    if (gamma) {
+      const uint4 g = __ldg(reinterpret_cast<const uint4*>(gamma + k0));
+      gv[0] = g.x; gv[1] = g.y; gv[2] = g.z; gv[3] = g.w;
+    }
+  } else if (kpt == 4) {
+    if (live) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(px));
+      xv[0] = v.x; xv[1] = v.y; xv[2] = v.z; xv[3] = v.w;
+    }
+    if (gamma) {
+      const uint2 g = __ldg(reinterpret_cast<const uint2*>(gamma + k0));
+      gv[0] = g.x; gv[1] = g.y;
+    }
+  } else {
+    if (live) {
+      const float2 v = __ldcg(reinterpret_cast<const float2*>(px));
+      xv[0] = v.x; xv[1] = v.y;
+    }
+    if (gamma) gv[0] = __ldg(reinterpret_cast<const uint32_t*>(gamma + k0));
   }
 }
 

@@ -109,6 +109,20 @@ __device__ __forceinline__ ulonglong2 ld_relaxed_v2u64(const uint64_t* p) {
   return v;
 }
 
+// Eight floats (one L2 sector) in one request, cached in L2 only; p 32-byte aligned.
+__device__ __forceinline__ void ldcg_v8f(const float* p, float (&v)[8]) {
+  asm volatile("ld.global.cg.v8.f32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3]), "=f"(v[4]), "=f"(v[5]), "=f"(v[6]), "=f"(v[7])
+               : "l"(p));
+}
+
+// 32 bytes (four pairs, one L2 sector) in one request; p 32-byte aligned.
+__device__ __forceinline__ void ld_relaxed_v4u64(const uint64_t* p, uint64_t (&v)[4]) {
+  asm volatile("ld.relaxed.gpu.global.v4.u64 {%0, %1, %2, %3}, [%4];"
+               : "=l"(v[0]), "=l"(v[1]), "=l"(v[2]), "=l"(v[3])
+               : "l"(p));
+}
+
 __device__ __forceinline__ uint64_t ld_relaxed_u64(const uint64_t* p) {
   uint64_t v;
   asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p));
