@@ -311,31 +311,34 @@ struct RingPos {
 };
 
 // ------------------------------------------------------------------ producer
-// Claim the next ring slot once the consumers have freed it and announce the
-// bytes the coming copies will deliver; *fb receives the slot's full
-// barrier.  Null on abort or timeout.
-__device__ __forceinline__ uint8_t* produce_slot(const KParams& p, uint8_t* ring, uint64_t* full, uint64_t* empty,
-                                                 RingPos& rp, uint32_t& issued, int task, uint32_t bytes,
-                                                 uint64_t** fb) {
-  const uint32_t slot = rp.slot;
-  if (!bar_wait(p, &empty[slot], rp.phase ^ 1u, task, true)) return nullptr;
-  mbar_arrive_expect_tx(&full[slot], bytes);
-  rp.advance(p.nstages);
-  ++issued;
-  *fb = &full[slot];
-  return ring + (size_t)slot * kStageBytes;
-}
+// Paced L2 warm-up at one or two rows.  During the attention phase HBM
+// idles while the partials and the combine run.  After a partial's slots
+// the copy thread plans the weight tiles of the next two GEMV tasks whose
+// records are made (the output projection and the gate and up projection),
+// up to kL2AheadBytes beyond what the ring will hold.  Once the consumers
+// have released the partial's first slot (its query and new key are
+// staged), it prefetches one kStageBytes chunk at a time, at most one per
+// kL2GapNs (about 1.5 times this SM's share of HBM), and only while it
+// waits for a free ring slot.  A burst of prefetches queued in front of the
+// polls of the partials and the combine and delayed them; so did a pace
+// much faster than this one, while a much slower one ran on into the
+// GEMVs' own streaming.
+constexpr uint32_t kL2AheadBytes = 768u * 1024u;
+constexpr uint32_t kL2GapNs = 500u;
 
-// During the attention phase of one or two rows HBM idles while the
-// partials and the combine run: after a partial's slots, the copy thread
-// warms the L2 with the weight tiles of the next GEMV tasks whose records
-// are already made: the next two (the output projection and the gate and
-// up projection), up to kL2AheadBytes beyond what the ring will hold.
-constexpr uint32_t kL2AheadBytes = 512u * 1024u;
+struct L2Warm {
+  const char* src[3];  // the ranges left, current first
+  uint32_t left[3];
+  const uint64_t* start;  // its phase start_par opens the warm-up (null: open)
+  uint32_t start_par;
+  uint64_t next;  // globaltimer of the earliest next prefetch
+};
 
-__device__ __forceinline__ void l2_ahead(const TaskRec* recs, uint64_t* rfull, uint32_t k) {
+__device__ __forceinline__ void l2_plan(const TaskRec* recs, uint64_t* rfull, uint32_t k, L2Warm& w) {
   uint32_t budget = kL2AheadBytes + (uint32_t)kMaxStages * kStageBytes;
-  int gemvs = 0;  // the output projection and the next (gate and up) GEMV only
+  w.left[0] = w.left[1] = w.left[2] = 0u;
+  w.next = 0;
+  int gemvs = 0, n = 0;
   for (uint32_t a = 1; a < (uint32_t)kRecs && budget > 0 && gemvs < 2; ++a) {
     const uint32_t kk = k + a, e = kk & (kRecs - 1);
     if (!mbar_test_wait(&rfull[e], (kk / kRecs) & 1u)) break;  // not made yet
@@ -347,18 +350,72 @@ __device__ __forceinline__ void l2_ahead(const TaskRec* recs, uint64_t* rfull, u
     const int seg = (d.flags & MK_F_SILU_MUL) ? 2 : 1;
     const char* W = reinterpret_cast<const char*>(r->ptr[kPIn1]);
     const uint64_t rowb = (uint64_t)d.k * 2u;
-    for (int sg = 0; sg < seg && budget > 0; ++sg) {
+    for (int sg = 0; sg < seg && budget > 0 && n < 3; ++sg, ++n) {
+      const uint32_t len = (uint32_t)min((uint64_t)d.reserved[1] * rowb, (uint64_t)budget);
       const char* src = W + ((uint64_t)(sg ? d.n : 0) + d.reserved[0]) * rowb;
-      uint64_t left = (uint64_t)d.reserved[1] * rowb;
-      while (left > 0 && budget > 0) {
-        const uint32_t c = (uint32_t)min(min(left, (uint64_t)kStageBytes), (uint64_t)budget);
-        prefetch_l2(src, c);
-        src += c;
-        left -= c;
-        budget -= c;
-      }
+      // appended at position n (0..2) through selects: no run-time array index
+#pragma unroll
+      for (int q = 0; q < 3; ++q)
+        if (q == n) {
+          w.src[q] = src;
+          w.left[q] = len;
+        }
+      budget -= len;
     }
   }
+}
+
+// One paced prefetch of the plan, if it is open and due.
+__device__ __forceinline__ void l2_step(L2Warm& w) {
+  if (w.left[0] == 0u) return;
+  if (w.start) {
+    if (!mbar_test_wait(const_cast<uint64_t*>(w.start), w.start_par)) return;
+    w.start = nullptr;
+  }
+  const uint64_t now = globaltimer();
+  if (now < w.next) return;
+  const uint32_t c = min(w.left[0], kStageBytes);
+  prefetch_l2(w.src[0], c);
+  w.src[0] += c;
+  w.left[0] -= c;
+  if (w.left[0] == 0u) {  // next range
+    w.src[0] = w.src[1];
+    w.left[0] = w.left[1];
+    w.src[1] = w.src[2];
+    w.left[1] = w.left[2];
+    w.left[2] = 0u;
+  }
+  w.next = now + kL2GapNs;
+}
+
+// Claim the next ring slot once the consumers have freed it and announce the
+// bytes the coming copies will deliver; *fb receives the slot's full
+// barrier.  Null on abort or timeout.
+__device__ __forceinline__ uint8_t* produce_slot(const KParams& p, uint8_t* ring, uint64_t* full, uint64_t* empty,
+                                                 RingPos& rp, uint32_t& issued, int task, uint32_t bytes,
+                                                 uint64_t** fb, L2Warm* w = nullptr) {
+  const uint32_t slot = rp.slot;
+  if (w && w->left[0] != 0u) {  // a warm-up is planned: step it while the slot is busy
+    const uint64_t t0 = globaltimer();
+    for (uint32_t it = 1; !mbar_test_wait(&empty[slot], rp.phase ^ 1u); ++it) {
+      l2_step(*w);
+      if ((it & 255u) == 0) {
+        if (aborted(p)) return nullptr;
+        if (globaltimer() - t0 > p.timeout_ns) {
+          raise_error(p, MK_DEV_RING_TIMEOUT, task);
+          return nullptr;
+        }
+      }
+    }
+  } else if (!bar_wait(p, &empty[slot], rp.phase ^ 1u, task, true)) {
+    return nullptr;
+  }
+  if (w && w->start == &empty[slot]) w->start = nullptr;  // reusing the slot: the opening phase completed
+  mbar_arrive_expect_tx(&full[slot], bytes);
+  rp.advance(p.nstages);
+  ++issued;
+  *fb = &full[slot];
+  return ring + (size_t)slot * kStageBytes;
 }
 
 // Producer (one thread): walks the task records and streams every task's
@@ -373,6 +430,14 @@ __device__ void producer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
   uint32_t issued = 0;
   bool stop = false;
   const int32_t* state = static_cast<const int32_t*>(p.bufs[MK_BUF_STATE]);
+  __shared__ L2Warm warm;  // the copy thread's plan (its registers are few)
+  L2Warm* wp = nullptr;
+  if (BCLASS == 0) {
+    warm.left[0] = warm.left[1] = warm.left[2] = 0u;
+    warm.start = nullptr;
+    warm.next = 0;
+    wp = &warm;
+  }
   for (uint32_t k = 0; !stop; ++k) {
     const uint32_t e = k & (kRecs - 1);
     const TaskRec* r = recs + e;
@@ -415,7 +480,7 @@ __device__ void producer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
               const int nr = min(G.rs, rows_g - r0);
               const uint32_t bytes = (uint32_t)nr * G.KS * 2u;
               uint64_t* fb;
-              uint8_t* dst = produce_slot(p, ring, full, empty, rp, issued, task, bytes, &fb);
+              uint8_t* dst = produce_slot(p, ring, full, empty, rp, issued, task, bytes, &fb, wp);
               if (!dst) { stop = true; break; }
               const int64_t row = (int64_t)(sg ? G.n : 0) + G.c0 + g0 + r0;
               const uint16_t* src = W + row * G.K + (int64_t)ks * G.KS;
@@ -463,17 +528,22 @@ __device__ void producer(const KParams& p, uint8_t* ring, uint64_t* full, uint64
         mbar_arrive(&rempty[e]);
         continue;
       }
+      const uint32_t s0 = rp.slot, ph0 = rp.phase;  // the chunk's first slot
       for (int i = 0; i < q.nstage && !stop; ++i) {
         const int j = q.j0 + i * q.R;
         const int nr = min(q.R, q.jst - j);
         const uint32_t bytes = (uint32_t)nr * q.D * 2u;
         uint64_t* fb;
-        uint8_t* dst = produce_slot(p, ring, full, empty, rp, issued, task, 2u * bytes, &fb);
+        uint8_t* dst = produce_slot(p, ring, full, empty, rp, issued, task, 2u * bytes, &fb, wp);
         if (!dst) { stop = true; break; }
         bulk_g2s(dst, Kc + (rowbase + j) * q.D, bytes, fb, pol);
         bulk_g2s(dst + kStageBytes / 2, Vc + (rowbase + j) * q.D, bytes, fb, pol);
       }
-      if (BCLASS == 0 && !stop) l2_ahead(recs, rfull, k);
+      if (wp && !stop && q.nstage > 0) {
+        l2_plan(recs, rfull, k, *wp);
+        wp->start = &empty[s0];
+        wp->start_par = ph0;
+      }
     }
     mbar_arrive(&rempty[e]);  // done with the record (the consumers arrive too)
   }
