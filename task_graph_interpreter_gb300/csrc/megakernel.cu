@@ -1142,28 +1142,17 @@ __device__ void gemv_task(Ctx& c, const mk_task_descriptor& d) {
   const float* res = (d.flags & MK_F_ADD_RESIDUAL) ? rec_ptr<const float>(c, kPIn2) : nullptr;
   const bool stage_res = (d.flags & MK_F_ADD_RESIDUAL) && G.cn <= kConsumerThreads && G.RG >= G.cn;
   float rv[8];
+  // tagged residual pairs (at most two rows): issued now, examined once the
+  // slots are consumed, so their round trip overlaps x's instead of
+  // preceding it (the residual was complete long before)
+  constexpr int RB = BCLASS < 2 ? 2 : 1;
+  uint64_t rq[RB];
+  const uint64_t* rc = nullptr;
   if (stage_res && rm) {
-    // warp-collective: threads past the tile's columns load nothing
-    const bool mine = threadIdx.x < G.cn;
-    const uint64_t* rc = rm + G.c0 + threadIdx.x;
-    uint64_t q[8];
+    rc = rm + G.c0 + threadIdx.x;
 #pragma unroll
-    for (int b = 0; b < 8; ++b) q[b] = mine && b < G.B ? ld_relaxed_u64(rc + (size_t)b * G.n) : ll_pack(0.f, p.tag);
-    for (;;) {
-      int first = -1;
-#pragma unroll
-      for (int b = 7; b >= 0; --b)
-        if (!ll_ready(q[b], p.tag)) first = b;
-      const uint32_t want = __ballot_sync(0xffffffffu, first >= 0);
-      if (!want) break;
-      const int leader = __ffs(want) - 1;
-      if (!ll_poll_warp(p, rc + (size_t)(first < 0 ? 0 : first) * G.n, leader, c.task)) break;
-#pragma unroll
-      for (int b = 0; b < 8; ++b)
-        if (!ll_ready(q[b], p.tag)) q[b] = ld_relaxed_u64(rc + (size_t)b * G.n);
-    }
-#pragma unroll
-    for (int b = 0; b < 8; ++b) rv[b] = __uint_as_float((uint32_t)q[b]);
+    for (int b = 0; b < RB; ++b)
+      rq[b] = threadIdx.x < G.cn && b < G.B ? ld_relaxed_u64(rc + (size_t)b * G.n) : ll_pack(0.f, p.tag);
   } else if (stage_res && threadIdx.x < G.cn) {
 #pragma unroll
     for (int b = 0; b < 8; ++b) rv[b] = b < G.B ? __ldcg(res + (size_t)b * G.n + G.c0 + threadIdx.x) : 0.f;
@@ -1185,6 +1174,24 @@ __device__ void gemv_task(Ctx& c, const mk_task_descriptor& d) {
       gemv_fold(d, G, rows_g, ks, g0 == 0, gemv_slots(c), gemv_acc(c), red);
     }
     trace_mark(c, 1);
+    if (rc) {  // warp-collective: a stale pair is polled, then every stale one reloaded
+      for (;;) {
+        int first = -1;
+#pragma unroll
+        for (int b = RB - 1; b >= 0; --b)
+          if (!ll_ready(rq[b], p.tag)) first = b;
+        const uint32_t want = __ballot_sync(0xffffffffu, first >= 0);
+        if (!want) break;
+        const int leader = __ffs(want) - 1;
+        if (!ll_poll_warp(p, rc + (size_t)(first < 0 ? 0 : first) * G.n, leader, c.task)) break;
+#pragma unroll
+        for (int b = 0; b < RB; ++b)
+          if (!ll_ready(rq[b], p.tag)) rq[b] = ld_relaxed_u64(rc + (size_t)b * G.n);
+      }
+#pragma unroll
+      for (int b = 0; b < 8; ++b) rv[b] = b < RB ? __uint_as_float((uint32_t)rq[b < RB ? b : 0]) : 0.f;
+      rc = nullptr;
+    }
     float* staged = nullptr;
     if (stage_res) {  // the fold's closing barrier has freed the slot area
       staged = gemv_slots(c);
