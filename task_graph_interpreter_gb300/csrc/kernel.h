@@ -22,7 +22,7 @@ static_assert(128 * kProducerRegs + 2 * 128 * kConsumerRegs <= kThreads * kLaunc
               "register split exceeds the launch allocation");
 constexpr int kStageBytes = 32768;               // one ring slot
 constexpr int kStageElems = kStageBytes / 2;     // bf16 elements per slot
-constexpr int kMaxStages = 6;
+constexpr int kMaxStages = 5;                    // ring slots (a sixth only lengthened the HBM queues)
 constexpr int kScratchBytes = 24576;             // per-task shared scratch
 constexpr int kXbufBytes = 24576;                // class-2 kernel: two 12 KB activation staging tiles
 constexpr int kTmemCols = 256;                   // class-2 kernel: GEMV accumulator columns
