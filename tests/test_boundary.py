@@ -658,3 +658,26 @@ def test_tagged_scratch_only_for_polling_combines(L):
             _check_sync_plan(tasks, L.mk_get_edges(g), L.mk_get_sync_plan(g, len(tasks)), (task_ll, buf_ll))
         finally:
             L.mk_destroy(g)
+
+
+# The largest dynamic shared memory a CTA may opt in to on sm_100-class
+# GPUs (227 KB); a kilobyte is left for the kernel's static shared words.
+_SMEM_OPT_IN = 227 * 1024
+
+
+@pytest.mark.parametrize("name", synth.WORKLOADS)
+def test_kernel_shared_memory_fits_one_cta_per_sm(L, name):
+    """The interpreter's shared memory at its full ring (one or two rows:
+    ring, control block, task records, scratch; three to eight: also the
+    tensor-core activation tiles) fits the opt-in limit, so the ring is
+    never shortened at launch on these workloads."""
+    w = synth.workload(name)
+    spec = llama_decode_spec(w.model, w.B, w.kv_len, w.capacity, w.chunk, 152)
+    g = _replay(L, spec, w.B)
+    try:
+        smem, threads, stages = L.mk_kernel_info(g)
+    finally:
+        L.mk_destroy(g)
+    assert threads == 384  # two consumer warpgroups and the producer warpgroup
+    assert stages == 5  # ring slots of 32 KB
+    assert stages * 32768 < smem <= _SMEM_OPT_IN - 1024
